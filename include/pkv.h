@@ -1,0 +1,220 @@
+/*
+ * pkv.h — C ABI of the paged KV-cache decode library (GB300, sm_103a).
+ *
+ * The library implements the data-parallel hot path of PagedAttention
+ * (Kwon et al., "Efficient Memory Management for Large Language Model Serving
+ * with PagedAttention", SOSP 2023):
+ *
+ *   pkv_reshape_and_cache        write each step's new K/V rows into cache slots
+ *   pkv_copy_blocks              copy whole physical blocks (copy-on-write)
+ *   pkv_paged_attention_decode   single-token attention over a block-paged cache
+ *
+ * Sources for the semantics (page title, then section):
+ *   [VM]  "PagedAttention: the KV cache was the bottleneck all along",
+ *         section "Virtual memory for attention": the cache is cut into
+ *         fixed-size blocks holding the keys and values of a fixed number of
+ *         tokens; a sequence's blocks may sit anywhere in memory; a per-sequence
+ *         block table translates logical block positions into physical blocks,
+ *         the way a page table does; blocks are acquired as a sequence grows;
+ *         the attention kernel reads K and V from those scattered blocks; sampled
+ *         completions of one prompt share its blocks and copy a block only when
+ *         they diverge (copy-on-write).
+ *   [ABS] "Efficient Memory Management for Large Language Model Serving with
+ *         PagedAttention", section "From the abstract": the attention algorithm
+ *         is modelled on virtual memory and paging.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor arguments are DEVICE pointers to contiguous, row-major memory
+ *    owned by the caller. The library allocates nothing, frees nothing, keeps
+ *    no per-call state, never synchronises the stream and never reads device
+ *    memory from the host. Work is enqueued on `stream` (a cudaStream_t; NULL
+ *    means the legacy default stream).
+ *  - Element type `dtype` is one of pkv_dtype. The kernels move 16-byte
+ *    vectors: q, out, k, v, k_cache and v_cache must be 16-byte aligned.
+ *  - Cache layout (one pool for K, one for V):
+ *        cache[num_blocks][num_kv_heads][block_size][head_dim]
+ *    so one (block, kv head) tile of block_size x head_dim elements is a
+ *    contiguous run of memory. A cache slot is
+ *        slot = physical_block * block_size + offset_in_block.
+ *  - Supported: head_dim in {64, 128}, block_size in {8, 16, 32},
+ *    num_heads % num_kv_heads == 0 (grouped-query heads h map to kv head
+ *    h / (num_heads / num_kv_heads)).
+ *  - Host-side checks run before anything is enqueued and return a
+ *    pkv_status; nothing is launched when the status is not PKV_OK.
+ *  - Device-side checks never trap. A kernel that meets a bad index skips (or
+ *    clamps, see each entry point) the access and ORs a PKV_DEV_ERR_* bit into
+ *    `*dev_err` when `dev_err` is not NULL. The caller reads that word after
+ *    synchronising; a non-zero word means the outputs of that call are not
+ *    valid.
+ *  - Every wait inside a kernel is bounded (pkv_set_wait_timeout_ns); a wait
+ *    that runs out sets PKV_DEV_ERR_TIMEOUT, lets its own copies land, and the
+ *    kernel returns normally, leaving the CUDA context usable.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t, declared here so that C callers need no CUDA
+ * header to use this one. */
+typedef struct CUstream_st* pkv_stream_t;
+
+typedef enum pkv_dtype {
+  PKV_F32 = 0,  /* IEEE binary32 */
+  PKV_F16 = 1,  /* IEEE binary16 */
+  PKV_BF16 = 2  /* bfloat16      */
+} pkv_dtype;
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1, /* NULL or misaligned pointer, negative or inconsistent size */
+  PKV_ERR_UNSUPPORTED = 2, /* well-formed but not built: head_dim, block_size, dtype, grid limit */
+  PKV_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than pkv_decode_workspace_bytes() */
+  PKV_ERR_CUDA = 4         /* a CUDA runtime call or a kernel launch failed */
+} pkv_status;
+
+/* Bits ORed into *dev_err by the kernels. */
+#define PKV_DEV_ERR_BLOCK_ID 0x1    /* block table entry outside [0, num_blocks) */
+#define PKV_DEV_ERR_SLOT 0x2        /* slot_mapping entry >= num_blocks * block_size */
+#define PKV_DEV_ERR_CONTEXT_LEN 0x4 /* context_lens entry < 0, > max_context_len or > max_blocks_per_seq * block_size */
+#define PKV_DEV_ERR_TIMEOUT 0x8     /* a bounded wait inside a kernel ran out */
+#define PKV_DEV_ERR_PAIR 0x10       /* copy_blocks pair entry outside [0, num_blocks) */
+
+/* Human-readable name of a pkv_status value (static string, never NULL). */
+const char* pkv_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int pkv_version(void);
+
+/*
+ * Limit, in nanoseconds, of every bounded wait inside the kernels (default
+ * 1e9 ns = 1 s). A value of 0 makes any wait that is not already satisfied on
+ * its first test give up at once; it exists so that the timeout path can be
+ * exercised. Process-wide; takes effect for launches enqueued after the call.
+ */
+void pkv_set_wait_timeout_ns(uint64_t ns);
+uint64_t pkv_get_wait_timeout_ns(void);
+
+/* -------------------------------------------------------------------------
+ * pkv_reshape_and_cache
+ *
+ * Operation [VM]: a decoding step appends one K row and one V row per kv
+ * head to each running sequence, into the cache slot of that token:
+ *     for t in [0, num_tokens), h in [0, num_kv_heads):
+ *         s = slot_mapping[t]; if s < 0: skip (padding token)
+ *         k_cache[s / block_size][h][s % block_size][:] = k[t][h][:]
+ *         v_cache[s / block_size][h][s % block_size][:] = v[t][h][:]
+ * It is a pure byte copy: the result is bit-exact.
+ *
+ *   k, v          [num_tokens][num_kv_heads][head_dim]   dtype, read
+ *   k_cache,
+ *   v_cache       [num_blocks][num_kv_heads][block_size][head_dim], written at the slots only
+ *   slot_mapping  int64 [num_tokens]
+ *   dev_err       optional int32 word (see PKV_DEV_ERR_*)
+ *
+ * Errors: host — INVALID_ARG for NULL/misaligned pointers or sizes < 0,
+ * UNSUPPORTED for head_dim/block_size/dtype outside the supported sets.
+ * Device — a slot >= num_blocks * block_size is skipped and sets
+ * PKV_DEV_ERR_SLOT. Two tokens with the same slot race (undefined which wins).
+ * num_tokens == 0 enqueues nothing.
+ * ---------------------------------------------------------------------- */
+pkv_status pkv_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                                 const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                 int head_dim, int block_size, int num_blocks, pkv_dtype dtype,
+                                 int32_t* dev_err, pkv_stream_t stream);
+
+/* -------------------------------------------------------------------------
+ * pkv_copy_blocks
+ *
+ * Operation [VM]: when sequences that share a block diverge, the writer gets
+ * its own copy of that block first (copy-on-write). For every pair i:
+ *     src = block_pairs[2*i], dst = block_pairs[2*i + 1]
+ *     k_cache[dst][:][:][:] = k_cache[src][:][:][:]     (all kv heads)
+ *     v_cache[dst][:][:][:] = v_cache[src][:][:][:]
+ * A byte copy: bit-exact.
+ *
+ *   k_cache, v_cache  [num_blocks][num_kv_heads][block_size][head_dim]
+ *   block_pairs       int64 [num_pairs][2] (device)
+ *
+ * Pairs are independent and may run in any order: a block that is the
+ * destination of one pair must not be the source or destination of another
+ * pair in the same call (undefined otherwise). Errors: host checks as for
+ * pkv_reshape_and_cache; a pair with an entry outside [0, num_blocks) is
+ * skipped and sets PKV_DEV_ERR_PAIR. num_pairs == 0 enqueues nothing.
+ * ---------------------------------------------------------------------- */
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pairs, int num_pairs,
+                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                           pkv_dtype dtype, int32_t* dev_err, pkv_stream_t stream);
+
+/* -------------------------------------------------------------------------
+ * pkv_paged_attention_decode
+ *
+ * Operation [VM], [ABS]: softmax attention of one new query token per
+ * sequence over the keys and values of that sequence's first context_lens[s]
+ * tokens, which live in scattered physical blocks reached through the block
+ * table. For sequence s, query head h, kv head g = h / (num_heads/num_kv_heads):
+ *     token t (0 <= t < L = context_lens[s]) is stored in block
+ *         p = block_tables[s][t / block_size], row t % block_size
+ *     x_t   = scale * sum_d q[s][h][d] * k_cache[p][g][t % block_size][d]
+ *     out[s][h][:] = sum_t softmax(x)_t * v_cache[p][g][t % block_size][:]
+ * L == 0 gives an all-zero output row. Accumulation is fp32; the result is
+ * rounded once to dtype.
+ *
+ *   out            [num_seqs][num_heads][head_dim]  dtype, written
+ *   q              [num_seqs][num_heads][head_dim]  dtype
+ *   k_cache,
+ *   v_cache        [num_blocks][num_kv_heads][block_size][head_dim] dtype
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]; only the first
+ *                  ceil(L / block_size) entries of row s are read
+ *   context_lens   int32 [num_seqs]
+ *   max_context_len  an upper bound of every context_lens entry, supplied by
+ *                  the caller (it sizes the grid; the host never reads the
+ *                  device array); must be <= max_blocks_per_seq * block_size
+ *   workspace      device scratch of at least pkv_decode_workspace_bytes()
+ *                  bytes (may be NULL when that is 0). Its first region holds
+ *                  int32 counters that MUST be zero before the first call; every
+ *                  call that ends with *dev_err == 0 leaves them zero again. After
+ *                  a call that reports a device error, zero the workspace again.
+ *                  Two calls that share a workspace must not overlap on the GPU.
+ *
+ * Long contexts are cut into partitions of pkv_decode_partition_tokens()
+ * tokens processed by separate thread blocks; their partial softmax states
+ * are combined by a log-sum-exp merge inside the same kernel launch.
+ *
+ * Errors: host — INVALID_ARG (NULL/misaligned pointers, num_heads not a
+ * multiple of num_kv_heads, max_context_len > max_blocks_per_seq*block_size,
+ * negative sizes), UNSUPPORTED (head_dim, block_size, dtype, num_seqs > 65535),
+ * WORKSPACE. Device — a block id outside [0, num_blocks) is read as block 0
+ * and sets PKV_DEV_ERR_BLOCK_ID; a context length outside its bounds is
+ * clamped and sets PKV_DEV_ERR_CONTEXT_LEN; a wait that runs out sets
+ * PKV_DEV_ERR_TIMEOUT. num_seqs == 0 enqueues nothing.
+ * ---------------------------------------------------------------------- */
+pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_cache,
+                                      const void* v_cache, const int32_t* block_tables,
+                                      const int32_t* context_lens, float scale, int num_heads,
+                                      int num_kv_heads, int head_dim, int block_size, int num_seqs,
+                                      int max_blocks_per_seq, int num_blocks, int max_context_len,
+                                      pkv_dtype dtype, void* workspace, size_t workspace_bytes,
+                                      int32_t* dev_err, pkv_stream_t stream);
+
+/* Tokens per context partition used by pkv_paged_attention_decode for these
+ * sizes (a multiple of 16 and of every supported block_size). Pure host
+ * function. */
+int pkv_decode_partition_tokens(int num_seqs, int num_heads, int max_context_len);
+
+/* Bytes of workspace pkv_paged_attention_decode needs for these sizes; 0 when
+ * no sequence can span more than one partition. Pure host function; returns 0
+ * for non-positive sizes. */
+size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

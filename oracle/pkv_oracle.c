@@ -1,0 +1,396 @@
+/*
+ * pkv_oracle.c — fp64 CPU oracle of the PagedAttention decode path.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product library links, loads or
+ * calls this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do. It shares no code, header, table or helper with the CUDA path.
+ *
+ * What it follows (page title, then section):
+ *   [VM]  "PagedAttention: the KV cache was the bottleneck all along",
+ *         "Virtual memory for attention": fixed-size blocks of K/V for a fixed
+ *         number of tokens; a per-sequence block table maps logical block
+ *         positions to physical blocks; attention reads K/V from the scattered
+ *         blocks; shared blocks are copied only when a sharer diverges.
+ *   [ABS] "Efficient Memory Management for Large Language Model Serving with
+ *         PagedAttention", "From the abstract": PagedAttention computes
+ *         attention (paging changes where K/V live, not what is computed).
+ *
+ * The attention result is therefore the plain definition of scaled
+ * dot-product attention of one query over the sequence's earlier tokens,
+ * evaluated in double precision after decoding each stored element exactly
+ * from its bit pattern. Paging only decides where token t of a sequence is
+ * read from; this oracle walks the block table one token at a time.
+ *
+ * Build: plain C99, -ffp-contract=off so that x86 and Arm round identically.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2 };
+
+/* ---- element decoding, from the storage formats' definitions ------------ */
+
+/* IEEE 754 binary16: sign(1) exponent(5, bias 15) fraction(10). */
+double orc_decode_f16(uint16_t bits) {
+  int sign = (bits >> 15) & 1;
+  int e = (bits >> 10) & 0x1f;
+  int f = bits & 0x3ff;
+  double mag;
+  if (e == 0)
+    mag = ldexp((double)f, -24); /* subnormal: f * 2^(1-15-10) */
+  else if (e == 31)
+    mag = f ? NAN : INFINITY;
+  else
+    mag = ldexp((double)(f + 1024), e - 25); /* (1.f) * 2^(e-15), as an integer times 2^-10 */
+  return sign ? -mag : mag;
+}
+
+/* bfloat16: sign(1) exponent(8, bias 127) fraction(7). */
+double orc_decode_bf16(uint16_t bits) {
+  int sign = (bits >> 15) & 1;
+  int e = (bits >> 7) & 0xff;
+  int f = bits & 0x7f;
+  double mag;
+  if (e == 0)
+    mag = ldexp((double)f, -133); /* subnormal: f * 2^(1-127-7) */
+  else if (e == 255)
+    mag = f ? NAN : INFINITY;
+  else
+    mag = ldexp((double)(f + 128), e - 134); /* (1.f) * 2^(e-127) */
+  return sign ? -mag : mag;
+}
+
+/* IEEE 754 binary32: sign(1) exponent(8, bias 127) fraction(23). */
+double orc_decode_f32(uint32_t bits) {
+  int sign = (int)((bits >> 31) & 1u);
+  int e = (int)((bits >> 23) & 0xffu);
+  uint32_t f = bits & 0x7fffffu;
+  double mag;
+  if (e == 0)
+    mag = ldexp((double)f, -149); /* subnormal: f * 2^(1-127-23) */
+  else if (e == 255)
+    mag = f ? NAN : INFINITY;
+  else
+    mag = ldexp((double)(f + 0x800000u), e - 150);
+  return sign ? -mag : mag;
+}
+
+static int elem_bytes(int dtype) {
+  return dtype == ORC_F32 ? 4 : (dtype == ORC_F16 || dtype == ORC_BF16) ? 2 : 0;
+}
+
+/* Element `idx` of an array of `dtype`, as a double. */
+static double elem(const void* base, size_t idx, int dtype) {
+  if (dtype == ORC_F32) {
+    uint32_t u;
+    memcpy(&u, (const unsigned char*)base + idx * 4, 4);
+    return orc_decode_f32(u);
+  }
+  uint16_t h;
+  memcpy(&h, (const unsigned char*)base + idx * 2, 2);
+  return dtype == ORC_F16 ? orc_decode_f16(h) : orc_decode_bf16(h);
+}
+
+/* ---- softmax-weighted sum over an explicit list of tokens --------------- */
+
+/* Given logits x[0..n) and a way to read V row t, write
+ *   out[d] = sum_t exp(x_t - m) * V_t[d] / sum_t exp(x_t - m),  m = max_t x_t
+ * (subtracting m is an exact identity of softmax that keeps exp finite).
+ * x is scratch: it is overwritten with the weights exp(x_t - m). */
+typedef struct {
+  const void* v;     /* value storage */
+  const size_t* row; /* element offset of token t's row */
+  int dtype;
+} vrows;
+
+static void softmax_combine(double* out, double* x, int n, vrows V, int head_dim) {
+  double m = -INFINITY, z = 0.0;
+  for (int t = 0; t < n; ++t)
+    if (x[t] > m) m = x[t];
+  for (int t = 0; t < n; ++t) {
+    x[t] = exp(x[t] - m);
+    z += x[t];
+  }
+  for (int d = 0; d < head_dim; ++d) {
+    double acc = 0.0;
+    for (int t = 0; t < n; ++t) acc += x[t] * elem(V.v, V.row[t] + (size_t)d, V.dtype);
+    out[d] = acc / z;
+  }
+}
+
+static double dot_rows(const void* a, size_t a_off, const void* b, size_t b_off, int n, int dtype) {
+  double acc = 0.0;
+  for (int d = 0; d < n; ++d) acc += elem(a, a_off + (size_t)d, dtype) * elem(b, b_off + (size_t)d, dtype);
+  return acc;
+}
+
+/* ---- paged decode attention ------------------------------------------- */
+
+/*
+ * out[s][h][d] (double) for s in [seq_begin, seq_end), every head h.
+ * Cache layout [num_blocks][num_kv_heads][block_size][head_dim]; token t of
+ * sequence s lives in physical block block_tables[s][t / block_size], row
+ * t % block_size ([VM]: block table = logical-to-physical map). Query head h
+ * reads kv head h / (num_heads / num_kv_heads).
+ * Returns 0, or a negative code for a bad argument / out-of-range block id.
+ */
+int orc_paged_attention(double* out, const void* q, const void* k_cache, const void* v_cache,
+                        const int32_t* block_tables, int max_blocks_per_seq,
+                        const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                        int head_dim, int block_size, int num_blocks, int dtype, double scale,
+                        int seq_begin, int seq_end) {
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return -1;
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return -2;
+  if (head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || !elem_bytes(dtype)) return -3;
+  if (seq_begin < 0 || seq_end > num_seqs || seq_begin > seq_end) return -4;
+  const int group = num_heads / num_kv_heads;
+  int max_len = 0;
+  for (int s = seq_begin; s < seq_end; ++s) {
+    if (context_lens[s] < 0 || context_lens[s] > max_blocks_per_seq * block_size) return -5;
+    if (context_lens[s] > max_len) max_len = context_lens[s];
+  }
+  double* x = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+  size_t* row = (size_t*)malloc(sizeof(size_t) * (size_t)(max_len > 0 ? max_len : 1));
+  if (!x || !row) {
+    free(x);
+    free(row);
+    return -6;
+  }
+  int rc = 0;
+  for (int s = seq_begin; s < seq_end && rc == 0; ++s) {
+    const int L = context_lens[s];
+    for (int h = 0; h < num_heads; ++h) {
+      const int g = h / group;
+      double* o = out + ((size_t)s * num_heads + h) * head_dim;
+      if (L == 0) {
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        continue;
+      }
+      const size_t q_off = ((size_t)s * num_heads + h) * head_dim;
+      for (int t = 0; t < L; ++t) {
+        const int32_t p = block_tables[(size_t)s * max_blocks_per_seq + t / block_size];
+        if (p < 0 || p >= num_blocks) {
+          rc = -7;
+          break;
+        }
+        row[t] = (((size_t)p * num_kv_heads + g) * block_size + (size_t)(t % block_size)) * head_dim;
+        x[t] = scale * dot_rows(q, q_off, k_cache, row[t], head_dim, dtype);
+      }
+      if (rc) break;
+      vrows V = {v_cache, row, dtype};
+      softmax_combine(o, x, L, V, head_dim);
+    }
+  }
+  free(x);
+  free(row);
+  return rc;
+}
+
+/*
+ * Same attention over K/V stored densely, sequence after sequence:
+ * k, v are [total_tokens][num_kv_heads][head_dim]; sequence s owns rows
+ * [seq_start[s], seq_start[s+1]). No block table is involved. Used to pin the
+ * paged oracle: paging must not change the result.
+ */
+int orc_dense_attention(double* out, const void* q, const void* k, const void* v,
+                        const int64_t* seq_start, int num_seqs, int num_heads, int num_kv_heads,
+                        int head_dim, int dtype, double scale) {
+  if (!out || !q || !k || !v || !seq_start) return -1;
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return -2;
+  if (head_dim <= 0 || !elem_bytes(dtype)) return -3;
+  const int group = num_heads / num_kv_heads;
+  int64_t max_len = 0;
+  for (int s = 0; s < num_seqs; ++s) {
+    int64_t n = seq_start[s + 1] - seq_start[s];
+    if (n < 0) return -5;
+    if (n > max_len) max_len = n;
+  }
+  double* x = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+  size_t* row = (size_t*)malloc(sizeof(size_t) * (size_t)(max_len > 0 ? max_len : 1));
+  if (!x || !row) {
+    free(x);
+    free(row);
+    return -6;
+  }
+  for (int s = 0; s < num_seqs; ++s) {
+    const int L = (int)(seq_start[s + 1] - seq_start[s]);
+    for (int h = 0; h < num_heads; ++h) {
+      const int g = h / group;
+      double* o = out + ((size_t)s * num_heads + h) * head_dim;
+      if (L == 0) {
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        continue;
+      }
+      const size_t q_off = ((size_t)s * num_heads + h) * head_dim;
+      for (int t = 0; t < L; ++t) {
+        row[t] = (((size_t)seq_start[s] + (size_t)t) * num_kv_heads + g) * head_dim;
+        x[t] = scale * dot_rows(q, q_off, k, row[t], head_dim, dtype);
+      }
+      vrows V = {v, row, dtype};
+      softmax_combine(o, x, L, V, head_dim);
+    }
+  }
+  free(x);
+  free(row);
+  return 0;
+}
+
+/*
+ * Split-context form of the same attention: the context of each (s, h) is cut
+ * into consecutive chunks of `chunk` tokens. Chunk c keeps its own maximum
+ * m_c, exp-sum l_c = sum_{t in c} exp(x_t - m_c) and normalised output
+ * o_c = sum_{t in c} exp(x_t - m_c) V_t / l_c. The chunks are then combined:
+ *   M = max_c m_c,  w_c = l_c * exp(m_c - M),  out = sum_c w_c o_c / sum_c w_c.
+ * Algebraically equal to the single pass (both are the same softmax); used to
+ * pin that combination rule. Paged layout as in orc_paged_attention.
+ */
+int orc_paged_attention_chunked(double* out, const void* q, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                int max_blocks_per_seq, const int32_t* context_lens, int num_seqs,
+                                int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                int num_blocks, int dtype, double scale, int chunk) {
+  if (chunk <= 0) return -8;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return -1;
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return -2;
+  if (head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || !elem_bytes(dtype)) return -3;
+  const int group = num_heads / num_kv_heads;
+  int max_len = 0;
+  for (int s = 0; s < num_seqs; ++s) {
+    if (context_lens[s] < 0 || context_lens[s] > max_blocks_per_seq * block_size) return -5;
+    if (context_lens[s] > max_len) max_len = context_lens[s];
+  }
+  const int max_chunks = max_len > 0 ? (max_len + chunk - 1) / chunk : 1;
+  double* x = (double*)malloc(sizeof(double) * (size_t)chunk);
+  size_t* row = (size_t*)malloc(sizeof(size_t) * (size_t)chunk);
+  double* cm = (double*)malloc(sizeof(double) * (size_t)max_chunks);               /* m_c */
+  double* cl = (double*)malloc(sizeof(double) * (size_t)max_chunks);               /* l_c */
+  double* co = (double*)malloc(sizeof(double) * (size_t)max_chunks * head_dim);    /* o_c */
+  if (!x || !row || !cm || !cl || !co) {
+    free(x);
+    free(row);
+    free(cm);
+    free(cl);
+    free(co);
+    return -6;
+  }
+  int rc = 0;
+  for (int s = 0; s < num_seqs && rc == 0; ++s) {
+    const int L = context_lens[s];
+    const int nchunks = (L + chunk - 1) / chunk;
+    for (int h = 0; h < num_heads && rc == 0; ++h) {
+      const int g = h / group;
+      double* o = out + ((size_t)s * num_heads + h) * head_dim;
+      const size_t q_off = ((size_t)s * num_heads + h) * head_dim;
+      /* each chunk on its own: (m_c, l_c, o_c) */
+      for (int c = 0; c < nchunks && rc == 0; ++c) {
+        const int t0 = c * chunk;
+        const int n = (L - t0) < chunk ? (L - t0) : chunk;
+        double mc = -INFINITY, lc = 0.0;
+        for (int i = 0; i < n; ++i) {
+          const int t = t0 + i;
+          const int32_t p = block_tables[(size_t)s * max_blocks_per_seq + t / block_size];
+          if (p < 0 || p >= num_blocks) {
+            rc = -7;
+            break;
+          }
+          row[i] = (((size_t)p * num_kv_heads + g) * block_size + (size_t)(t % block_size)) * head_dim;
+          x[i] = scale * dot_rows(q, q_off, k_cache, row[i], head_dim, dtype);
+          if (x[i] > mc) mc = x[i];
+        }
+        if (rc) break;
+        for (int i = 0; i < n; ++i) lc += exp(x[i] - mc);
+        vrows V = {v_cache, row, dtype};
+        softmax_combine(co + (size_t)c * head_dim, x, n, V, head_dim);
+        cm[c] = mc;
+        cl[c] = lc;
+      }
+      if (rc) break;
+      if (L == 0) {
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        continue;
+      }
+      /* merge: M = max_c m_c, w_c = l_c exp(m_c - M), out = sum w_c o_c / sum w_c */
+      double M = -INFINITY, wsum = 0.0;
+      for (int c = 0; c < nchunks; ++c)
+        if (cm[c] > M) M = cm[c];
+      for (int c = 0; c < nchunks; ++c) wsum += cl[c] * exp(cm[c] - M);
+      for (int d = 0; d < head_dim; ++d) {
+        double acc = 0.0;
+        for (int c = 0; c < nchunks; ++c) acc += cl[c] * exp(cm[c] - M) * co[(size_t)c * head_dim + d];
+        o[d] = acc / wsum;
+      }
+    }
+  }
+  free(x);
+  free(row);
+  free(cm);
+  free(cl);
+  free(co);
+  return rc;
+}
+
+/* ---- cache maintenance (byte copies) ------------------------------------ */
+
+/*
+ * [VM] a sequence grows one token per step into its blocks: for token t with
+ * slot s = slot_mapping[t] >= 0, every kv head's K row and V row is copied to
+ * cache[s / block_size][h][s % block_size][:]. Negative slots are padding and
+ * are skipped. Returns the number of slots that were out of range (not
+ * written), or a negative code for a bad argument.
+ */
+int orc_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                          const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                          int head_dim, int block_size, int num_blocks, int dtype) {
+  const int es = elem_bytes(dtype);
+  if (!es || num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return -1;
+  if (num_tokens && (!k || !v || !k_cache || !v_cache || !slot_mapping)) return -1;
+  const size_t row_bytes = (size_t)head_dim * es;
+  int bad = 0;
+  for (int t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= (int64_t)num_blocks * block_size) {
+      ++bad;
+      continue;
+    }
+    const int64_t blk = slot / block_size, off = slot % block_size;
+    for (int h = 0; h < num_kv_heads; ++h) {
+      const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + (size_t)off) * row_bytes;
+      const size_t src = ((size_t)t * num_kv_heads + h) * row_bytes;
+      memcpy((unsigned char*)k_cache + dst, (const unsigned char*)k + src, row_bytes);
+      memcpy((unsigned char*)v_cache + dst, (const unsigned char*)v + src, row_bytes);
+    }
+  }
+  return bad;
+}
+
+/*
+ * [VM] copy-on-write: for each pair (src, dst) the whole physical block src
+ * (every kv head, every row) of both pools is copied onto block dst, in pair
+ * order. Returns the number of pairs skipped for out-of-range ids, or a
+ * negative code for a bad argument.
+ */
+int orc_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pairs, int num_pairs,
+                    int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype) {
+  const int es = elem_bytes(dtype);
+  if (!es || num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return -1;
+  if (num_pairs && (!k_cache || !v_cache || !block_pairs)) return -1;
+  const size_t block_bytes = (size_t)num_kv_heads * block_size * head_dim * es;
+  int bad = 0;
+  for (int i = 0; i < num_pairs; ++i) {
+    const int64_t src = block_pairs[2 * i], dst = block_pairs[2 * i + 1];
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+      ++bad;
+      continue;
+    }
+    memmove((unsigned char*)k_cache + (size_t)dst * block_bytes,
+            (const unsigned char*)k_cache + (size_t)src * block_bytes, block_bytes);
+    memmove((unsigned char*)v_cache + (size_t)dst * block_bytes,
+            (const unsigned char*)v_cache + (size_t)src * block_bytes, block_bytes);
+  }
+  return bad;
+}

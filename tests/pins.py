@@ -1,0 +1,375 @@
+"""Checks that pin the oracle to facts other than itself.
+
+Each pin takes an oracle build `L` (None = the default build) and raises
+AssertionError when the oracle disagrees with:
+  - the storage formats' definitions (element decoders vs numpy's binary16 and
+    the bfloat16 = upper-half-of-binary32 definition);
+  - closed forms of softmax attention (context 1 returns V; a zero query or
+    identical keys average V; one dominant logit selects its V; two tokens
+    reduce to the logistic function; grouped heads read kv head h // group);
+  - high-precision brute force (mpmath, 200-bit) on tiny inputs;
+  - the paging facts of "PagedAttention: the KV cache was the bottleneck all
+    along", section "Virtual memory for attention": the block table only says
+    where a token lives (paged == dense over the same tokens; any physical
+    permutation gives identical bits), and copy-on-write sharing gives the
+    same result as private copies;
+  - the log-sum-exp combination of split contexts;
+  - byte-level placement of cache writes and block copies, checked with numpy
+    indexing of the [num_blocks][kv_heads][block_size][head_dim] layout.
+
+tests/test_oracle_pins.py runs them on the oracle; tests/test_oracle_mutations.py
+runs them on copies with planted mistakes and expects each copy to fail one.
+"""
+from __future__ import annotations
+
+import numpy as np
+import scipy.special
+
+import oracle
+import synth
+import synth.host as H
+
+DTYPES = ("f32", "f16", "bf16")
+
+
+def _rand_store(rng, shape, dtype, scale=1.0):
+    return H.round_to_storage(rng.standard_normal(shape) * scale, dtype)
+
+
+def _dec(a, dtype):
+    """Reference decode with numpy (not the oracle's decoders)."""
+    if dtype == "f32":
+        return a.astype(np.float64)
+    if dtype == "f16":
+        return a.view(np.float16).astype(np.float64)
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _random_paged(rng, B, H_, Hkv, D, bs, NB, lens, dtype, q_scale=1.0):
+    """Random q and pools; each sequence gets distinct random blocks; rows past
+    a sequence's length are poison."""
+    lens = np.asarray(lens, dtype=np.int32)
+    MB = max(1, int(-(-lens.max() // bs)))
+    perm = rng.permutation(NB)
+    bt = np.full((B, MB), -1, dtype=np.int32)
+    k = 0
+    for s in range(B):
+        n = -(-int(lens[s]) // bs)
+        bt[s, :n] = perm[k:k + n]
+        k += n
+    assert k <= NB
+    kc = H.poison((NB, Hkv, bs, D), dtype)
+    vc = H.poison((NB, Hkv, bs, D), dtype)
+    for s in range(B):
+        for t in range(int(lens[s])):
+            p = bt[s, t // bs]
+            kc[p, :, t % bs, :] = _rand_store(rng, (Hkv, D), dtype)
+            vc[p, :, t % bs, :] = _rand_store(rng, (Hkv, D), dtype)
+    q = _rand_store(rng, (B, H_, D), dtype, q_scale)
+    return q, kc, vc, bt, lens
+
+
+def _attn(L, q, kc, vc, bt, lens, H_, Hkv, D, bs, dtype, scale):
+    return oracle.paged_attention(q, kc, vc, bt, lens, scale=scale, num_heads=H_,
+                                  num_kv_heads=Hkv, head_dim=D, block_size=bs, dtype=dtype, L=L)
+
+
+def _gather_dense(kc, bt, lens, bs):
+    """Each sequence's rows, in token order, by numpy indexing of the layout."""
+    rows = []
+    for s in range(len(lens)):
+        t = np.arange(int(lens[s]))
+        rows.append(kc[bt[s, t // bs], :, t % bs, :])
+    return np.ascontiguousarray(np.concatenate(rows, axis=0)) if rows else kc[:0, :, 0, :]
+
+
+# ---------------------------------------------------------------- decoders
+@np.errstate(invalid="ignore")
+def pin_decoders(L=None):
+    bits = np.arange(65536, dtype=np.uint16)
+    got = oracle.decode_elements(bits, "f16", L)
+    assert np.array_equal(got, bits.view(np.float16).astype(np.float64), equal_nan=True), "f16 decode"
+    ref = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    got = oracle.decode_elements(bits, "bf16", L)
+    assert np.array_equal(got, ref, equal_nan=True), "bf16 decode"
+    rng = np.random.default_rng(7)
+    u = np.concatenate([rng.integers(0, 2 ** 32, 50000, dtype=np.uint64).astype(np.uint32),
+                        np.array([0, 1, 0x7FFFFF, 0x800000, 0x7F7FFFFF, 0x7F800000, 0xFF800000,
+                                  0x80000001, 0x3F800000], dtype=np.uint32)])
+    got = oracle.decode_elements(u.view(np.float32), "f32", L)
+    assert np.array_equal(got, u.view(np.float32).astype(np.float64), equal_nan=True), "f32 decode"
+
+
+# ---------------------------------------------------------------- closed forms
+def pin_context_one(L=None):
+    """A context of one token returns that token's V row exactly."""
+    rng = np.random.default_rng(11)
+    for dtype in DTYPES:
+        B, H_, Hkv, D, bs, NB = 5, 4, 2, 64, 8, 16
+        q, kc, vc, bt, lens = _random_paged(rng, B, H_, Hkv, D, bs, NB, [1] * B, dtype)
+        out = _attn(L, q, kc, vc, bt, lens, H_, Hkv, D, bs, dtype, 0.3)
+        for s in range(B):
+            for h in range(H_):
+                assert np.array_equal(out[s, h], _dec(vc[bt[s, 0], h // 2, 0], dtype)), \
+                    f"context 1 {dtype} s={s} h={h}"
+
+
+def pin_uniform_weights(L=None):
+    """q = 0, or all keys of a head equal: every weight is the same, so the
+    output is the mean of the V rows."""
+    rng = np.random.default_rng(12)
+    B, H_, Hkv, D, bs, NB = 4, 2, 2, 64, 16, 40
+    lens = [37, 1, 64, 100]
+    for dtype in DTYPES:
+        q, kc, vc, bt, lens_ = _random_paged(rng, B, H_, Hkv, D, bs, NB, lens, dtype)
+        q0 = np.zeros_like(q)
+        out = _attn(L, q0, kc, vc, bt, lens_, H_, Hkv, D, bs, dtype, 0.125)
+        kq = kc.copy()
+        for s in range(B):  # identical keys within each (sequence, head)
+            for t in range(lens[s]):
+                kq[bt[s, t // bs], :, t % bs, :] = kc[bt[s, 0], :, 0, :]
+        out2 = _attn(L, q, kq, vc, bt, lens_, H_, Hkv, D, bs, dtype, 0.125)
+        for s in range(B):
+            t = np.arange(lens[s])
+            mean = _dec(vc[bt[s, t // bs], :, t % bs, :], dtype).mean(axis=0)  # [Hkv, D]
+            assert np.allclose(out[s], mean, rtol=0, atol=1e-12), f"q=0 mean {dtype}"
+            assert np.allclose(out2[s], mean, rtol=0, atol=1e-12), f"equal keys mean {dtype}"
+
+
+def pin_dominant_logit(L=None):
+    """One logit 80 above all others (weights e^-80 elsewhere): the output is
+    that token's V to within 1e-30 relative."""
+    rng = np.random.default_rng(13)
+    B, H_, Hkv, D, bs, NB = 3, 1, 1, 64, 16, 30
+    lens = [50, 50, 50]
+    q, kc, vc, bt, lens_ = _random_paged(rng, B, H_, Hkv, D, bs, NB, lens, "f32")
+    q[:] = 0.0
+    q[:, :, 0] = 1.0
+    for s, star in enumerate((0, 23, 49)):
+        for t in range(50):
+            kc[bt[s, t // bs], 0, t % bs, :] = 0.0
+        kc[bt[s, star // bs], 0, star % bs, 0] = 80.0
+    out = _attn(L, q, kc, vc, bt, lens_, H_, Hkv, D, bs, "f32", 1.0)
+    for s, star in enumerate((0, 23, 49)):
+        v = _dec(vc[bt[s, star // bs], 0, star % bs], "f32")
+        assert np.allclose(out[s, 0], v, rtol=1e-25, atol=1e-30), f"dominant logit s={s}"
+
+
+def pin_two_tokens(L=None):
+    """Softmax over two tokens is the logistic function of the logit gap:
+    out = (1 - w) V0 + w V1 with w = expit(scale * q.(k1 - k0)). Tokens sit in
+    different physical blocks (block_size 1)."""
+    for scale, a, b0, b1 in ((0.125, 3.0, 2.0, -5.0), (0.5, -1.5, 4.0, 0.25), (1.0, 0.0, 1.0, 9.0)):
+        D, NB = 64, 7
+        q = np.zeros((1, 1, D), np.float32)
+        q[0, 0, 5] = a
+        kc = H.poison((NB, 1, 1, D), "f32")
+        vc = H.poison((NB, 1, 1, D), "f32")
+        bt = np.array([[4, 2]], np.int32)
+        kc[4, 0, 0, :] = 0.0
+        kc[2, 0, 0, :] = 0.0
+        kc[4, 0, 0, 5] = b0
+        kc[2, 0, 0, 5] = b1
+        rng = np.random.default_rng(14)
+        vc[4, 0, 0, :] = rng.standard_normal(D).astype(np.float32)
+        vc[2, 0, 0, :] = rng.standard_normal(D).astype(np.float32)
+        out = _attn(L, q, kc, vc, bt, np.array([2], np.int32), 1, 1, D, 1, "f32", scale)
+        w = scipy.special.expit(scale * a * (b1 - b0))
+        ref = (1 - w) * vc[4, 0, 0].astype(np.float64) + w * vc[2, 0, 0].astype(np.float64)
+        assert np.allclose(out[0, 0], ref, rtol=1e-14, atol=1e-15), f"two tokens scale={scale}"
+
+
+def pin_gqa_mapping(L=None):
+    """Grouped heads: query head h reads kv head h // (H / Hkv). With V of kv
+    head g equal to the constant 2^(g-1) everywhere, every output element of
+    head h is exactly 2^(h//group - 1)."""
+    rng = np.random.default_rng(15)
+    B, H_, Hkv, D, bs, NB = 3, 6, 3, 64, 8, 24
+    for dtype in DTYPES:
+        q, kc, vc, bt, lens = _random_paged(rng, B, H_, Hkv, D, bs, NB, [9, 17, 30], dtype)
+        for g in range(Hkv):
+            c = H.round_to_storage(np.array(2.0 ** (g - 1)), dtype)
+            used = vc[:, g][~H.is_poison(vc[:, g])]
+            vc[:, g][~H.is_poison(vc[:, g])] = c
+            assert used.size
+        out = _attn(L, q, kc, vc, bt, lens, H_, Hkv, D, bs, dtype, 0.2)
+        for h in range(H_):
+            assert np.all(out[:, h, :] == 2.0 ** (h // 2 - 1)), f"gqa head {h} {dtype}"
+
+
+# ---------------------------------------------------------------- brute force
+def pin_brute_force(L=None):
+    """Tiny inputs against 200-bit mpmath evaluation of the definition."""
+    import mpmath
+    mpmath.mp.prec = 200
+    rng = np.random.default_rng(16)
+    for dtype in DTYPES:
+        B, H_, Hkv, D, bs, NB = 3, 2, 1, 4, 2, 12
+        lens = [1, 4, 5]
+        q, kc, vc, bt, lens_ = _random_paged(rng, B, H_, Hkv, D, bs, NB, lens, dtype)
+        scale = 0.7
+        out = _attn(L, q, kc, vc, bt, lens_, H_, Hkv, D, bs, dtype, scale)
+        for s in range(B):
+            for h in range(H_):
+                qs = [mpmath.mpf(float(x)) for x in _dec(q[s, h], dtype)]
+                xs, vs = [], []
+                for t in range(lens[s]):
+                    p, r = bt[s, t // bs], t % bs
+                    kr = _dec(kc[p, 0, r], dtype)
+                    xs.append(mpmath.mpf(scale) * mpmath.fsum(qi * mpmath.mpf(float(ki))
+                                                            for qi, ki in zip(qs, kr)))
+                    vs.append(_dec(vc[p, 0, r], dtype))
+                z = mpmath.fsum(mpmath.exp(x) for x in xs)
+                for d in range(D):
+                    ref = mpmath.fsum(mpmath.exp(x) * mpmath.mpf(float(v[d])) for x, v in zip(xs, vs)) / z
+                    assert abs(float(ref) - out[s, h, d]) <= 1e-15 * (1 + abs(float(ref))), \
+                        f"brute force {dtype} s={s} h={h} d={d}"
+
+
+# ---------------------------------------------------------------- paging facts
+def pin_dense_equivalence(L=None):
+    """Paging only decides where token t lives: paged attention equals the same
+    attention over the tokens laid out contiguously, bit for bit."""
+    rng = np.random.default_rng(17)
+    cases = [  # (B, H, Hkv, D, bs, NB, max_len, dtype)
+        (4, 2, 2, 64, 16, 64, 100, "f32"),
+        (5, 8, 2, 128, 8, 200, 150, "f16"),
+        (3, 4, 4, 128, 32, 40, 300, "bf16"),
+        (4, 6, 3, 64, 16, 80, 200, "f16"),
+    ]
+    for B, H_, Hkv, D, bs, NB, maxlen, dtype in cases:
+        lens = rng.integers(1, maxlen + 1, B)
+        q, kc, vc, bt, lens_ = _random_paged(rng, B, H_, Hkv, D, bs, NB, lens, dtype)
+        scale = 1.0 / np.sqrt(D)
+        out = _attn(L, q, kc, vc, bt, lens_, H_, Hkv, D, bs, dtype, scale)
+        kd, vd = _gather_dense(kc, bt, lens_, bs), _gather_dense(vc, bt, lens_, bs)
+        st = np.concatenate([[0], np.cumsum(lens_)]).astype(np.int64)
+        ref = oracle.dense_attention(q, kd, vd, st, scale=scale, num_heads=H_, num_kv_heads=Hkv,
+                                     head_dim=D, dtype=dtype, L=L)
+        assert np.isfinite(out).all(), "poison reached the output"
+        assert np.array_equal(out, ref), f"paged != dense {dtype} bs={bs}"
+
+
+def pin_placement_invariance(L=None):
+    """Any permutation of physical block ids (pool rows moved, tables
+    renumbered) gives identical bits."""
+    rng = np.random.default_rng(18)
+    B, H_, Hkv, D, bs, NB = 6, 4, 2, 64, 8, 120
+    for dtype in DTYPES:
+        lens = rng.integers(1, 120, B)
+        q, kc, vc, bt, lens_ = _random_paged(rng, B, H_, Hkv, D, bs, NB, lens, dtype)
+        out = _attn(L, q, kc, vc, bt, lens_, H_, Hkv, D, bs, dtype, 0.1)
+        perm = rng.permutation(NB)
+        kc2, vc2 = np.empty_like(kc), np.empty_like(vc)
+        kc2[perm], vc2[perm] = kc, vc
+        bt2 = np.where(bt >= 0, perm[np.maximum(bt, 0)], -1).astype(np.int32)
+        out2 = _attn(L, q, kc2, vc2, bt2, lens_, H_, Hkv, D, bs, dtype, 0.1)
+        assert np.array_equal(out, out2), f"placement changed the result {dtype}"
+
+
+def logical_streams(hw, hp):
+    """Each served sequence's K and V rows in token order, built without the
+    step's cache operations: prefix tokens from the pre-step pool through the
+    pre-step tables, then the sequence's new rows. (This is what private,
+    unshared copies of every sequence would hold.)"""
+    st, cfg = hw.st, hw.cfg
+    bs = cfg.block_size
+    k0, v0 = hp.k_cache, hp.v_cache   # must be the pre-step pools
+    ks, vs, lens = [], [], []
+    for i, s in enumerate(hp.seqs):
+        t = np.arange(int(st.prefix_lens[s]))
+        p = hp.prefix_tables[i, t // bs]
+        new = slice(int(st.new_start[s]), int(st.new_start[s + 1]))
+        ks.append(np.concatenate([k0[p, :, t % bs, :], hw.new_k[new]], axis=0))
+        vs.append(np.concatenate([v0[p, :, t % bs, :], hw.new_v[new]], axis=0))
+        lens.append(ks[-1].shape[0])
+    start = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    return np.ascontiguousarray(np.concatenate(ks)), np.ascontiguousarray(np.concatenate(vs)), start
+
+
+def pin_copy_on_write(L=None):
+    """Ref-counted sharing of prompt blocks + copy-on-write at divergence gives
+    the same bits as every sample owning a private copy of its tokens; the
+    step with new-token writes does the same for a plain batch."""
+    for cfg, B in ((synth.get("cow").replace(num_heads=4, num_kv_heads=4, num_blocks=3000), 12),
+                   (synth.get("cow").replace(num_heads=2, num_kv_heads=2, head_dim=64, block_size=8,
+                                             dtype="bf16", num_blocks=3000), 9),
+                   (synth.get("llama13b").replace(num_heads=4, num_kv_heads=2, num_blocks=2000), 10)):
+        hw = H.generate(cfg, num_seqs=B)
+        hp = H.compact_pools(hw)
+        kd, vd, start = logical_streams(hw, hp)
+        assert np.array_equal(start[1:] - start[:-1], hw.st.context_lens), "stream lengths"
+        out, _, _ = oracle.decode_step(hp, hw, L=L)
+        ref = oracle.dense_attention(hw.q, kd, vd, start, scale=cfg.scale, num_heads=cfg.num_heads,
+                                     num_kv_heads=cfg.num_kv_heads, head_dim=cfg.head_dim,
+                                     dtype=cfg.dtype, L=L)
+        assert np.isfinite(out).all(), "poison reached the output"
+        assert np.array_equal(out, ref), f"shared+CoW != private copies ({cfg.name})"
+
+
+def pin_split_merge(L=None):
+    """Chunked evaluation + log-sum-exp merge equals the single pass."""
+    rng = np.random.default_rng(19)
+    B, H_, Hkv, D, bs, NB = 4, 2, 1, 64, 16, 80
+    for dtype in ("f32", "bf16"):
+        lens = [1, 200, 333, 17]
+        q, kc, vc, bt, lens_ = _random_paged(rng, B, H_, Hkv, D, bs, NB, lens, dtype, q_scale=3.0)
+        ref = _attn(L, q, kc, vc, bt, lens_, H_, Hkv, D, bs, dtype, 0.5)
+        for chunk in (1, 3, 16, 64, 256, 4096):
+            got = oracle.paged_attention_chunked(q, kc, vc, bt, lens_, scale=0.5, num_heads=H_,
+                                                 num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                                                 dtype=dtype, chunk=chunk, L=L)
+            assert np.allclose(got, ref, rtol=1e-13, atol=1e-13), f"chunk {chunk} {dtype}"
+
+
+# ---------------------------------------------------------------- cache operations
+def pin_reshape_and_cache(L=None):
+    """Token t's rows land at cache[slot // bs][h][slot % bs]; padding (slot < 0)
+    and out-of-range slots write nothing; every other byte is untouched."""
+    rng = np.random.default_rng(20)
+    for dtype in DTYPES:
+        NB, Hkv, bs, D, T = 10, 3, 4, 64, 14
+        kc = H.poison((NB, Hkv, bs, D), dtype)
+        vc = H.poison((NB, Hkv, bs, D), dtype)
+        slots = rng.permutation(NB * bs)[:T].astype(np.int64)
+        slots[3] = -1
+        slots[7] = NB * bs + 5   # out of range
+        k = _rand_store(rng, (T, Hkv, D), dtype)
+        v = _rand_store(rng, (T, Hkv, D), dtype)
+        bad = oracle.reshape_and_cache(k, v, kc, vc, slots, num_kv_heads=Hkv, head_dim=D,
+                                       block_size=bs, dtype=dtype, L=L)
+        assert bad == 1, "out-of-range slot count"
+        written = 0
+        for t in range(T):
+            s = slots[t]
+            if 0 <= s < NB * bs:
+                assert np.array_equal(kc[s // bs, :, s % bs, :], k[t]), f"k row {t} {dtype}"
+                assert np.array_equal(vc[s // bs, :, s % bs, :], v[t]), f"v row {t} {dtype}"
+                written += 1
+        untouched = NB * Hkv * bs * D - written * Hkv * D
+        assert H.is_poison(kc).sum() == untouched and H.is_poison(vc).sum() == untouched, \
+            f"bytes outside the slots changed {dtype}"
+
+
+def pin_copy_blocks(L=None):
+    """Block dst of both pools becomes a copy of block src; all else unchanged."""
+    rng = np.random.default_rng(21)
+    for dtype in DTYPES:
+        NB, Hkv, bs, D = 12, 3, 8, 64
+        kc = _rand_store(rng, (NB, Hkv, bs, D), dtype)
+        vc = _rand_store(rng, (NB, Hkv, bs, D), dtype)
+        k0, v0 = kc.copy(), vc.copy()
+        pairs = np.array([[3, 7], [1, 2], [5, 0], [4, NB]], np.int64)
+        bad = oracle.copy_blocks(kc, vc, pairs, num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                                 dtype=dtype, L=L)
+        assert bad == 1, "bad pair count"
+        ek, ev = k0.copy(), v0.copy()
+        for s, d in pairs[:3]:
+            ek[d], ev[d] = k0[s], v0[s]
+        assert np.array_equal(kc, ek) and np.array_equal(vc, ev), f"copy_blocks {dtype}"
+
+
+ALL_PINS = [pin_decoders, pin_context_one, pin_uniform_weights, pin_dominant_logit,
+            pin_two_tokens, pin_gqa_mapping, pin_brute_force, pin_dense_equivalence,
+            pin_placement_invariance, pin_copy_on_write, pin_split_merge,
+            pin_reshape_and_cache, pin_copy_blocks]
