@@ -1,0 +1,90 @@
+// Cache maintenance kernels: slot-mapped write of new K/V rows and whole-block
+// copies for copy-on-write ("PagedAttention: the KV cache was the bottleneck
+// all along", section "Virtual memory for attention": sequences acquire
+// blocks as they grow; shared blocks are copied when a sharer diverges).
+// Both are byte moves in 16-byte vectors: results are bit-exact.
+#include "cache_ops.h"
+#include "common.cuh"
+
+namespace pkv {
+
+// One thread block per new token: its num_kv_heads rows of K and of V (each
+// row_chunks 16-byte chunks) go to cache[slot / bs][h][slot % bs].
+__global__ void __launch_bounds__(128)
+    reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                             uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                             const int64_t* __restrict__ slot_mapping, int num_kv_heads,
+                             int row_chunks, int block_size, int64_t num_slots, int32_t* dev_err) {
+  const int t = blockIdx.x;
+  const int64_t slot = __ldg(slot_mapping + t);
+  if (slot < 0) return;  // padding token
+  if (slot >= num_slots) {
+    if (threadIdx.x == 0) set_err(dev_err, PKV_DEV_ERR_SLOT);
+    return;
+  }
+  const int64_t blk = slot / block_size;
+  const int off = static_cast<int>(slot - blk * block_size);
+  const int n = num_kv_heads * row_chunks;
+  const uint4* ks = k + (size_t)t * n;
+  const uint4* vs = v + (size_t)t * n;
+  for (int c = threadIdx.x; c < n; c += blockDim.x) {
+    const int h = c / row_chunks;
+    const int cc = c - h * row_chunks;
+    const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * row_chunks + cc;
+    const uint4 kx = __ldg(ks + c);
+    const uint4 vx = __ldg(vs + c);
+    k_cache[dst] = kx;
+    v_cache[dst] = vx;
+  }
+}
+
+// grid = (pair, pool K|V, piece). Each piece streams part of one block with
+// 4 independent 16-byte loads in flight per thread.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                       const int64_t* __restrict__ pairs, int64_t block_chunks, int num_blocks,
+                       int32_t* dev_err) {
+  const int64_t src = __ldg(pairs + 2 * (size_t)blockIdx.x);
+  const int64_t dst = __ldg(pairs + 2 * (size_t)blockIdx.x + 1);
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) set_err(dev_err, PKV_DEV_ERR_PAIR);
+    return;
+  }
+  uint4* pool = blockIdx.y == 0 ? k_cache : v_cache;
+  const uint4* s = pool + (size_t)src * block_chunks;
+  uint4* d = pool + (size_t)dst * block_chunks;
+  const int64_t stride = (int64_t)gridDim.z * blockDim.x;
+  int64_t c = (int64_t)blockIdx.z * blockDim.x + threadIdx.x;
+  for (; c + 3 * stride < block_chunks; c += 4 * stride) {
+    const uint4 a = s[c], b = s[c + stride], e = s[c + 2 * stride], f = s[c + 3 * stride];
+    d[c] = a;
+    d[c + stride] = b;
+    d[c + 2 * stride] = e;
+    d[c + 3 * stride] = f;
+  }
+  for (; c < block_chunks; c += stride) d[c] = s[c];
+}
+
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                                     const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                     int row_bytes, int block_size, int num_blocks, int32_t* dev_err,
+                                     cudaStream_t stream) {
+  reshape_and_cache_kernel<<<num_tokens, 128, 0, stream>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache), slot_mapping, num_kv_heads, row_bytes / 16, block_size,
+      (int64_t)num_blocks * block_size, dev_err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,
+                               int64_t block_bytes, int num_blocks, int32_t* dev_err, cudaStream_t stream) {
+  const int64_t chunks = block_bytes / 16;
+  int64_t pieces = (chunks + 256 * 4 - 1) / (256 * 4);
+  if (pieces > 64) pieces = 64;
+  dim3 grid(num_pairs, 2, static_cast<unsigned>(pieces));
+  copy_blocks_kernel<<<grid, 256, 0, stream>>>(static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                                               pairs, chunks, num_blocks, dev_err);
+  return cudaGetLastError();
+}
+
+}  // namespace pkv

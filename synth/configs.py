@@ -24,7 +24,7 @@ class DecodeConfig:
     block_size: int
     dtype: str              # "f32" | "f16" | "bf16"
     num_blocks: int         # physical blocks in each pool
-    lengths: tuple          # ("uniform", lo, hi) | ("lognormal", median, sigma, lo, hi)
+    lengths: tuple          # ("uniform", lo, hi) | ("lognormal", median, sigma, lo, hi) | ("fixed", (..))
     value_scale: float      # K, V, q values are N(0, 1) * value_scale, rounded to dtype
     scale: float            # softmax scale applied to q . k
     seed: int
@@ -43,7 +43,7 @@ class DecodeConfig:
     @property
     def max_len(self) -> int:
         """Largest context length the distribution can produce."""
-        hi = self.lengths[-1]
+        hi = max(self.lengths[1]) if self.lengths[0] == "fixed" else self.lengths[-1]
         if self.tail is not None:
             hi += self.tail[-1]
         return int(hi)

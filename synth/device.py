@@ -97,8 +97,9 @@ def from_host(hw, device="cuda") -> DeviceWorkload:
     td = TORCH_DTYPE[cfg.dtype]
 
     def up(a: np.ndarray) -> torch.Tensor:
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        return (t if cfg.dtype == "f32" else t.view(torch.int16)).to(dev).view(td)
+        a = np.ascontiguousarray(a)
+        t = torch.from_numpy(a if cfg.dtype == "f32" else a.view(np.int16))
+        return t.to(dev).view(td)
 
     shape = (cfg.num_blocks, cfg.num_kv_heads, cfg.block_size, cfg.head_dim)
     kc = torch.empty(shape, dtype=td, device=dev)

@@ -104,9 +104,11 @@ class HostPools:
         return int(self.k_cache.shape[0])
 
 
-def compact_pools(w: HostWorkload, seqs: np.ndarray | None = None) -> HostPools:
+def compact_pools(w: HostWorkload, seqs: np.ndarray | None = None, fetch=None) -> HostPools:
     """Compact host pools for the whole step, or for a subset of sequences
-    (then only their blocks, rows and the new tokens that land in them)."""
+    (then only their blocks, the copies into them and their new tokens).
+    `fetch(ids) -> (k, v)` supplies the pre-step content of physical blocks
+    `ids` (default: the workload's prefilled blocks, poison elsewhere)."""
     st, cfg = w.st, w.cfg
     bs = cfg.block_size
     bt = st.block_tables if seqs is None else st.block_tables[seqs]
@@ -121,12 +123,15 @@ def compact_pools(w: HostWorkload, seqs: np.ndarray | None = None) -> HostPools:
         ids = np.unique(np.concatenate([mine, pairs[:, 0].astype(np.int64)]))
     remap = lambda a: np.searchsorted(ids, a)
     Hkv, D = cfg.num_kv_heads, cfg.head_dim
-    kc = poison((ids.shape[0], Hkv, bs, D), cfg.dtype)
-    vc = poison((ids.shape[0], Hkv, bs, D), cfg.dtype)
-    sel = np.isin(st.prefill_blocks, ids)
-    dst = remap(st.prefill_blocks[sel])
-    kc[dst] = w.prefill_k[sel]
-    vc[dst] = w.prefill_v[sel]
+    if fetch is None:
+        kc = poison((ids.shape[0], Hkv, bs, D), cfg.dtype)
+        vc = poison((ids.shape[0], Hkv, bs, D), cfg.dtype)
+        sel = np.isin(st.prefill_blocks, ids)
+        dst = remap(st.prefill_blocks[sel])
+        kc[dst] = w.prefill_k[sel]
+        vc[dst] = w.prefill_v[sel]
+    else:
+        kc, vc = fetch(ids)
     bt_c = np.where(bt >= 0, remap(np.maximum(bt, 0)), -1).astype(np.int32)
     pbt_c = np.where(pbt >= 0, remap(np.maximum(pbt, 0)), -1).astype(np.int32)
     sm = st.slot_mapping

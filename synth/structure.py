@@ -3,6 +3,7 @@ that already hold K/V before the step, and the step's writes (slots of new
 rows, copy-on-write pairs). No K/V values here (see host.py / device.py).
 
 Lengths:
+  ("fixed", (l0, l1, ...))              the given lengths, repeated cyclically
   ("uniform", lo, hi)                   integers uniform in [lo, hi]
   ("lognormal", median, sigma, lo, hi)  rint(exp(ln(median) + sigma * z)), clipped
 """
@@ -72,6 +73,9 @@ def draw_lengths(spec: tuple, n: int, rng: np.random.Generator) -> np.ndarray:
         _, median, sigma, lo, hi = spec
         z = rng.standard_normal(n)
         return np.clip(np.rint(np.exp(np.log(median) + sigma * z)), lo, hi).astype(np.int64)
+    if kind == "fixed":
+        vals = np.asarray(spec[1], dtype=np.int64)
+        return np.resize(vals, n)
     raise ValueError(f"unknown length distribution {spec!r}")
 
 

@@ -1,0 +1,133 @@
+"""The C-ABI library (no GPU needed): it loads, exports exactly the entry
+points include/*.h declares, and its host-side checks reject bad arguments
+before anything would reach the device."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from paged_kv_cache_204_gb300 import build as b
+    b.build()
+    import paged_kv_cache_204_gb300 as m
+    return m
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        names |= set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_exports_match_header(pkv):
+    declared = _declared()
+    assert {"pkv_paged_attention_decode", "pkv_reshape_and_cache", "pkv_copy_blocks"} <= declared
+    for name in declared:
+        assert hasattr(pkv.lib, name), f"{name} declared but not exported"
+    out = subprocess.run(["nm", "-D", "--defined-only", pkv.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (pkv_[a-z0-9_]+)$", out, flags=re.M))
+    assert exported == declared, f"exported {exported ^ declared} differ from the header"
+
+
+def test_status_strings_and_version(pkv):
+    assert pkv.status_string(0) == "PKV_OK"
+    assert pkv.status_string(3) == "PKV_ERR_WORKSPACE"
+    assert pkv.status_string(99) == "PKV_ERR_UNKNOWN"
+    assert pkv.version() >= 100
+
+
+def test_timeout_setting_round_trip(pkv):
+    old = pkv.get_wait_timeout_ns()
+    assert old == 10 ** 9
+    pkv.set_wait_timeout_ns(12345)
+    assert pkv.get_wait_timeout_ns() == 12345
+    pkv.set_wait_timeout_ns(old)
+
+
+def test_workspace_size(pkv):
+    P = pkv.decode_partition_tokens(128, 40, 2048)
+    assert P % 16 == 0 and P % 32 == 0
+    assert pkv.decode_workspace_bytes(128, 40, 128, P) == 0        # one partition: no workspace
+    S = -(-2048 // P)
+    rows = 128 * 40
+    align = lambda x: -(-x // 256) * 256
+    expect = align(rows * 4) + align(rows * S * 8) + rows * S * 128 * 4
+    assert pkv.decode_workspace_bytes(128, 40, 128, 2048) == expect
+    assert pkv.decode_workspace_bytes(0, 40, 128, 2048) == 0
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every call below returns before any device work
+
+
+def _decode(pkv, **kw):
+    a = dict(out=FAKE, q=FAKE, k=FAKE, v=FAKE, bt=FAKE, cl=FAKE, scale=0.1, H=8, Hkv=8, D=128, bs=16,
+             B=4, MB=8, NB=100, mcl=128, dtype=1, ws=None, ws_bytes=0, err=None, stream=None)
+    a.update(kw)
+    return pkv.lib.pkv_paged_attention_decode(a["out"], a["q"], a["k"], a["v"], a["bt"], a["cl"], a["scale"],
+                                              a["H"], a["Hkv"], a["D"], a["bs"], a["B"], a["MB"], a["NB"],
+                                              a["mcl"], a["dtype"], a["ws"], a["ws_bytes"], a["err"],
+                                              a["stream"])
+
+
+def test_decode_host_checks(pkv):
+    INV, UNS, WS, OK = pkv.PKV_ERR_INVALID_ARG, pkv.PKV_ERR_UNSUPPORTED, pkv.PKV_ERR_WORKSPACE, pkv.PKV_OK
+    assert _decode(pkv, B=0) == OK                       # nothing to do
+    assert _decode(pkv, q=None) == INV
+    assert _decode(pkv, out=FAKE + 8) == INV             # misaligned
+    assert _decode(pkv, Hkv=3) == INV                    # 8 % 3 != 0
+    assert _decode(pkv, mcl=129) == INV                  # > MB * bs
+    assert _decode(pkv, B=-1) == INV
+    assert _decode(pkv, scale=float("nan")) == INV
+    assert _decode(pkv, D=96) == UNS
+    assert _decode(pkv, bs=64) == UNS
+    assert _decode(pkv, dtype=7) == UNS
+    assert _decode(pkv, B=70000, MB=1, mcl=16) == UNS
+    big = dict(MB=200, mcl=3000)
+    assert _decode(pkv, **big) == WS                     # needs a workspace, none given
+    need = pkv.decode_workspace_bytes(4, 8, 128, 3000)
+    assert _decode(pkv, ws=FAKE, ws_bytes=need - 1, **big) == WS
+    assert _decode(pkv, ws=FAKE + 4, ws_bytes=need, **big) == INV
+
+
+def test_cache_op_host_checks(pkv):
+    L = pkv.lib
+    INV, UNS, OK = pkv.PKV_ERR_INVALID_ARG, pkv.PKV_ERR_UNSUPPORTED, pkv.PKV_OK
+    # (k, v, k_cache, v_cache, slots, T, Hkv, D, bs, NB, dtype, err, stream)
+    assert L.pkv_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 128, 16, 10, 2, None, None) == OK
+    assert L.pkv_reshape_and_cache(None, FAKE, FAKE, FAKE, FAKE, 3, 4, 128, 16, 10, 2, None, None) == INV
+    assert L.pkv_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE + 4, 3, 4, 128, 16, 10, 2, None, None) == INV
+    assert L.pkv_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, 3, 4, 80, 16, 10, 2, None, None) == UNS
+    assert L.pkv_reshape_and_cache(FAKE, FAKE, FAKE, FAKE, FAKE, -1, 4, 128, 16, 10, 2, None, None) == INV
+    # (k_cache, v_cache, pairs, n, Hkv, D, bs, NB, dtype, err, stream)
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 0, 4, 128, 16, 10, 1, None, None) == OK
+    assert L.pkv_copy_blocks(FAKE, None, FAKE, 2, 4, 128, 16, 10, 1, None, None) == INV
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 2, 4, 128, 12, 10, 1, None, None) == UNS
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 2, 0, 128, 16, 10, 1, None, None) == INV
+
+
+def test_no_fallback_without_library(tmp_path):
+    """A copy of the binding without its compiled library refuses to import."""
+    import shutil
+    pkg = tmp_path / "paged_kv_cache_204_gb300"
+    shutil.copytree(os.path.join(ROOT, "paged_kv_cache_204_gb300"), pkg,
+                    ignore=shutil.ignore_patterns("_build", "__pycache__"))
+    code = ("import sys\n"
+            f"sys.path.insert(0, {str(tmp_path)!r})\n"
+            "try:\n"
+            "    import paged_kv_cache_204_gb300\n"
+            "    print('imported')\n"
+            "except ImportError as e:\n"
+            "    print('ImportError', e)\n")
+    r = subprocess.run(["python", "-c", code], capture_output=True, text=True)
+    assert "ImportError" in r.stdout and "missing" in r.stdout, r.stdout + r.stderr
