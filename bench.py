@@ -264,6 +264,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
     cfg = synth.get(WORKLOAD)
+    if args.num_blocks:
+        cfg = cfg.replace(num_blocks=args.num_blocks)
     if world > 1:
         cfg = cfg.replace(seed=cfg.seed + rank)
     dw = SD.generate(cfg, device=dev)
@@ -391,6 +393,9 @@ def main() -> int:
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum time of the CPU baseline")
     ap.add_argument("--cpu-seqs", type=int, default=32, help="sequences in the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--num-blocks", type=int, default=0,
+                    help="physical blocks per pool (default: the workload's 40000); the same "
+                         "sequences and K/V bytes in a smaller pool, for profiler captures")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

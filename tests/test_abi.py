@@ -14,8 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def pkv():
-    from paged_kv_cache_204_gb300 import build as b
-    b.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import paged_kv_cache_204_gb300 as m
     return m
 
