@@ -376,9 +376,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     float Ls = 0.f, O = 0.f;
     for (int j = 0; j < nsplit; ++j) {
       const float2 v = __ldcg(ml + j);
-      const float sc = exp2f(v.x - M);
-      Ls += v.y * sc;
-      O += __ldcg(po + (size_t)j * D) * sc;
+      const float w = v.y * exp2f(v.x - M);  // l_j 2^(m_j - M)
+      Ls += w;
+      O += __ldcg(po + (size_t)j * D) * w;   // partials hold o_j / l_j
     }
     store_elem(static_cast<T*>(p.out) + row * D + d, O / Ls);
   }
