@@ -203,6 +203,51 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
                                       pkv_dtype dtype, void* workspace, size_t workspace_bytes,
                                       int32_t* dev_err, pkv_stream_t stream);
 
+/* -------------------------------------------------------------------------
+ * pkv_paged_attention_decode_noalloc
+ *
+ * No counterpart in the paper: this is a packaging variant, not part of the
+ * method. Same operation, arguments, layouts and error reporting as
+ * pkv_paged_attention_decode, minus the workspace: the scratch that holds
+ * the partial results of long contexts is a fixed array of
+ * PKV_NOALLOC_SCRATCH_BYTES bytes of device memory that the library itself
+ * declares, so neither the library nor the caller allocates anything.
+ *
+ * It is meant for callers that cannot call cudaMalloc or any other device
+ * allocator at the point where they run attention: for example a plugin
+ * inside a host application that has already reserved all device memory for
+ * its own allocator, or code with a fixed memory budget that must not grow
+ * at run time, or a loop that cannot afford the latency and implicit
+ * synchronisation of an allocation. Such callers cannot size and provide a
+ * workspace; this entry point needs none.
+ *
+ * Limits and rules:
+ *  - PKV_NOALLOC_SCRATCH_BYTES (32 MiB) is reserved on every device that
+ *    loads the library, for the life of the process.
+ *  - Sizes whose pkv_decode_workspace_bytes() exceeds that limit are rejected
+ *    with PKV_ERR_WORKSPACE before anything is enqueued (the LLaMA-13B-shaped
+ *    step, 128 sequences x 40 heads x 2048 tokens, needs 21 MB).
+ *  - The first call on a device looks up the array's device address once for
+ *    that device (with that device current); make that first call before any
+ *    stream capture begins.
+ *  - Every call on a device shares the same array and leaves its last
+ *    contents in it. Each call first clears the partition counters it needs
+ *    (an asynchronous memset on `stream`; this happens even when the call
+ *    then fails its host-side checks, and touches only the library's own
+ *    array). Two calls whose work overlaps on the GPU — different streams, or
+ *    different host threads — race on the array and give wrong results:
+ *    serialise them.
+ * ---------------------------------------------------------------------- */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+pkv_status pkv_paged_attention_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* block_tables,
+                                              const int32_t* context_lens, float scale, int num_heads,
+                                              int num_kv_heads, int head_dim, int block_size,
+                                              int num_seqs, int max_blocks_per_seq, int num_blocks,
+                                              int max_context_len, pkv_dtype dtype, int32_t* dev_err,
+                                              pkv_stream_t stream);
+
 /* Tokens per context partition used by pkv_paged_attention_decode for these
  * sizes (a multiple of 16 and of every supported block_size). Pure host
  * function. */

@@ -56,6 +56,10 @@ lib.pkv_copy_blocks.restype = _I
 lib.pkv_paged_attention_decode.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I,
                                            _I, _I, _P, _SZ, _P, _P]
 lib.pkv_paged_attention_decode.restype = _I
+lib.pkv_paged_attention_decode_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I,
+                                                   _I, _I, _I, _P, _P]
+lib.pkv_paged_attention_decode_noalloc.restype = _I
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024  # PKV_NOALLOC_SCRATCH_BYTES
 
 
 class PkvError(RuntimeError):
@@ -145,6 +149,23 @@ def paged_attention_decode(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Te
         float(scale), H, Hkv, D, bs, B, block_tables.shape[1], nb, int(max_context_len),
         DTYPE_CODE[q.dtype], _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)),
         "pkv_paged_attention_decode")
+
+
+def paged_attention_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                   v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                   context_lens: torch.Tensor, scale: float, max_context_len: int,
+                                   dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """paged_attention_decode without a workspace: for callers that cannot
+    allocate device memory, the library keeps the partial results of long
+    contexts in its own fixed 32 MiB device array (sizes that need more are
+    rejected). Calls that overlap on the GPU share that array and race."""
+    B, H, D = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    _check(lib.pkv_paged_attention_decode_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        float(scale), H, Hkv, D, bs, B, block_tables.shape[1], nb, int(max_context_len),
+        DTYPE_CODE[q.dtype], _ptr(dev_err), _stream(stream)),
+        "pkv_paged_attention_decode_noalloc")
 
 
 def new_workspace(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
