@@ -177,15 +177,17 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pa
  *                  the caller (it sizes the grid; the host never reads the
  *                  device array); must be <= max_blocks_per_seq * block_size
  *   workspace      device scratch of at least pkv_decode_workspace_bytes()
- *                  bytes (may be NULL when that is 0). Its first region holds
- *                  int32 counters that MUST be zero before the first call; every
- *                  call that ends with *dev_err == 0 leaves them zero again. After
- *                  a call that reports a device error, zero the workspace again.
- *                  Two calls that share a workspace must not overlap on the GPU.
+ *                  bytes (required whenever num_seqs > 0). Its first region
+ *                  holds int32 counters that MUST be zero before the first call;
+ *                  every call that ends with *dev_err == 0 leaves them zero
+ *                  again. After a call that reports a device error, zero the
+ *                  workspace again. Two calls that share a workspace must not
+ *                  overlap on the GPU.
  *
- * Long contexts are cut into partitions of pkv_decode_partition_tokens()
- * tokens processed by separate thread blocks; their partial softmax states
- * are combined by a log-sum-exp merge inside the same kernel launch.
+ * Work split: the (sequence, head group) pairs are laid end to end as one
+ * sequence of 16-token tiles and every warp of a device-sized, resident grid
+ * takes an equal contiguous range of it. Pairs cut by range boundaries are
+ * finished by a log-sum-exp merge of their pieces inside the same launch.
  *
  * Errors: host — INVALID_ARG (NULL/misaligned pointers, num_heads not a
  * multiple of num_kv_heads, max_context_len > max_blocks_per_seq*block_size,
@@ -226,12 +228,13 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
  *    loads the library, for the life of the process.
  *  - Sizes whose pkv_decode_workspace_bytes() exceeds that limit are rejected
  *    with PKV_ERR_WORKSPACE before anything is enqueued (the LLaMA-13B-shaped
- *    step, 128 sequences x 40 heads x 2048 tokens, needs 21 MB).
+ *    step, 128 sequences x 40 heads, needs 16.5 MB; the limit is reached near
+ *    four million sequence x head pairs).
  *  - The first call on a device looks up the array's device address once for
  *    that device (with that device current); make that first call before any
  *    stream capture begins.
  *  - Every call on a device shares the same array and leaves its last
- *    contents in it. Each call first clears the partition counters it needs
+ *    contents in it. Each call first clears the segment counters it needs
  *    (an asynchronous memset on `stream`; this happens even when the call
  *    then fails its host-side checks, and touches only the library's own
  *    array). Two calls whose work overlaps on the GPU — different streams, or
@@ -248,14 +251,11 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, const void* q, const vo
                                               int max_context_len, pkv_dtype dtype, int32_t* dev_err,
                                               pkv_stream_t stream);
 
-/* Tokens per context partition used by pkv_paged_attention_decode for these
- * sizes (a multiple of 16 and of every supported block_size). Pure host
- * function. */
-int pkv_decode_partition_tokens(int num_seqs, int num_heads, int max_context_len);
-
-/* Bytes of workspace pkv_paged_attention_decode needs for these sizes; 0 when
- * no sequence can span more than one partition. Pure host function; returns 0
- * for non-positive sizes. */
+/* Bytes of workspace pkv_paged_attention_decode needs for these sizes: the
+ * segment counters (num_seqs * num_heads int32) plus a fixed area for the
+ * partial results of the split segments (independent of the context lengths;
+ * about 16.3 MB for head_dim 128). Pure host function; returns 0 for
+ * non-positive sizes. */
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len);
 
 #ifdef __cplusplus

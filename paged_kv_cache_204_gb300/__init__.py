@@ -11,7 +11,6 @@ Functions mirror the C entry points:
   copy_blocks             -> pkv_copy_blocks
   paged_attention_decode  -> pkv_paged_attention_decode
   decode_workspace_bytes  -> pkv_decode_workspace_bytes
-  decode_partition_tokens -> pkv_decode_partition_tokens
   set_wait_timeout_ns / get_wait_timeout_ns, status_string, version
 """
 from __future__ import annotations
@@ -45,8 +44,6 @@ lib.pkv_set_wait_timeout_ns.argtypes = [_U64]
 lib.pkv_set_wait_timeout_ns.restype = None
 lib.pkv_get_wait_timeout_ns.argtypes = []
 lib.pkv_get_wait_timeout_ns.restype = _U64
-lib.pkv_decode_partition_tokens.argtypes = [_I, _I, _I]
-lib.pkv_decode_partition_tokens.restype = _I
 lib.pkv_decode_workspace_bytes.argtypes = [_I, _I, _I, _I]
 lib.pkv_decode_workspace_bytes.restype = _SZ
 lib.pkv_reshape_and_cache.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]
@@ -82,10 +79,6 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 def get_wait_timeout_ns() -> int:
     return lib.pkv_get_wait_timeout_ns()
-
-
-def decode_partition_tokens(num_seqs: int, num_heads: int, max_context_len: int) -> int:
-    return lib.pkv_decode_partition_tokens(num_seqs, num_heads, max_context_len)
 
 
 def decode_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int) -> int:

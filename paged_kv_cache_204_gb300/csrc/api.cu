@@ -12,8 +12,6 @@ namespace {
 
 std::atomic<uint64_t> g_wait_limit_ns{1000000000ull};
 
-constexpr int kPartitionTokens = 256;  // multiple of 16 and of every block size
-
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 bool supported_head_dim(int d) { return d == 64 || d == 128; }
 bool supported_block_size(int b) { return b == 8 || b == 16 || b == 32; }
@@ -22,21 +20,19 @@ int elem_bytes(int t) { return t == PKV_F32 ? 4 : 2; }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WorkspaceLayout {
-  int splits = 1;
   size_t counter_off = 0, ml_off = 0, o_off = 0, total = 0;
 };
 
-WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int max_context_len) {
+// Counters of the (sequence, head group) segments, then the partial slots of
+// the persistent warps (two per warp, up to kMaxGroupPerWarp heads each).
+WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim) {
   WorkspaceLayout w;
-  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || max_context_len <= 0) return w;
-  const int P = pkv_decode_partition_tokens(num_seqs, num_heads, max_context_len);
-  w.splits = (max_context_len + P - 1) / P;
-  if (w.splits <= 1) return w;
-  const size_t rows = (size_t)num_seqs * num_heads;
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0) return w;
+  const size_t slots = (size_t)pkv::kMaxDecodeWarps * 2 * pkv::kMaxGroupPerWarp;
   w.counter_off = 0;
-  w.ml_off = align_up(rows * sizeof(int32_t), 256);
-  w.o_off = w.ml_off + align_up(rows * w.splits * sizeof(float2), 256);
-  w.total = w.o_off + rows * w.splits * head_dim * sizeof(float);
+  w.ml_off = align_up((size_t)num_seqs * num_heads * sizeof(int32_t), 256);
+  w.o_off = w.ml_off + align_up(slots * sizeof(float2), 256);
+  w.total = w.o_off + slots * head_dim * sizeof(float);
   return w;
 }
 
@@ -62,15 +58,9 @@ int pkv_version(void) { return 100; }
 void pkv_set_wait_timeout_ns(uint64_t ns) { g_wait_limit_ns.store(ns, std::memory_order_relaxed); }
 uint64_t pkv_get_wait_timeout_ns(void) { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 
-int pkv_decode_partition_tokens(int num_seqs, int num_heads, int max_context_len) {
-  (void)num_seqs;
-  (void)num_heads;
-  (void)max_context_len;
-  return kPartitionTokens;
-}
-
 size_t pkv_decode_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len) {
-  return workspace_layout(num_seqs, num_heads, head_dim, max_context_len).total;
+  if (max_context_len < 0) return 0;
+  return workspace_layout(num_seqs, num_heads, head_dim).total;
 }
 
 pkv_status pkv_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
@@ -130,14 +120,9 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
       !aligned(block_tables, 4) || !aligned(context_lens, 4) || (dev_err && !aligned(dev_err, 4)))
     return PKV_ERR_INVALID_ARG;
 
-  const WorkspaceLayout ws = workspace_layout(num_seqs, num_heads, head_dim, max_context_len);
-  if (ws.splits > 65535) return PKV_ERR_UNSUPPORTED;
-  if (ws.total > 0) {
-    if (!workspace || workspace_bytes < ws.total) return PKV_ERR_WORKSPACE;
-    if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
-  }
-  const int P = pkv_decode_partition_tokens(num_seqs, num_heads, max_context_len);
-  if (P / block_size > pkv::kMaxSplitBlocks) return PKV_ERR_UNSUPPORTED;
+  const WorkspaceLayout ws = workspace_layout(num_seqs, num_heads, head_dim);
+  if (!workspace || workspace_bytes < ws.total) return PKV_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
 
   const int group = num_heads / num_kv_heads;
   const int gpw = group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1);
@@ -155,25 +140,22 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
   p.block_tables = block_tables;
   p.context_lens = context_lens;
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+  p.num_seqs = num_seqs;
   p.num_heads = num_heads;
   p.num_kv_heads = num_kv_heads;
   p.group = group;
-  p.head_subgroups = group / gpw;
+  p.head_groups = num_heads / gpw;
   p.block_size = block_size;
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.num_blocks = num_blocks;
   p.max_context_len = max_context_len;
-  p.partition_tokens = P;
-  p.max_splits = ws.splits;
   char* wsb = static_cast<char*>(workspace);
-  p.ws_counter = ws.total ? reinterpret_cast<int32_t*>(wsb + ws.counter_off) : nullptr;
-  p.ws_ml = ws.total ? reinterpret_cast<float2*>(wsb + ws.ml_off) : nullptr;
-  p.ws_o = ws.total ? reinterpret_cast<float*>(wsb + ws.o_off) : nullptr;
+  p.ws_counter = reinterpret_cast<int32_t*>(wsb + ws.counter_off);
+  p.ws_ml = reinterpret_cast<float2*>(wsb + ws.ml_off);
+  p.ws_o = reinterpret_cast<float*>(wsb + ws.o_off);
   p.dev_err = dev_err;
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
-
-  const dim3 grid(num_heads / gpw, num_seqs, ws.splits);
-  return launch_status(launch(p, grid, reinterpret_cast<cudaStream_t>(stream)));
+  return launch_status(launch(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -106,6 +106,9 @@ struct Chunk<float> {
     f[2] = __uint_as_float(u.z);
     f[3] = __uint_as_float(u.w);
   }
+  __device__ __forceinline__ static uint4 narrow(const float (&f)[4]) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
 };
 
 template <>
@@ -122,6 +125,15 @@ struct Chunk<__half> {
       f[2 * i + 1] = t.y;
     }
   }
+  __device__ __forceinline__ static uint4 narrow(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+      memcpy(&w[i], &h, 4);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
 };
 
 template <>
@@ -135,6 +147,15 @@ struct Chunk<__nv_bfloat16> {
       f[2 * i] = __uint_as_float(w[i] << 16);
       f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
+  }
+  __device__ __forceinline__ static uint4 narrow(const float (&f)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      memcpy(&w[i], &h, 4);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
   }
 };
 

@@ -5,31 +5,34 @@
 // attends over its context, whose K/V rows sit in fixed-size blocks scattered
 // through a pool and are found through the sequence's block table.
 //
-// Work decomposition
-//   grid.x  kv head x query-head subgroup (GPW query heads share one kv head)
-//   grid.y  sequence
-//   grid.z  context partition of P tokens (split-context decode); CUDA hands
-//           out all partition-0 blocks first, so the last wave holds short
-//           partitions only.
-//   block   4 warps. A partition is cut into 16-token tiles; warp w takes
-//           tiles w, w+4, ... and runs its own pipeline of STAGES shared-memory
-//           slots. Lane 0 of the warp issues 1-D bulk copies (cp.async.bulk,
-//           completion counted in bytes on an mbarrier) of the tile's K rows
-//           and V rows; all lanes wait on the slot's mbarrier (bounded), then
-//           compute. No block-wide barrier inside the loop.
+// Work decomposition (persistent, balanced by construction)
+//   Every (sequence s, head group hg) pair is a "segment" of nt_s tiles of 16
+//   tokens (an empty context still has one, empty, tile so that its zero
+//   output gets written). Segments are laid end to end, sequence-major, into
+//   one global sequence of T tiles. The grid is sized to the GPU (blocks that
+//   stay resident); its W warps each take one contiguous range of about T/W
+//   tiles, so every warp streams the same number of bytes.
+//   A warp walks its range tile by tile across segment boundaries. Lane 0
+//   issues 1-D bulk copies (cp.async.bulk, completion counted in bytes on an
+//   mbarrier) of the next tiles' K rows and V rows (plus the segment's query
+//   rows at the first tile of a segment) into the warp's own ring of
+//   shared-memory slots, while all lanes compute on the current tile. There
+//   is no block-wide barrier after the start-up scan.
+//   A segment that lies entirely inside one warp's range is finished by that
+//   warp, which writes the output. A segment cut by range boundaries (at most
+//   two per warp: its first and its last) gets one partial (m, l, o/l) per
+//   piece in the workspace; the last piece to finish (atomic counter) merges
+//   them with the log-sum-exp rule, writes the output and re-zeroes the
+//   counter.
 //
 // Per tile and warp: lanes form 4 groups of 8; group g holds tokens g, g+4,
 // g+8, g+12 of the tile and lane i of a group owns 16-byte chunks i, i+8, ...
 // of every row (a quarter-warp reads 128 contiguous bytes of one row: no
 // shared-memory bank conflicts). q.k partial sums are reduced over the 8
 // lanes of a group with shuffles; the running max m, exp-sum l and output o
-// are updated with the online softmax in base 2 (q is pre-scaled by
-// scale * log2(e)); tokens past the context are masked by select, never by
-// multiplication, so poisoned rows never reach the result.
-//
-// Partitions of one (sequence, head group) write (m, l, o/l) to the workspace;
-// the last thread block to finish (atomic counter) merges them with the
-// log-sum-exp rule and writes the output, then re-zeroes its counter.
+// follow the online softmax in base 2 (q is pre-scaled by scale * log2(e));
+// tokens past the context are masked by select, never by multiplication, so
+// poisoned rows never reach the result.
 #pragma once
 
 #include "common.cuh"
@@ -44,366 +47,496 @@ struct DecodeParams {
   const int32_t* block_tables;
   const int32_t* context_lens;
   float scale_log2;  // scale * log2(e)
+  int num_seqs;
   int num_heads;
   int num_kv_heads;
-  int group;           // num_heads / num_kv_heads
-  int head_subgroups;  // group / GPW
+  int group;        // num_heads / num_kv_heads
+  int head_groups;  // num_heads / GPW
   int block_size;
   int max_blocks_per_seq;
   int num_blocks;
   int max_context_len;
-  int partition_tokens;  // P
-  int max_splits;        // S = ceil(max_context_len / P)
-  int32_t* ws_counter;   // [num_seqs * num_heads / GPW]
-  float2* ws_ml;         // [num_seqs][num_heads][S]  (m, l)
-  float* ws_o;           // [num_seqs][num_heads][S][head_dim]
+  int32_t* ws_counter;  // [num_seqs * head_groups]
+  float2* ws_ml;        // [kMaxDecodeWarps][2][GPW]  (m, l)
+  float* ws_o;          // [kMaxDecodeWarps][2][GPW][head_dim]
   int32_t* dev_err;
   uint64_t wait_limit_ns;
 };
 
 constexpr int kTileTokens = 16;
-constexpr int kDecodeWarps = 4;
-constexpr int kMaxSplitBlocks = 64;  // block-table entries of one partition (P / min block_size)
+constexpr int kDecodeWarps = 8;  // one resident block of 8 warps per SM (measured best)
+constexpr int kMaxDecodeWarps = 4096;  // bound of the persistent grid (partial slots in the workspace)
+constexpr int kMaxGroupPerWarp = 4;    // query heads one warp serves against one kv head
+constexpr int kBtChunk = 128;          // block-table entries a warp keeps in shared memory
 
-template <typename T, int D>
+template <typename T, int D, int GPW>
 struct DecodeShape {
   static constexpr int kElemBytes = sizeof(T);
   static constexpr int kRowBytes = D * kElemBytes;
-  static constexpr int kTileBytes = kTileTokens * kRowBytes;  // K (or V) rows of one tile
-  static constexpr int kStageBytes = 2 * kTileBytes;          // K and V
-  static constexpr int kRingBudget = 64 * 1024;
-  static constexpr int kStagesRaw = kRingBudget / (kDecodeWarps * kStageBytes);
+  static constexpr int kTileBytes = kTileTokens * kRowBytes;             // K (or V) rows of one tile
+  static constexpr int kStageBytes = 2 * kTileBytes + GPW * kRowBytes;   // K, V, query rows
+  static constexpr int kRingBudget = 128 * 1024;
+  static constexpr int kStagesRaw = kRingBudget / (kDecodeWarps * 2 * kTileBytes);
   static constexpr int kStages = kStagesRaw < 1 ? 1 : (kStagesRaw > 4 ? 4 : kStagesRaw);
   static constexpr int kChunksPerRow = kRowBytes / 16;
   static constexpr int kChunksPerLane = kChunksPerRow / 8;
   static constexpr int kVec = Chunk<T>::kElems;
   static constexpr int kDimsPerLane = kChunksPerLane * kVec;  // = D / 8
   static constexpr int kRingBytes = kDecodeWarps * kStages * kStageBytes;
-  static constexpr int kSmemBytes =
-      kRingBytes + kDecodeWarps * kStages * 8 + kMaxSplitBlocks * 4 + 16;
+  static constexpr int kBarOff = kRingBytes;
+  static constexpr int kBtOff = kBarOff + kDecodeWarps * kStages * 8;
+  static constexpr int kScanOff = kBtOff + kDecodeWarps * kBtChunk * 4;
+  static constexpr int kStartOff = kScanOff + kDecodeWarps * 8;
+  static constexpr int kSmemBytes = kStartOff + kDecodeWarps * 16;
   static_assert(kChunksPerRow % 8 == 0, "row must split into 8 lanes of 16-byte chunks");
   static_assert(kDimsPerLane * 8 == D, "lane mapping");
+  static_assert(kStageBytes % 16 == 0 && kRowBytes % 16 == 0, "bulk copy alignment");
 };
+
+__device__ __forceinline__ int tiles_of(int L) { return L > 0 ? (L + kTileTokens - 1) / kTileTokens : 1; }
+
+// Context length of sequence s, clamped into [0, cap] (out-of-range lengths
+// are reported once, by block 0).
+__device__ __forceinline__ int load_len(const DecodeParams& p, int s, int cap) {
+  int L = __ldg(p.context_lens + s);
+  if (L < 0 || L > cap) {
+    if (blockIdx.x == 0) set_err(p.dev_err, PKV_DEV_ERR_CONTEXT_LEN);
+    L = L < 0 ? 0 : cap;
+  }
+  return L;
+}
+
+// Exclusive scan of one value per thread over the block; `total` gets the sum.
+__device__ __forceinline__ long long block_exclusive_scan(long long v, long long* scratch, long long& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long y = __shfl_up_sync(kFullMask, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  long long before = 0;
+  total = 0;
+#pragma unroll
+  for (int i = 0; i < kDecodeWarps; ++i) {
+    const long long t = scratch[i];
+    if (i < warp) before += t;
+    total += t;
+  }
+  __syncthreads();
+  return before + x - v;
+}
+
+// Position in the global tile sequence.
+struct TileCursor {
+  long long g;  // global tile index
+  int s, hg, t, nt, L;
+};
+
+__device__ __forceinline__ void cursor_next(TileCursor& c, const DecodeParams& p, int cap) {
+  ++c.g;
+  if (++c.t < c.nt) return;
+  c.t = 0;
+  if (++c.hg < p.head_groups) return;
+  c.hg = 0;
+  if (++c.s < p.num_seqs) {
+    c.L = load_len(p, c.s, cap);
+    c.nt = tiles_of(c.L);
+  }
+}
 
 template <typename T, int D, int GPW>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     pa_decode_kernel(const DecodeParams p) {
-  using S = DecodeShape<T, D>;
+  using S = DecodeShape<T, D, GPW>;
   constexpr int NW = kDecodeWarps;
   constexpr int ST = S::kStages;
   constexpr int DPL = S::kDimsPerLane;
   constexpr int CPL = S::kChunksPerLane;
   constexpr int VEC = S::kVec;
+  constexpr int ROW = S::kRowBytes;
 
   extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* ring = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kRingBytes);
-  int32_t* s_bt = reinterpret_cast<int32_t*>(bars + NW * ST);
-  int32_t* s_last = s_bt + kMaxSplitBlocks;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+  long long* scan = reinterpret_cast<long long*>(smem + S::kScanOff);
+  longlong2* starts = reinterpret_cast<longlong2*>(smem + S::kStartOff);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int grp = lane >> 3;  // token sub-index within a 4-row step
   const int sub = lane & 7;   // chunk index within a row
-  const int seq = blockIdx.y;
-  const int split = blockIdx.z;
-  const int kvh = blockIdx.x / p.head_subgroups;
-  const int h0 = kvh * p.group + (blockIdx.x % p.head_subgroups) * GPW;
   const int bs = p.block_size;
+  const int cap = min(p.max_context_len, p.max_blocks_per_seq * bs);
+  const int HG = p.head_groups;
 
-  // ---- context range of this partition ---------------------------------
-  int L = __ldg(p.context_lens + seq);
-  const int L_cap = min(p.max_context_len, p.max_blocks_per_seq * bs);
-  if (L < 0 || L > L_cap) {
-    if (threadIdx.x == 0 && split == 0) set_err(p.dev_err, PKV_DEV_ERR_CONTEXT_LEN);
-    L = L < 0 ? 0 : L_cap;
-  }
-  const int P = p.partition_tokens;
-  const int nsplit = L > 0 ? (L + P - 1) / P : 1;
-  if (split >= nsplit) return;  // uniform over the block, before any barrier
-  const int t_begin = split * P;
-  const int t_end = min(L, t_begin + P);
-  const int ntiles = (t_end - t_begin + kTileTokens - 1) / kTileTokens;  // 0 iff L == 0
-  const int blk0 = t_begin / bs;
-  const int nblk = L > 0 ? (t_end + bs - 1) / bs - blk0 : 0;
-
-  // ---- stage the partition's block-table entries in shared memory ------
-  const int32_t* bt_row = p.block_tables + (size_t)seq * p.max_blocks_per_seq;
-  for (int i = threadIdx.x; i < nblk; i += NW * 32) {
-    int id = __ldg(bt_row + blk0 + i);
-    if (id < 0 || id >= p.num_blocks) {
-      set_err(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
-      id = 0;
-    }
-    s_bt[i] = id;
-  }
-  if (lane == 0) {
+  // ---- start-up: total tiles T, then each warp's first (sequence, offset) --
+  long long mine = 0;
+  for (int s = threadIdx.x; s < p.num_seqs; s += NW * 32) mine += tiles_of(load_len(p, s, cap));
+  long long Ttot;
+  block_exclusive_scan(mine, scan, Ttot);
+  Ttot *= HG;
+  const long long W = (long long)gridDim.x * NW;
+  const long long Weff = W < Ttot ? W : Ttot;  // every active warp gets >= 1 tile
+  const long long wid = (long long)blockIdx.x * NW + warp;
+  const long long a_begin = wid < Weff ? wid * Ttot / Weff : Ttot;
+  const long long a_end = wid < Weff ? (wid + 1) * Ttot / Weff : Ttot;
+  if (threadIdx.x < NW) starts[threadIdx.x] = make_longlong2(-1, 0);
+  __syncthreads();
+  long long carry = 0;
+  for (int base = 0; base < p.num_seqs; base += NW * 32) {
+    const int s = base + threadIdx.x;
+    const long long cnt = s < p.num_seqs ? (long long)tiles_of(load_len(p, s, cap)) * HG : 0;
+    long long chunk_total;
+    const long long excl = carry + block_exclusive_scan(cnt, scan, chunk_total);
 #pragma unroll
-    for (int s = 0; s < ST; ++s) mbar_init(&bars[warp * ST + s], 1);
-    mbar_init_fence();
+    for (int i = 0; i < NW; ++i) {
+      const long long w = (long long)blockIdx.x * NW + i;
+      if (w < Weff) {
+        const long long a = w * Ttot / Weff;
+        if (cnt > 0 && a >= excl && a < excl + cnt) starts[i] = make_longlong2(s, a - excl);
+      }
+    }
+    carry += chunk_total;
   }
   __syncthreads();
+  if (a_begin >= a_end) return;  // idle warp (more warps than tiles); no block barrier follows
 
-  const int my_tiles = ntiles > warp ? (ntiles - warp + NW - 1) / NW : 0;
-  unsigned char* my_ring = ring + warp * ST * S::kStageBytes;
+  // ---- per-warp pipeline ------------------------------------------------
+  unsigned char* my_ring = smem + warp * ST * S::kStageBytes;
   uint64_t* my_bars = bars + warp * ST;
+  int32_t* my_bt = reinterpret_cast<int32_t*>(smem + S::kBtOff) + warp * kBtChunk;
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < ST; ++i) mbar_init(&my_bars[i], 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+
+  TileCursor ci;  // issue cursor
+  {
+    const longlong2 st0 = starts[warp];
+    ci.s = static_cast<int>(st0.x);
+    ci.L = load_len(p, ci.s, cap);
+    ci.nt = tiles_of(ci.L);
+    ci.hg = static_cast<int>(st0.y / ci.nt);
+    ci.t = static_cast<int>(st0.y % ci.nt);
+    ci.g = a_begin;
+  }
+  TileCursor cc = ci;  // consume cursor
+  int bt_s = -1, bt_j0 = 0;
+
   const char* kbase = static_cast<const char*>(p.k_cache);
   const char* vbase = static_cast<const char*>(p.v_cache);
+  const char* qbase = static_cast<const char*>(p.q);
   const int seg = bs < kTileTokens ? bs : kTileTokens;  // rows per bulk copy
   const int nseg = kTileTokens / seg;
 
-  // Lane 0: copy the K rows and V rows of the warp's kt-th tile into slot kt % ST.
-  auto issue = [&](int kt) {
-    if (kt >= my_tiles) return;
-    const int t0 = t_begin + (warp + kt * NW) * kTileTokens;
-    unsigned char* kdst = my_ring + (kt % ST) * S::kStageBytes;
-    unsigned char* vdst = kdst + S::kTileBytes;
-    uint64_t* bar = my_bars + (kt % ST);
-    uint32_t bytes = 0;
-    for (int c = 0; c < nseg; ++c)
-      if (t0 + c * seg < t_end) bytes += 2u * seg * S::kRowBytes;
-    mbar_arrive_expect_tx(bar, bytes);
-    for (int c = 0; c < nseg; ++c) {
-      const int t = t0 + c * seg;
-      if (t >= t_end) break;
-      const size_t off =
-          (((size_t)s_bt[t / bs - blk0] * p.num_kv_heads + kvh) * bs + (t % bs)) * S::kRowBytes;
-      bulk_copy_g2s(kdst + c * seg * S::kRowBytes, kbase + off, seg * S::kRowBytes, bar);
-      bulk_copy_g2s(vdst + c * seg * S::kRowBytes, vbase + off, seg * S::kRowBytes, bar);
+  // Issue the copies of the tile under `c` into slot n % ST (warp-uniform call).
+  auto issue = [&](const TileCursor& c, int n) {
+    const int t0 = c.t * kTileTokens;
+    const int nvalid = min(max(c.L - t0, 0), kTileTokens);
+    const bool with_q = (c.t == 0 || c.g == a_begin) && nvalid > 0;
+    if (nvalid > 0) {
+      const int j_first = t0 / bs;
+      const int j_last = (t0 + nvalid - 1) / bs;
+      if (c.s != bt_s || j_first < bt_j0 || j_last >= bt_j0 + kBtChunk) {
+        // stage block-table entries [j_first, j_first + kBtChunk) of row c.s
+        const int nblk = (c.L + bs - 1) / bs;
+        const int32_t* row = p.block_tables + (size_t)c.s * p.max_blocks_per_seq;
+        __syncwarp();
+        for (int i = lane; i < kBtChunk; i += 32) {
+          const int j = j_first + i;
+          int id = 0;
+          if (j < nblk) {
+            id = __ldg(row + j);
+            if (id < 0 || id >= p.num_blocks) {
+              set_err(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
+              id = 0;
+            }
+          }
+          my_bt[i] = id;
+        }
+        __syncwarp();
+        bt_s = c.s;
+        bt_j0 = j_first;
+      }
+    }
+    if (lane == 0) {
+      unsigned char* kdst = my_ring + (n % ST) * S::kStageBytes;
+      unsigned char* vdst = kdst + S::kTileBytes;
+      uint64_t* bar = my_bars + (n % ST);
+      uint32_t bytes = with_q ? GPW * ROW : 0;
+      for (int c2 = 0; c2 < nseg; ++c2)
+        if (t0 + c2 * seg < c.L) bytes += 2u * seg * ROW;
+      mbar_arrive_expect_tx(bar, bytes);
+      const int kvh = (c.hg * GPW) / p.group;
+      for (int c2 = 0; c2 < nseg; ++c2) {
+        const int t = t0 + c2 * seg;
+        if (t >= c.L) break;
+        const size_t off =
+            (((size_t)my_bt[t / bs - bt_j0] * p.num_kv_heads + kvh) * bs + (t % bs)) * ROW;
+        bulk_copy_g2s(kdst + c2 * seg * ROW, kbase + off, seg * ROW, bar);
+        bulk_copy_g2s(vdst + c2 * seg * ROW, vbase + off, seg * ROW, bar);
+      }
+      if (with_q)
+        bulk_copy_g2s(kdst + 2 * S::kTileBytes,
+                      qbase + ((size_t)c.s * p.num_heads + (size_t)c.hg * GPW) * ROW, GPW * ROW, bar);
     }
   };
-  if (lane == 0)
-    for (int kt = 0; kt < ST; ++kt) issue(kt);
 
-  // ---- query rows (fp32, pre-scaled into the base-2 exponent domain) ------
+  int issued = 0;
+  for (; issued < ST && ci.g < a_end; ++issued) {
+    issue(ci, issued);
+    cursor_next(ci, p, cap);
+  }
+
   float qf[GPW][DPL];
-#pragma unroll
-  for (int g = 0; g < GPW; ++g) {
-    const uint4* qrow = reinterpret_cast<const uint4*>(
-        static_cast<const char*>(p.q) + ((size_t)seq * p.num_heads + h0 + g) * S::kRowBytes);
-#pragma unroll
-    for (int k = 0; k < CPL; ++k) {
-      float f[VEC];
-      Chunk<T>::widen(__ldg(qrow + sub + 8 * k), f);
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) qf[g][k * VEC + e] = f[e] * p.scale_log2;
-    }
-  }
-
   float m[GPW], l[GPW], o[GPW][DPL];
-#pragma unroll
-  for (int g = 0; g < GPW; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) o[g][e] = 0.f;
-  }
+  bool visit_from_start = true;
+  const size_t H = p.num_heads;
 
-  // ---- main loop over this warp's tiles -------------------------------
-  bool ok = true;
-  int kt = 0;
-  for (; kt < my_tiles; ++kt) {
-    const bool arrived = mbar_wait_bounded(my_bars + (kt % ST), (kt / ST) & 1, p.wait_limit_ns);
-    if (!__all_sync(kFullMask, arrived)) {
-      ok = false;
-      break;
+  for (int n = 0; cc.g < a_end; ++n) {
+    if (!__all_sync(kFullMask, mbar_wait_bounded(my_bars + (n % ST), (n / ST) & 1, p.wait_limit_ns))) {
+      // A wait ran out: report it, let this warp's copies in flight land
+      // (bounded), and stop. Outputs of this call are not valid.
+      if (lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+      for (int k2 = n; k2 < issued; ++k2) mbar_wait_bounded(my_bars + (k2 % ST), (k2 / ST) & 1, kDrainLimitNs);
+      return;
     }
-    const unsigned char* ks = my_ring + (kt % ST) * S::kStageBytes;
+    const unsigned char* ks = my_ring + (n % ST) * S::kStageBytes;
     const unsigned char* vs = ks + S::kTileBytes;
-    const int t0 = t_begin + (warp + kt * NW) * kTileTokens;
-    const int nvalid = min(kTileTokens, t_end - t0);
+    const int t0 = cc.t * kTileTokens;
+    const int nvalid = min(max(cc.L - t0, 0), kTileTokens);
+    const bool first = cc.t == 0 || cc.g == a_begin;
+    const bool last = cc.t == cc.nt - 1 || cc.g == a_end - 1;
 
-    // logits of rows grp, grp+4, grp+8, grp+12
-    float x[GPW][4];
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int r = it * 4 + grp;
-      const uint4* krow = reinterpret_cast<const uint4*>(ks + r * S::kRowBytes);
-      float acc[GPW];
-#pragma unroll
-      for (int g = 0; g < GPW; ++g) acc[g] = 0.f;
-#pragma unroll
-      for (int k = 0; k < CPL; ++k) {
-        float f[VEC];
-        Chunk<T>::widen(krow[sub + 8 * k], f);
-#pragma unroll
-        for (int g = 0; g < GPW; ++g)
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) acc[g] = fmaf(qf[g][k * VEC + e], f[e], acc[g]);
-      }
+    if (first) {
+      visit_from_start = cc.t == 0;
 #pragma unroll
       for (int g = 0; g < GPW; ++g) {
-        float a = acc[g];
-        a += __shfl_xor_sync(kFullMask, a, 1);
-        a += __shfl_xor_sync(kFullMask, a, 2);
-        a += __shfl_xor_sync(kFullMask, a, 4);
-        x[g][it] = r < nvalid ? a : -INFINITY;
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[g][e] = 0.f;
+      }
+      if (nvalid > 0) {
+        const unsigned char* qs = ks + 2 * S::kTileBytes;
+#pragma unroll
+        for (int g = 0; g < GPW; ++g) {
+          const uint4* qrow = reinterpret_cast<const uint4*>(qs + g * ROW);
+#pragma unroll
+          for (int k = 0; k < CPL; ++k) {
+            float f[VEC];
+            Chunk<T>::widen(qrow[sub + 8 * k], f);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) qf[g][k * VEC + e] = f[e] * p.scale_log2;
+          }
+        }
       }
     }
 
-    // online softmax update (base 2)
-    float pw[GPW][4];
-#pragma unroll
-    for (int g = 0; g < GPW; ++g) {
-      float mt = fmaxf(fmaxf(x[g][0], x[g][1]), fmaxf(x[g][2], x[g][3]));
-      mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
-      mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
-      const float mn = fmaxf(m[g], mt);
-      const float alpha = exp2f(m[g] - mn);  // 0 on the first tile (m = -inf)
-      float ps = 0.f;
+    if (nvalid > 0) {
+      // logits of rows grp, grp+4, grp+8, grp+12
+      float x[GPW][4];
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
-        pw[g][it] = exp2f(x[g][it] - mn);
-        ps += pw[g][it];
-      }
-      l[g] = l[g] * alpha + ps;
+        const int r = it * 4 + grp;
+        const uint4* krow = reinterpret_cast<const uint4*>(ks + r * ROW);
+        float acc[GPW];
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) o[g][e] *= alpha;
-      m[g] = mn;
-    }
-
-    // o += p . V over the valid rows (masked rows may hold poison: skip them)
-#pragma unroll
-    for (int it = 0; it < 4; ++it) {
-      const int r = it * 4 + grp;
-      if (r < nvalid) {
-        const uint4* vrow = reinterpret_cast<const uint4*>(vs + r * S::kRowBytes);
+        for (int g = 0; g < GPW; ++g) acc[g] = 0.f;
 #pragma unroll
         for (int k = 0; k < CPL; ++k) {
           float f[VEC];
-          Chunk<T>::widen(vrow[sub + 8 * k], f);
+          Chunk<T>::widen(krow[sub + 8 * k], f);
 #pragma unroll
           for (int g = 0; g < GPW; ++g)
 #pragma unroll
-            for (int e = 0; e < VEC; ++e) o[g][k * VEC + e] = fmaf(pw[g][it], f[e], o[g][k * VEC + e]);
+            for (int e = 0; e < VEC; ++e) acc[g] = fmaf(qf[g][k * VEC + e], f[e], acc[g]);
+        }
+#pragma unroll
+        for (int g = 0; g < GPW; ++g) {
+          float a = acc[g];
+          a += __shfl_xor_sync(kFullMask, a, 1);
+          a += __shfl_xor_sync(kFullMask, a, 2);
+          a += __shfl_xor_sync(kFullMask, a, 4);
+          x[g][it] = r < nvalid ? a : -INFINITY;
+        }
+      }
+      // online softmax update (base 2)
+      float pw[GPW][4];
+#pragma unroll
+      for (int g = 0; g < GPW; ++g) {
+        float mt = fmaxf(fmaxf(x[g][0], x[g][1]), fmaxf(x[g][2], x[g][3]));
+        mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
+        mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
+        const float mn = fmaxf(m[g], mt);
+        const float alpha = exp2f(m[g] - mn);  // 0 on the first tile (m = -inf)
+        float ps = 0.f;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+          pw[g][it] = exp2f(x[g][it] - mn);
+          ps += pw[g][it];
+        }
+        l[g] = l[g] * alpha + ps;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[g][e] *= alpha;
+        m[g] = mn;
+      }
+      // o += p . V over the valid rows (masked rows may hold poison: skip them)
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int r = it * 4 + grp;
+        if (r < nvalid) {
+          const uint4* vrow = reinterpret_cast<const uint4*>(vs + r * ROW);
+#pragma unroll
+          for (int k = 0; k < CPL; ++k) {
+            float f[VEC];
+            Chunk<T>::widen(vrow[sub + 8 * k], f);
+#pragma unroll
+            for (int g = 0; g < GPW; ++g)
+#pragma unroll
+              for (int e = 0; e < VEC; ++e) o[g][k * VEC + e] = fmaf(pw[g][it], f[e], o[g][k * VEC + e]);
+          }
         }
       }
     }
     __syncwarp();  // every lane is done with this slot before it is refilled
-    if (lane == 0) issue(kt + ST);
-  }
+    if (ci.g < a_end) {
+      issue(ci, issued++);
+      cursor_next(ci, p, cap);
+    }
 
-  if (!ok) {
-    // A wait ran out: report it, then let this warp's copies in flight land
-    // (bounded) before the shared memory they target is reused or released.
-    if (lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-    const int issued_end = min(my_tiles, kt + ST);
-    for (int k2 = kt; k2 < issued_end; ++k2)
-      mbar_wait_bounded(my_bars + (k2 % ST), (k2 / ST) & 1, kDrainLimitNs);
-  }
-
-  // ---- combine the 4 row groups of the warp -----------------------------
+    if (last) {
+      // ---- end of this warp's visit of segment (cc.s, cc.hg) -----------
 #pragma unroll
-  for (int g = 0; g < GPW; ++g) {
-    l[g] += __shfl_xor_sync(kFullMask, l[g], 8);
-    l[g] += __shfl_xor_sync(kFullMask, l[g], 16);
+      for (int g = 0; g < GPW; ++g) {
+        l[g] += __shfl_xor_sync(kFullMask, l[g], 8);
+        l[g] += __shfl_xor_sync(kFullMask, l[g], 16);
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-      o[g][e] += __shfl_xor_sync(kFullMask, o[g][e], 8);
-      o[g][e] += __shfl_xor_sync(kFullMask, o[g][e], 16);
+        for (int e = 0; e < DPL; ++e) {
+          o[g][e] += __shfl_xor_sync(kFullMask, o[g][e], 8);
+          o[g][e] += __shfl_xor_sync(kFullMask, o[g][e], 16);
+        }
+      }
+      const size_t row0 = (size_t)cc.s * H + (size_t)cc.hg * GPW;
+      if (visit_from_start && cc.t == cc.nt - 1) {
+        // the whole segment was ours: write the output rows
+        if (grp == 0) {
+#pragma unroll
+          for (int g = 0; g < GPW; ++g) {
+            const float inv = cc.L > 0 ? 1.f / l[g] : 0.f;
+            uint4* orow = reinterpret_cast<uint4*>(static_cast<char*>(p.out) + (row0 + g) * ROW);
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) {
+              float f[VEC];
+#pragma unroll
+              for (int e = 0; e < VEC; ++e) f[e] = o[g][k * VEC + e] * inv;
+              orow[sub + 8 * k] = Chunk<T>::narrow(f);
+            }
+          }
+        }
+      } else {
+        // one piece of a segment shared with neighbouring warps
+        const int slot = cc.g - cc.t <= a_begin ? 0 : 1;  // segment is this warp's first visit -> 0
+        const size_t base = ((size_t)wid * 2 + slot) * GPW;
+        if (grp == 0) {
+#pragma unroll
+          for (int g = 0; g < GPW; ++g) {
+            const float inv = 1.f / l[g];
+            float4* po = reinterpret_cast<float4*>(p.ws_o + (base + g) * D);
+#pragma unroll
+            for (int k = 0; k < CPL; ++k)
+#pragma unroll
+              for (int e = 0; e < VEC; e += 4)
+                po[((sub + 8 * k) * VEC + e) / 4] =
+                    make_float4(o[g][k * VEC + e] * inv, o[g][k * VEC + e + 1] * inv,
+                                o[g][k * VEC + e + 2] * inv, o[g][k * VEC + e + 3] * inv);
+          }
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int g = 0; g < GPW; ++g) p.ws_ml[base + g] = make_float2(m[g], l[g]);
+        }
+        __threadfence();
+        __syncwarp();
+        const long long seg_start = cc.g - cc.t;
+        const long long seg_end = seg_start + cc.nt;
+        // warps whose ranges meet this segment: w(x) = ceil((x+1) Weff / T) - 1
+        const long long w_first = ((seg_start + 1) * Weff + Ttot - 1) / Ttot - 1;
+        const long long w_last = (seg_end * Weff + Ttot - 1) / Ttot - 1;
+        int is_last = 0;
+        if (lane == 0) {
+          int32_t* ctr = p.ws_counter + (size_t)cc.s * HG + cc.hg;
+          const int prev = atomicAdd(ctr, 1);
+          is_last = prev == (int)(w_last - w_first);
+          if (is_last) *ctr = 0;  // every piece has counted: leave the counter zero
+        }
+        is_last = __shfl_sync(kFullMask, is_last, 0);
+        if (is_last) {
+          __threadfence();
+          constexpr int DL = D / 32;  // output dims per lane in the merge
+#pragma unroll
+          for (int g = 0; g < GPW; ++g) {
+            float M = -INFINITY;
+            for (long long w = w_first; w <= w_last; ++w) {
+              const int sl = (w == w_first && w * Ttot / Weff < seg_start) ? 1 : 0;
+              M = fmaxf(M, __ldcg(p.ws_ml + ((size_t)w * 2 + sl) * GPW + g).x);
+            }
+            float Ls = 0.f, O[DL];
+#pragma unroll
+            for (int e = 0; e < DL; ++e) O[e] = 0.f;
+            for (long long w = w_first; w <= w_last; ++w) {
+              const int sl = (w == w_first && w * Ttot / Weff < seg_start) ? 1 : 0;
+              const size_t idx = ((size_t)w * 2 + sl) * GPW + g;
+              const float2 v = __ldcg(p.ws_ml + idx);
+              const float wt = v.y * exp2f(v.x - M);  // l_j 2^(m_j - M); partials hold o_j / l_j
+              Ls += wt;
+              const float* po = p.ws_o + idx * D + lane * DL;
+#pragma unroll
+              for (int e = 0; e < DL; ++e) O[e] += __ldcg(po + e) * wt;
+            }
+            T* orow = static_cast<T*>(p.out) + (row0 + g) * D + lane * DL;
+#pragma unroll
+            for (int e = 0; e < DL; ++e) store_elem(orow + e, O[e] / Ls);
+          }
+        }
+      }
     }
-  }
-
-  // ---- combine the warps through shared memory (each warp its own ring) --
-  float* wsm = reinterpret_cast<float*>(my_ring);  // [GPW][D] o, [GPW] m, [GPW] l
-  __syncwarp();
-  if (grp == 0) {
-#pragma unroll
-    for (int g = 0; g < GPW; ++g)
-#pragma unroll
-      for (int k = 0; k < CPL; ++k)
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) wsm[g * D + (sub + 8 * k) * VEC + e] = o[g][k * VEC + e];
-  }
-  if (lane == 0) {
-#pragma unroll
-    for (int g = 0; g < GPW; ++g) {
-      wsm[GPW * D + g] = m[g];
-      wsm[GPW * D + GPW + g] = l[g];
-    }
-  }
-  __syncthreads();
-
-  const size_t H = p.num_heads;
-  const bool direct = nsplit == 1;  // the whole context was this block's partition
-  for (int idx = threadIdx.x; idx < GPW * D; idx += NW * 32) {
-    const int g = idx / D, d = idx - g * D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float* ww = reinterpret_cast<const float*>(ring + w * ST * S::kStageBytes);
-      M = fmaxf(M, ww[GPW * D + g]);
-    }
-    float Ls = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      const float* ww = reinterpret_cast<const float*>(ring + w * ST * S::kStageBytes);
-      const float mw = ww[GPW * D + g];
-      const float sc = mw == -INFINITY ? 0.f : exp2f(mw - M);
-      Ls += ww[GPW * D + GPW + g] * sc;
-      O += ww[g * D + d] * sc;
-    }
-    const size_t row = (size_t)seq * H + h0 + g;
-    if (direct) {
-      store_elem(static_cast<T*>(p.out) + row * D + d, L > 0 ? O / Ls : 0.f);
-    } else {
-      p.ws_o[(row * p.max_splits + split) * D + d] = O / Ls;
-      if (d == 0) p.ws_ml[row * p.max_splits + split] = make_float2(M, Ls);
-    }
-  }
-  if (direct) return;
-
-  // ---- last partition to finish merges all of them (log-sum-exp) --------
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int32_t* ctr = p.ws_counter + (size_t)seq * gridDim.x + blockIdx.x;
-    const int prev = atomicAdd(ctr, 1);
-    const int last = prev == nsplit - 1;
-    if (last) *ctr = 0;  // every partition has counted: leave the counter zero
-    *s_last = last;
-  }
-  __syncthreads();
-  if (!*s_last) return;
-  __threadfence();
-  for (int idx = threadIdx.x; idx < GPW * D; idx += NW * 32) {
-    const int g = idx / D, d = idx - g * D;
-    const size_t row = (size_t)seq * H + h0 + g;
-    const float2* ml = p.ws_ml + row * p.max_splits;
-    const float* po = p.ws_o + row * p.max_splits * D + d;
-    float M = -INFINITY;
-    for (int j = 0; j < nsplit; ++j) M = fmaxf(M, __ldcg(ml + j).x);
-    float Ls = 0.f, O = 0.f;
-    for (int j = 0; j < nsplit; ++j) {
-      const float2 v = __ldcg(ml + j);
-      const float w = v.y * exp2f(v.x - M);  // l_j 2^(m_j - M)
-      Ls += w;
-      O += __ldcg(po + (size_t)j * D) * w;   // partials hold o_j / l_j
-    }
-    store_elem(static_cast<T*>(p.out) + row * D + d, O / Ls);
+    cursor_next(cc, p, cap);
   }
 }
 
-// Launch one instantiation (sets the dynamic shared-memory limit once per device).
+// Launch one instantiation as a persistent grid sized to the device.
 template <typename T, int D, int GPW>
-cudaError_t launch_pa_decode(const DecodeParams& p, dim3 grid, cudaStream_t stream) {
-  using S = DecodeShape<T, D>;
-  static unsigned long long configured = 0;  // one bit per device ordinal < 64
+cudaError_t launch_pa_decode(const DecodeParams& p, cudaStream_t stream) {
+  using S = DecodeShape<T, D, GPW>;
+  static int grid_of_device[64] = {0};  // cached per device ordinal (0 = not yet known)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
-  if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+  int grid = (dev >= 0 && dev < 64) ? __atomic_load_n(&grid_of_device[dev], __ATOMIC_ACQUIRE) : 0;
+  if (grid == 0) {
     e = cudaFuncSetAttribute(pa_decode_kernel<T, D, GPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::kSmemBytes);
     if (e != cudaSuccess) return e;
-    __atomic_fetch_or(&configured, bit, __ATOMIC_ACQ_REL);
+    int sms = 0, per_sm = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_decode_kernel<T, D, GPW>,
+                                                      kDecodeWarps * 32, S::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    grid = sms * (per_sm > 0 ? per_sm : 1);
+    if (grid > kMaxDecodeWarps / kDecodeWarps) grid = kMaxDecodeWarps / kDecodeWarps;
+    if (dev >= 0 && dev < 64) __atomic_store_n(&grid_of_device[dev], grid, __ATOMIC_RELEASE);
   }
   pa_decode_kernel<T, D, GPW><<<grid, kDecodeWarps * 32, S::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
-using DecodeLauncher = cudaError_t (*)(const DecodeParams&, dim3, cudaStream_t);
+using DecodeLauncher = cudaError_t (*)(const DecodeParams&, cudaStream_t);
 
 // Per-dtype tables, defined in decode_<dtype>.cu. gpw_index: 0 -> 1, 1 -> 2, 2 -> 4.
 DecodeLauncher decode_launcher_f32(int head_dim, int gpw_index);

@@ -53,7 +53,7 @@ extern "C" pkv_status pkv_paged_attention_decode_noalloc(
                                       0, dev_err, stream);
   void* scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return PKV_ERR_CUDA;
-  // The partition counters at the start of the scratch must be zero when the
+  // The segment counters at the start of the scratch must be zero when the
   // kernel starts; a previous call that reported a device error may have left
   // some set, so clear them on the caller's stream (no allocation involved).
   const size_t counter_bytes = (size_t)num_seqs * num_heads * sizeof(int32_t);

@@ -56,15 +56,14 @@ def test_timeout_setting_round_trip(pkv):
 
 
 def test_workspace_size(pkv):
-    P = pkv.decode_partition_tokens(128, 40, 2048)
-    assert P % 16 == 0 and P % 32 == 0
-    assert pkv.decode_workspace_bytes(128, 40, 128, P) == 0        # one partition: no workspace
-    S = -(-2048 // P)
-    rows = 128 * 40
+    slots = 4096 * 2 * 4
     align = lambda x: -(-x // 256) * 256
-    expect = align(rows * 4) + align(rows * S * 8) + rows * S * 128 * 4
-    assert pkv.decode_workspace_bytes(128, 40, 128, 2048) == expect
+    for B, H, D in ((128, 40, 128), (8, 32, 128), (4, 2, 64)):
+        expect = align(B * H * 4) + align(slots * 8) + slots * D * 4
+        assert pkv.decode_workspace_bytes(B, H, D, 2048) == expect
+        assert pkv.decode_workspace_bytes(B, H, D, 1) == expect     # independent of context length
     assert pkv.decode_workspace_bytes(0, 40, 128, 2048) == 0
+    assert pkv.decode_workspace_bytes(128, 40, 128, 2048) <= pkv.NOALLOC_SCRATCH_BYTES
 
 
 FAKE = 0x10000  # aligned, never dereferenced: every call below returns before any device work
@@ -94,7 +93,7 @@ def test_decode_host_checks(pkv):
     assert _decode(pkv, dtype=7) == UNS
     assert _decode(pkv, B=70000, MB=1, mcl=16) == UNS
     big = dict(MB=200, mcl=3000)
-    assert _decode(pkv, **big) == WS                     # needs a workspace, none given
+    assert _decode(pkv, **big) == WS                     # a workspace is always needed
     need = pkv.decode_workspace_bytes(4, 8, 128, 3000)
     assert _decode(pkv, ws=FAKE, ws_bytes=need - 1, **big) == WS
     assert _decode(pkv, ws=FAKE + 4, ws_bytes=need, **big) == INV

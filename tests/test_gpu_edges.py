@@ -1,7 +1,7 @@
 """Edge cases of the GPU path through the C ABI: every dtype / head_dim /
-block_size / grouped-head combination, context lengths at the tile,
-block and partition boundaries (including 0 and 1), oversized grids,
-workspace reuse, and the device error word."""
+block_size / grouped-head combination, context lengths at the tile and
+block boundaries (including 0 and 1), segments split across many warps,
+an oversized max_context_len, workspace reuse, and the device error word."""
 import numpy as np
 import pytest
 import torch
@@ -61,8 +61,8 @@ def test_new_token_write_then_read():
 
 
 def test_oversized_grid_and_workspace_reuse():
-    """max_context_len far above the real lengths (empty partitions), and
-    one workspace reused by consecutive calls (its counters return to 0)."""
+    """max_context_len far above the real lengths, and one workspace reused
+    by consecutive calls (its counters return to 0)."""
     import paged_kv_cache_204_gb300 as pkv
     cfg = _cfg("f16", 128, 16, 2, 1, lens=(3, 300, 900, 1500))
     hw = H.generate(cfg)
@@ -76,9 +76,7 @@ def test_oversized_grid_and_workspace_reuse():
         out = run_step(dw, workspace=ws, dev_err=err, max_context_len=mcl)
         assert device_error(err) == 0
         assert_close(to_f64(out), ref, "reuse")
-    P = pkv.decode_partition_tokens(4, cfg.num_heads, mcl)
     assert int(ws[: 4 * cfg.num_heads * 4].view(torch.int32).abs().sum()) == 0, "counters not reset"
-    assert P % 16 == 0
 
 
 def test_zero_sequences_is_a_no_op():

@@ -30,9 +30,9 @@ def _close(a, b):
 
 
 @pytest.mark.parametrize("name,B,over", [
-    ("llama13b", 16, {}),                                       # partitions merged through the scratch
-    ("longctx_bs16", 2, {"num_heads": 4, "num_kv_heads": 4}),  # many partitions per head
-    ("tiny", 4, {}),                                            # one partition: scratch untouched
+    ("llama13b", 16, {}),                                       # segments split across warps
+    ("longctx_bs16", 2, {"num_heads": 4, "num_kv_heads": 4}),  # each segment split many ways
+    ("tiny", 4, {}),                                            # fewer tiles than warps
 ])
 def test_noalloc_matches_workspace_entry_point(name, B, over):
     import paged_kv_cache_204_gb300 as pkv
@@ -61,7 +61,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     import paged_kv_cache_204_gb300 as pkv
     dw = _workload("tiny", 4)
     cfg = dw.cfg
-    B, H, D, L = 4096, 64, 128, 8192   # needs far more than 32 MiB of partials
+    B, H, D, L = 65535, 128, 128, 8192   # segment counters alone exceed 32 MiB
     assert pkv.decode_workspace_bytes(B, H, D, L) > pkv.NOALLOC_SCRATCH_BYTES
     rc = pkv.lib.pkv_paged_attention_decode_noalloc(
         dw.q.data_ptr(), dw.q.data_ptr(), dw.k_cache.data_ptr(), dw.v_cache.data_ptr(),
