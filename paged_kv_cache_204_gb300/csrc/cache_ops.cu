@@ -8,8 +8,9 @@
 
 namespace pkv {
 
-// One thread block per new token: its num_kv_heads rows of K and of V (each
-// row_chunks 16-byte chunks) go to cache[slot / bs][h][slot % bs].
+// grid = (new token, group of 128 chunks): each thread moves one 16-byte
+// chunk of the token's K rows and of its V rows (all kv heads) to
+// cache[slot / bs][h][slot % bs], so every load of the step is in flight at once.
 __global__ void __launch_bounds__(128)
     reshape_and_cache_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                              uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
@@ -19,23 +20,21 @@ __global__ void __launch_bounds__(128)
   const int64_t slot = __ldg(slot_mapping + t);
   if (slot < 0) return;  // padding token
   if (slot >= num_slots) {
-    if (threadIdx.x == 0) set_err(dev_err, PKV_DEV_ERR_SLOT);
+    if (threadIdx.x == 0 && blockIdx.y == 0) set_err(dev_err, PKV_DEV_ERR_SLOT);
     return;
   }
+  const int n = num_kv_heads * row_chunks;
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;
+  if (c >= n) return;
   const int64_t blk = slot / block_size;
   const int off = static_cast<int>(slot - blk * block_size);
-  const int n = num_kv_heads * row_chunks;
-  const uint4* ks = k + (size_t)t * n;
-  const uint4* vs = v + (size_t)t * n;
-  for (int c = threadIdx.x; c < n; c += blockDim.x) {
-    const int h = c / row_chunks;
-    const int cc = c - h * row_chunks;
-    const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * row_chunks + cc;
-    const uint4 kx = __ldg(ks + c);
-    const uint4 vx = __ldg(vs + c);
-    k_cache[dst] = kx;
-    v_cache[dst] = vx;
-  }
+  const int h = c / row_chunks;
+  const int cc = c - h * row_chunks;
+  const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * row_chunks + cc;
+  const uint4 kx = __ldg(k + (size_t)t * n + c);
+  const uint4 vx = __ldg(v + (size_t)t * n + c);
+  k_cache[dst] = kx;
+  v_cache[dst] = vx;
 }
 
 // grid = (pair, pool K|V, piece). Each piece streams part of one block with
@@ -69,7 +68,9 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache
                                      const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
                                      int row_bytes, int block_size, int num_blocks, int32_t* dev_err,
                                      cudaStream_t stream) {
-  reshape_and_cache_kernel<<<num_tokens, 128, 0, stream>>>(
+  const int n = num_kv_heads * (row_bytes / 16);
+  const dim3 grid(num_tokens, (n + 127) / 128);
+  reshape_and_cache_kernel<<<grid, 128, 0, stream>>>(
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
       static_cast<uint4*>(v_cache), slot_mapping, num_kv_heads, row_bytes / 16, block_size,
       (int64_t)num_blocks * block_size, dev_err);
