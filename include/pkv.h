@@ -85,6 +85,7 @@ typedef enum pkv_status {
 #define PKV_DEV_ERR_CONTEXT_LEN 0x4 /* context_lens entry < 0, > max_context_len or > max_blocks_per_seq * block_size */
 #define PKV_DEV_ERR_TIMEOUT 0x8     /* a bounded wait inside a kernel ran out */
 #define PKV_DEV_ERR_PAIR 0x10       /* copy_blocks pair entry outside [0, num_blocks) */
+#define PKV_DEV_ERR_GROUP 0x20      /* grouped decode: grouping not a partition, or shared blocks differ */
 
 /* Human-readable name of a pkv_status value (static string, never NULL). */
 const char* pkv_status_string(int status);
@@ -204,6 +205,54 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
                                       int max_blocks_per_seq, int num_blocks, int max_context_len,
                                       pkv_dtype dtype, void* workspace, size_t workspace_bytes,
                                       int32_t* dev_err, pkv_stream_t stream);
+
+/* -------------------------------------------------------------------------
+ * pkv_paged_attention_decode_grouped
+ *
+ * Operation [VM]: the same result as pkv_paged_attention_decode, for batches
+ * in which sampled completions (or beams) of one prompt share the prompt's
+ * physical blocks. The caller groups such sequences:
+ *     group g = sequences [group_start[g], group_start[g+1])
+ *     the first shared_blocks[g] entries of their block-table rows are the
+ *     same physical blocks
+ * and the kernel then reads each shared K/V tile once for all members of the
+ * group (up to 4 members per pass) instead of once per member, adding each
+ * member's own tail afterwards with a log-sum-exp merge. Groups of one
+ * sequence, or with shared_blocks 0, are plain sequences.
+ *
+ *   group_start    int32 [num_groups + 1] (device); must partition
+ *                  [0, num_seqs): group_start[0] = 0, non-decreasing,
+ *                  group_start[num_groups] = num_seqs
+ *   shared_blocks  int32 [num_groups] (device)
+ *   workspace      at least pkv_decode_grouped_workspace_bytes() bytes,
+ *                  zeroed before the first call; left zeroed by every call
+ *                  that ends with *dev_err == 0 (other rules as for
+ *                  pkv_paged_attention_decode)
+ *   other arguments as for pkv_paged_attention_decode.
+ *
+ * The grouping is checked on the device before use: if group_start is not a
+ * partition the grouping is ignored, and a group whose members' block-table
+ * entries differ inside the promised prefix uses only the part that matches;
+ * both set PKV_DEV_ERR_GROUP and still give the plain result. The shared
+ * prefix actually read once is cut to whole 16-token tiles, whole blocks and
+ * the shortest member's context. Each call enqueues two kernels (the check,
+ * then the attention). Host errors as for pkv_paged_attention_decode, plus
+ * INVALID_ARG when num_groups < 1 or group_start / shared_blocks is NULL.
+ * ---------------------------------------------------------------------- */
+pkv_status pkv_paged_attention_decode_grouped(void* out, const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* block_tables,
+                                              const int32_t* context_lens, float scale, int num_heads,
+                                              int num_kv_heads, int head_dim, int block_size,
+                                              int num_seqs, int max_blocks_per_seq, int num_blocks,
+                                              int max_context_len, const int32_t* group_start,
+                                              const int32_t* shared_blocks, int num_groups,
+                                              pkv_dtype dtype, void* workspace, size_t workspace_bytes,
+                                              int32_t* dev_err, pkv_stream_t stream);
+
+/* Bytes of workspace pkv_paged_attention_decode_grouped needs. Pure host
+ * function; 0 for non-positive sizes. */
+size_t pkv_decode_grouped_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                          int num_groups);
 
 /* -------------------------------------------------------------------------
  * pkv_paged_attention_decode_noalloc

@@ -11,6 +11,8 @@ Functions mirror the C entry points:
   copy_blocks             -> pkv_copy_blocks
   paged_attention_decode  -> pkv_paged_attention_decode
   decode_workspace_bytes  -> pkv_decode_workspace_bytes
+  paged_attention_decode_grouped  -> pkv_paged_attention_decode_grouped
+  decode_grouped_workspace_bytes  -> pkv_decode_grouped_workspace_bytes
   set_wait_timeout_ns / get_wait_timeout_ns, status_string, version
 """
 from __future__ import annotations
@@ -32,6 +34,7 @@ lib = ctypes.CDLL(LIB_PATH)
 
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
 DEV_ERR_BLOCK_ID, DEV_ERR_SLOT, DEV_ERR_CONTEXT_LEN, DEV_ERR_TIMEOUT, DEV_ERR_PAIR = 1, 2, 4, 8, 16
+DEV_ERR_GROUP = 32
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
 
 _P, _I, _I64, _U64, _F, _SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64,
@@ -53,6 +56,11 @@ lib.pkv_copy_blocks.restype = _I
 lib.pkv_paged_attention_decode.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I,
                                            _I, _I, _P, _SZ, _P, _P]
 lib.pkv_paged_attention_decode.restype = _I
+lib.pkv_paged_attention_decode_grouped.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I,
+                                                   _I, _I, _P, _P, _I, _I, _P, _SZ, _P, _P]
+lib.pkv_paged_attention_decode_grouped.restype = _I
+lib.pkv_decode_grouped_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
+lib.pkv_decode_grouped_workspace_bytes.restype = _SZ
 lib.pkv_paged_attention_decode_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I,
                                                    _I, _I, _I, _P, _P]
 lib.pkv_paged_attention_decode_noalloc.restype = _I
@@ -159,6 +167,38 @@ def paged_attention_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: 
         float(scale), H, Hkv, D, bs, B, block_tables.shape[1], nb, int(max_context_len),
         DTYPE_CODE[q.dtype], _ptr(dev_err), _stream(stream)),
         "pkv_paged_attention_decode_noalloc")
+
+
+def decode_grouped_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
+                                   num_groups: int) -> int:
+    return lib.pkv_decode_grouped_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, num_groups)
+
+
+def paged_attention_decode_grouped(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                   v_cache: torch.Tensor, block_tables: torch.Tensor,
+                                   context_lens: torch.Tensor, scale: float, max_context_len: int,
+                                   group_start: torch.Tensor, shared_blocks: torch.Tensor,
+                                   workspace: torch.Tensor, dev_err: torch.Tensor | None = None,
+                                   stream=None) -> None:
+    """paged_attention_decode for groups of sequences sharing prefix blocks:
+    group g = sequences group_start[g]:group_start[g+1] (int32 [G+1]) whose
+    first shared_blocks[g] (int32 [G]) block-table entries are the same
+    physical blocks. workspace: zero-initialised, decode_grouped_workspace_bytes()."""
+    B, H, D = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    G = shared_blocks.numel()
+    _check(lib.pkv_paged_attention_decode_grouped(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        float(scale), H, Hkv, D, bs, B, block_tables.shape[1], nb, int(max_context_len),
+        _ptr(group_start), _ptr(shared_blocks), G, DTYPE_CODE[q.dtype], _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_err), _stream(stream)),
+        "pkv_paged_attention_decode_grouped")
+
+
+def new_grouped_workspace(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,
+                          num_groups: int, device="cuda") -> torch.Tensor:
+    n = decode_grouped_workspace_bytes(num_seqs, num_heads, head_dim, max_context_len, num_groups)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
 def new_workspace(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,

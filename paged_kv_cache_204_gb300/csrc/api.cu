@@ -6,6 +6,7 @@
 
 #include "cache_ops.h"
 #include "decode.cuh"
+#include "decode_grouped.cuh"
 #include "pkv.h"
 
 namespace {
@@ -36,7 +37,95 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim) {
   return w;
 }
 
+// Grouped decode: grouping scratch, piece and row counters, per-row results
+// of the prefix and tail parts, then the warps' partial slots.
+struct GroupedLayout {
+  size_t flag = 0, group_S = 0, seq_P = 0, seg_ctr = 0, row_ctr = 0, row_ml = 0, row_o = 0;
+  size_t slot_ml = 0, slot_o = 0, total = 0;
+};
+
+GroupedLayout grouped_layout(int num_seqs, int num_heads, int head_dim, int num_groups) {
+  GroupedLayout w;
+  if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || num_groups <= 0) return w;
+  const size_t rows = (size_t)num_seqs * num_heads;
+  const size_t slots = (size_t)pkv::kMaxDecodeWarps * 2 * pkv::kMaxGroupPerWarp;
+  size_t off = 0;
+  w.flag = off;
+  off += 256;
+  w.group_S = off;
+  off += align_up((size_t)num_groups * 4, 256);
+  w.seq_P = off;
+  off += align_up((size_t)num_seqs * 4, 256);
+  w.seg_ctr = off;
+  off += align_up(2 * rows * 4, 256);
+  w.row_ctr = off;
+  off += align_up(rows * 4, 256);
+  w.row_ml = off;
+  off += align_up(rows * 2 * sizeof(float2), 256);
+  w.row_o = off;
+  off += align_up(rows * 2 * head_dim * sizeof(float), 256);
+  w.slot_ml = off;
+  off += align_up(slots * sizeof(float2), 256);
+  w.slot_o = off;
+  off += slots * head_dim * sizeof(float);
+  w.total = off;
+  return w;
+}
+
 pkv_status launch_status(cudaError_t e) { return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA; }
+
+// Host checks shared by the decode entry points (nothing is enqueued).
+pkv_status check_decode_args(void* out, const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* block_tables, const int32_t* context_lens, float scale,
+                             int num_heads, int num_kv_heads, int head_dim, int block_size, int num_seqs,
+                             int max_blocks_per_seq, int num_blocks, int max_context_len, pkv_dtype dtype,
+                             int32_t* dev_err) {
+  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+      max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 || !std::isfinite(scale))
+    return PKV_ERR_INVALID_ARG;
+  if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
+  if ((int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size) return PKV_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype) || !supported_head_dim(head_dim) || !supported_block_size(block_size))
+    return PKV_ERR_UNSUPPORTED;
+  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PKV_OK;
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
+  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(block_tables, 4) || !aligned(context_lens, 4) || (dev_err && !aligned(dev_err, 4)))
+    return PKV_ERR_INVALID_ARG;
+  return PKV_OK;
+}
+
+pkv::DecodeParams decode_params(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, const int32_t* context_lens, float scale,
+                                int num_heads, int num_kv_heads, int block_size, int num_seqs,
+                                int max_blocks_per_seq, int num_blocks, int max_context_len, int gpw,
+                                int32_t* dev_err) {
+  pkv::DecodeParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
+  p.num_seqs = num_seqs;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.head_groups = num_heads / gpw;
+  p.block_size = block_size;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.max_context_len = max_context_len;
+  p.dev_err = dev_err;
+  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  return p;
+}
+
+// Query heads one warp serves against one kv head: the largest of 4, 2, 1
+// that divides the group.
+int heads_per_warp(int group) { return group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1); }
 
 }  // namespace
 
@@ -106,56 +195,78 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
                                       int max_blocks_per_seq, int num_blocks, int max_context_len,
                                       pkv_dtype dtype, void* workspace, size_t workspace_bytes,
                                       int32_t* dev_err, pkv_stream_t stream) {
-  if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-      max_blocks_per_seq <= 0 || num_blocks <= 0 || max_context_len < 0 || !std::isfinite(scale))
-    return PKV_ERR_INVALID_ARG;
-  if (num_heads % num_kv_heads != 0) return PKV_ERR_INVALID_ARG;
-  if ((int64_t)max_context_len > (int64_t)max_blocks_per_seq * block_size) return PKV_ERR_INVALID_ARG;
-  if (!valid_dtype(dtype) || !supported_head_dim(head_dim) || !supported_block_size(block_size))
-    return PKV_ERR_UNSUPPORTED;
-  if (num_seqs > 65535) return PKV_ERR_UNSUPPORTED;
-  if (num_seqs == 0) return PKV_OK;
-  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return PKV_ERR_INVALID_ARG;
-  if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
-      !aligned(block_tables, 4) || !aligned(context_lens, 4) || (dev_err && !aligned(dev_err, 4)))
-    return PKV_ERR_INVALID_ARG;
-
+  const pkv_status st = check_decode_args(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                          num_heads, num_kv_heads, head_dim, block_size, num_seqs,
+                                          max_blocks_per_seq, num_blocks, max_context_len, dtype, dev_err);
+  if (st != PKV_OK || num_seqs == 0) return st;
   const WorkspaceLayout ws = workspace_layout(num_seqs, num_heads, head_dim);
   if (!workspace || workspace_bytes < ws.total) return PKV_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
 
-  const int group = num_heads / num_kv_heads;
-  const int gpw = group % 4 == 0 ? 4 : (group % 2 == 0 ? 2 : 1);
+  const int gpw = heads_per_warp(num_heads / num_kv_heads);
   const int gpw_index = gpw == 4 ? 2 : (gpw == 2 ? 1 : 0);
   pkv::DecodeLauncher launch = dtype == PKV_F32   ? pkv::decode_launcher_f32(head_dim, gpw_index)
                                : dtype == PKV_F16 ? pkv::decode_launcher_f16(head_dim, gpw_index)
                                                   : pkv::decode_launcher_bf16(head_dim, gpw_index);
   if (!launch) return PKV_ERR_UNSUPPORTED;
-
-  pkv::DecodeParams p{};
-  p.out = out;
-  p.q = q;
-  p.k_cache = k_cache;
-  p.v_cache = v_cache;
-  p.block_tables = block_tables;
-  p.context_lens = context_lens;
-  p.scale_log2 = scale * 1.4426950408889634f;  // log2(e)
-  p.num_seqs = num_seqs;
-  p.num_heads = num_heads;
-  p.num_kv_heads = num_kv_heads;
-  p.group = group;
-  p.head_groups = num_heads / gpw;
-  p.block_size = block_size;
-  p.max_blocks_per_seq = max_blocks_per_seq;
-  p.num_blocks = num_blocks;
-  p.max_context_len = max_context_len;
+  pkv::DecodeParams p = decode_params(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                      num_heads, num_kv_heads, block_size, num_seqs, max_blocks_per_seq,
+                                      num_blocks, max_context_len, gpw, dev_err);
   char* wsb = static_cast<char*>(workspace);
   p.ws_counter = reinterpret_cast<int32_t*>(wsb + ws.counter_off);
   p.ws_ml = reinterpret_cast<float2*>(wsb + ws.ml_off);
   p.ws_o = reinterpret_cast<float*>(wsb + ws.o_off);
-  p.dev_err = dev_err;
-  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   return launch_status(launch(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t pkv_decode_grouped_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,
+                                          int num_groups) {
+  if (max_context_len < 0) return 0;
+  return grouped_layout(num_seqs, num_heads, head_dim, num_groups).total;
+}
+
+pkv_status pkv_paged_attention_decode_grouped(void* out, const void* q, const void* k_cache,
+                                              const void* v_cache, const int32_t* block_tables,
+                                              const int32_t* context_lens, float scale, int num_heads,
+                                              int num_kv_heads, int head_dim, int block_size,
+                                              int num_seqs, int max_blocks_per_seq, int num_blocks,
+                                              int max_context_len, const int32_t* group_start,
+                                              const int32_t* shared_blocks, int num_groups,
+                                              pkv_dtype dtype, void* workspace, size_t workspace_bytes,
+                                              int32_t* dev_err, pkv_stream_t stream) {
+  const pkv_status st = check_decode_args(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                          num_heads, num_kv_heads, head_dim, block_size, num_seqs,
+                                          max_blocks_per_seq, num_blocks, max_context_len, dtype, dev_err);
+  if (st != PKV_OK || num_seqs == 0) return st;
+  if (num_groups < 1 || !group_start || !shared_blocks || !aligned(group_start, 4) ||
+      !aligned(shared_blocks, 4))
+    return PKV_ERR_INVALID_ARG;
+  const GroupedLayout ws = grouped_layout(num_seqs, num_heads, head_dim, num_groups);
+  if (!workspace || workspace_bytes < ws.total) return PKV_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
+
+  pkv::GroupedLauncher launch = dtype == PKV_F32   ? pkv::grouped_launcher_f32(head_dim)
+                                : dtype == PKV_F16 ? pkv::grouped_launcher_f16(head_dim)
+                                                   : pkv::grouped_launcher_bf16(head_dim);
+  if (!launch) return PKV_ERR_UNSUPPORTED;
+  pkv::GroupedParams gp{};
+  gp.base = decode_params(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_heads,
+                          num_kv_heads, block_size, num_seqs, max_blocks_per_seq, num_blocks,
+                          max_context_len, heads_per_warp(num_heads / num_kv_heads), dev_err);
+  char* wsb = static_cast<char*>(workspace);
+  gp.base.ws_ml = reinterpret_cast<float2*>(wsb + ws.slot_ml);
+  gp.base.ws_o = reinterpret_cast<float*>(wsb + ws.slot_o);
+  gp.group_start = group_start;
+  gp.shared_blocks = shared_blocks;
+  gp.num_groups = num_groups;
+  gp.ws_flag = reinterpret_cast<int32_t*>(wsb + ws.flag);
+  gp.ws_group_S = reinterpret_cast<int32_t*>(wsb + ws.group_S);
+  gp.ws_seq_P = reinterpret_cast<int32_t*>(wsb + ws.seq_P);
+  gp.ws_seg_ctr = reinterpret_cast<int32_t*>(wsb + ws.seg_ctr);
+  gp.ws_row_ctr = reinterpret_cast<int32_t*>(wsb + ws.row_ctr);
+  gp.ws_row_ml = reinterpret_cast<float2*>(wsb + ws.row_ml);
+  gp.ws_row_o = reinterpret_cast<float*>(wsb + ws.row_o);
+  return launch_status(launch(gp, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -1,5 +1,6 @@
 // Instantiations of the paged decode kernel for float storage.
 #include "decode.cuh"
+#include "decode_grouped.cuh"
 
 namespace pkv {
 
@@ -12,6 +13,13 @@ DecodeLauncher decode_launcher_f32(int head_dim, int gpw_index) {
   if (gpw_index < 0 || gpw_index > 2) return nullptr;
   if (head_dim == 64) return d64[gpw_index];
   if (head_dim == 128) return d128[gpw_index];
+  return nullptr;
+}
+
+GroupedLauncher grouped_launcher_f32(int head_dim) {
+  using T = float;
+  if (head_dim == 64) return launch_pa_decode_grouped<T, 64>;
+  if (head_dim == 128) return launch_pa_decode_grouped<T, 128>;
   return nullptr;
 }
 

@@ -43,9 +43,10 @@ class DecodeConfig:
     @property
     def max_len(self) -> int:
         """Largest context length the distribution can produce."""
-        hi = max(self.lengths[1]) if self.lengths[0] == "fixed" else self.lengths[-1]
+        top = lambda spec: max(spec[1]) if spec[0] == "fixed" else spec[-1]
+        hi = top(self.lengths)
         if self.tail is not None:
-            hi += self.tail[-1]
+            hi += top(self.tail)
         return int(hi)
 
     @property

@@ -34,6 +34,8 @@ class Structure:
     prefix_lens: np.ndarray      # int32 [B]: tokens already cached before the step
     prefix_tables: np.ndarray    # int32 [B, MB]: block tables before the step (shared rows for forks)
     new_start: np.ndarray        # int64 [B+1]: slot_mapping rows [new_start[s], new_start[s+1]) are s's
+    group_start: np.ndarray | None = None    # int32 [G+1]: forks of one prompt are consecutive sequences
+    shared_blocks: np.ndarray | None = None  # int32 [G]: leading blocks every member maps identically
 
     @property
     def num_seqs(self) -> int:
@@ -108,12 +110,14 @@ def build(cfg: DecodeConfig, seed: int | None = None, num_seqs: int | None = Non
             prefill(root, int(plen[p]))
             seqs.append([root] + [mgr.fork(root) for _ in range(cfg.samples - 1)])
         order = [s for group in seqs for s in group]
+        group_sizes = [len(gr) for gr in seqs]
         for s in order:
             snapshot[s] = (mgr.lengths[s], list(mgr.tables[s]))
         for i, s in enumerate(order):  # divergence: each sample appends its own tail
             slots.extend(mgr.append(s, int(tails[i])))
             new_count[s] = int(tails[i])
     else:
+        group_sizes = None
         lens = draw_lengths(cfg.lengths, B, len_rng)
         order = []
         for i in range(B):
@@ -144,10 +148,77 @@ def build(cfg: DecodeConfig, seed: int | None = None, num_seqs: int | None = Non
         nstart[row + 1] = nstart[row] + new_count.get(s, 0)
     pb = np.array(sorted(prefill_rows), dtype=np.int64)
     pr = np.array([prefill_rows[b] for b in pb], dtype=np.int32)
+    gstart, shared = _groups(bt, group_sizes)
     return Structure(cfg=cfg, context_lens=cl, block_tables=bt,
                      max_context_len=int(cl.max()) if B else 0,
                      prefill_blocks=pb, prefill_rows=pr,
                      copy_pairs=np.array(mgr.cow_pairs, dtype=np.int64).reshape(-1, 2),
                      slot_mapping=np.array(slots, dtype=np.int64),
                      refcount=mgr.ref.copy(), waste_tokens=waste, prefix_lens=plen,
-                     prefix_tables=pbt, new_start=nstart)
+                     prefix_tables=pbt, new_start=nstart, group_start=gstart, shared_blocks=shared)
+
+
+def _groups(bt: np.ndarray, group_sizes):
+    """Group boundaries and the number of leading block-table entries every
+    member of a group shares (read off the final tables)."""
+    if group_sizes is None:
+        return None, None
+    gstart = np.concatenate([[0], np.cumsum(group_sizes)]).astype(np.int32)
+    shared = np.zeros(len(group_sizes), dtype=np.int32)
+    for g in range(len(group_sizes)):
+        rows = bt[gstart[g]:gstart[g + 1]]
+        same = (rows == rows[0]).all(axis=0) & (rows[0] >= 0)
+        shared[g] = int(np.argmin(same)) if not same.all() else same.size
+    return gstart, shared
+
+
+def build_grouped(cfg: DecodeConfig, prompts: list, seed: int | None = None) -> Structure:
+    """A copy-on-write batch with explicit shapes: prompts = [(prompt_len,
+    [tail_len, ...]), ...]; each prompt is prefilled, forked into one sequence
+    per tail, and each fork appends its tail (tails may be 0). Sequences of one
+    prompt are consecutive and form a group."""
+    seed = cfg.seed if seed is None else seed
+    mgr = BlockManager(cfg.num_blocks, cfg.block_size, np.random.default_rng([seed, 2]))
+    prefill_rows: dict[int, int] = {}
+    order, group_sizes, snapshot, new_count, slots = [], [], {}, {}, []
+    for plen, tails in prompts:
+        root = mgr.new_seq()
+        for slot in mgr.append(root, int(plen)):
+            b = slot // cfg.block_size
+            prefill_rows[b] = prefill_rows.get(b, 0) + 1
+        members = [root] + [mgr.fork(root) for _ in range(len(tails) - 1)]
+        order += members
+        group_sizes.append(len(members))
+        for m in members:
+            snapshot[m] = (mgr.lengths[m], list(mgr.tables[m]))
+    i = 0
+    for plen, tails in prompts:
+        for tl in tails:
+            s = order[i]
+            slots.extend(mgr.append(s, int(tl)))
+            new_count[s] = int(tl)
+            i += 1
+    B, MB = len(order), cfg.max_blocks_per_seq
+    bt = np.full((B, MB), PAD_BLOCK, dtype=np.int32)
+    pbt = np.full((B, MB), PAD_BLOCK, dtype=np.int32)
+    cl = np.zeros(B, dtype=np.int32)
+    plen_a = np.zeros(B, dtype=np.int32)
+    waste = np.zeros(B, dtype=np.int32)
+    nstart = np.zeros(B + 1, dtype=np.int64)
+    for row, s in enumerate(order):
+        t = mgr.tables[s]
+        bt[row, :len(t)] = t
+        cl[row] = mgr.lengths[s]
+        waste[row] = mgr.waste_tokens(s)
+        plen_a[row], pt = snapshot[s]
+        pbt[row, :len(pt)] = pt
+        nstart[row + 1] = nstart[row] + new_count.get(s, 0)
+    pb = np.array(sorted(prefill_rows), dtype=np.int64)
+    pr = np.array([prefill_rows[b] for b in pb], dtype=np.int32)
+    gstart, shared = _groups(bt, group_sizes)
+    return Structure(cfg=cfg, context_lens=cl, block_tables=bt, max_context_len=int(cl.max()),
+                     prefill_blocks=pb, prefill_rows=pr,
+                     copy_pairs=np.array(mgr.cow_pairs, dtype=np.int64).reshape(-1, 2),
+                     slot_mapping=np.array(slots, dtype=np.int64), refcount=mgr.ref.copy(),
+                     waste_tokens=waste, prefix_lens=plen_a, prefix_tables=pbt, new_start=nstart,
+                     group_start=gstart, shared_blocks=shared)
