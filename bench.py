@@ -9,6 +9,7 @@ data resident in HBM; L2 is flushed (256 MiB write) between timed steps and
 each step is timed with CUDA events on the launching stream.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--attention plain|grouped]
 
 Prints one JSON line (rank 0). Under torchrun each rank runs its own replica
 of the workload (different seed): weak scaling, no collective on the data path.
@@ -41,25 +42,46 @@ FALLBACK_HBM_GBS = 6800.0
 def workload_bytes(st) -> dict:
     """Algorithmic bytes of one step: attention reads each distinct cached
     (block, row) once for K and once for V plus q, and writes out; the cache
-    write reads the new rows and writes them into the pools."""
+    write reads the new rows and writes them into the pools; each
+    copy-on-write pair reads and writes one whole block of both pools."""
     cfg = st.cfg
     es = cfg.elem_bytes
     row = cfg.num_kv_heads * cfg.head_dim * es           # one token, one of K/V, all kv heads
     qo = st.num_seqs * cfg.num_heads * cfg.head_dim * es
     attn = 2 * st.unique_kv_tokens() * row + 2 * qo
     cache_write = 2 * 2 * st.num_new_tokens * row
-    return {"attention": attn, "cache_write": cache_write, "step": attn + cache_write}
+    copies = 2 * 2 * st.copy_pairs.shape[0] * cfg.block_size * row
+    return {"attention": attn, "cache_write": cache_write, "copy": copies,
+            "step": attn + cache_write + copies}
 
 
-def config_json(cfg, st, world: int) -> dict:
+def describe_lengths(spec) -> str:
+    if spec[0] == "lognormal":
+        return f"lognormal(median {spec[1]}, sigma {spec[2]}) clipped to [{spec[3]}, {spec[4]}]"
+    if spec[0] == "uniform":
+        return f"uniform in [{spec[1]}, {spec[2]}]"
+    return f"fixed {list(spec[1])}"
+
+
+def config_json(cfg, st, world: int, attention: str = "plain") -> dict:
+    parts = [f"{cfg.name}-shaped decode step: {st.num_seqs} seqs, {cfg.num_heads} heads "
+             f"({cfg.num_kv_heads} kv), head_dim {cfg.head_dim}, block_size {cfg.block_size}, "
+             f"{cfg.dtype} storage with fp32 accumulation"]
+    if cfg.samples > 1:
+        parts.append(f"{st.num_seqs // cfg.samples} prompts x {cfg.samples} samples sharing "
+                     f"ref-counted prompt blocks, prompt lengths {describe_lengths(cfg.lengths)}, "
+                     f"divergent tails {describe_lengths(cfg.tail)}, {st.copy_pairs.shape[0]} "
+                     f"copy-on-write block copies and {st.num_new_tokens} tail rows written per step")
+    else:
+        parts.append(f"context lengths {describe_lengths(cfg.lengths)} "
+                     f"(mean {st.context_lens.mean():.0f})")
+        if st.num_new_tokens:
+            parts.append(f"plus reshape_and_cache of {st.num_new_tokens} new rows")
+    parts.append(f"{cfg.num_blocks}-block pools")
+    parts.append(f"{attention} attention")
     return {
-        "workload": (f"{cfg.name}-shaped decode step: {cfg.num_seqs} seqs, {cfg.num_heads} heads "
-                     f"({cfg.num_kv_heads} kv), head_dim {cfg.head_dim}, block_size {cfg.block_size}, "
-                     f"{cfg.dtype} storage with fp32 accumulation, lognormal(median {cfg.lengths[1]}, "
-                     f"sigma {cfg.lengths[2]}) context lengths clipped to [{cfg.lengths[3]}, "
-                     f"{cfg.lengths[4]}] (mean {st.context_lens.mean():.0f}), {cfg.num_blocks}-block "
-                     f"pools, plus reshape_and_cache of {st.num_new_tokens} new rows"),
-        "global_batch": cfg.num_seqs * world,
+        "workload": ", ".join(parts),
+        "global_batch": st.num_seqs * world,
         "seq_len": int(st.max_context_len),
         "parallelism": "single GPU" if world == 1 else f"{world} independent replicas",
         "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write); step inputs "
@@ -155,11 +177,13 @@ class ClockSampler:
 def cpu_sample(cfg, n_seqs: int):
     """The first n_seqs sequences of the workload (same length draws), on the host."""
     import synth.host as H
+    n_seqs = max(cfg.samples, n_seqs // cfg.samples * cfg.samples)
     hw = H.generate(cfg, num_seqs=n_seqs)
     return hw, H.compact_pools(hw)
 
 
 def time_oracle(cfg, min_seconds: float, n_seqs: int, max_runs: int | None = None) -> dict:
+    n_seqs = max(cfg.samples, n_seqs // cfg.samples * cfg.samples)
     """The fp64 oracle, as it stands, on the host cores: one step (new rows
     written, then attention) over a bounded sample of the workload."""
     import oracle
@@ -196,7 +220,7 @@ def run_reference(args, rank: int, world: int) -> int:
     import oracle
     import synth
     import synth.host as H
-    cfg = synth.get(WORKLOAD)
+    cfg = synth.get(args.workload)
     st_full = synth.build(cfg)
     threads = len(os.sched_getaffinity(0))
     n = max(1, min(cfg.num_seqs, threads))
@@ -263,7 +287,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
     dev = torch.device("cuda", local_rank)
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
-    cfg = synth.get(WORKLOAD)
+    cfg = synth.get(args.workload)
     if args.num_blocks:
         cfg = cfg.replace(num_blocks=args.num_blocks)
     if world > 1:
@@ -273,16 +297,40 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
     nbytes = workload_bytes(st)
     B, H, D = st.num_seqs, cfg.num_heads, cfg.head_dim
     mcl = st.max_context_len
-    ws = pkv.new_workspace(B, H, D, mcl, device=dev)
+    grouped = args.attention == "grouped"
+    if grouped and st.group_start is None:
+        raise SystemExit(f"--attention grouped needs a workload with sharing groups, not {cfg.name}")
+    if grouped:
+        gs = torch.from_numpy(st.group_start).to(dev)
+        sb = torch.from_numpy(st.shared_blocks).to(dev)
+        ws = pkv.new_grouped_workspace(B, H, D, mcl, sb.numel(), device=dev)
+    else:
+        ws = pkv.new_workspace(B, H, D, mcl, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     out = torch.empty_like(dw.q)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    has_copy, has_new = dw.copy_pairs.numel() > 0, dw.slot_mapping.numel() > 0
+
+    def cache_ops():
+        if has_copy:
+            pkv.copy_blocks(dw.k_cache, dw.v_cache, dw.copy_pairs, dev_err=err)
+        if has_new:
+            pkv.reshape_and_cache(dw.new_k, dw.new_v, dw.k_cache, dw.v_cache, dw.slot_mapping, dev_err=err)
+
+    def attention():
+        if grouped:
+            pkv.paged_attention_decode_grouped(out, dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
+                                               dw.context_lens, cfg.scale, mcl, gs, sb, ws, dev_err=err)
+        else:
+            pkv.paged_attention_decode(out, dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
+                                       dw.context_lens, cfg.scale, mcl, workspace=ws, dev_err=err)
 
     def step():
-        pkv.reshape_and_cache(dw.new_k, dw.new_v, dw.k_cache, dw.v_cache, dw.slot_mapping, dev_err=err)
-        pkv.paged_attention_decode(out, dw.q, dw.k_cache, dw.v_cache, dw.block_tables, dw.context_lens,
-                                   cfg.scale, mcl, workspace=ws, dev_err=err)
+        cache_ops()
+        attention()
+
+    launches_per_step = int(has_copy) + int(has_new) + (2 if grouped else 1)
 
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1)
@@ -303,10 +351,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         for i in range(K):
             flush.fill_(i & 0xFF)        # evict the previous step's lines from L2
             ev[i][0].record(stream)
-            pkv.reshape_and_cache(dw.new_k, dw.new_v, dw.k_cache, dw.v_cache, dw.slot_mapping, dev_err=err)
+            cache_ops()
             ev[i][1].record(stream)
-            pkv.paged_attention_decode(out, dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
-                                       dw.context_lens, cfg.scale, mcl, workspace=ws, dev_err=err)
+            attention()
             ev[i][2].record(stream)
         torch.cuda.synchronize()
         if world > 1:
@@ -320,9 +367,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
 
     # end to end through the same API with host buffers: per step, copy the
     # step's inputs from pinned host memory, run the step, read the output back
-    host_in = [t.cpu().pin_memory() for t in (dw.q, dw.new_k, dw.new_v, dw.slot_mapping,
-                                               dw.block_tables, dw.context_lens)]
-    dev_in = [dw.q, dw.new_k, dw.new_v, dw.slot_mapping, dw.block_tables, dw.context_lens]
+    dev_in = [t for t in (dw.q, dw.new_k, dw.new_v, dw.slot_mapping, dw.block_tables, dw.context_lens,
+                          dw.copy_pairs) if t.numel()]
+    if grouped:
+        dev_in += [gs, sb]
+    host_in = [t.cpu().pin_memory() for t in dev_in]
     host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host_in)
     d2h = host_out.numel() * host_out.element_size()
@@ -364,17 +413,20 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         "ms_per_step": agg["step_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": cfg.dtype, "data": "synthetic",
-        "config": config_json(cfg, st, world),
+        "config": config_json(cfg, st, world, args.attention),
         "seqs_per_s": world * B / (agg["step_ms"] * 1e-3),
-        "attention_ms": agg["decode_ms"], "cache_write_ms": agg["cache_ms"],
+        "attention_ms": agg["decode_ms"], "cache_ops_ms": agg["cache_ms"],
         "bytes_per_step": nbytes["step"], "roofline_frac_step": nbytes["step"] / (agg["step_ms"] * 1e-3) / 1e9 / peak,
-        "roofline": {"bound": "hbm", "kernel": "pa_decode_kernel", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": profiled_traffic(),
+        "roofline": {"bound": "hbm",
+                     "kernel": "pa_group_prologue + pa_decode_grouped_kernel" if grouped else "pa_decode_kernel",
+                     "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": profiled_traffic() if (cfg.name == WORKLOAD and not grouped) else None,
                      "algorithmic_bytes_per_launch": nbytes["attention"], "peak_source": peak_src},
         "cpu_baseline": cpu,
         "e2e": {"value": world * nbytes["step"] / (agg["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": agg["e2e_ms"], "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * K,
+        "gpu_launches": launches_per_step * K,
         "clocks": clocks.summary(),
         "timed_region_wall_s": wall,
     }
@@ -390,6 +442,10 @@ def main() -> int:
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="synthetic workload preset (default: the LLaMA-13B-shaped step)")
+    ap.add_argument("--attention", choices=("plain", "grouped"), default="plain",
+                    help="grouped: siblings read shared prefix blocks once (copy-on-write workloads)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum time of the CPU baseline")
     ap.add_argument("--cpu-seqs", type=int, default=32, help="sequences in the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

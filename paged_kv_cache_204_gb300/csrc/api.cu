@@ -37,10 +37,10 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim) {
   return w;
 }
 
-// Grouped decode: grouping scratch, piece and row counters, per-row results
-// of the prefix and tail parts, then the warps' partial slots.
+// Grouped decode: grouping scratch and phase counters, piece counters, each
+// row's prefix result, then the warps' partial slots.
 struct GroupedLayout {
-  size_t flag = 0, group_S = 0, seq_P = 0, seg_ctr = 0, row_ctr = 0, row_ml = 0, row_o = 0;
+  size_t flag = 0, group_S = 0, seq_P = 0, seg_ctr = 0, row_ml = 0, row_o = 0;
   size_t slot_ml = 0, slot_o = 0, total = 0;
 };
 
@@ -50,7 +50,7 @@ GroupedLayout grouped_layout(int num_seqs, int num_heads, int head_dim, int num_
   const size_t rows = (size_t)num_seqs * num_heads;
   const size_t slots = (size_t)pkv::kMaxDecodeWarps * 2 * pkv::kMaxGroupPerWarp;
   size_t off = 0;
-  w.flag = off;
+  w.flag = off;  // flag word, then the two phase counters
   off += 256;
   w.group_S = off;
   off += align_up((size_t)num_groups * 4, 256);
@@ -58,12 +58,10 @@ GroupedLayout grouped_layout(int num_seqs, int num_heads, int head_dim, int num_
   off += align_up((size_t)num_seqs * 4, 256);
   w.seg_ctr = off;
   off += align_up(2 * rows * 4, 256);
-  w.row_ctr = off;
-  off += align_up(rows * 4, 256);
   w.row_ml = off;
-  off += align_up(rows * 2 * sizeof(float2), 256);
+  off += align_up(rows * sizeof(float2), 256);
   w.row_o = off;
-  off += align_up(rows * 2 * head_dim * sizeof(float), 256);
+  off += align_up(rows * head_dim * sizeof(float), 256);
   w.slot_ml = off;
   off += align_up(slots * sizeof(float2), 256);
   w.slot_o = off;
@@ -245,14 +243,16 @@ pkv_status pkv_paged_attention_decode_grouped(void* out, const void* q, const vo
   if (!workspace || workspace_bytes < ws.total) return PKV_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
 
-  pkv::GroupedLauncher launch = dtype == PKV_F32   ? pkv::grouped_launcher_f32(head_dim)
-                                : dtype == PKV_F16 ? pkv::grouped_launcher_f16(head_dim)
-                                                   : pkv::grouped_launcher_bf16(head_dim);
+  const int gpw = heads_per_warp(num_heads / num_kv_heads);
+  const int gpw_index = gpw == 4 ? 2 : (gpw == 2 ? 1 : 0);
+  pkv::GroupedLauncher launch = dtype == PKV_F32   ? pkv::grouped_launcher_f32(head_dim, gpw_index)
+                                : dtype == PKV_F16 ? pkv::grouped_launcher_f16(head_dim, gpw_index)
+                                                   : pkv::grouped_launcher_bf16(head_dim, gpw_index);
   if (!launch) return PKV_ERR_UNSUPPORTED;
   pkv::GroupedParams gp{};
   gp.base = decode_params(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_heads,
                           num_kv_heads, block_size, num_seqs, max_blocks_per_seq, num_blocks,
-                          max_context_len, heads_per_warp(num_heads / num_kv_heads), dev_err);
+                          max_context_len, gpw, dev_err);
   char* wsb = static_cast<char*>(workspace);
   gp.base.ws_ml = reinterpret_cast<float2*>(wsb + ws.slot_ml);
   gp.base.ws_o = reinterpret_cast<float*>(wsb + ws.slot_o);
@@ -260,10 +260,10 @@ pkv_status pkv_paged_attention_decode_grouped(void* out, const void* q, const vo
   gp.shared_blocks = shared_blocks;
   gp.num_groups = num_groups;
   gp.ws_flag = reinterpret_cast<int32_t*>(wsb + ws.flag);
+  gp.ws_sync = reinterpret_cast<int32_t*>(wsb + ws.flag) + 1;
   gp.ws_group_S = reinterpret_cast<int32_t*>(wsb + ws.group_S);
   gp.ws_seq_P = reinterpret_cast<int32_t*>(wsb + ws.seq_P);
   gp.ws_seg_ctr = reinterpret_cast<int32_t*>(wsb + ws.seg_ctr);
-  gp.ws_row_ctr = reinterpret_cast<int32_t*>(wsb + ws.row_ctr);
   gp.ws_row_ml = reinterpret_cast<float2*>(wsb + ws.row_ml);
   gp.ws_row_o = reinterpret_cast<float*>(wsb + ws.row_o);
   return launch_status(launch(gp, reinterpret_cast<cudaStream_t>(stream)));

@@ -16,10 +16,16 @@ DecodeLauncher decode_launcher_f32(int head_dim, int gpw_index) {
   return nullptr;
 }
 
-GroupedLauncher grouped_launcher_f32(int head_dim) {
+GroupedLauncher grouped_launcher_f32(int head_dim, int gpw_index) {
   using T = float;
-  if (head_dim == 64) return launch_pa_decode_grouped<T, 64>;
-  if (head_dim == 128) return launch_pa_decode_grouped<T, 128>;
+  static const GroupedLauncher d64[3] = {launch_pa_decode_grouped<T, 64, 1>, launch_pa_decode_grouped<T, 64, 2>,
+                                          launch_pa_decode_grouped<T, 64, 4>};
+  static const GroupedLauncher d128[3] = {launch_pa_decode_grouped<T, 128, 1>,
+                                           launch_pa_decode_grouped<T, 128, 2>,
+                                           launch_pa_decode_grouped<T, 128, 4>};
+  if (gpw_index < 0 || gpw_index > 2) return nullptr;
+  if (head_dim == 64) return d64[gpw_index];
+  if (head_dim == 128) return d128[gpw_index];
   return nullptr;
 }
 

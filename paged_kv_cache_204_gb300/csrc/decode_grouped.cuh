@@ -14,10 +14,11 @@
 //     siblings (head h of members 4c .. 4c+3);
 //   tail segments (sequence s, head group hg): rows [S_g, L_s) of s's own
 //     blocks against its query heads, as in the plain kernel.
-// A row (s, h) whose sequence has a shared prefix gets two results — the
-// prefix segment's and the tail segment's — which the second to arrive
-// merges (log-sum-exp) into the output. Pieces of a segment cut by warp
-// range boundaries are first merged as in the plain kernel.
+// The prefix segments run first, balanced over all warps, then the tails,
+// balanced again; a grid-wide counter separates the two phases. A tail row of
+// a sequence with a shared prefix merges its prefix result (log-sum-exp) when
+// it writes the output. Pieces of a segment cut by warp range boundaries are
+// merged as in the plain kernel.
 //
 // A prologue kernel checks the caller's grouping: group_start must partition
 // [0, num_seqs) and the first shared_blocks[g] block-table entries of every
@@ -40,12 +41,12 @@ struct GroupedParams {
   const int32_t* shared_blocks;  // [num_groups]
   int num_groups;
   int32_t* ws_flag;     // [1] 1 = grouping rejected
+  int32_t* ws_sync;     // [2] phase arrivals, warps done (zero between launches)
   int32_t* ws_group_S;  // [num_groups] usable shared prefix tokens
   int32_t* ws_seq_P;    // [num_seqs] prefix tokens of the sequence's group
   int32_t* ws_seg_ctr;  // [2][num_seqs * num_heads] piece counters (prefix, tail)
-  int32_t* ws_row_ctr;  // [num_seqs * num_heads] prefix + tail arrivals
-  float2* ws_row_ml;    // [num_seqs * num_heads][2] (m, l) of the prefix / tail result
-  float* ws_row_o;      // [num_seqs * num_heads][2][head_dim] o / l
+  float2* ws_row_ml;    // [num_seqs * num_heads] (m, l) of each row's prefix result
+  float* ws_row_o;      // [num_seqs * num_heads][head_dim] o / l of each row's prefix result
 };
 
 __device__ __forceinline__ int warp_min(int v) {
@@ -121,6 +122,7 @@ struct GCursor {
   int lo, M;            // part 0: members [lo, lo + M)
   int tok0, tok_end;    // token range of the K/V source
   int sbt;              // block-table row of the K/V source
+  int sbt_len;          // context length of that row (bounds the entries read from it)
   int kvh, nrows;
 };
 
@@ -164,6 +166,7 @@ __device__ __forceinline__ void gseg_enter(GCursor& c, const GCtx& x) {
     c.tok0 = 0;
     c.tok_end = x.group_S[c.a];
     c.sbt = c.lo;
+    c.sbt_len = ctx_len(x, c.lo);
     c.kvh = c.b / x.group;
     c.nrows = min(kGroupRows, c.M - kGroupRows * c.c);
     c.nt = c.tok_end / kTileTokens;
@@ -172,6 +175,7 @@ __device__ __forceinline__ void gseg_enter(GCursor& c, const GCtx& x) {
     c.tok0 = seq_prefix(x, c.a);
     c.tok_end = L;
     c.sbt = c.a;
+    c.sbt_len = L;
     c.kvh = (c.b * x.gpw) / x.group;
     c.nrows = x.gpw;
     c.nt = tiles_of(L - c.tok0);
@@ -225,60 +229,331 @@ __device__ __forceinline__ int row_head(const GCursor& c, const GCtx& x, int r) 
   return c.part == 0 ? c.b : c.b * x.gpw + r;
 }
 
-// Second-level merge of row (seq, head): the caller has deposited its
-// result (m, l, o/l) in the row's slot for its part; the second of the two
-// results to arrive merges both and writes the output.
-template <typename T, int D>
-__device__ __forceinline__ void row_merge_tail(const GroupedParams& gp, int seq, int head) {
-  const DecodeParams& p = gp.base;
-  const int lane = threadIdx.x & 31;
-  const size_t row = (size_t)seq * p.num_heads + head;
-  __threadfence();
-  __syncwarp();
-  int last = 0;
-  if (lane == 0) {
-    const int prev = atomicAdd(gp.ws_row_ctr + row, 1);
-    last = prev == 1;
-    if (last) gp.ws_row_ctr[row] = 0;
+// ---- tensor-core q.k for prefix tiles ---------------------------------------
+// m16n8k16 MMA with fp32 accumulation. Only query rows 0..7 are used, so the
+// A registers of rows 8..15 are zero. a_lo / a_hi hold row g's k-positions
+// 2t, 2t+1 and 2t+8, 2t+9; b_lo / b_hi the same k-positions of column g.
+template <typename T>
+struct Mma16816 {
+  static constexpr bool kOk = false;
+  __device__ __forceinline__ static void run(float (&)[4], uint32_t, uint32_t, uint32_t, uint32_t) {}
+  __device__ __forceinline__ static void run2(float&, float&, uint32_t, uint32_t, uint32_t, uint32_t) {}
+  __device__ __forceinline__ static uint32_t pack(float, float) { return 0u; }
+  __device__ __forceinline__ static float2 unpack(uint32_t) { return make_float2(0.f, 0.f); }
+};
+template <>
+struct Mma16816<__nv_bfloat16> {
+  static constexpr bool kOk = true;
+  __device__ __forceinline__ static void run(float (&d)[4], uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                             uint32_t b_hi) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a_lo), "r"(0u), "r"(a_hi), "r"(0u), "r"(b_lo), "r"(b_hi));
   }
-  last = __shfl_sync(kFullMask, last, 0);
-  if (!last) return;
-  __threadfence();
-  constexpr int DL = D / 32;
-  const float2 a = __ldcg(gp.ws_row_ml + row * 2), b = __ldcg(gp.ws_row_ml + row * 2 + 1);
-  const float M = fmaxf(a.x, b.x);
-  const float wa = a.x == -INFINITY ? 0.f : a.y * exp2f(a.x - M);
-  const float wb = b.x == -INFINITY ? 0.f : b.y * exp2f(b.x - M);
-  const float inv = 1.f / (wa + wb);
-  const float* oa = gp.ws_row_o + (row * 2) * D + lane * DL;
-  const float* ob = gp.ws_row_o + (row * 2 + 1) * D + lane * DL;
-  T* orow = static_cast<T*>(p.out) + row * D + lane * DL;
-#pragma unroll
-  for (int e = 0; e < DL; ++e) store_elem(orow + e, (__ldcg(oa + e) * wa + __ldcg(ob + e) * wb) * inv);
+  // rows 0..7 only: accumulators of rows 8..15 are discarded
+  __device__ __forceinline__ static void run2(float& c0, float& c1, uint32_t a_lo, uint32_t a_hi,
+                                              uint32_t b_lo, uint32_t b_hi) {
+    float d2, d3;
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(c0), "=f"(c1), "=f"(d2), "=f"(d3)
+        : "r"(a_lo), "r"(0u), "r"(a_hi), "r"(0u), "r"(b_lo), "r"(b_hi), "f"(c0), "f"(c1), "f"(0.f), "f"(0.f));
+    (void)d2;
+    (void)d3;
+  }
+  __device__ __forceinline__ static uint32_t pack(float x, float y) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    uint32_t u;
+    memcpy(&u, &h, 4);
+    return u;
+  }
+  __device__ __forceinline__ static float2 unpack(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+  }
+};
+template <>
+struct Mma16816<__half> {
+  static constexpr bool kOk = true;
+  __device__ __forceinline__ static void run(float (&d)[4], uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
+                                             uint32_t b_hi) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a_lo), "r"(0u), "r"(a_hi), "r"(0u), "r"(b_lo), "r"(b_hi));
+  }
+  __device__ __forceinline__ static void run2(float& c0, float& c1, uint32_t a_lo, uint32_t a_hi,
+                                              uint32_t b_lo, uint32_t b_hi) {
+    float d2, d3;
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(c0), "=f"(c1), "=f"(d2), "=f"(d3)
+        : "r"(a_lo), "r"(0u), "r"(a_hi), "r"(0u), "r"(b_lo), "r"(b_hi), "f"(c0), "f"(c1), "f"(0.f), "f"(0.f));
+    (void)d2;
+    (void)d3;
+  }
+  __device__ __forceinline__ static uint32_t pack(float x, float y) {
+    const __half2 h = __floats2half2_rn(x, y);
+    uint32_t u;
+    memcpy(&u, &h, 4);
+    return u;
+  }
+  __device__ __forceinline__ static float2 unpack(uint32_t u) {
+    __half2 h;
+    memcpy(&h, &u, 4);
+    return __half22float2(h);
+  }
+};
+
+// Transpose an 8x8 matrix of 16-bit elements held one 32-bit register per
+// lane (lane 4r + c holds row r, columns 2c and 2c+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
 }
 
+// q.k is a sum over head dims, so any permutation of the dims applied to both
+// operands leaves it unchanged. Within each 32-dim chunk, lane t of an MMA
+// group feeds dims [8t, 8t+4) to k-step 0 and [8t+4, 8t+8) to k-step 1, so
+// its K operand for both k-steps of a chunk is one 16-byte shared-memory load
+// of one token row. The query operand uses the same mapping.
+
+// One 16-token tile of a prefix segment, entirely on tensor cores. The query
+// rows (rows < nr of the MMA's M = 16; only rows 0..7 are ever used) are the
+// siblings' queries against one K/V tile.
+//   S = Q K^T: K operand from token rows, head dims permuted as above.
+//   Online softmax on the S accumulators: lane 4r + t holds row r, tokens
+//   2t, 2t+1, 2t+8, 2t+9, so a row's max and sum reduce over its 4 lanes.
+//   O += P V: the S accumulators are already P's A-operand layout (k =
+//   tokens). P is fed as a hi + lo pair of 16-bit values (two MMAs) so that
+//   it keeps ~16 significant bits; V's B operand comes from one 16-byte load
+//   per lane per 32-dim chunk and 16-token half, cut into four 8x8 blocks
+//   over a permutation of the head dims and transposed with movmatrix.
+//   Lane 4r + t ends up with row r, dims [32c + 8t, 32c + 8t + 8) of chunk c
+//   in po[c][0..3][0..1].
 template <typename T, int D>
+__device__ __forceinline__ void mma_prefix_tile(const unsigned char* ks, const unsigned char* vs,
+                                                const uint32_t (&qa)[D / 32][2][2], float (&po)[D / 32][4][2],
+                                                float& pm, float& pl, int nvalid, float scale_log2) {
+  constexpr int ROW = D * (int)sizeof(T);
+  const int lane = threadIdx.x & 31;
+  const int mg = lane >> 2, mt = lane & 3;
+  float s[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const uint4 kk = *reinterpret_cast<const uint4*>(ks + (mg + 8 * nt) * ROW + c * 64 + mt * 16);
+      Mma16816<T>::run(s[nt], qa[c][0][0], qa[c][0][1], kk.x, kk.y);
+      Mma16816<T>::run(s[nt], qa[c][1][0], qa[c][1][1], kk.z, kk.w);
+    }
+  float xs[4], tmax = -INFINITY;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int tok = nt * 8 + 2 * mt + e;
+      xs[nt * 2 + e] = tok < nvalid ? s[nt][e] * scale_log2 : -INFINITY;
+      tmax = fmaxf(tmax, xs[nt * 2 + e]);
+    }
+  tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 1));
+  tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 2));
+  const float mn = fmaxf(pm, tmax);
+  const float alpha = exp2f(pm - mn);  // 0 on the segment's first tile (pm = -inf)
+  float pe[4], psum = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    pe[i] = exp2f(xs[i] - mn);
+    psum += pe[i];
+  }
+  psum += __shfl_xor_sync(kFullMask, psum, 1);
+  psum += __shfl_xor_sync(kFullMask, psum, 2);
+  pl = pl * alpha + psum;
+  pm = mn;
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      po[c][q][0] *= alpha;
+      po[c][q][1] *= alpha;
+    }
+  // P (k = tokens 2t, 2t+1 | 2t+8, 2t+9) as hi + lo 16-bit pairs
+  const uint32_t hi0 = Mma16816<T>::pack(pe[0], pe[1]);
+  const uint32_t hi1 = Mma16816<T>::pack(pe[2], pe[3]);
+  const float2 h0 = Mma16816<T>::unpack(hi0), h1 = Mma16816<T>::unpack(hi1);
+  const uint32_t lo0 = Mma16816<T>::pack(pe[0] - h0.x, pe[1] - h0.y);
+  const uint32_t lo1 = Mma16816<T>::pack(pe[2] - h1.x, pe[3] - h1.y);
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint4 v0 = *reinterpret_cast<const uint4*>(vs + mg * ROW + c * 64 + mt * 16);        // token mg
+    uint4 v1 = *reinterpret_cast<const uint4*>(vs + (mg + 8) * ROW + c * 64 + mt * 16);  // token mg + 8
+    if (mg >= nvalid) v0 = make_uint4(0u, 0u, 0u, 0u);  // rows past the context may hold poison
+    if (mg + 8 >= nvalid) v1 = make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
+    const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint32_t b_lo = movmatrix_trans(w0[q]);
+      const uint32_t b_hi = movmatrix_trans(w1[q]);
+      Mma16816<T>::run2(po[c][q][0], po[c][q][1], hi0, hi1, b_lo, b_hi);
+      Mma16816<T>::run2(po[c][q][0], po[c][q][1], lo0, lo1, b_lo, b_hi);
+    }
+  }
+}
+
+// One 16-token tile on CUDA cores for NR query rows against one K/V tile
+// (rows >= nr skipped when PRED): the same math as the plain kernel.
+template <typename T, int D, int QR, int NR, bool PRED, int ORows>
+__device__ __forceinline__ void core_tile(const unsigned char* ks, const unsigned char* vs,
+                                          const float (&qf)[QR][D / 8], float (&o)[ORows][D / 8],
+                                          float (&m)[ORows], float (&l)[ORows], int nvalid, int nr) {
+  constexpr int ROW = D * (int)sizeof(T);
+  constexpr int VEC = Chunk<T>::kElems;
+  constexpr int CPL = ROW / 16 / 8;
+  const int lane = threadIdx.x & 31;
+  const int grp = lane >> 3, sub = lane & 7;
+  float x4[NR][4];
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 4 + grp;
+    const uint4* krow = reinterpret_cast<const uint4*>(ks + r * ROW);
+    float acc[NR];
+#pragma unroll
+    for (int g = 0; g < NR; ++g) acc[g] = 0.f;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) {
+      float f[VEC];
+      Chunk<T>::widen(krow[sub + 8 * k], f);
+#pragma unroll
+      for (int g = 0; g < NR; ++g)
+        if (!PRED || g < nr) {
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[g] = fmaf(qf[g][k * VEC + e], f[e], acc[g]);
+        }
+    }
+#pragma unroll
+    for (int g = 0; g < NR; ++g)
+      if (!PRED || g < nr) {
+        float a = acc[g];
+        a += __shfl_xor_sync(kFullMask, a, 1);
+        a += __shfl_xor_sync(kFullMask, a, 2);
+        a += __shfl_xor_sync(kFullMask, a, 4);
+        x4[g][it] = r < nvalid ? a : -INFINITY;
+      }
+  }
+  float pw[NR][4];
+#pragma unroll
+  for (int g = 0; g < NR; ++g)
+    if (!PRED || g < nr) {
+      float mt = fmaxf(fmaxf(x4[g][0], x4[g][1]), fmaxf(x4[g][2], x4[g][3]));
+      mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
+      mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
+      const float mn = fmaxf(m[g], mt);
+      const float alpha = exp2f(m[g] - mn);
+      float ps = 0.f;
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        pw[g][it] = exp2f(x4[g][it] - mn);
+        ps += pw[g][it];
+      }
+      l[g] = l[g] * alpha + ps;
+#pragma unroll
+      for (int e = 0; e < D / 8; ++e) o[g][e] *= alpha;
+      m[g] = mn;
+    }
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int r = it * 4 + grp;
+    if (r < nvalid) {
+      const uint4* vrow = reinterpret_cast<const uint4*>(vs + r * ROW);
+#pragma unroll
+      for (int k = 0; k < CPL; ++k) {
+        float f[VEC];
+        Chunk<T>::widen(vrow[sub + 8 * k], f);
+#pragma unroll
+        for (int g = 0; g < NR; ++g)
+          if (!PRED || g < nr) {
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) o[g][k * VEC + e] = fmaf(pw[g][it], f[e], o[g][k * VEC + e]);
+          }
+      }
+    }
+  }
+}
+
+// ---- grid-wide phase barrier (the grid is co-resident: cooperative launch) --
+// Called by the whole warp: every lane's earlier writes are made visible
+// before lane 0 counts the warp in.
+__device__ __forceinline__ void arrive_gpu(int32_t* ctr) {
+  __threadfence();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(1) : "memory");
+}
+
+__device__ __forceinline__ int load_acquire_gpu(const int32_t* ctr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+  return v;
+}
+
+// Lane 0 waits until *ctr >= target, for at most limit_ns; false if it ran out.
+__device__ __forceinline__ bool wait_count(const int32_t* ctr, int target, uint64_t limit_ns) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0 && load_acquire_gpu(ctr) < target) {
+    const uint64_t t0 = globaltimer_ns();
+    while (load_acquire_gpu(ctr) < target) {
+      if (globaltimer_ns() - t0 >= limit_ns) {
+        ok = 0;
+        break;
+      }
+      __nanosleep(256);
+    }
+  }
+  ok = __shfl_sync(kFullMask, ok, 0);
+  __threadfence();
+  return ok != 0;
+}
+
+// Two phases over the same persistent warps: first every prefix segment
+// (balanced over all warps), then every tail segment (balanced again). A
+// warp starts fetching its tail tiles before the phase barrier; only the end
+// of a tail visit — which needs the row's prefix result — waits for it.
+template <typename T, int D, int TG>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     pa_decode_grouped_kernel(const GroupedParams gp) {
   using S = DecodeShape<T, D, kGroupRows>;
   constexpr int NW = kDecodeWarps;
   constexpr int R = kGroupRows;
+  constexpr bool kMma = Mma16816<T>::kOk;
+  constexpr int QR = kMma ? TG : R;  // query rows kept in fp32 registers
+  constexpr int OR = kMma ? TG : R;  // rows of the CUDA-core accumulators
   constexpr int ST = S::kStages;
   constexpr int DPL = S::kDimsPerLane;
   constexpr int CPL = S::kChunksPerLane;
   constexpr int VEC = S::kVec;
   constexpr int ROW = S::kRowBytes;
+  constexpr int DL = D / 32;  // dims per lane in merges
   const DecodeParams& p = gp.base;
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
   long long* scan = reinterpret_cast<long long*>(smem + S::kScanOff);
-  longlong2* starts = reinterpret_cast<longlong2*>(smem + S::kStartOff);
+  __shared__ longlong2 starts[2 * NW];  // per phase: (group or sequence, offset)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int grp = lane >> 3;
   const int sub = lane & 7;
+  const int mg = lane >> 2, mt = lane & 3;
   const int bs = p.block_size;
   GCtx x;
   x.group_start = gp.group_start;
@@ -294,27 +569,23 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   x.cap = min(p.max_context_len, p.max_blocks_per_seq * bs);
   x.gpw = p.num_heads / p.head_groups;
   x.use_groups = __ldcg(gp.ws_flag) == 0;
-  const int B = p.num_seqs, G = gp.num_groups, HG = p.head_groups;
+  const int B = p.num_seqs, G = gp.num_groups, HG = p.head_groups, H = p.num_heads;
 
-  // ---- start-up: tiles of both parts, then each warp's first segment --------
+  // ---- start-up: tiles of both phases, then each warp's first segment --------
   long long mine = 0;
   for (int g = threadIdx.x; g < G; g += NW * 32) mine += prefix_tiles(x, g);
   long long TA;
   block_exclusive_scan(mine, scan, TA);
   mine = 0;
-  for (int s = threadIdx.x; s < B; s += NW * 32)
-    mine += (long long)HG * tiles_of(ctx_len(x, s) - seq_prefix(x, s));
+  for (int s = threadIdx.x; s < B; s += NW * 32) mine += (long long)HG * tiles_of(ctx_len(x, s) - seq_prefix(x, s));
   long long TB;
   block_exclusive_scan(mine, scan, TB);
-  const long long Ttot = TA + TB;
   const long long W = (long long)gridDim.x * NW;
-  const long long Weff = W < Ttot ? W : Ttot;
+  const long long WA = W < TA ? W : TA;  // 0 when no group shares a prefix
+  const long long WB = W < TB ? W : TB;
   const long long wid = (long long)blockIdx.x * NW + warp;
-  const long long a_begin = wid < Weff ? wid * Ttot / Weff : Ttot;
-  const long long a_end = wid < Weff ? (wid + 1) * Ttot / Weff : Ttot;
-  if (threadIdx.x < NW) starts[threadIdx.x] = make_longlong2(-1, 0);
+  if (threadIdx.x < 2 * NW) starts[threadIdx.x] = make_longlong2(-1, 0);
   __syncthreads();
-  // starts[i].x: group (prefix part) or B + sequence (tail part); .y: offset in it
   long long carry = 0;
   for (int base = 0; base < G; base += NW * 32) {
     const int g = base + threadIdx.x;
@@ -324,32 +595,30 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 #pragma unroll
     for (int i = 0; i < NW; ++i) {
       const long long w = (long long)blockIdx.x * NW + i;
-      if (w < Weff) {
-        const long long a = w * Ttot / Weff;
+      if (w < WA) {
+        const long long a = w * TA / WA;
         if (cnt > 0 && a >= excl && a < excl + cnt) starts[i] = make_longlong2(g, a - excl);
       }
     }
     carry += tot;
   }
-  carry = TA;
+  carry = 0;
   for (int base = 0; base < B; base += NW * 32) {
     const int s = base + threadIdx.x;
-    const long long cnt =
-        s < B ? (long long)HG * tiles_of(ctx_len(x, s) - seq_prefix(x, s)) : 0;
+    const long long cnt = s < B ? (long long)HG * tiles_of(ctx_len(x, s) - seq_prefix(x, s)) : 0;
     long long tot;
     const long long excl = carry + block_exclusive_scan(cnt, scan, tot);
 #pragma unroll
     for (int i = 0; i < NW; ++i) {
       const long long w = (long long)blockIdx.x * NW + i;
-      if (w < Weff) {
-        const long long a = w * Ttot / Weff;
-        if (cnt > 0 && a >= excl && a < excl + cnt) starts[i] = make_longlong2((long long)G + s, a - excl);
+      if (w < WB) {
+        const long long a = w * TB / WB;
+        if (cnt > 0 && a >= excl && a < excl + cnt) starts[NW + i] = make_longlong2(s, a - excl);
       }
     }
     carry += tot;
   }
-  __syncthreads();
-  if (a_begin >= a_end) return;  // idle warp; no block barrier follows
+  __syncthreads();  // the last block-wide barrier
 
   unsigned char* my_ring = smem + warp * ST * S::kStageBytes;
   uint64_t* my_bars = bars + warp * ST;
@@ -361,353 +630,390 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   }
   __syncwarp();
 
-  GCursor ci;
-  {
-    const longlong2 st0 = starts[warp];
-    ci.g = a_begin;
-    ci.c = 0;
-    if (st0.x < G) {
-      ci.part = 0;
-      ci.a = static_cast<int>(st0.x);
-      ci.b = 0;
-      gseg_enter(ci, x);  // sets M and nt (nt does not depend on b or c)
-      const long long per_seg = ci.nt;
-      const long long seg = st0.y / per_seg;
-      ci.t = static_cast<int>(st0.y % per_seg);
-      ci.b = static_cast<int>(seg / group_rows(ci.M));
-      ci.c = static_cast<int>(seg % group_rows(ci.M));
-      gseg_enter(ci, x);
-    } else {
-      ci.part = 1;
-      ci.a = static_cast<int>(st0.x - G);
-      ci.b = 0;
-      gseg_enter(ci, x);
-      ci.b = static_cast<int>(st0.y / ci.nt);
-      ci.t = static_cast<int>(st0.y % ci.nt);
-      gseg_enter(ci, x);
-    }
-  }
-  GCursor cc = ci;
-  int bt_s = -1, bt_j0 = 0;
-
   const char* kbase = static_cast<const char*>(p.k_cache);
   const char* vbase = static_cast<const char*>(p.v_cache);
   const char* qbase = static_cast<const char*>(p.q);
   const int seg = bs < kTileTokens ? bs : kTileTokens;
   const int nseg = kTileTokens / seg;
-  const int H = p.num_heads;
+  int32_t* sync_arrive = gp.ws_sync;
+  int32_t* sync_exit = gp.ws_sync + 1;
+  int bt_s = -1, bt_j0 = 0;
+  int ring = 0;  // tiles this warp has consumed so far (ring position)
+  bool failed = false, synced = false;
 
-  auto issue = [&](const GCursor& c, int n) {
-    const int t0 = c.tok0 + c.t * kTileTokens;
-    const int nvalid = min(max(c.tok_end - t0, 0), kTileTokens);
-    const bool with_q = (c.t == 0 || c.g == a_begin) && nvalid > 0;
-    if (nvalid > 0) {
-      const int j_first = t0 / bs;
-      const int j_last = (t0 + nvalid - 1) / bs;
-      if (c.sbt != bt_s || j_first < bt_j0 || j_last >= bt_j0 + kBtChunk) {
-        const int nblk = (c.tok_end + bs - 1) / bs;
-        const int32_t* row = p.block_tables + (size_t)c.sbt * p.max_blocks_per_seq;
-        __syncwarp();
-        for (int i = lane; i < kBtChunk; i += 32) {
-          const int j = j_first + i;
-          int id = 0;
-          if (j < nblk) {
-            id = __ldg(row + j);
-            if (id < 0 || id >= p.num_blocks) {
-              set_err(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
-              id = 0;
-            }
-          }
-          my_bt[i] = id;
-        }
-        __syncwarp();
-        bt_s = c.sbt;
-        bt_j0 = j_first;
-      }
-    }
-    if (lane == 0) {
-      unsigned char* kdst = my_ring + (n % ST) * S::kStageBytes;
-      unsigned char* vdst = kdst + S::kTileBytes;
-      unsigned char* qdst = kdst + 2 * S::kTileBytes;
-      uint64_t* bar = my_bars + (n % ST);
-      uint32_t bytes = with_q ? c.nrows * ROW : 0;
-      for (int c2 = 0; c2 < nseg; ++c2)
-        if (t0 + c2 * seg < c.tok_end) bytes += 2u * seg * ROW;
-      mbar_arrive_expect_tx(bar, bytes);
-      for (int c2 = 0; c2 < nseg; ++c2) {
-        const int t = t0 + c2 * seg;
-        if (t >= c.tok_end) break;
-        const size_t off =
-            (((size_t)my_bt[t / bs - bt_j0] * p.num_kv_heads + c.kvh) * bs + (t % bs)) * ROW;
-        bulk_copy_g2s(kdst + c2 * seg * ROW, kbase + off, seg * ROW, bar);
-        bulk_copy_g2s(vdst + c2 * seg * ROW, vbase + off, seg * ROW, bar);
-      }
-      if (with_q) {
-        if (c.part == 1) {
-          bulk_copy_g2s(qdst, qbase + ((size_t)c.a * H + (size_t)c.b * c.nrows) * ROW, c.nrows * ROW, bar);
+  float qf[QR][DPL];
+  uint32_t qa[D / 32][2][2];        // prefix query rows as MMA A-operands (16-bit types)
+  float m[OR], l[OR], o[OR][DPL];   // CUDA-core state (tails; prefixes of fp32 data)
+  float pm = -INFINITY, pl = 0.f;   // tensor-core state of a prefix: row mg
+  float po[D / 32][4][2];
+
+  for (int phase = 0; phase < 2; ++phase) {
+    const long long Tp = phase == 0 ? TA : TB, Wp = phase == 0 ? WA : WB;
+    const long long a_begin = wid < Wp ? wid * Tp / Wp : Tp;
+    const long long a_end = wid < Wp ? (wid + 1) * Tp / Wp : Tp;
+    if (!failed && a_begin < a_end) {
+      GCursor ci;
+      {
+        const longlong2 st0 = starts[phase * NW + warp];
+        ci.g = a_begin;
+        ci.part = phase;
+        ci.a = static_cast<int>(st0.x);
+        ci.b = 0;
+        ci.c = 0;
+        gseg_enter(ci, x);  // nt does not depend on b or c
+        const long long seg_idx = st0.y / ci.nt;
+        ci.t = static_cast<int>(st0.y % ci.nt);
+        if (phase == 0) {
+          ci.b = static_cast<int>(seg_idx / group_rows(ci.M));
+          ci.c = static_cast<int>(seg_idx % group_rows(ci.M));
         } else {
-          for (int r = 0; r < c.nrows; ++r)
-            bulk_copy_g2s(qdst + r * ROW, qbase + ((size_t)row_seq(c, r) * H + c.b) * ROW, ROW, bar);
+          ci.b = static_cast<int>(seg_idx);
         }
+        gseg_enter(ci, x);
       }
-    }
-  };
+      GCursor cc = ci;
 
-  int issued = 0;
-  for (; issued < ST && ci.g < a_end; ++issued) {
-    issue(ci, issued);
-    gcursor_next(ci, x);
-  }
-
-  float qf[R][DPL];
-  float m[R], l[R], o[R][DPL];
-  bool visit_from_start = true;
-
-  for (int n = 0; cc.g < a_end; ++n) {
-    if (!__all_sync(kFullMask, mbar_wait_bounded(my_bars + (n % ST), (n / ST) & 1, p.wait_limit_ns))) {
-      if (lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-      for (int k2 = n; k2 < issued; ++k2) mbar_wait_bounded(my_bars + (k2 % ST), (k2 / ST) & 1, kDrainLimitNs);
-      return;
-    }
-    const unsigned char* ks = my_ring + (n % ST) * S::kStageBytes;
-    const unsigned char* vs = ks + S::kTileBytes;
-    const int t0 = cc.tok0 + cc.t * kTileTokens;
-    const int nvalid = min(max(cc.tok_end - t0, 0), kTileTokens);
-    const bool first = cc.t == 0 || cc.g == a_begin;
-    const bool last = cc.t == cc.nt - 1 || cc.g == a_end - 1;
-    const int nr = cc.nrows;
-
-    if (first) {
-      visit_from_start = cc.t == 0;
-#pragma unroll
-      for (int g = 0; g < R; ++g) {
-        m[g] = -INFINITY;
-        l[g] = 0.f;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) o[g][e] = 0.f;
-      }
-      if (nvalid > 0) {
-        const unsigned char* qs = ks + 2 * S::kTileBytes;
-#pragma unroll
-        for (int g = 0; g < R; ++g) {
-          if (g < nr) {
-            const uint4* qrow = reinterpret_cast<const uint4*>(qs + g * ROW);
-#pragma unroll
-            for (int k = 0; k < CPL; ++k) {
-              float f[VEC];
-              Chunk<T>::widen(qrow[sub + 8 * k], f);
-#pragma unroll
-              for (int e = 0; e < VEC; ++e) qf[g][k * VEC + e] = f[e] * p.scale_log2;
-            }
-          }
-        }
-      }
-    }
-
-    if (nvalid > 0) {
-      float x4[R][4];
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int r = it * 4 + grp;
-        const uint4* krow = reinterpret_cast<const uint4*>(ks + r * ROW);
-        float acc[R];
-#pragma unroll
-        for (int g = 0; g < R; ++g) acc[g] = 0.f;
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) {
-          float f[VEC];
-          Chunk<T>::widen(krow[sub + 8 * k], f);
-#pragma unroll
-          for (int g = 0; g < R; ++g)
-            if (g < nr) {
-#pragma unroll
-              for (int e = 0; e < VEC; ++e) acc[g] = fmaf(qf[g][k * VEC + e], f[e], acc[g]);
-            }
-        }
-#pragma unroll
-        for (int g = 0; g < R; ++g)
-          if (g < nr) {
-            float a = acc[g];
-            a += __shfl_xor_sync(kFullMask, a, 1);
-            a += __shfl_xor_sync(kFullMask, a, 2);
-            a += __shfl_xor_sync(kFullMask, a, 4);
-            x4[g][it] = r < nvalid ? a : -INFINITY;
-          }
-      }
-      float pw[R][4];
-#pragma unroll
-      for (int g = 0; g < R; ++g)
-        if (g < nr) {
-          float mt = fmaxf(fmaxf(x4[g][0], x4[g][1]), fmaxf(x4[g][2], x4[g][3]));
-          mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
-          mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
-          const float mn = fmaxf(m[g], mt);
-          const float alpha = exp2f(m[g] - mn);
-          float ps = 0.f;
-#pragma unroll
-          for (int it = 0; it < 4; ++it) {
-            pw[g][it] = exp2f(x4[g][it] - mn);
-            ps += pw[g][it];
-          }
-          l[g] = l[g] * alpha + ps;
-#pragma unroll
-          for (int e = 0; e < DPL; ++e) o[g][e] *= alpha;
-          m[g] = mn;
-        }
-#pragma unroll
-      for (int it = 0; it < 4; ++it) {
-        const int r = it * 4 + grp;
-        if (r < nvalid) {
-          const uint4* vrow = reinterpret_cast<const uint4*>(vs + r * ROW);
-#pragma unroll
-          for (int k = 0; k < CPL; ++k) {
-            float f[VEC];
-            Chunk<T>::widen(vrow[sub + 8 * k], f);
-#pragma unroll
-            for (int g = 0; g < R; ++g)
-              if (g < nr) {
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) o[g][k * VEC + e] = fmaf(pw[g][it], f[e], o[g][k * VEC + e]);
+      auto issue = [&](const GCursor& c, int n) {
+        const int t0 = c.tok0 + c.t * kTileTokens;
+        const int nvalid = min(max(c.tok_end - t0, 0), kTileTokens);
+        const bool with_q = (c.t == 0 || c.g == a_begin) && nvalid > 0;
+        if (nvalid > 0) {
+          const int j_first = t0 / bs;
+          const int j_last = (t0 + nvalid - 1) / bs;
+          if (c.sbt != bt_s || j_first < bt_j0 || j_last >= bt_j0 + kBtChunk) {
+            // entries of the row's whole context: the chunk then serves any
+            // segment that reads this row (prefix or tail)
+            const int nblk = (c.sbt_len + bs - 1) / bs;
+            const int32_t* row = p.block_tables + (size_t)c.sbt * p.max_blocks_per_seq;
+            __syncwarp();
+            for (int i = lane; i < kBtChunk; i += 32) {
+              const int j = j_first + i;
+              int id = 0;
+              if (j < nblk) {
+                id = __ldg(row + j);
+                if (id < 0 || id >= p.num_blocks) {
+                  set_err(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
+                  id = 0;
+                }
               }
+              my_bt[i] = id;
+            }
+            __syncwarp();
+            bt_s = c.sbt;
+            bt_j0 = j_first;
           }
         }
-      }
-    }
-    __syncwarp();
-    if (ci.g < a_end) {
-      issue(ci, issued++);
-      gcursor_next(ci, x);
-    }
+        if (lane == 0) {
+          unsigned char* kdst = my_ring + (n % ST) * S::kStageBytes;
+          unsigned char* vdst = kdst + S::kTileBytes;
+          unsigned char* qdst = kdst + 2 * S::kTileBytes;
+          uint64_t* bar = my_bars + (n % ST);
+          uint32_t bytes = with_q ? c.nrows * ROW : 0;
+          for (int c2 = 0; c2 < nseg; ++c2)
+            if (t0 + c2 * seg < c.tok_end) bytes += 2u * seg * ROW;
+          mbar_arrive_expect_tx(bar, bytes);
+          for (int c2 = 0; c2 < nseg; ++c2) {
+            const int t = t0 + c2 * seg;
+            if (t >= c.tok_end) break;
+            const size_t off =
+                (((size_t)my_bt[t / bs - bt_j0] * p.num_kv_heads + c.kvh) * bs + (t % bs)) * ROW;
+            bulk_copy_g2s(kdst + c2 * seg * ROW, kbase + off, seg * ROW, bar);
+            bulk_copy_g2s(vdst + c2 * seg * ROW, vbase + off, seg * ROW, bar);
+          }
+          if (with_q) {
+            if (c.part == 1) {
+              bulk_copy_g2s(qdst, qbase + ((size_t)c.a * H + (size_t)c.b * c.nrows) * ROW, c.nrows * ROW, bar);
+            } else {
+              for (int r = 0; r < c.nrows; ++r)
+                bulk_copy_g2s(qdst + r * ROW, qbase + ((size_t)row_seq(c, r) * H + c.b) * ROW, ROW, bar);
+            }
+          }
+        }
+      };
 
-    if (last) {
+      int issued = ring;
+      for (; issued < ring + ST && ci.g < a_end; ++issued) {
+        issue(ci, issued);
+        gcursor_next(ci, x);
+      }
+      bool visit_from_start = true;
+
+      for (; cc.g < a_end; ++ring) {
+        if (!__all_sync(kFullMask, mbar_wait_bounded(my_bars + (ring % ST), (ring / ST) & 1, p.wait_limit_ns))) {
+          if (lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+          for (int k2 = ring; k2 < issued; ++k2)
+            mbar_wait_bounded(my_bars + (k2 % ST), (k2 / ST) & 1, kDrainLimitNs);
+          failed = true;
+          break;
+        }
+        const unsigned char* ks = my_ring + (ring % ST) * S::kStageBytes;
+        const unsigned char* vs = ks + S::kTileBytes;
+        const int t0 = cc.tok0 + cc.t * kTileTokens;
+        const int nvalid = min(max(cc.tok_end - t0, 0), kTileTokens);
+        const bool first = cc.t == 0 || cc.g == a_begin;
+        const bool last = cc.t == cc.nt - 1 || cc.g == a_end - 1;
+        const int nr = cc.nrows;
+        const bool tc_prefix = kMma && phase == 0;  // state in the tensor-core layout
+
+        if (first) {
+          visit_from_start = cc.t == 0;
+          pm = -INFINITY;
+          pl = 0.f;
 #pragma unroll
-      for (int g = 0; g < R; ++g)
-        if (g < nr) {
-          l[g] += __shfl_xor_sync(kFullMask, l[g], 8);
-          l[g] += __shfl_xor_sync(kFullMask, l[g], 16);
+          for (int c = 0; c < D / 32; ++c)
 #pragma unroll
-          for (int e = 0; e < DPL; ++e) {
-            o[g][e] += __shfl_xor_sync(kFullMask, o[g][e], 8);
-            o[g][e] += __shfl_xor_sync(kFullMask, o[g][e], 16);
+            for (int q = 0; q < 4; ++q) po[c][q][0] = po[c][q][1] = 0.f;
+#pragma unroll
+          for (int g = 0; g < OR; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[g][e] = 0.f;
+          }
+          if (nvalid > 0) {
+            const unsigned char* qs = ks + 2 * S::kTileBytes;
+            if (tc_prefix) {
+#pragma unroll
+              for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                  const int d0 = c * 32 + 8 * mt + 4 * j;  // dims d0, d0+1 | d0+2, d0+3 (see Mma16816)
+                  const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qs + mg * ROW);
+                  qa[c][j][0] = mg < nr ? qrow[d0 / 2] : 0u;
+                  qa[c][j][1] = mg < nr ? qrow[d0 / 2 + 1] : 0u;
+                }
+            } else {
+#pragma unroll
+              for (int g = 0; g < QR; ++g) {
+                if (g < nr) {
+                  const uint4* qrow = reinterpret_cast<const uint4*>(qs + g * ROW);
+#pragma unroll
+                  for (int k = 0; k < CPL; ++k) {
+                    float f[VEC];
+                    Chunk<T>::widen(qrow[sub + 8 * k], f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) qf[g][k * VEC + e] = f[e] * p.scale_log2;
+                  }
+                }
+              }
+            }
           }
         }
-      // a row has two results when its sequence has a shared prefix
-      const bool two_source = cc.part == 0 || cc.tok0 > 0;
-      if (visit_from_start && cc.t == cc.nt - 1) {
+
+        if (nvalid > 0) {
+          if (phase == 1) {
+            core_tile<T, D, QR, TG, false, OR>(ks, vs, qf, o, m, l, nvalid, TG);
+          } else if constexpr (kMma) {
+            mma_prefix_tile<T, D>(ks, vs, qa, po, pm, pl, nvalid, p.scale_log2);
+          } else {
+            core_tile<T, D, QR, R, true, OR>(ks, vs, qf, o, m, l, nvalid, nr);
+          }
+        }
+        __syncwarp();
+        if (ci.g < a_end) {
+          issue(ci, issued++);
+          gcursor_next(ci, x);
+        }
+
+        if (last) {
+          // ---- end of this warp's visit of the segment under cc --------------
+          if (phase == 1 && !synced) {
+            // prefix results, and the partial slots phase 0 used, are settled
+            synced = wait_count(sync_arrive, (int)W, p.wait_limit_ns);
+            if (!synced && lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+            synced = true;
+          }
 #pragma unroll
-        for (int g = 0; g < R; ++g) {
-          if (g >= nr) continue;
-          const int seq = row_seq(cc, g), head = row_head(cc, x, g);
-          const size_t row = (size_t)seq * H + head;
-          const float inv = l[g] > 0.f ? 1.f / l[g] : 0.f;
-          if (!two_source) {
-            if (grp == 0) {
-              uint4* orow = reinterpret_cast<uint4*>(static_cast<char*>(p.out) + row * ROW);
+          for (int g = 0; g < OR; ++g)
+            if (!tc_prefix && g < nr) {
+              l[g] += __shfl_xor_sync(kFullMask, l[g], 8);
+              l[g] += __shfl_xor_sync(kFullMask, l[g], 16);
 #pragma unroll
-              for (int k = 0; k < CPL; ++k) {
-                float f[VEC];
+              for (int e = 0; e < DPL; ++e) {
+                o[g][e] += __shfl_xor_sync(kFullMask, o[g][e], 8);
+                o[g][e] += __shfl_xor_sync(kFullMask, o[g][e], 16);
+              }
+            }
+          // phase 1 rows of a sequence with a shared prefix merge with its result
+          const bool with_prefix = phase == 1 && cc.tok0 > 0;
+          const bool whole = visit_from_start && cc.t == cc.nt - 1;
+          if (whole && tc_prefix) {
+            // prefix result of each sibling row (rows are quads of lanes)
+            if (mg < nr) {
+              const size_t row = (size_t)row_seq(cc, mg) * H + row_head(cc, x, mg);
+              const float inv = 1.f / pl;
+              float4* dst = reinterpret_cast<float4*>(gp.ws_row_o + row * D);
 #pragma unroll
-                for (int e = 0; e < VEC; ++e) f[e] = o[g][k * VEC + e] * inv;
-                orow[sub + 8 * k] = Chunk<T>::narrow(f);
+              for (int c = 0; c < D / 32; ++c) {
+                dst[(c * 32 + 8 * mt) / 4] = make_float4(po[c][0][0] * inv, po[c][0][1] * inv,
+                                                         po[c][1][0] * inv, po[c][1][1] * inv);
+                dst[(c * 32 + 8 * mt) / 4 + 1] = make_float4(po[c][2][0] * inv, po[c][2][1] * inv,
+                                                             po[c][3][0] * inv, po[c][3][1] * inv);
+              }
+              if (mt == 0) gp.ws_row_ml[row] = make_float2(pm, pl);
+            }
+          } else if (whole) {
+#pragma unroll
+            for (int g = 0; g < OR; ++g) {
+              if (g >= nr) continue;
+              const size_t row = (size_t)row_seq(cc, g) * H + row_head(cc, x, g);
+              if (phase == 0) {  // prefix result (fp32 data)
+                const float inv = 1.f / l[g];
+                if (grp == 0) {
+                  float4* dst = reinterpret_cast<float4*>(gp.ws_row_o + row * D);
+#pragma unroll
+                  for (int k = 0; k < CPL; ++k)
+#pragma unroll
+                    for (int e = 0; e < VEC; e += 4)
+                      dst[((sub + 8 * k) * VEC + e) / 4] =
+                          make_float4(o[g][k * VEC + e] * inv, o[g][k * VEC + e + 1] * inv,
+                                      o[g][k * VEC + e + 2] * inv, o[g][k * VEC + e + 3] * inv);
+                }
+                if (lane == 0) gp.ws_row_ml[row] = make_float2(m[g], l[g]);
+                continue;
+              }
+              float w_own = 1.f, w_pre = 0.f, denom = l[g];
+              if (with_prefix) {
+                const float2 pr = __ldcg(gp.ws_row_ml + row);
+                const float M = fmaxf(m[g], pr.x);
+                w_own = m[g] == -INFINITY ? 0.f : exp2f(m[g] - M);
+                w_pre = pr.y * exp2f(pr.x - M);
+                denom = l[g] * w_own + w_pre;
+              }
+              const float inv = denom > 0.f ? 1.f / denom : 0.f;
+              if (grp == 0) {
+                uint4* orow = reinterpret_cast<uint4*>(static_cast<char*>(p.out) + row * ROW);
+                const float* pre = gp.ws_row_o + row * D;
+#pragma unroll
+                for (int k = 0; k < CPL; ++k) {
+                  float f[VEC];
+#pragma unroll
+                  for (int e = 0; e < VEC; ++e) {
+                    const float pv = with_prefix ? __ldcg(pre + (sub + 8 * k) * VEC + e) : 0.f;
+                    f[e] = (o[g][k * VEC + e] * w_own + pv * w_pre) * inv;
+                  }
+                  orow[sub + 8 * k] = Chunk<T>::narrow(f);
+                }
               }
             }
           } else {
-            const size_t slot = row * 2 + cc.part;
-            if (grp == 0) {
-              float4* po = reinterpret_cast<float4*>(gp.ws_row_o + slot * D);
+            // one piece of a segment shared with neighbouring warps
+            const long long Wq = Wp, Tq = Tp;
+            const int slot = cc.g - cc.t <= a_begin ? 0 : 1;
+            const size_t base = ((size_t)wid * 2 + slot) * R;
+            if (tc_prefix) {
+              if (mg < nr) {
+                const float inv = 1.f / pl;
+                float4* dst = reinterpret_cast<float4*>(p.ws_o + (base + mg) * D);
 #pragma unroll
-              for (int k = 0; k < CPL; ++k)
-#pragma unroll
-                for (int e = 0; e < VEC; e += 4)
-                  po[((sub + 8 * k) * VEC + e) / 4] =
-                      make_float4(o[g][k * VEC + e] * inv, o[g][k * VEC + e + 1] * inv,
-                                  o[g][k * VEC + e + 2] * inv, o[g][k * VEC + e + 3] * inv);
-            }
-            if (lane == 0) gp.ws_row_ml[slot] = make_float2(m[g], l[g]);
-            row_merge_tail<T, D>(gp, seq, head);
-          }
-        }
-      } else {
-        const int slot = cc.g - cc.t <= a_begin ? 0 : 1;
-        const size_t base = ((size_t)wid * 2 + slot) * R;
-#pragma unroll
-        for (int g = 0; g < R; ++g) {
-          if (g >= nr) continue;
-          const float inv = 1.f / l[g];
-          if (grp == 0) {
-            float4* po = reinterpret_cast<float4*>(p.ws_o + (base + g) * D);
-#pragma unroll
-            for (int k = 0; k < CPL; ++k)
-#pragma unroll
-              for (int e = 0; e < VEC; e += 4)
-                po[((sub + 8 * k) * VEC + e) / 4] =
-                    make_float4(o[g][k * VEC + e] * inv, o[g][k * VEC + e + 1] * inv,
-                                o[g][k * VEC + e + 2] * inv, o[g][k * VEC + e + 3] * inv);
-          }
-          if (lane == 0) p.ws_ml[base + g] = make_float2(m[g], l[g]);
-        }
-        __threadfence();
-        __syncwarp();
-        const long long seg_start = cc.g - cc.t;
-        const long long seg_end = seg_start + cc.nt;
-        const long long w_first = ((seg_start + 1) * Weff + Ttot - 1) / Ttot - 1;
-        const long long w_last = (seg_end * Weff + Ttot - 1) / Ttot - 1;
-        int is_last = 0;
-        if (lane == 0) {
-          const size_t ci_idx = cc.part == 0 ? (size_t)(cc.lo + kGroupRows * cc.c) * H + cc.b
-                                             : (size_t)B * H + (size_t)cc.a * HG + cc.b;
-          int32_t* ctr = gp.ws_seg_ctr + ci_idx;
-          const int prev = atomicAdd(ctr, 1);
-          is_last = prev == (int)(w_last - w_first);
-          if (is_last) *ctr = 0;
-        }
-        is_last = __shfl_sync(kFullMask, is_last, 0);
-        if (is_last) {
-          __threadfence();
-          constexpr int DL = D / 32;
-          for (int g = 0; g < nr; ++g) {
-            float M = -INFINITY;
-            for (long long w = w_first; w <= w_last; ++w) {
-              const int sl = (w == w_first && w * Ttot / Weff < seg_start) ? 1 : 0;
-              M = fmaxf(M, __ldcg(p.ws_ml + ((size_t)w * 2 + sl) * R + g).x);
-            }
-            float Ls = 0.f, O[DL];
-#pragma unroll
-            for (int e = 0; e < DL; ++e) O[e] = 0.f;
-            for (long long w = w_first; w <= w_last; ++w) {
-              const int sl = (w == w_first && w * Ttot / Weff < seg_start) ? 1 : 0;
-              const size_t idx = ((size_t)w * 2 + sl) * R + g;
-              const float2 v = __ldcg(p.ws_ml + idx);
-              const float wt = v.y * exp2f(v.x - M);
-              Ls += wt;
-              const float* po = p.ws_o + idx * D + lane * DL;
-#pragma unroll
-              for (int e = 0; e < DL; ++e) O[e] += __ldcg(po + e) * wt;
-            }
-            const int seq = row_seq(cc, g), head = row_head(cc, x, g);
-            const size_t row = (size_t)seq * H + head;
-            if (!two_source) {
-              T* orow = static_cast<T*>(p.out) + row * D + lane * DL;
-#pragma unroll
-              for (int e = 0; e < DL; ++e) store_elem(orow + e, O[e] / Ls);
+                for (int c = 0; c < D / 32; ++c) {
+                  dst[(c * 32 + 8 * mt) / 4] = make_float4(po[c][0][0] * inv, po[c][0][1] * inv,
+                                                           po[c][1][0] * inv, po[c][1][1] * inv);
+                  dst[(c * 32 + 8 * mt) / 4 + 1] = make_float4(po[c][2][0] * inv, po[c][2][1] * inv,
+                                                               po[c][3][0] * inv, po[c][3][1] * inv);
+                }
+                if (mt == 0) p.ws_ml[base + mg] = make_float2(pm, pl);
+              }
             } else {
-              const size_t slot2 = row * 2 + cc.part;
-              float* po = gp.ws_row_o + slot2 * D + lane * DL;
 #pragma unroll
-              for (int e = 0; e < DL; ++e) po[e] = O[e] / Ls;
-              if (lane == 0) gp.ws_row_ml[slot2] = make_float2(M, Ls);
-              row_merge_tail<T, D>(gp, seq, head);
+              for (int g = 0; g < OR; ++g) {
+                if (g >= nr) continue;
+                const float inv = l[g] > 0.f ? 1.f / l[g] : 0.f;
+                if (grp == 0) {
+                  float4* dst = reinterpret_cast<float4*>(p.ws_o + (base + g) * D);
+#pragma unroll
+                  for (int k = 0; k < CPL; ++k)
+#pragma unroll
+                    for (int e = 0; e < VEC; e += 4)
+                      dst[((sub + 8 * k) * VEC + e) / 4] =
+                          make_float4(o[g][k * VEC + e] * inv, o[g][k * VEC + e + 1] * inv,
+                                      o[g][k * VEC + e + 2] * inv, o[g][k * VEC + e + 3] * inv);
+                }
+                if (lane == 0) p.ws_ml[base + g] = make_float2(m[g], l[g]);
+              }
+            }
+            __threadfence();
+            __syncwarp();
+            const long long seg_start = cc.g - cc.t;
+            const long long seg_end = seg_start + cc.nt;
+            const long long w_first = ((seg_start + 1) * Wq + Tq - 1) / Tq - 1;
+            const long long w_last = (seg_end * Wq + Tq - 1) / Tq - 1;
+            int is_last = 0;
+            if (lane == 0) {
+              const size_t ci_idx = phase == 0 ? (size_t)(cc.lo + kGroupRows * cc.c) * H + cc.b
+                                               : (size_t)B * H + (size_t)cc.a * HG + cc.b;
+              int32_t* ctr = gp.ws_seg_ctr + ci_idx;
+              const int prev = atomicAdd(ctr, 1);
+              is_last = prev == (int)(w_last - w_first);
+              if (is_last) *ctr = 0;
+            }
+            is_last = __shfl_sync(kFullMask, is_last, 0);
+            if (is_last) {
+              __threadfence();
+              for (int g = 0; g < nr; ++g) {
+                const size_t row = (size_t)row_seq(cc, g) * H + row_head(cc, x, g);
+                float M = -INFINITY;
+                for (long long w = w_first; w <= w_last; ++w) {
+                  const int sl = (w == w_first && w * Tq / Wq < seg_start) ? 1 : 0;
+                  M = fmaxf(M, __ldcg(p.ws_ml + ((size_t)w * 2 + sl) * R + g).x);
+                }
+                float2 pr = make_float2(-INFINITY, 0.f);
+                if (with_prefix) {
+                  pr = __ldcg(gp.ws_row_ml + row);
+                  M = fmaxf(M, pr.x);
+                }
+                float Ls = 0.f, O[DL];
+#pragma unroll
+                for (int e = 0; e < DL; ++e) O[e] = 0.f;
+                for (long long w = w_first; w <= w_last; ++w) {
+                  const int sl = (w == w_first && w * Tq / Wq < seg_start) ? 1 : 0;
+                  const size_t idx = ((size_t)w * 2 + sl) * R + g;
+                  const float2 v = __ldcg(p.ws_ml + idx);
+                  const float wt = v.x == -INFINITY ? 0.f : v.y * exp2f(v.x - M);
+                  Ls += wt;
+                  const float* src = p.ws_o + idx * D + lane * DL;
+#pragma unroll
+                  for (int e = 0; e < DL; ++e) O[e] += __ldcg(src + e) * wt;
+                }
+                if (with_prefix) {
+                  const float wt = pr.y * exp2f(pr.x - M);
+                  Ls += wt;
+                  const float* src = gp.ws_row_o + row * D + lane * DL;
+#pragma unroll
+                  for (int e = 0; e < DL; ++e) O[e] += __ldcg(src + e) * wt;
+                }
+                if (phase == 0) {  // merged prefix result of this row
+                  float* dst = gp.ws_row_o + row * D + lane * DL;
+#pragma unroll
+                  for (int e = 0; e < DL; ++e) dst[e] = O[e] / Ls;
+                  if (lane == 0) gp.ws_row_ml[row] = make_float2(M, Ls);
+                } else {
+                  T* orow = static_cast<T*>(p.out) + row * D + lane * DL;
+#pragma unroll
+                  for (int e = 0; e < DL; ++e) store_elem(orow + e, Ls > 0.f ? O[e] / Ls : 0.f);
+                }
+              }
             }
           }
         }
+        gcursor_next(cc, x);
       }
     }
-    gcursor_next(cc, x);
+    if (phase == 0) arrive_gpu(sync_arrive);
+  }
+  // last warp out re-zeroes the phase counters for the next launch
+  __syncwarp();
+  if (lane == 0) {
+    const int prev = atomicAdd(sync_exit, 1);
+    if (prev == (int)W - 1) {
+      *sync_arrive = 0;
+      *sync_exit = 0;
+    }
   }
 }
 
 // Validation prologue, then the persistent grid sized to the device.
-template <typename T, int D>
+template <typename T, int D, int TG>
 cudaError_t launch_pa_decode_grouped(const GroupedParams& gp, cudaStream_t stream) {
   using S = DecodeShape<T, D, kGroupRows>;
   static int grid_of_device[64] = {0};
@@ -716,13 +1022,13 @@ cudaError_t launch_pa_decode_grouped(const GroupedParams& gp, cudaStream_t strea
   if (e != cudaSuccess) return e;
   int grid = (dev >= 0 && dev < 64) ? __atomic_load_n(&grid_of_device[dev], __ATOMIC_ACQUIRE) : 0;
   if (grid == 0) {
-    e = cudaFuncSetAttribute(pa_decode_grouped_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(pa_decode_grouped_kernel<T, D, TG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::kSmemBytes);
     if (e != cudaSuccess) return e;
     int sms = 0, per_sm = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_decode_grouped_kernel<T, D>,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_decode_grouped_kernel<T, D, TG>,
                                                       kDecodeWarps * 32, S::kSmemBytes);
     if (e != cudaSuccess) return e;
     grid = sms * (per_sm > 0 ? per_sm : 1);
@@ -734,14 +1040,19 @@ cudaError_t launch_pa_decode_grouped(const GroupedParams& gp, cudaStream_t strea
   pa_group_prologue_kernel<T><<<pro, 256, 0, stream>>>(gp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  pa_decode_grouped_kernel<T, D><<<grid, kDecodeWarps * 32, S::kSmemBytes, stream>>>(gp);
+  // co-residency of every block is required by the phase barrier
+  void* args[] = {const_cast<GroupedParams*>(&gp)};
+  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(pa_decode_grouped_kernel<T, D, TG>), dim3(grid),
+                                  dim3(kDecodeWarps * 32), args, S::kSmemBytes, stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
 using GroupedLauncher = cudaError_t (*)(const GroupedParams&, cudaStream_t);
 
-GroupedLauncher grouped_launcher_f32(int head_dim);
-GroupedLauncher grouped_launcher_f16(int head_dim);
-GroupedLauncher grouped_launcher_bf16(int head_dim);
+// gpw_index: query heads per warp in the tails, 0 -> 1, 1 -> 2, 2 -> 4.
+GroupedLauncher grouped_launcher_f32(int head_dim, int gpw_index);
+GroupedLauncher grouped_launcher_f16(int head_dim, int gpw_index);
+GroupedLauncher grouped_launcher_bf16(int head_dim, int gpw_index);
 
 }  // namespace pkv
