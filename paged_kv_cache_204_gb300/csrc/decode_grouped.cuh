@@ -35,6 +35,14 @@ namespace pkv {
 
 constexpr int kGroupRows = 4;  // query rows one warp serves against one K/V tile
 
+// The work split charges every segment a fixed cost, in tile units, on top of
+// its tiles: entering a segment (metadata, query rows) and finishing it
+// (reductions, the prefix merge, the output row) take about as long as
+// streaming that many tiles. A warp whose range holds many short tails then
+// gets fewer tiles. The charged units hold no tile: a cursor skips them.
+constexpr int kSegCostPrefix = 1;
+constexpr int kSegCostTail = 2;
+
 struct GroupedParams {
   DecodeParams base;             // ws_counter is unused here
   const int32_t* group_start;    // [num_groups + 1]
@@ -148,13 +156,14 @@ __device__ __forceinline__ int ctx_len(const GCtx& x, int s) {
 
 __device__ __forceinline__ int group_rows(int M) { return (M + kGroupRows - 1) / kGroupRows; }
 
-// Prefix tiles of group g (0 when it has no usable shared prefix).
-__device__ __forceinline__ long long prefix_tiles(const GCtx& x, int g) {
+// Work units of group g's prefix segments: tiles plus the per-segment cost
+// (0 when the group has no usable shared prefix).
+__device__ __forceinline__ long long prefix_units(const GCtx& x, int g) {
   if (!x.use_groups) return 0;
   const int M = __ldg(x.group_start + g + 1) - __ldg(x.group_start + g);
   const int S = x.group_S[g];
   if (M < 2 || S <= 0) return 0;
-  return (long long)x.num_heads * group_rows(M) * (S / kTileTokens);
+  return (long long)x.num_heads * group_rows(M) * (S / kTileTokens + kSegCostPrefix);
 }
 
 __device__ __forceinline__ int seq_prefix(const GCtx& x, int s) { return x.use_groups ? x.seq_P[s] : 0; }
@@ -184,7 +193,7 @@ __device__ __forceinline__ void gseg_enter(GCursor& c, const GCtx& x) {
 
 // Move to the first group at or after c.a with prefix tiles; else to the tails.
 __device__ __forceinline__ void gseek_prefix(GCursor& c, const GCtx& x) {
-  while (c.a < x.num_groups && prefix_tiles(x, c.a) == 0) ++c.a;
+  while (c.a < x.num_groups && prefix_units(x, c.a) == 0) ++c.a;
   if (c.a < x.num_groups) {
     c.part = 0;
   } else {
@@ -197,10 +206,8 @@ __device__ __forceinline__ void gseek_prefix(GCursor& c, const GCtx& x) {
   if (c.part == 0 || c.a < x.num_seqs) gseg_enter(c, x);
 }
 
-__device__ __forceinline__ void gcursor_next(GCursor& c, const GCtx& x) {
-  ++c.g;
-  if (++c.t < c.nt) return;
-  c.t = 0;
+// Next segment (c.t is 0).
+__device__ __forceinline__ void gseg_next(GCursor& c, const GCtx& x) {
   if (c.part == 0) {
     if (++c.c < group_rows(c.M)) {
       gseg_enter(c, x);
@@ -221,6 +228,15 @@ __device__ __forceinline__ void gcursor_next(GCursor& c, const GCtx& x) {
   }
   c.b = 0;
   if (++c.a < x.num_seqs) gseg_enter(c, x);
+}
+
+// Next tile: c.g is its work unit (the next segment's charged units skipped).
+__device__ __forceinline__ void gcursor_next(GCursor& c, const GCtx& x) {
+  ++c.g;
+  if (++c.t < c.nt) return;
+  c.t = 0;
+  gseg_next(c, x);
+  c.g += c.part == 0 ? kSegCostPrefix : kSegCostTail;
 }
 
 // (sequence, head) of row r of the segment under c.
@@ -573,11 +589,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
   // ---- start-up: tiles of both phases, then each warp's first segment --------
   long long mine = 0;
-  for (int g = threadIdx.x; g < G; g += NW * 32) mine += prefix_tiles(x, g);
+  for (int g = threadIdx.x; g < G; g += NW * 32) mine += prefix_units(x, g);
   long long TA;
   block_exclusive_scan(mine, scan, TA);
   mine = 0;
-  for (int s = threadIdx.x; s < B; s += NW * 32) mine += (long long)HG * tiles_of(ctx_len(x, s) - seq_prefix(x, s));
+  for (int s = threadIdx.x; s < B; s += NW * 32)
+    mine += (long long)HG * (tiles_of(ctx_len(x, s) - seq_prefix(x, s)) + kSegCostTail);
   long long TB;
   block_exclusive_scan(mine, scan, TB);
   const long long W = (long long)gridDim.x * NW;
@@ -589,7 +606,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   long long carry = 0;
   for (int base = 0; base < G; base += NW * 32) {
     const int g = base + threadIdx.x;
-    const long long cnt = g < G ? prefix_tiles(x, g) : 0;
+    const long long cnt = g < G ? prefix_units(x, g) : 0;
     long long tot;
     const long long excl = carry + block_exclusive_scan(cnt, scan, tot);
 #pragma unroll
@@ -605,7 +622,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   carry = 0;
   for (int base = 0; base < B; base += NW * 32) {
     const int s = base + threadIdx.x;
-    const long long cnt = s < B ? (long long)HG * tiles_of(ctx_len(x, s) - seq_prefix(x, s)) : 0;
+    const long long cnt = s < B ? (long long)HG * (tiles_of(ctx_len(x, s) - seq_prefix(x, s)) + kSegCostTail) : 0;
     long long tot;
     const long long excl = carry + block_exclusive_scan(cnt, scan, tot);
 #pragma unroll
@@ -649,20 +666,23 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
   for (int phase = 0; phase < 2; ++phase) {
     const long long Tp = phase == 0 ? TA : TB, Wp = phase == 0 ? WA : WB;
+    const int E = phase == 0 ? kSegCostPrefix : kSegCostTail;
     const long long a_begin = wid < Wp ? wid * Tp / Wp : Tp;
     const long long a_end = wid < Wp ? (wid + 1) * Tp / Wp : Tp;
     if (!failed && a_begin < a_end) {
       GCursor ci;
       {
         const longlong2 st0 = starts[phase * NW + warp];
-        ci.g = a_begin;
         ci.part = phase;
         ci.a = static_cast<int>(st0.x);
         ci.b = 0;
         ci.c = 0;
         gseg_enter(ci, x);  // nt does not depend on b or c
-        const long long seg_idx = st0.y / ci.nt;
-        ci.t = static_cast<int>(st0.y % ci.nt);
+        const long long per = ci.nt + E;  // units of one segment
+        const long long seg_idx = st0.y / per;
+        const int r = static_cast<int>(st0.y % per) - E;
+        ci.t = r < 0 ? 0 : r;  // a range that starts on charged units starts at tile 0
+        ci.g = a_begin + (ci.t - r);
         if (phase == 0) {
           ci.b = static_cast<int>(seg_idx / group_rows(ci.M));
           ci.c = static_cast<int>(seg_idx % group_rows(ci.M));
@@ -672,11 +692,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         gseg_enter(ci, x);
       }
       GCursor cc = ci;
+      const long long g_first = ci.g;  // unit of this warp's first tile in the phase
 
       auto issue = [&](const GCursor& c, int n) {
         const int t0 = c.tok0 + c.t * kTileTokens;
         const int nvalid = min(max(c.tok_end - t0, 0), kTileTokens);
-        const bool with_q = (c.t == 0 || c.g == a_begin) && nvalid > 0;
+        const bool with_q = (c.t == 0 || c.g == g_first) && nvalid > 0;
         if (nvalid > 0) {
           const int j_first = t0 / bs;
           const int j_last = (t0 + nvalid - 1) / bs;
@@ -750,7 +771,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         const unsigned char* vs = ks + S::kTileBytes;
         const int t0 = cc.tok0 + cc.t * kTileTokens;
         const int nvalid = min(max(cc.tok_end - t0, 0), kTileTokens);
-        const bool first = cc.t == 0 || cc.g == a_begin;
+        const bool first = cc.t == 0 || cc.g == g_first;
         const bool last = cc.t == cc.nt - 1 || cc.g == a_end - 1;
         const int nr = cc.nrows;
         const bool tc_prefix = kMma && phase == 0;  // state in the tensor-core layout
@@ -899,7 +920,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
           } else {
             // one piece of a segment shared with neighbouring warps
             const long long Wq = Wp, Tq = Tp;
-            const int slot = cc.g - cc.t <= a_begin ? 0 : 1;
+            // slot 0: the piece holding the warp's first tile (its range starts
+            // in this segment, charged units included); slot 1: its last piece
+            const int slot = cc.g - cc.t - E <= a_begin ? 0 : 1;
             const size_t base = ((size_t)wid * 2 + slot) * R;
             if (tc_prefix) {
               if (mg < nr) {
@@ -934,8 +957,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
             }
             __threadfence();
             __syncwarp();
-            const long long seg_start = cc.g - cc.t;
+            const long long seg_start = cc.g - cc.t;  // unit of the segment's first tile
             const long long seg_end = seg_start + cc.nt;
+            const long long seg_units0 = seg_start - E;  // its first charged unit
             const long long w_first = ((seg_start + 1) * Wq + Tq - 1) / Tq - 1;
             const long long w_last = (seg_end * Wq + Tq - 1) / Tq - 1;
             int is_last = 0;
@@ -954,7 +978,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
                 const size_t row = (size_t)row_seq(cc, g) * H + row_head(cc, x, g);
                 float M = -INFINITY;
                 for (long long w = w_first; w <= w_last; ++w) {
-                  const int sl = (w == w_first && w * Tq / Wq < seg_start) ? 1 : 0;
+                  const int sl = (w == w_first && w * Tq / Wq < seg_units0) ? 1 : 0;
                   M = fmaxf(M, __ldcg(p.ws_ml + ((size_t)w * 2 + sl) * R + g).x);
                 }
                 float2 pr = make_float2(-INFINITY, 0.f);
@@ -966,7 +990,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 #pragma unroll
                 for (int e = 0; e < DL; ++e) O[e] = 0.f;
                 for (long long w = w_first; w <= w_last; ++w) {
-                  const int sl = (w == w_first && w * Tq / Wq < seg_start) ? 1 : 0;
+                  const int sl = (w == w_first && w * Tq / Wq < seg_units0) ? 1 : 0;
                   const size_t idx = ((size_t)w * 2 + sl) * R + g;
                   const float2 v = __ldcg(p.ws_ml + idx);
                   const float wt = v.x == -INFINITY ? 0.f : v.y * exp2f(v.x - M);
