@@ -460,8 +460,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 #pragma unroll
           for (int g = 0; g < GPW; ++g) p.ws_ml[base + g] = make_float2(m[g], l[g]);
         }
-        __threadfence();
-        __syncwarp();
+        __syncwarp();  // the partial's writes precede lane 0's release below
         const long long seg_start = cc.g - cc.t;
         const long long seg_end = seg_start + cc.nt;
         // warps whose ranges meet this segment: w(x) = ceil((x+1) Weff / T) - 1
@@ -470,13 +469,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         int is_last = 0;
         if (lane == 0) {
           int32_t* ctr = p.ws_counter + (size_t)cc.s * HG + cc.hg;
-          const int prev = atomicAdd(ctr, 1);
+          const int prev = atomic_add_acq_rel_gpu(ctr, 1);
           is_last = prev == (int)(w_last - w_first);
           if (is_last) *ctr = 0;  // every piece has counted: leave the counter zero
         }
         is_last = __shfl_sync(kFullMask, is_last, 0);
         if (is_last) {
-          __threadfence();
+          __syncwarp();  // the other pieces' partials, acquired by lane 0, are visible to all lanes
           constexpr int DL = D / 32;  // output dims per lane in the merge
 #pragma unroll
           for (int g = 0; g < GPW; ++g) {

@@ -507,10 +507,9 @@ __device__ __forceinline__ void core_tile(const unsigned char* ks, const unsigne
 }
 
 // ---- grid-wide phase barrier (the grid is co-resident: cooperative launch) --
-// Called by the whole warp: every lane's earlier writes are made visible
-// before lane 0 counts the warp in.
+// Called by the whole warp: the warp barrier orders every lane's earlier
+// writes before lane 0's release, which counts the warp in.
 __device__ __forceinline__ void arrive_gpu(int32_t* ctr) {
-  __threadfence();
   __syncwarp();
   if ((threadIdx.x & 31) == 0) asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(1) : "memory");
 }
@@ -535,7 +534,7 @@ __device__ __forceinline__ bool wait_count(const int32_t* ctr, int target, uint6
     }
   }
   ok = __shfl_sync(kFullMask, ok, 0);
-  __threadfence();
+  __syncwarp();  // every lane's later reads follow lane 0's acquire
   return ok != 0;
 }
 
@@ -955,8 +954,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
                 if (lane == 0) p.ws_ml[base + g] = make_float2(m[g], l[g]);
               }
             }
-            __threadfence();
-            __syncwarp();
+            __syncwarp();  // the partial's writes precede lane 0's release below
             const long long seg_start = cc.g - cc.t;  // unit of the segment's first tile
             const long long seg_end = seg_start + cc.nt;
             const long long seg_units0 = seg_start - E;  // its first charged unit
@@ -967,13 +965,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
               const size_t ci_idx = phase == 0 ? (size_t)(cc.lo + kGroupRows * cc.c) * H + cc.b
                                                : (size_t)B * H + (size_t)cc.a * HG + cc.b;
               int32_t* ctr = gp.ws_seg_ctr + ci_idx;
-              const int prev = atomicAdd(ctr, 1);
+              const int prev = atomic_add_acq_rel_gpu(ctr, 1);
               is_last = prev == (int)(w_last - w_first);
               if (is_last) *ctr = 0;
             }
             is_last = __shfl_sync(kFullMask, is_last, 0);
             if (is_last) {
-              __threadfence();
+              __syncwarp();  // the other pieces' partials, acquired by lane 0, are visible to all lanes
               for (int g = 0; g < nr; ++g) {
                 const size_t row = (size_t)row_seq(cc, g) * H + row_head(cc, x, g);
                 float M = -INFINITY;
