@@ -275,6 +275,33 @@ def aggregate(values: dict, world: int, device=None) -> dict:
     return {k: float(v) for k, v in zip(keys, t.tolist())}
 
 
+def kv_memory(cfg) -> dict:
+    """KV memory of the workload as the library's host block manager lays it
+    out ("PagedAttention: the KV cache was the bottleneck all along", sections
+    "Virtual memory for attention" and "The number that made us read the
+    code"), and the host time of one decode step's bookkeeping (one more slot
+    for every sequence, then the block tables and context lengths)."""
+    import paged_kv_cache_204_gb300.block_manager as pbm
+    from synth.replay import replay
+
+    m = pbm.BlockManager(cfg.num_blocks, cfg.block_size, seed=cfg.seed)
+    seqs = replay(m, cfg)
+    st = m.stats()
+    mm = pbm.memory_metrics(st, cfg.block_size)
+    ones = [1] * len(seqs)
+    reps = 50
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        m.append_batch(seqs, ones)
+        m.export(seqs, cfg.max_blocks_per_seq + reps)
+    step_us = (time.perf_counter() - t0) / reps * 1e6
+    return {"waste_fraction": mm["waste_fraction"], "sharing_saving": mm["sharing_saving"],
+            "contiguous_reservation_waste": 1.0 - st["logical_tokens"] / (st["live_seqs"] * cfg.max_len),
+            "reserved_tokens_per_sequence": cfg.max_len,
+            "used_blocks": st["used_blocks"], "logical_blocks": st["logical_blocks"],
+            "cow_copies": st["cow_copies"], "host_step_us": step_us}
+
+
 def run_ours(args, rank: int, world: int, local_rank: int) -> int:
     import torch
     import torch.distributed as dist
@@ -429,6 +456,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         "gpu_launches": launches_per_step * K,
         "clocks": clocks.summary(),
         "timed_region_wall_s": wall,
+        "kv_memory": kv_memory(cfg),
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -76,7 +76,8 @@ typedef enum pkv_status {
   PKV_ERR_INVALID_ARG = 1, /* NULL or misaligned pointer, negative or inconsistent size */
   PKV_ERR_UNSUPPORTED = 2, /* well-formed but not built: head_dim, block_size, dtype, grid limit */
   PKV_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than pkv_decode_workspace_bytes() */
-  PKV_ERR_CUDA = 4         /* a CUDA runtime call or a kernel launch failed */
+  PKV_ERR_CUDA = 4,        /* a CUDA runtime call or a kernel launch failed */
+  PKV_ERR_OUT_OF_BLOCKS = 5 /* host block manager: the free blocks cannot hold the request */
 } pkv_status;
 
 /* Bits ORed into *dev_err by the kernels. */

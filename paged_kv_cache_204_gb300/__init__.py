@@ -14,6 +14,8 @@ Functions mirror the C entry points:
   paged_attention_decode_grouped  -> pkv_paged_attention_decode_grouped
   decode_grouped_workspace_bytes  -> pkv_decode_grouped_workspace_bytes
   set_wait_timeout_ns / get_wait_timeout_ns, status_string, version
+The host block manager (include/pkv_block_manager.h) is wrapped by
+``paged_kv_cache_204_gb300.block_manager.BlockManager``.
 """
 from __future__ import annotations
 
@@ -32,7 +34,7 @@ if not os.path.exists(LIB_PATH):
 
 lib = ctypes.CDLL(LIB_PATH)
 
-PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA = range(5)
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA, PKV_ERR_OUT_OF_BLOCKS = range(6)
 DEV_ERR_BLOCK_ID, DEV_ERR_SLOT, DEV_ERR_CONTEXT_LEN, DEV_ERR_TIMEOUT, DEV_ERR_PAIR = 1, 2, 4, 8, 16
 DEV_ERR_GROUP = 32
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}

@@ -1,6 +1,7 @@
 """Build the CUDA library in-tree: every .cu under csrc/ is compiled for
-sm_103a in parallel and linked into _build/libpkv.so (CUDA runtime linked
-statically, so the library loads beside any PyTorch build)."""
+sm_103a (and every .cpp, host-only code, by nvcc's host compiler) in
+parallel and linked into _build/libpkv.so (CUDA runtime linked statically,
+so the library loads beside any PyTorch build)."""
 from __future__ import annotations
 
 import glob
@@ -27,7 +28,7 @@ def _nvcc() -> str:
 
 
 def _sources() -> list[str]:
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps() -> list[str]:
