@@ -464,6 +464,233 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
     return 0
 
 
+def beam_cpu_baseline(cfg, kc, vc, plan, q, min_seconds: float, n_beams: int) -> dict:
+    """The fp64 oracle, as it stands, on the host cores: paged attention of
+    the first n_beams beams of the last step over host copies of their
+    blocks, repeated for about min_seconds."""
+    import numpy as np
+    import oracle
+    from synth.device import to_storage
+    threads = len(os.sched_getaffinity(0))
+    n = max(1, min(n_beams, plan.seqs.size))
+    bt, cl = plan.block_tables[:n], plan.context_lens[:n]
+    ids = np.unique(bt[bt >= 0])
+    remap = np.full(cfg.num_blocks, -1, dtype=np.int32)
+    remap[ids] = np.arange(ids.size, dtype=np.int32)
+    bt_c = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
+    import torch
+    idx = torch.from_numpy(ids.astype(np.int64)).to(kc.device)
+    k_h, v_h, q_h = to_storage(kc[idx]), to_storage(vc[idx]), to_storage(q[:n])
+    rows = {(int(b), r) for i in range(n) for j, b in enumerate(bt[i][bt[i] >= 0])
+            for r in range(min(cfg.block_size, int(cl[i]) - j * cfg.block_size))}
+    nbytes = len(rows) * cfg.kv_bytes_per_token() + 2 * n * cfg.num_heads * cfg.head_dim * cfg.elem_bytes
+    times, t_start = [], time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        oracle.paged_attention(q_h, k_h, v_h, bt_c, cl, scale=cfg.scale, num_heads=cfg.num_heads,
+                               num_kv_heads=cfg.num_kv_heads, head_dim=cfg.head_dim, block_size=cfg.block_size,
+                               dtype=cfg.dtype, threads=threads)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start >= min_seconds:
+            break
+    mean = sum(times) / len(times)
+    return {"value": nbytes / mean / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": (f"attention of the first {n} of {plan.seqs.size} beams at the last step "
+                       f"({int(cl.sum())} tokens x {cfg.num_heads} heads, {len(rows)} distinct cached tokens), "
+                       f"{len(times)} run(s), {mean * 1e3:.1f} ms each")}
+
+
+def run_beam(args, rank: int, world: int, local_rank: int) -> int:
+    """Beam-search decode steps: per step the block manager forks and ends
+    beams, copy_blocks copies shared partly filled blocks, reshape_and_cache
+    writes every new beam's K/V row, and the grouped decode reads each
+    request's shared prefix once for all its beams. The timed region runs the
+    device part of each step with that step's plan (block tables, slots,
+    copy pairs, groups) already resident; e2e runs further steps through
+    BeamDecoder.step, host bookkeeping and transfers included."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_204_gb300 as pkv
+    import synth.beam as SB
+    from paged_kv_cache_204_gb300.beam import BeamDecoder, DevicePlan
+    from synth.device import fill_poison
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    warm = max(args.warmup, 3)
+    K = args.steps
+    e2e_steps = max(10, K // 4)
+    cfg = SB.get(args.workload)
+    cfg = cfg.replace(steps=max(cfg.steps, warm + K + e2e_steps + 3))
+    if args.num_blocks:
+        cfg = cfg.replace(num_blocks=args.num_blocks)
+    if world > 1:
+        cfg = cfg.replace(seed=cfg.seed + rank)
+    td = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float32}[cfg.dtype]
+    shape = (cfg.num_blocks, cfg.num_kv_heads, cfg.block_size, cfg.head_dim)
+    kc = torch.empty(shape, dtype=td, device=dev)
+    vc = torch.empty(shape, dtype=td, device=dev)
+    fill_poison(kc)
+    fill_poison(vc)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg.seed * 1000003 + 29)
+    randn = lambda *shp: (torch.randn(shp, generator=gen, device=dev) * cfg.value_scale).to(td)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    dec = BeamDecoder(kc, vc, cfg.width, cfg.max_blocks_per_seq, seed=cfg.seed)
+    for P in SB.prompt_lengths(cfg):
+        dec.add_request(randn(int(P), cfg.num_kv_heads, cfg.head_dim), randn(int(P), cfg.num_kv_heads, cfg.head_dim),
+                        dev_err=err)
+    B, H, D = cfg.num_seqs, cfg.num_heads, cfg.head_dim
+    nk, nv, q = randn(B, cfg.num_kv_heads, D), randn(B, cfg.num_kv_heads, D), randn(B, H, D)
+    out = torch.empty_like(q)
+    parents_of = SB.parent_stream(cfg)
+    row_bytes = cfg.kv_bytes_per_token()
+    block_bytes = row_bytes * cfg.block_size
+    dplans, step_bytes, attn_bytes, n_copies = [], [], [], 0
+    for i in range(warm + K):
+        plan = dec.plan(next(parents_of))
+        st = dec.manager.stats()  # the live sequences are exactly the beams
+        a_bytes = st["filled_slots"] * row_bytes + 2 * B * H * D * cfg.elem_bytes
+        c = plan.copy_pairs.shape[0]
+        n_copies += c
+        attn_bytes.append(a_bytes)
+        step_bytes.append(a_bytes + 2 * B * row_bytes + 2 * c * block_bytes)
+        dplans.append(DevicePlan(max_context_len=plan.max_context_len, **{
+            name: torch.from_numpy(np.ascontiguousarray(getattr(plan, name))).to(dev)
+            for name in ("slots", "copy_pairs", "block_tables", "context_lens", "group_start", "shared_blocks")}))
+    ws = dec.workspace(H, D)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def device_step(dp, e_write=None):
+        if dp.copy_pairs.numel():
+            pkv.copy_blocks(kc, vc, dp.copy_pairs, dev_err=err)
+        pkv.reshape_and_cache(nk, nv, kc, vc, dp.slots, dev_err=err)
+        if e_write is not None:  # copies and row writes done
+            e_write.record(stream)
+        pkv.paged_attention_decode_grouped(out, q, kc, vc, dp.block_tables, dp.context_lens, cfg.scale,
+                                           dp.max_context_len, dp.group_start, dp.shared_blocks, ws, dev_err=err)
+
+    for i in range(warm):
+        flush.fill_(1)
+        device_step(dplans[i])
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x} during warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches = 0
+    with ClockSampler(local_rank) as clocks:
+        t_wall0 = time.perf_counter()
+        for i in range(K):
+            dp = dplans[warm + i]
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            device_step(dp, ev[i][1])
+            ev[i][2].record(stream)
+            launches += (1 if dp.copy_pairs.numel() else 0) + 1 + 2
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        wall = time.perf_counter() - t_wall0
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x} in the timed region")
+    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / K
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    cache_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    bytes_step = sum(step_bytes[warm:]) / K
+    bytes_attn = sum(attn_bytes[warm:]) / K
+
+    # end to end: host bookkeeping, transfers of the plan and of q / new rows
+    # from pinned host memory, the device step, and the outputs read back
+    host_k, host_v, host_q = nk.cpu().pin_memory(), nv.cpu().pin_memory(), q.cpu().pin_memory()
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e2e_total, h2d = 0.0, 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_bytes = 0
+    for i in range(e2e_steps + 3):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        plan = dec.plan(next(parents_of))
+        dp = dec.upload(plan)
+        nk.copy_(host_k, non_blocking=True)
+        nv.copy_(host_v, non_blocking=True)
+        q.copy_(host_q, non_blocking=True)
+        dec.run(dp, nk, nv, q, cfg.scale, out, dev_err=err)
+        host_out.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        if i >= 3:
+            e2e_total += time.perf_counter() - t0
+            st = dec.manager.stats()
+            e2e_bytes += (st["filled_slots"] * row_bytes + 2 * B * H * D * cfg.elem_bytes + 2 * B * row_bytes
+                          + 2 * plan.copy_pairs.shape[0] * block_bytes)
+            h2d += sum(getattr(plan, f).nbytes for f in ("slots", "copy_pairs", "block_tables", "context_lens",
+                                                         "group_start", "shared_blocks"))
+            h2d += sum(t.numel() * t.element_size() for t in (host_k, host_v, host_q))
+    e2e_ms = e2e_total / e2e_steps * 1e3
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x} in the end-to-end steps")
+
+    agg = aggregate({"step_ms": step_ms, "attn_ms": attn_ms, "cache_ms": cache_ms, "e2e_ms": e2e_ms},
+                    world, device=dev if world > 1 else None)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_src = peak_hbm()
+    achieved = bytes_attn / (agg["attn_ms"] * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = beam_cpu_baseline(cfg, kc, vc, plan, q, args.cpu_seconds, args.cpu_seqs)
+    st = dec.manager.stats()
+    import paged_kv_cache_204_gb300.block_manager as pbm
+    mm = pbm.memory_metrics(st, cfg.block_size)
+    line = {
+        "metric": METRIC,
+        "value": world * bytes_step / (agg["step_ms"] * 1e-3) / 1e9,
+        "unit": "GB/s",
+        "n_gpus": world, "steps": K, "warmup": warm,
+        "ms_per_step": agg["step_ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": cfg.dtype, "data": "synthetic",
+        "config": {"workload": (f"beam-search decode steps: {cfg.requests} requests x {cfg.width} beams, "
+                                f"{H} heads ({cfg.num_kv_heads} kv), head_dim {D}, block_size {cfg.block_size}, "
+                                f"{cfg.dtype} storage with fp32 accumulation, prompts {cfg.prompt[0]} in "
+                                f"[{cfg.prompt[1]}, {cfg.prompt[2]}], parents drawn with rank weights (W-j)^2, "
+                                f"{cfg.num_blocks}-block pools, grouped attention (one group per request)"),
+                   "global_batch": B, "parallelism": "single GPU" if world == 1 else f"{world} replicas",
+                   "l2": "flushed between timed steps (256 MiB write)", "seed": cfg.seed,
+                   "copies_per_step": n_copies / (warm + K)},
+        "seqs_per_s": world * B / (agg["step_ms"] * 1e-3),
+        "attention_ms": agg["attn_ms"], "cache_ops_ms": agg["cache_ms"],
+        "bytes_per_step": bytes_step,
+        "roofline": {"bound": "hbm", "kernel": "pa_group_prologue + pa_decode_grouped_kernel",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "algorithmic_bytes_per_launch": bytes_attn, "peak_source": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * (e2e_bytes / e2e_steps) / (agg["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
+                "ms_per_step": agg["e2e_ms"], "h2d_bytes_per_step": h2d // e2e_steps,
+                "d2h_bytes_per_step": host_out.numel() * host_out.element_size()},
+        "gpu_launches": launches,
+        "clocks": clocks.summary(),
+        "timed_region_wall_s": wall,
+        "kv_memory": {"waste_fraction": mm["waste_fraction"], "sharing_saving": mm["sharing_saving"],
+                      "used_blocks": st["used_blocks"], "logical_blocks": st["logical_blocks"],
+                      "cow_copies": st["cow_copies"]},
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -471,7 +698,8 @@ def main() -> int:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=WORKLOAD,
-                    help="synthetic workload preset (default: the LLaMA-13B-shaped step)")
+                    help="synthetic workload preset (default: the LLaMA-13B-shaped step); "
+                         "'beam': beam-search decode steps")
     ap.add_argument("--attention", choices=("plain", "grouped"), default="plain",
                     help="grouped: siblings read shared prefix blocks once (copy-on-write workloads)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum time of the CPU baseline")
@@ -486,6 +714,11 @@ def main() -> int:
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if world != args.gpus:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.workload.startswith("beam"):
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the default workload"}))
+            return 0
+        return run_beam(args, rank, world, local_rank)
     if args.impl == "reference":
         return run_reference(args, rank, world)
     return run_ours(args, rank, world, local_rank)

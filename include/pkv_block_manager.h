@@ -113,6 +113,27 @@ pkv_status pkv_bm_append(pkv_block_manager* bm, int32_t seq, int32_t n, int64_t*
 pkv_status pkv_bm_append_batch(pkv_block_manager* bm, const int32_t* seqs, const int32_t* counts, int32_t n,
                                int64_t* slots, int64_t* cow_pairs, int32_t* num_cow);
 
+/* One beam-search step of one request ([VM]: beams share long prefixes and
+ * are forked and discarded all the time). beams[0..width) are the request's
+ * current beams (distinct live sequences); new beam i continues beam
+ * beams[parents[i]] (parents[i] in [0, width)) with n_new more tokens.
+ * After the call new_beams[i] is the sequence of new beam i: the first new
+ * beam (lowest i) of a parent takes over the parent's sequence id, further
+ * ones are forks of it, and beams that no new beam continues are ended
+ * (their blocks freed unless other sequences hold them). Then every new beam
+ * appends n_new tokens in order i = 0, 1, ..., exactly as pkv_bm_append_batch
+ * does, so children writing into a shared partly filled block get private
+ * copies except the last, which writes in place. slots ([width * n_new],
+ * packed by i), cow_pairs ([width][2]) and num_cow as in
+ * pkv_bm_append_batch; each may be NULL. All or nothing:
+ * PKV_ERR_OUT_OF_BLOCKS (nothing changed) when the step does not fit even
+ * after the ended beams' blocks return; PKV_ERR_INVALID_ARG when width < 1,
+ * n_new < 0, a beam repeats or is not live, or a parent index is out of
+ * range. */
+pkv_status pkv_bm_beam_step(pkv_block_manager* bm, const int32_t* beams, const int32_t* parents, int32_t width,
+                            int32_t n_new, int32_t* new_beams, int64_t* slots, int64_t* cow_pairs,
+                            int32_t* num_cow);
+
 /* Length (tokens) and table length (blocks) of live sequence `seq`. */
 pkv_status pkv_bm_seq_info(const pkv_block_manager* bm, int32_t seq, int64_t* length, int32_t* num_blocks);
 

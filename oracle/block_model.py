@@ -22,6 +22,8 @@ Plain Python, slow on purpose: state is recomputed from the tables.
 """
 from __future__ import annotations
 
+import copy
+
 
 class OutOfBlocks(RuntimeError):
     pass
@@ -128,6 +130,27 @@ class BlockModel:
             self.lengths[h] = L + 1
         assert copied == copies
         return copied
+
+    def beam_step(self, beams, parents, n_new: int = 1) -> list[int]:
+        """New beam i continues beams[parents[i]]: the parent's first new beam
+        keeps its sequence, later ones fork it; beams no new beam continues
+        end; then each new beam appends n_new tokens in order. Raises
+        OutOfBlocks with nothing changed when the step does not fit."""
+        trial = copy.deepcopy(self)
+        for j, b in enumerate(beams):
+            if j not in parents:
+                trial.free_seq(b)
+        new, kept = [], set()
+        for j in parents:
+            if j in kept:
+                new.append(trial.fork(beams[j]))
+            else:
+                kept.add(j)
+                new.append(beams[j])
+        for h in new:
+            trial.append(h, n_new)
+        self.__dict__.update(trial.__dict__)
+        return new
 
     def common_prefix(self, handles) -> int:
         ts = [self.tables[h] for h in handles]

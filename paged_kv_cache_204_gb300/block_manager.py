@@ -39,6 +39,8 @@ lib.pkv_bm_append.argtypes = [_P, _I32, _I32, _P, _P, ctypes.POINTER(_I32)]
 lib.pkv_bm_append.restype = ctypes.c_int
 lib.pkv_bm_append_batch.argtypes = [_P, _P, _P, _I32, _P, _P, ctypes.POINTER(_I32)]
 lib.pkv_bm_append_batch.restype = ctypes.c_int
+lib.pkv_bm_beam_step.argtypes = [_P, _P, _P, _I32, _I32, _P, _P, _P, ctypes.POINTER(_I32)]
+lib.pkv_bm_beam_step.restype = ctypes.c_int
 lib.pkv_bm_seq_info.argtypes = [_P, _I32, ctypes.POINTER(_I64), ctypes.POINTER(_I32)]
 lib.pkv_bm_seq_info.restype = ctypes.c_int
 lib.pkv_bm_export.argtypes = [_P, _P, _I32, _I32, _P, _P]
@@ -124,6 +126,22 @@ class BlockManager:
         _check(lib.pkv_bm_append_batch(self._h, s.ctypes.data, c.ctypes.data, s.size, slots.ctypes.data,
                                        pairs.ctypes.data, ctypes.byref(ncow)), "pkv_bm_append_batch")
         return slots, pairs[:ncow.value].copy()
+
+    def beam_step(self, beams, parents, n_new: int = 1) -> tuple[np.ndarray, np.ndarray, np.ndarray]:
+        """One beam-search step of one request: new beam i continues
+        beams[parents[i]] with n_new tokens; beams nobody continues end.
+        Returns (new beam sequence ids int32 [W], slots int64 [W * n_new],
+        copy-on-write pairs int64 [k][2])."""
+        b, p = _i32(beams), _i32(parents)
+        if b.shape != p.shape:
+            raise ValueError("beams and parents differ in length")
+        new = np.empty(b.size, dtype=np.int32)
+        slots = np.empty(b.size * max(int(n_new), 0), dtype=np.int64)
+        pairs = np.empty((b.size, 2), dtype=np.int64)
+        ncow = _I32()
+        _check(lib.pkv_bm_beam_step(self._h, b.ctypes.data, p.ctypes.data, b.size, int(n_new), new.ctypes.data,
+                                    slots.ctypes.data, pairs.ctypes.data, ctypes.byref(ncow)), "pkv_bm_beam_step")
+        return new, slots, pairs[:ncow.value].copy()
 
     def seq_info(self, seq: int) -> tuple[int, int]:
         """(length in tokens, table length in blocks) of seq."""

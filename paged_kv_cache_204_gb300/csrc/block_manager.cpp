@@ -245,6 +245,75 @@ pkv_status pkv_bm_append_batch(pkv_block_manager* bm, const int32_t* seqs, const
   return PKV_OK;
 }
 
+pkv_status pkv_bm_beam_step(pkv_block_manager* bm, const int32_t* beams, const int32_t* parents, int32_t width,
+                            int32_t n_new, int32_t* new_beams, int64_t* slots, int64_t* cow_pairs,
+                            int32_t* num_cow) {
+  if (bm == nullptr || beams == nullptr || parents == nullptr || new_beams == nullptr || width < 1 || n_new < 0)
+    return PKV_ERR_INVALID_ARG;
+  if (num_cow != nullptr) *num_cow = 0;
+  const int64_t bs = bm->block_size;
+  std::vector<int32_t> children((size_t)width, 0);
+  try {
+    std::vector<int32_t> ids(beams, beams + width);
+    std::sort(ids.begin(), ids.end());
+    if (std::adjacent_find(ids.begin(), ids.end()) != ids.end()) return PKV_ERR_INVALID_ARG;
+    for (int32_t j = 0; j < width; ++j)
+      if (!bm->is_live(beams[j])) return PKV_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < width; ++i) {
+      if (parents[i] < 0 || parents[i] >= width) return PKV_ERR_INVALID_ARG;
+      ++children[(size_t)parents[i]];
+    }
+    // reference counts after the step's forks and ends, for the blocks involved
+    std::unordered_map<int32_t, int32_t> delta;
+    for (int32_t j = 0; j < width; ++j) {
+      const int32_t d = children[(size_t)j] == 0 ? -1 : children[(size_t)j] - 1;
+      if (d == 0) continue;
+      for (int32_t b : bm->seqs[(size_t)beams[j]].table) delta[b] += d;
+    }
+    int64_t released = 0;
+    for (const auto& kv : delta)
+      if (bm->ref[(size_t)kv.first] + kv.second == 0) ++released;
+    // blocks the appends take (copies made earlier in the step counted)
+    int64_t need = 0;
+    std::unordered_map<int32_t, int32_t> dropped;
+    if (n_new > 0) {
+      for (int32_t i = 0; i < width; ++i) {
+        const pkv_block_manager::Seq& s = bm->seqs[(size_t)beams[parents[i]]];
+        if (s.len % bs != 0) {
+          const int32_t last = s.table.back();
+          auto it = delta.find(last);
+          const int32_t holders = bm->ref[(size_t)last] + (it == delta.end() ? 0 : it->second) - dropped[last];
+          if (holders > 1) {
+            ++need;
+            ++dropped[last];
+          }
+        }
+        need += (s.len + n_new + bs - 1) / bs - (s.len + bs - 1) / bs;
+      }
+    }
+    if (need > (int64_t)bm->free_stack.size() + released) return PKV_ERR_OUT_OF_BLOCKS;
+    bm->seqs.reserve(bm->seqs.size() + (size_t)width);
+    bm->free_ids.reserve(bm->free_ids.size() + (size_t)width);
+  } catch (...) {
+    return PKV_ERR_OUT_OF_BLOCKS;
+  }
+  // end the beams nobody continues, then hand out the survivors
+  for (int32_t j = 0; j < width; ++j)
+    if (children[(size_t)j] == 0) pkv_bm_free_seq(bm, beams[j]);
+  std::vector<char> taken((size_t)width, 0);
+  for (int32_t i = 0; i < width; ++i) {
+    const int32_t j = parents[i];
+    if (!taken[(size_t)j]) {
+      taken[(size_t)j] = 1;
+      new_beams[i] = beams[j];
+    } else if (pkv_bm_fork(bm, beams[j], &new_beams[i]) != PKV_OK) {
+      return PKV_ERR_OUT_OF_BLOCKS;  // host memory ran out while copying a table
+    }
+  }
+  std::vector<int32_t> counts((size_t)width, n_new);
+  return pkv_bm_append_batch(bm, new_beams, counts.data(), width, slots, cow_pairs, num_cow);
+}
+
 pkv_status pkv_bm_seq_info(const pkv_block_manager* bm, int32_t seq, int64_t* length, int32_t* num_blocks) {
   if (bm == nullptr || !bm->is_live(seq)) return PKV_ERR_INVALID_ARG;
   const pkv_block_manager::Seq& s = bm->seqs[(size_t)seq];

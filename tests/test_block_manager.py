@@ -406,3 +406,138 @@ def test_contiguous_reservation_waste(pb):
         contiguous = 1.0 - st["logical_tokens"] / reserved
         assert g["min_waste_fraction"] <= contiguous <= g["max_waste_fraction"], (name, contiguous)
         assert mm["waste_fraction"] < contiguous / 10
+
+
+# ---- beam search steps ---------------------------------------------------------------
+
+def draw_parents(rng, W):
+    """Skewed parent choice: better-ranked beams are continued more often,
+    so some beams end and others continue more than once."""
+    p = np.arange(W, 0, -1, dtype=float) ** 2
+    return [int(x) for x in rng.choice(W, size=W, p=p / p.sum())]
+
+
+def test_model_beam_step_matches_brute_force_views():
+    rng = np.random.default_rng(11)
+    for bs in (2, 4):
+        m = BlockModel(100000, bs)
+        labels, nxt = {}, 0
+        reqs = []
+        for r in range(3):
+            root = m.add_seq()
+            P = int(rng.integers(1, 5 * bs))
+            m.append(root, P)
+            labels[root] = list(range(nxt, nxt + P))
+            nxt += P
+            W = 4
+            beams = [root] + [m.fork(root) for _ in range(W - 1)]
+            for b in beams[1:]:
+                labels[b] = list(labels[root])
+            reqs.append(beams)
+        for step in range(12):
+            for r, beams in enumerate(reqs):
+                parents = draw_parents(rng, len(beams))
+                old = {b: list(labels[b]) for b in beams}
+                new = m.beam_step(beams, parents, 1)
+                for b in beams:
+                    labels.pop(b, None)
+                for i, h in enumerate(new):
+                    labels[h] = old[beams[parents[i]]] + [nxt]
+                    nxt += 1
+                reqs[r] = new
+            assert (m.used_blocks(), m.filled_slots()) == distinct_views(labels, bs)
+            assert m.logical_tokens() == sum(len(v) for v in labels.values())
+
+
+class KeepDeadBeamsModel(BlockModel):
+    """Planted mistake: beams nobody continues are not ended."""
+    def beam_step(self, beams, parents, n_new=1):
+        new, kept = [], set()
+        for j in parents:
+            new.append(self.fork(beams[j]) if j in kept else beams[j])
+            kept.add(j)
+        for h in new:
+            self.append(h, n_new)
+        return new
+
+
+def test_beam_pin_catches_kept_dead_beams():
+    rng = np.random.default_rng(3)
+    m = KeepDeadBeamsModel(100000, 4)
+    root = m.add_seq()
+    m.append(root, 10)
+    beams = [root] + [m.fork(root) for _ in range(3)]
+    labels = {b: list(range(10)) for b in beams}
+    nxt = 10
+    for _ in range(6):
+        parents = [0, 0, 1, 1]
+        old = {b: list(labels[b]) for b in beams}
+        new = m.beam_step(beams, parents)
+        labels = {h: old[beams[parents[i]]] + [nxt + i] for i, h in enumerate(new)}
+        nxt += 4
+        beams = new
+    assert (m.used_blocks(), m.filled_slots()) != distinct_views(labels, 4)
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("bs,num_blocks", [(4, 60), (16, 2000)])
+def test_manager_beam_steps_match_model(pb, seed, bs, num_blocks):
+    rng = np.random.default_rng(200 + seed)
+    prod = pb.BlockManager(num_blocks, bs, seed=seed + 3)
+    model = BlockModel(num_blocks, bs)
+    handle_of = {}
+    reqs = []
+    for r in range(3):
+        P = int(rng.integers(1, 4 * bs))
+        pr, mr = prod.add_seq(), model.add_seq()
+        handle_of[pr] = mr
+        try:
+            model.append(mr, P)
+            prod.append(pr, P)
+        except ModelOutOfBlocks:
+            with pytest.raises(pb.OutOfBlocks):
+                prod.append(pr, P)
+            continue
+        beams = [pr]
+        for _ in range(int(rng.integers(2, 6)) - 1):
+            c = prod.fork(pr)
+            handle_of[c] = model.fork(mr)
+            beams.append(c)
+        reqs.append(beams)
+    for step in range(30):
+        for r, beams in enumerate(reqs):
+            parents = draw_parents(rng, len(beams))
+            n_new = int(rng.integers(1, 3))
+            try:
+                mnew = model.beam_step([handle_of[b] for b in beams], parents, n_new)
+            except ModelOutOfBlocks:
+                with pytest.raises(pb.OutOfBlocks):
+                    prod.beam_step(beams, parents, n_new)
+                continue
+            new, slots, pairs = prod.beam_step(beams, parents, n_new)
+            assert len(slots) == len(new) * n_new
+            gone = [b for j, b in enumerate(beams) if j not in parents]
+            for b in gone:
+                handle_of.pop(b)
+            for pid, h in zip(new, mnew):
+                handle_of[pid] = h
+            reqs[r] = list(new)
+            assert len(pairs) <= len(new)
+        assert prod.stats() == model.stats(), step
+        check_relabelling(prod, model, handle_of)
+        for beams in reqs:
+            assert prod.common_prefix(beams) == model.common_prefix([handle_of[b] for b in beams])
+
+
+def test_beam_step_host_checks(pb):
+    m = pb.BlockManager(20, 4)
+    a = m.add_seq()
+    m.append(a, 5)
+    b = m.fork(a)
+    with pytest.raises(pb.PkvError):
+        m.beam_step([a, b], [0, 2])
+    with pytest.raises(pb.PkvError):
+        m.beam_step([a, a], [0, 1])
+    with pytest.raises(pb.OutOfBlocks):
+        m.beam_step([a, b], [0, 0], 100)
+    assert m.stats()["live_seqs"] == 2 and m.seq_info(a) == (5, 2) and m.seq_info(b) == (5, 2)
