@@ -39,17 +39,18 @@ FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 
 
-def workload_bytes(st) -> dict:
+def workload_bytes(st, kv_elem_bytes: int | None = None) -> dict:
     """Algorithmic bytes of one step: attention reads each distinct cached
     (block, row) once for K and once for V plus q, and writes out; the cache
     write reads the new rows and writes them into the pools; each
     copy-on-write pair reads and writes one whole block of both pools."""
     cfg = st.cfg
     es = cfg.elem_bytes
-    row = cfg.num_kv_heads * cfg.head_dim * es           # one token, one of K/V, all kv heads
+    kes = es if kv_elem_bytes is None else kv_elem_bytes  # cached element (1 for fp8 pools)
+    row = cfg.num_kv_heads * cfg.head_dim * kes          # one token, one of K/V, all kv heads, as cached
     qo = st.num_seqs * cfg.num_heads * cfg.head_dim * es
     attn = 2 * st.unique_kv_tokens() * row + 2 * qo
-    cache_write = 2 * 2 * st.num_new_tokens * row
+    cache_write = 2 * st.num_new_tokens * (row // kes * es + row)  # read the new rows, write them cached
     copies = 2 * 2 * st.copy_pairs.shape[0] * cfg.block_size * row
     return {"attention": attn, "cache_write": cache_write, "copy": copies,
             "step": attn + cache_write + copies}
@@ -63,7 +64,7 @@ def describe_lengths(spec) -> str:
     return f"fixed {list(spec[1])}"
 
 
-def config_json(cfg, st, world: int, attention: str = "plain") -> dict:
+def config_json(cfg, st, world: int, attention: str = "plain", kv: str | None = None) -> dict:
     parts = [f"{cfg.name}-shaped decode step: {st.num_seqs} seqs, {cfg.num_heads} heads "
              f"({cfg.num_kv_heads} kv), head_dim {cfg.head_dim}, block_size {cfg.block_size}, "
              f"{cfg.dtype} storage with fp32 accumulation"]
@@ -79,13 +80,15 @@ def config_json(cfg, st, world: int, attention: str = "plain") -> dict:
             parts.append(f"plus reshape_and_cache of {st.num_new_tokens} new rows")
     parts.append(f"{cfg.num_blocks}-block pools")
     parts.append(f"{attention} attention")
+    if kv:
+        parts.append(kv)
     return {
         "workload": ", ".join(parts),
         "global_batch": st.num_seqs * world,
         "seq_len": int(st.max_context_len),
         "parallelism": "single GPU" if world == 1 else f"{world} independent replicas",
         "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write); step inputs "
-              f"{workload_bytes(st)['step'] / 1e9:.2f} GB",
+              f"{workload_bytes(st, 1 if kv else None)['step'] / 1e9:.2f} GB",
         "seed": cfg.seed,
     }
 
@@ -275,6 +278,23 @@ def aggregate(values: dict, world: int, device=None) -> dict:
     return {k: float(v) for k, v in zip(keys, t.tolist())}
 
 
+# fp8 pools: one scale per pool; |x| up to 6 (6 sigma of the N(0, 1) values) maps to 448
+FP8_SCALE = 6.0 / 448.0
+
+
+def fp8_pool(pool, scale: float, chunk: int = 2048):
+    """A 16-bit pool as e4m3 codes (uint8, same shape): x / scale clamped to
+    +-448 and rounded by PyTorch's float8 conversion; poisoned (NaN) rows stay
+    NaN. Input generation only: the timed step writes its rows with the
+    library's fp8 cache write."""
+    import torch
+    out = torch.empty(pool.shape, dtype=torch.uint8, device=pool.device)
+    for a in range(0, pool.shape[0], chunk):
+        x = (pool[a:a + chunk].float() / scale).clamp_(-448.0, 448.0)
+        out[a:a + chunk] = x.to(torch.float8_e4m3fn).view(torch.uint8)
+    return out
+
+
 def kv_memory(cfg) -> dict:
     """KV memory of the workload as the library's host block manager lays it
     out ("PagedAttention: the KV cache was the bottleneck all along", sections
@@ -321,7 +341,15 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         cfg = cfg.replace(seed=cfg.seed + rank)
     dw = SD.generate(cfg, device=dev)
     st = dw.st
-    nbytes = workload_bytes(st)
+    fp8 = args.kv == "fp8"
+    if fp8:
+        if args.attention != "plain" or cfg.dtype == "f32":
+            raise SystemExit("--kv fp8 takes the plain attention of a 16-bit workload")
+        dw.k_cache = fp8_pool(dw.k_cache, FP8_SCALE)
+        dw.v_cache = fp8_pool(dw.v_cache, FP8_SCALE)
+        torch.cuda.empty_cache()
+    kv_desc = (f"fp8 e4m3 K/V pools (per-pool scale {FP8_SCALE:.6g}; new rows rounded on write)" if fp8 else None)
+    nbytes = workload_bytes(st, 1 if fp8 else None)
     B, H, D = st.num_seqs, cfg.num_heads, cfg.head_dim
     mcl = st.max_context_len
     grouped = args.attention == "grouped"
@@ -343,10 +371,17 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         if has_copy:
             pkv.copy_blocks(dw.k_cache, dw.v_cache, dw.copy_pairs, dev_err=err)
         if has_new:
-            pkv.reshape_and_cache(dw.new_k, dw.new_v, dw.k_cache, dw.v_cache, dw.slot_mapping, dev_err=err)
+            if fp8:
+                pkv.reshape_and_cache_fp8(dw.new_k, dw.new_v, dw.k_cache, dw.v_cache, dw.slot_mapping, FP8_SCALE,
+                                          FP8_SCALE, dev_err=err)
+            else:
+                pkv.reshape_and_cache(dw.new_k, dw.new_v, dw.k_cache, dw.v_cache, dw.slot_mapping, dev_err=err)
 
     def attention():
-        if grouped:
+        if fp8:
+            pkv.paged_attention_decode_fp8(out, dw.q, dw.k_cache, dw.v_cache, dw.block_tables, dw.context_lens,
+                                           cfg.scale, FP8_SCALE, FP8_SCALE, mcl, workspace=ws, dev_err=err)
+        elif grouped:
             pkv.paged_attention_decode_grouped(out, dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
                                                dw.context_lens, cfg.scale, mcl, gs, sb, ws, dev_err=err)
         else:
@@ -430,8 +465,13 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
     achieved = nbytes["attention"] / (agg["decode_ms"] * 1e-3) / 1e9
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = time_oracle(cfg, args.cpu_seconds, args.cpu_seqs)
-        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        if fp8:
+            cpu = sampled_attention_baseline(cfg, dw.k_cache, dw.v_cache, st.block_tables, st.context_lens, dw.q,
+                                             args.cpu_seconds, args.cpu_seqs, "sequences (fp8 pools)",
+                                             fp8_scales=(FP8_SCALE, FP8_SCALE))
+        else:
+            cpu = time_oracle(cfg, args.cpu_seconds, args.cpu_seqs)
+            cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
     line = {
         "metric": METRIC,
         "value": world * nbytes["step"] / (agg["step_ms"] * 1e-3) / 1e9,
@@ -439,16 +479,17 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3),
         "ms_per_step": agg["step_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": cfg.dtype, "data": "synthetic",
-        "config": config_json(cfg, st, world, args.attention),
+        "dtype": f"{cfg.dtype} queries, fp8_e4m3 K/V" if fp8 else cfg.dtype, "data": "synthetic",
+        "config": config_json(cfg, st, world, args.attention, kv_desc),
         "seqs_per_s": world * B / (agg["step_ms"] * 1e-3),
         "attention_ms": agg["decode_ms"], "cache_ops_ms": agg["cache_ms"],
         "bytes_per_step": nbytes["step"], "roofline_frac_step": nbytes["step"] / (agg["step_ms"] * 1e-3) / 1e9 / peak,
         "roofline": {"bound": "hbm",
-                     "kernel": "pa_group_prologue + pa_decode_grouped_kernel" if grouped else "pa_decode_kernel",
+                     "kernel": ("pa_group_prologue + pa_decode_grouped_kernel" if grouped else
+                                "pa_decode_kernel<fp8 e4m3 cache>" if fp8 else "pa_decode_kernel"),
                      "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": profiled_traffic() if (cfg.name == WORKLOAD and not grouped) else None,
+                     "traffic": profiled_traffic() if (cfg.name == WORKLOAD and not grouped and not fp8) else None,
                      "algorithmic_bytes_per_launch": nbytes["attention"], "peak_source": peak_src},
         "cpu_baseline": cpu,
         "e2e": {"value": world * nbytes["step"] / (agg["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
@@ -464,38 +505,48 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
     return 0
 
 
-def beam_cpu_baseline(cfg, kc, vc, plan, q, min_seconds: float, n_beams: int) -> dict:
+def sampled_attention_baseline(cfg, kc, vc, block_tables, context_lens, q, min_seconds: float, n_seqs: int,
+                               what: str, fp8_scales=None) -> dict:
     """The fp64 oracle, as it stands, on the host cores: paged attention of
-    the first n_beams beams of the last step over host copies of their
-    blocks, repeated for about min_seconds."""
+    the first n_seqs sequences over host copies of their blocks (fp8 pools
+    when fp8_scales = (k_scale, v_scale)), repeated for about min_seconds."""
     import numpy as np
     import oracle
     from synth.device import to_storage
     threads = len(os.sched_getaffinity(0))
-    n = max(1, min(n_beams, plan.seqs.size))
-    bt, cl = plan.block_tables[:n], plan.context_lens[:n]
+    n = max(1, min(n_seqs, len(context_lens)))
+    bt, cl = np.ascontiguousarray(block_tables[:n]), np.ascontiguousarray(context_lens[:n])
     ids = np.unique(bt[bt >= 0])
     remap = np.full(cfg.num_blocks, -1, dtype=np.int32)
     remap[ids] = np.arange(ids.size, dtype=np.int32)
     bt_c = np.where(bt >= 0, remap[np.maximum(bt, 0)], -1).astype(np.int32)
     import torch
     idx = torch.from_numpy(ids.astype(np.int64)).to(kc.device)
-    k_h, v_h, q_h = to_storage(kc[idx]), to_storage(vc[idx]), to_storage(q[:n])
+    q_h = to_storage(q[:n])
+    if fp8_scales is None:
+        k_h, v_h = to_storage(kc[idx]), to_storage(vc[idx])
+    else:
+        k_h, v_h = kc[idx].cpu().numpy(), vc[idx].cpu().numpy()
     rows = {(int(b), r) for i in range(n) for j, b in enumerate(bt[i][bt[i] >= 0])
             for r in range(min(cfg.block_size, int(cl[i]) - j * cfg.block_size))}
-    nbytes = len(rows) * cfg.kv_bytes_per_token() + 2 * n * cfg.num_heads * cfg.head_dim * cfg.elem_bytes
+    kv_row = cfg.kv_bytes_per_token() // (1 if fp8_scales is None else cfg.elem_bytes)
+    nbytes = len(rows) * kv_row + 2 * n * cfg.num_heads * cfg.head_dim * cfg.elem_bytes
+    kw = dict(num_heads=cfg.num_heads, num_kv_heads=cfg.num_kv_heads, head_dim=cfg.head_dim,
+              block_size=cfg.block_size, threads=threads)
     times, t_start = [], time.perf_counter()
     while True:
         t0 = time.perf_counter()
-        oracle.paged_attention(q_h, k_h, v_h, bt_c, cl, scale=cfg.scale, num_heads=cfg.num_heads,
-                               num_kv_heads=cfg.num_kv_heads, head_dim=cfg.head_dim, block_size=cfg.block_size,
-                               dtype=cfg.dtype, threads=threads)
+        if fp8_scales is None:
+            oracle.paged_attention(q_h, k_h, v_h, bt_c, cl, scale=cfg.scale, dtype=cfg.dtype, **kw)
+        else:
+            oracle.paged_attention_fp8(q_h, k_h, v_h, bt_c, cl, scale=cfg.scale, k_scale=fp8_scales[0],
+                                       v_scale=fp8_scales[1], q_dtype=cfg.dtype, **kw)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_start >= min_seconds:
             break
     mean = sum(times) / len(times)
     return {"value": nbytes / mean / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": (f"attention of the first {n} of {plan.seqs.size} beams at the last step "
+            "sample": (f"attention of the first {n} of {len(context_lens)} {what} "
                        f"({int(cl.sum())} tokens x {cfg.num_heads} heads, {len(rows)} distinct cached tokens), "
                        f"{len(times)} run(s), {mean * 1e3:.1f} ms each")}
 
@@ -648,7 +699,8 @@ def run_beam(args, rank: int, world: int, local_rank: int) -> int:
     achieved = bytes_attn / (agg["attn_ms"] * 1e-3) / 1e9
     cpu = None
     if not args.no_cpu_baseline:
-        cpu = beam_cpu_baseline(cfg, kc, vc, plan, q, args.cpu_seconds, args.cpu_seqs)
+        cpu = sampled_attention_baseline(cfg, kc, vc, plan.block_tables, plan.context_lens, q, args.cpu_seconds,
+                                         args.cpu_seqs, "beams at the last step")
     st = dec.manager.stats()
     import paged_kv_cache_204_gb300.block_manager as pbm
     mm = pbm.memory_metrics(st, cfg.block_size)
@@ -700,6 +752,8 @@ def main() -> int:
     ap.add_argument("--workload", default=WORKLOAD,
                     help="synthetic workload preset (default: the LLaMA-13B-shaped step); "
                          "'beam': beam-search decode steps")
+    ap.add_argument("--kv", choices=("native", "fp8"), default="native",
+                    help="fp8: K/V pools of e4m3 codes with one scale per pool (plain attention)")
     ap.add_argument("--attention", choices=("plain", "grouped"), default="plain",
                     help="grouped: siblings read shared prefix blocks once (copy-on-write workloads)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum time of the CPU baseline")

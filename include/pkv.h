@@ -66,9 +66,11 @@ extern "C" {
 typedef struct CUstream_st* pkv_stream_t;
 
 typedef enum pkv_dtype {
-  PKV_F32 = 0,  /* IEEE binary32 */
-  PKV_F16 = 1,  /* IEEE binary16 */
-  PKV_BF16 = 2  /* bfloat16      */
+  PKV_F32 = 0,      /* IEEE binary32 */
+  PKV_F16 = 1,      /* IEEE binary16 */
+  PKV_BF16 = 2,     /* bfloat16      */
+  PKV_FP8_E4M3 = 3  /* 8-bit float, 1 sign, 4 exponent (bias 7), 3 mantissa bits, no infinities,
+                       largest finite 448 (OCP "E4M3"); cache element type only, see the fp8 entry points */
 } pkv_dtype;
 
 typedef enum pkv_status {
@@ -300,6 +302,47 @@ pkv_status pkv_paged_attention_decode_noalloc(void* out, const void* q, const vo
                                               int num_seqs, int max_blocks_per_seq, int num_blocks,
                                               int max_context_len, pkv_dtype dtype, int32_t* dev_err,
                                               pkv_stream_t stream);
+
+/* ----------------------------------------------------------------------
+ * fp8 KV cache
+ *
+ * [QKV] "Efficient Memory Management for Large Language Model Serving with
+ * PagedAttention" (hackerpapers page), section "In the conversation": a
+ * reader notes that quantising the KV cache cuts its memory footprint. The
+ * format here is this library's choice: the two pools hold PKV_FP8_E4M3
+ * codes (one byte per element, same [num_blocks][num_kv_heads][block_size]
+ * [head_dim] layout, so a block is half the bytes of a 16-bit one) with one
+ * scale per pool: element x is stored as e4m3(x / scale), the quotient taken
+ * in binary32 with round-to-nearest-even, then rounded to the nearest e4m3
+ * value (ties to even) and saturated to +-448; the value read back is
+ * scale * code. Queries and outputs stay binary16 or bfloat16. Attention
+ * over an fp8 cache computes exactly what pkv_paged_attention_decode
+ * computes over the decoded values (in fp32, up to rounding order).
+ * pkv_copy_blocks copies fp8 blocks when given dtype PKV_FP8_E4M3.
+ * ---------------------------------------------------------------------- */
+
+/* Write new K/V rows into fp8 caches ([QKV], [VM]): k, v [num_tokens]
+ * [num_kv_heads][head_dim] of src_dtype (PKV_F16 or PKV_BF16, 16-byte
+ * aligned); caches of PKV_FP8_E4M3 codes; slots as in pkv_reshape_and_cache.
+ * k_scale, v_scale: finite and > 0 (PKV_ERR_INVALID_ARG otherwise). */
+pkv_status pkv_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                                     const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                     int head_dim, int block_size, int num_blocks, pkv_dtype src_dtype,
+                                     float k_scale, float v_scale, int32_t* dev_err, pkv_stream_t stream);
+
+/* pkv_paged_attention_decode over fp8 caches ([QKV], [VM]): the same
+ * arguments, layouts, workspace and error behaviour, with k_cache and v_cache
+ * holding PKV_FP8_E4M3 codes and `dtype` (PKV_F16 or PKV_BF16) the type of q
+ * and out. Logits are scale * (q . (k_scale * K_code)) and the output is the
+ * softmax-weighted sum of v_scale * V_code. k_scale, v_scale: finite, > 0. */
+pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* block_tables,
+                                          const int32_t* context_lens, float scale, float k_scale,
+                                          float v_scale, int num_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int num_seqs, int max_blocks_per_seq,
+                                          int num_blocks, int max_context_len, pkv_dtype dtype,
+                                          void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                          pkv_stream_t stream);
 
 /* Bytes of workspace pkv_paged_attention_decode needs for these sizes: the
  * segment counters (num_seqs * num_heads int32) plus a fixed area for the

@@ -69,6 +69,15 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.orc_decode_bf16.restype = D
     L.orc_decode_f32.argtypes = [ctypes.c_uint32]
     L.orc_decode_f32.restype = D
+    L.orc_decode_e4m3.argtypes = [ctypes.c_uint8]
+    L.orc_decode_e4m3.restype = D
+    L.orc_encode_e4m3.argtypes = [D]
+    L.orc_encode_e4m3.restype = ctypes.c_uint8
+    F = ctypes.c_float
+    L.orc_reshape_and_cache_fp8.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, F]
+    L.orc_reshape_and_cache_fp8.restype = I
+    L.orc_paged_attention_fp8.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, D, D, D, I, I]
+    L.orc_paged_attention_fp8.restype = I
     return L
 
 
@@ -243,3 +252,65 @@ def decode_step(hp, hw, threads: int = 1, L=None) -> tuple[np.ndarray, np.ndarra
                           head_dim=cfg.head_dim, block_size=cfg.block_size, dtype=cfg.dtype,
                           threads=threads, L=L)
     return out, hp.k_cache, hp.v_cache
+
+
+# ---- fp8 (e4m3) KV cache ------------------------------------------------------
+
+def decode_e4m3(codes: np.ndarray, L=None) -> np.ndarray:
+    """E4M3 codes (uint8) -> float64, with the oracle's own decoder."""
+    L = L or lib()
+    flat = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1)
+    return np.array([L.orc_decode_e4m3(int(c)) for c in flat], dtype=np.float64).reshape(np.shape(codes))
+
+
+def encode_e4m3(values: np.ndarray, L=None) -> np.ndarray:
+    """float64 values -> nearest E4M3 codes (ties to even, saturating)."""
+    L = L or lib()
+    flat = np.ascontiguousarray(values, dtype=np.float64).reshape(-1)
+    return np.array([L.orc_encode_e4m3(float(x)) for x in flat], dtype=np.uint8).reshape(np.shape(values))
+
+
+def reshape_and_cache_fp8(k, v, k_cache, v_cache, slot_mapping, *, num_kv_heads, head_dim, block_size,
+                          src_dtype, k_scale, v_scale, L=None) -> int:
+    """In place on the uint8 pools: token t's rows, divided by the scale in
+    binary32 and rounded to E4M3, go to slot slot_mapping[t]. Returns the
+    number of out-of-range slots."""
+    L = L or lib()
+    for a, n in ((k, "k"), (v, "v")):
+        _check_store(a, src_dtype, n)
+    for a, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        if a.dtype != np.uint8:
+            raise TypeError(f"{n}: e4m3 pools must be uint8, got {a.dtype}")
+    sl = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    rc = L.orc_reshape_and_cache_fp8(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(sl), sl.shape[0],
+                                     num_kv_heads, head_dim, block_size, k_cache.shape[0], DTYPE_CODE[src_dtype],
+                                     float(k_scale), float(v_scale))
+    if rc < 0:
+        raise ValueError(f"orc_reshape_and_cache_fp8 failed with code {rc}")
+    return rc
+
+
+def paged_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, *, scale, k_scale, v_scale, num_heads,
+                        num_kv_heads, head_dim, block_size, q_dtype, threads: int = 1, L=None) -> np.ndarray:
+    """Decode attention over E4M3 pools, fp64: paged_attention with K
+    elements k_scale * code and V elements v_scale * code."""
+    L = L or lib()
+    _check_store(q, q_dtype, "q")
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B = cl.shape[0]
+    out = np.zeros((B, num_heads, head_dim), dtype=np.float64)
+
+    def run(lo, hi):
+        return L.orc_paged_attention_fp8(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), bt.shape[1],
+                                         _ptr(cl), B, num_heads, num_kv_heads, head_dim, block_size,
+                                         k_cache.shape[0], DTYPE_CODE[q_dtype], float(scale), float(k_scale),
+                                         float(v_scale), lo, hi)
+
+    n = max(1, min(threads, B))
+    cuts = [B * i // n for i in range(n + 1)]
+    with ThreadPoolExecutor(max_workers=n) as ex:
+        rcs = list(ex.map(lambda i: run(cuts[i], cuts[i + 1]), range(n)))
+    if any(rc != 0 for rc in rcs):
+        raise ValueError(f"orc_paged_attention_fp8 failed with codes {rcs}")
+    return out

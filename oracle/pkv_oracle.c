@@ -394,3 +394,159 @@ int orc_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pairs, in
   }
   return bad;
 }
+
+/* ---- fp8 (e4m3) KV cache ------------------------------------------------ */
+/*
+ * [QKV] "Efficient Memory Management for Large Language Model Serving with
+ * PagedAttention" (hackerpapers page), "In the conversation": quantising the
+ * KV cache cuts its memory footprint. Format (the reading this oracle takes):
+ * OCP E4M3 codes, sign(1) exponent(4, bias 7) mantissa(3), no infinities,
+ * S.1111.111 is NaN, largest finite 448; one scale per pool; element x is
+ * stored as e4m3(binary32(x / scale)) and read back as scale * code.
+ */
+
+/* E4M3 code -> value. */
+double orc_decode_e4m3(uint8_t bits) {
+  int sign = (bits >> 7) & 1;
+  int e = (bits >> 3) & 0xf;
+  int m = bits & 0x7;
+  double mag;
+  if (e == 0)
+    mag = ldexp((double)m, -9); /* subnormal: m/8 * 2^(1-7) */
+  else if (e == 15 && m == 7)
+    mag = NAN;
+  else
+    mag = ldexp((double)(m + 8), e - 10); /* (1 + m/8) * 2^(e-7) */
+  return sign ? -mag : mag;
+}
+
+/* value -> nearest E4M3 code, ties to the even code, finite values beyond
+ * the largest (and infinities) saturated to +-448, NaN to 0x7f. The grid is
+ * uniform with spacing 2^-9 below 2^-6 (subnormals) and 2^(E-3) in
+ * [2^E, 2^(E+1)); codes count up along it, so a rounded grid index that
+ * carries into the next binade is still the right code. */
+uint8_t orc_encode_e4m3(double x) {
+  if (isnan(x)) return 0x7f;
+  const uint8_t sign = signbit(x) ? 0x80 : 0x00;
+  const double a = fabs(x);
+  if (a > 448.0) return sign | 0x7e;
+  int code;
+  if (a < ldexp(1.0, -6)) {
+    code = (int)rint(a * 512.0); /* multiples of 2^-9; 8 is the smallest normal */
+  } else {
+    int k;
+    frexp(a, &k); /* a = f * 2^k, f in [0.5, 1) */
+    const int E = k - 1;
+    const int n = (int)rint(ldexp(a, 3 - E)); /* in [8, 16] */
+    code = (E + 7) * 8 + (n - 8);
+  }
+  if (code > 0x7e) code = 0x7e;
+  return (uint8_t)(sign | code);
+}
+
+/*
+ * Cache write into e4m3 pools ([QKV], [VM]): for token t with slot s >= 0,
+ * every element x of its K (V) rows becomes orc_encode_e4m3 of the binary32
+ * quotient (float)x / k_scale (v_scale), stored at cache[s / bs][h][s % bs].
+ * k, v are binary16 or bfloat16 (src_dtype). Returns the number of
+ * out-of-range slots (not written), or a negative code.
+ */
+int orc_reshape_and_cache_fp8(const void* k, const void* v, uint8_t* k_cache, uint8_t* v_cache,
+                              const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                              int block_size, int num_blocks, int src_dtype, float k_scale, float v_scale) {
+  if ((src_dtype != ORC_F16 && src_dtype != ORC_BF16) || num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      block_size <= 0 || num_blocks <= 0 || !(k_scale > 0.0f) || !(v_scale > 0.0f))
+    return -1;
+  if (num_tokens && (!k || !v || !k_cache || !v_cache || !slot_mapping)) return -1;
+  int bad = 0;
+  for (int t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= (int64_t)num_blocks * block_size) {
+      ++bad;
+      continue;
+    }
+    const int64_t blk = slot / block_size, off = slot % block_size;
+    for (int h = 0; h < num_kv_heads; ++h)
+      for (int d = 0; d < head_dim; ++d) {
+        const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + (size_t)off) * head_dim + d;
+        const size_t src = ((size_t)t * num_kv_heads + h) * head_dim + d;
+        const float kq = (float)elem(k, src, src_dtype) / k_scale; /* binary32 division */
+        const float vq = (float)elem(v, src, src_dtype) / v_scale;
+        k_cache[dst] = orc_encode_e4m3((double)kq);
+        v_cache[dst] = orc_encode_e4m3((double)vq);
+      }
+  }
+  return bad;
+}
+
+/*
+ * Paged decode attention over e4m3 pools ([QKV], [VM]): the definition of
+ * orc_paged_attention with K element = k_scale * decode(code) and V element =
+ * v_scale * decode(code); q in q_dtype. out[s][h][:] for s in
+ * [seq_begin, seq_end). Returns 0 or a negative code.
+ */
+int orc_paged_attention_fp8(double* out, const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                            const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                            int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                            int num_blocks, int q_dtype, double scale, double k_scale, double v_scale,
+                            int seq_begin, int seq_end) {
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return -1;
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return -2;
+  if (head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || !elem_bytes(q_dtype)) return -3;
+  if (seq_begin < 0 || seq_end > num_seqs || seq_begin > seq_end) return -4;
+  const int group = num_heads / num_kv_heads;
+  int max_len = 0;
+  for (int s = seq_begin; s < seq_end; ++s) {
+    if (context_lens[s] < 0 || context_lens[s] > max_blocks_per_seq * block_size) return -5;
+    if (context_lens[s] > max_len) max_len = context_lens[s];
+  }
+  double* x = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+  size_t* row = (size_t*)malloc(sizeof(size_t) * (size_t)(max_len > 0 ? max_len : 1));
+  if (!x || !row) {
+    free(x);
+    free(row);
+    return -6;
+  }
+  int rc = 0;
+  for (int s = seq_begin; s < seq_end && rc == 0; ++s) {
+    const int L = context_lens[s];
+    for (int h = 0; h < num_heads; ++h) {
+      const int g = h / group;
+      double* o = out + ((size_t)s * num_heads + h) * head_dim;
+      if (L == 0) {
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        continue;
+      }
+      const size_t q_off = ((size_t)s * num_heads + h) * head_dim;
+      for (int t = 0; t < L; ++t) {
+        const int32_t p = block_tables[(size_t)s * max_blocks_per_seq + t / block_size];
+        if (p < 0 || p >= num_blocks) {
+          rc = -7;
+          break;
+        }
+        row[t] = (((size_t)p * num_kv_heads + g) * block_size + (size_t)(t % block_size)) * head_dim;
+        double acc = 0.0;
+        for (int d = 0; d < head_dim; ++d)
+          acc += elem(q, q_off + (size_t)d, q_dtype) * (k_scale * orc_decode_e4m3(k_cache[row[t] + (size_t)d]));
+        x[t] = scale * acc;
+      }
+      if (rc) break;
+      double m = -INFINITY, z = 0.0;
+      for (int t = 0; t < L; ++t)
+        if (x[t] > m) m = x[t];
+      for (int t = 0; t < L; ++t) {
+        x[t] = exp(x[t] - m);
+        z += x[t];
+      }
+      for (int d = 0; d < head_dim; ++d) {
+        double acc = 0.0;
+        for (int t = 0; t < L; ++t) acc += x[t] * (v_scale * orc_decode_e4m3(v_cache[row[t] + (size_t)d]));
+        o[d] = acc / z;
+      }
+    }
+  }
+  free(x);
+  free(row);
+  return rc;
+}

@@ -12,6 +12,7 @@ Functions mirror the C entry points:
   paged_attention_decode  -> pkv_paged_attention_decode
   decode_workspace_bytes  -> pkv_decode_workspace_bytes
   paged_attention_decode_grouped  -> pkv_paged_attention_decode_grouped
+  reshape_and_cache_fp8, paged_attention_decode_fp8  -> the fp8 (e4m3) cache entry points
   decode_grouped_workspace_bytes  -> pkv_decode_grouped_workspace_bytes
   set_wait_timeout_ns / get_wait_timeout_ns, status_string, version
 The host block manager (include/pkv_block_manager.h) is wrapped by
@@ -37,7 +38,8 @@ lib = ctypes.CDLL(LIB_PATH)
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_WORKSPACE, PKV_ERR_CUDA, PKV_ERR_OUT_OF_BLOCKS = range(6)
 DEV_ERR_BLOCK_ID, DEV_ERR_SLOT, DEV_ERR_CONTEXT_LEN, DEV_ERR_TIMEOUT, DEV_ERR_PAIR = 1, 2, 4, 8, 16
 DEV_ERR_GROUP = 32
-DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.uint8: 3}  # uint8: e4m3 codes
+PKV_FP8_E4M3 = 3
 
 _P, _I, _I64, _U64, _F, _SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64,
                                ctypes.c_float, ctypes.c_size_t)
@@ -63,6 +65,11 @@ lib.pkv_paged_attention_decode_grouped.argtypes = [_P, _P, _P, _P, _P, _P, _F, _
 lib.pkv_paged_attention_decode_grouped.restype = _I
 lib.pkv_decode_grouped_workspace_bytes.argtypes = [_I, _I, _I, _I, _I]
 lib.pkv_decode_grouped_workspace_bytes.restype = _SZ
+lib.pkv_reshape_and_cache_fp8.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _F, _F, _P, _P]
+lib.pkv_reshape_and_cache_fp8.restype = _I
+lib.pkv_paged_attention_decode_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _F, _F, _F, _I, _I, _I, _I, _I, _I, _I,
+                                               _I, _I, _P, _SZ, _P, _P]
+lib.pkv_paged_attention_decode_fp8.restype = _I
 lib.pkv_paged_attention_decode_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I,
                                                    _I, _I, _I, _P, _P]
 lib.pkv_paged_attention_decode_noalloc.restype = _I
@@ -169,6 +176,35 @@ def paged_attention_decode_noalloc(out: torch.Tensor, q: torch.Tensor, k_cache: 
         float(scale), H, Hkv, D, bs, B, block_tables.shape[1], nb, int(max_context_len),
         DTYPE_CODE[q.dtype], _ptr(dev_err), _stream(stream)),
         "pkv_paged_attention_decode_noalloc")
+
+
+def reshape_and_cache_fp8(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          slot_mapping: torch.Tensor, k_scale: float, v_scale: float,
+                          dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """k, v [T, Hkv, D] fp16/bf16; k_cache, v_cache uint8 [num_blocks, Hkv,
+    block_size, D] of e4m3 codes; element x is stored as e4m3(x / scale)."""
+    T, Hkv, D = k.shape
+    nb, _, bs, _ = k_cache.shape
+    _check(lib.pkv_reshape_and_cache_fp8(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), T, Hkv,
+                                         D, bs, nb, DTYPE_CODE[k.dtype], float(k_scale), float(v_scale), _ptr(dev_err),
+                                         _stream(stream)), "pkv_reshape_and_cache_fp8")
+
+
+def paged_attention_decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                               k_scale: float, v_scale: float, max_context_len: int,
+                               workspace: torch.Tensor | None = None, dev_err: torch.Tensor | None = None,
+                               stream=None) -> None:
+    """paged_attention_decode over uint8 pools of e4m3 codes: K values are
+    k_scale * code, V values v_scale * code; q, out fp16/bf16."""
+    B, H, D = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pkv_paged_attention_decode_fp8(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        float(scale), float(k_scale), float(v_scale), H, Hkv, D, bs, B, block_tables.shape[1], nb,
+        int(max_context_len), DTYPE_CODE[q.dtype], _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)),
+        "pkv_paged_attention_decode_fp8")
 
 
 def decode_grouped_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,

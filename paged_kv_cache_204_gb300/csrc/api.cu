@@ -17,7 +17,9 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 bool supported_head_dim(int d) { return d == 64 || d == 128; }
 bool supported_block_size(int b) { return b == 8 || b == 16 || b == 32; }
 bool valid_dtype(int t) { return t == PKV_F32 || t == PKV_F16 || t == PKV_BF16; }
-int elem_bytes(int t) { return t == PKV_F32 ? 4 : 2; }
+bool valid_cache_dtype(int t) { return valid_dtype(t) || t == PKV_FP8_E4M3; }
+int elem_bytes(int t) { return t == PKV_F32 ? 4 : (t == PKV_FP8_E4M3 ? 1 : 2); }
+bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WorkspaceLayout {
@@ -118,6 +120,7 @@ pkv::DecodeParams decode_params(void* out, const void* q, const void* k_cache, c
   p.max_context_len = max_context_len;
   p.dev_err = dev_err;
   p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
+  p.v_scale = 1.f;
   return p;
 }
 
@@ -175,7 +178,7 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pa
                            pkv_dtype dtype, int32_t* dev_err, pkv_stream_t stream) {
   if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
     return PKV_ERR_INVALID_ARG;
-  if (!valid_dtype(dtype) || !supported_head_dim(head_dim) || !supported_block_size(block_size))
+  if (!valid_cache_dtype(dtype) || !supported_head_dim(head_dim) || !supported_block_size(block_size))
     return PKV_ERR_UNSUPPORTED;
   if (num_pairs == 0) return PKV_OK;
   if (!k_cache || !v_cache || !block_pairs) return PKV_ERR_INVALID_ARG;
@@ -211,6 +214,58 @@ pkv_status pkv_paged_attention_decode(void* out, const void* q, const void* k_ca
   pkv::DecodeParams p = decode_params(out, q, k_cache, v_cache, block_tables, context_lens, scale,
                                       num_heads, num_kv_heads, block_size, num_seqs, max_blocks_per_seq,
                                       num_blocks, max_context_len, gpw, dev_err);
+  char* wsb = static_cast<char*>(workspace);
+  p.ws_counter = reinterpret_cast<int32_t*>(wsb + ws.counter_off);
+  p.ws_ml = reinterpret_cast<float2*>(wsb + ws.ml_off);
+  p.ws_o = reinterpret_cast<float*>(wsb + ws.o_off);
+  return launch_status(launch(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                                     const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                     int head_dim, int block_size, int num_blocks, pkv_dtype src_dtype,
+                                     float k_scale, float v_scale, int32_t* dev_err, pkv_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0 ||
+      !valid_scale(k_scale) || !valid_scale(v_scale))
+    return PKV_ERR_INVALID_ARG;
+  if ((src_dtype != PKV_F16 && src_dtype != PKV_BF16) || !supported_head_dim(head_dim) ||
+      !supported_block_size(block_size))
+    return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8) || (dev_err && !aligned(dev_err, 4)))
+    return PKV_ERR_INVALID_ARG;
+  return launch_status(pkv::launch_reshape_and_cache_fp8(
+      k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim, block_size, num_blocks,
+      src_dtype == PKV_BF16 ? 1 : 0, k_scale, v_scale, dev_err, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, const void* k_cache,
+                                          const void* v_cache, const int32_t* block_tables,
+                                          const int32_t* context_lens, float scale, float k_scale,
+                                          float v_scale, int num_heads, int num_kv_heads, int head_dim,
+                                          int block_size, int num_seqs, int max_blocks_per_seq,
+                                          int num_blocks, int max_context_len, pkv_dtype dtype,
+                                          void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                                          pkv_stream_t stream) {
+  if (!valid_scale(k_scale) || !valid_scale(v_scale)) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F16 && dtype != PKV_BF16 && valid_dtype(dtype)) return PKV_ERR_UNSUPPORTED;
+  const pkv_status st = check_decode_args(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                          num_heads, num_kv_heads, head_dim, block_size, num_seqs,
+                                          max_blocks_per_seq, num_blocks, max_context_len, dtype, dev_err);
+  if (st != PKV_OK || num_seqs == 0) return st;
+  const WorkspaceLayout ws = workspace_layout(num_seqs, num_heads, head_dim);
+  if (!workspace || workspace_bytes < ws.total) return PKV_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
+  const int gpw = heads_per_warp(num_heads / num_kv_heads);
+  const int gpw_index = gpw == 4 ? 2 : (gpw == 2 ? 1 : 0);
+  pkv::DecodeLauncher launch = pkv::decode_launcher_fp8(dtype == PKV_BF16 ? 1 : 0, head_dim, gpw_index);
+  if (!launch) return PKV_ERR_UNSUPPORTED;
+  pkv::DecodeParams p = decode_params(out, q, k_cache, v_cache, block_tables, context_lens, scale * k_scale,
+                                      num_heads, num_kv_heads, block_size, num_seqs, max_blocks_per_seq,
+                                      num_blocks, max_context_len, gpw, dev_err);
+  p.v_scale = v_scale;
   char* wsb = static_cast<char*>(workspace);
   p.ws_counter = reinterpret_cast<int32_t*>(wsb + ws.counter_off);
   p.ws_ml = reinterpret_cast<float2*>(wsb + ws.ml_off);

@@ -37,6 +37,45 @@ __global__ void __launch_bounds__(128)
   v_cache[dst] = vx;
 }
 
+// fp8 e4m3 cache write. grid = (new token, group of 128 eight-element runs):
+// each thread reads 8 elements (16 bytes) of the token's K row and V row,
+// divides them by k_scale / v_scale in fp32 (IEEE rounding) and stores the
+// e4m3 codes (8 bytes) at cache[slot / bs][h][slot % bs].
+template <typename T>
+__global__ void __launch_bounds__(128)
+    reshape_and_cache_fp8_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                 uint2* __restrict__ k_cache, uint2* __restrict__ v_cache,
+                                 const int64_t* __restrict__ slot_mapping, int num_kv_heads, int row_runs,
+                                 int block_size, int64_t num_slots, float k_scale, float v_scale,
+                                 int32_t* dev_err) {
+  const int t = blockIdx.x;
+  const int64_t slot = __ldg(slot_mapping + t);
+  if (slot < 0) return;
+  if (slot >= num_slots) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) set_err(dev_err, PKV_DEV_ERR_SLOT);
+    return;
+  }
+  const int n = num_kv_heads * row_runs;
+  const int c = blockIdx.y * blockDim.x + threadIdx.x;
+  if (c >= n) return;
+  const int64_t blk = slot / block_size;
+  const int off = static_cast<int>(slot - blk * block_size);
+  const int h = c / row_runs;
+  const int cc = c - h * row_runs;
+  const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * row_runs + cc;
+  float fk[8], fv[8];
+  Chunk<T>::widen(__ldg(k + (size_t)t * n + c), fk);
+  Chunk<T>::widen(__ldg(v + (size_t)t * n + c), fv);
+  uint32_t wk[4], wv[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    wk[i] = narrow_e4m3x2(__fdiv_rn(fk[2 * i], k_scale), __fdiv_rn(fk[2 * i + 1], k_scale));
+    wv[i] = narrow_e4m3x2(__fdiv_rn(fv[2 * i], v_scale), __fdiv_rn(fv[2 * i + 1], v_scale));
+  }
+  k_cache[dst] = make_uint2(wk[0] | (wk[1] << 16), wk[2] | (wk[3] << 16));
+  v_cache[dst] = make_uint2(wv[0] | (wv[1] << 16), wv[2] | (wv[3] << 16));
+}
+
 // grid = (pair, pool K|V, piece). Each piece streams part of one block with
 // 4 independent 16-byte loads in flight per thread.
 __global__ void __launch_bounds__(256)
@@ -74,6 +113,25 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
       static_cast<uint4*>(v_cache), slot_mapping, num_kv_heads, row_bytes / 16, block_size,
       (int64_t)num_blocks * block_size, dev_err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                                         const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                         int head_dim, int block_size, int num_blocks, int is_bf16, float k_scale,
+                                         float v_scale, int32_t* dev_err, cudaStream_t stream) {
+  const int runs = head_dim / 8;
+  const int n = num_kv_heads * runs;
+  const dim3 grid(num_tokens, (n + 127) / 128);
+  const int64_t slots = (int64_t)num_blocks * block_size;
+  if (is_bf16)
+    reshape_and_cache_fp8_kernel<__nv_bfloat16><<<grid, 128, 0, stream>>>(
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint2*>(k_cache),
+        static_cast<uint2*>(v_cache), slot_mapping, num_kv_heads, runs, block_size, slots, k_scale, v_scale, dev_err);
+  else
+    reshape_and_cache_fp8_kernel<__half><<<grid, 128, 0, stream>>>(
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint2*>(k_cache),
+        static_cast<uint2*>(v_cache), slot_mapping, num_kv_heads, runs, block_size, slots, k_scale, v_scale, dev_err);
   return cudaGetLastError();
 }
 

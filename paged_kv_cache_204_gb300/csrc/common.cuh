@@ -3,6 +3,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -167,6 +168,28 @@ struct Chunk<__nv_bfloat16> {
     return make_uint4(w[0], w[1], w[2], w[3]);
   }
 };
+
+// fp8 e4m3 cache elements: 8 codes (one uint2) <-> 8 floats. Every e4m3
+// value is exactly a binary16 value, so widening is exact; narrowing rounds
+// to nearest even and saturates finite values to +-448 (NaN stays NaN).
+__device__ __forceinline__ void widen_e4m3x8(const uint2& u, float (&f)[8]) {
+  const uint32_t w[2] = {u.x, u.y};
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * j)) & 0xffffu);
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+      __half2 h;
+      memcpy(&h, &hr, 4);
+      const float2 t = __half22float2(h);
+      f[4 * i + 2 * j] = t.x;
+      f[4 * i + 2 * j + 1] = t.y;
+    }
+}
+__device__ __forceinline__ uint16_t narrow_e4m3x2(float a, float b) {
+  return static_cast<uint16_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3));
+}
 
 __device__ __forceinline__ void store_elem(float* p, float x) { *p = x; }
 __device__ __forceinline__ void store_elem(__half* p, float x) { *p = __float2half_rn(x); }

@@ -35,6 +35,8 @@
 // poisoned rows never reach the result.
 #pragma once
 
+#include <type_traits>
+
 #include "common.cuh"
 
 namespace pkv {
@@ -61,19 +63,88 @@ struct DecodeParams {
   float* ws_o;          // [kMaxDecodeWarps][2][GPW][head_dim]
   int32_t* dev_err;
   uint64_t wait_limit_ns;
+  float v_scale;  // fp8 caches: stored V times v_scale is the value (1 otherwise)
 };
 
-constexpr int kTileTokens = 16;
+constexpr int kTileTokens = 16;  // tokens of a tile of a 16- or 32-bit cache
+
+// Tokens per tile of the plain kernel: fp8 caches take 32-token tiles, so a
+// tile carries as many bytes (and a warp's per-tile work as much data) as a
+// 16-token tile of a 16-bit cache.
+template <typename KT>
+constexpr int tile_tokens_for() { return sizeof(KT) == 1 ? 2 * kTileTokens : kTileTokens; }
 constexpr int kDecodeWarps = 8;  // one resident block of 8 warps per SM (measured best)
 constexpr int kMaxDecodeWarps = 4096;  // bound of the persistent grid (partial slots in the workspace)
 constexpr int kMaxGroupPerWarp = 4;    // query heads one warp serves against one kv head
 constexpr int kBtChunk = 128;          // block-table entries a warp keeps in shared memory
 
-template <typename T, int D, int GPW>
+// Which head dims lane `sub` of an 8-lane row group owns, and how it reads
+// them from a cache row (element KT) and from a query / output row (T).
+// Same element type: 16-byte chunks sub, sub + 8, ... of the row. fp8
+// caches: one run of D / 8 dims starting at dim sub * D / 8 (8 or 16 codes),
+// so a quarter-warp still reads one whole cache row.
+template <typename T, typename KT, int D>
+struct LaneDims {
+  static constexpr int kVec = Chunk<T>::kElems;
+  static constexpr int kParts = D * (int)sizeof(T) / 16 / 8;  // chunks per lane per row
+  static constexpr int kPartElems = kVec;
+  __device__ __forceinline__ static int dim(int sub, int k, int e) { return (sub + 8 * k) * kVec + e; }
+  __device__ __forceinline__ static void kv(const unsigned char* row, int sub, int k, float (&f)[kPartElems]) {
+    Chunk<T>::widen(reinterpret_cast<const uint4*>(row)[sub + 8 * k], f);
+  }
+  __device__ __forceinline__ static void q(const unsigned char* row, int sub, int k, float (&f)[kPartElems]) {
+    Chunk<T>::widen(reinterpret_cast<const uint4*>(row)[sub + 8 * k], f);
+  }
+  __device__ __forceinline__ static void out(unsigned char* row, int sub, int k, const float (&f)[kPartElems]) {
+    reinterpret_cast<uint4*>(row)[sub + 8 * k] = Chunk<T>::narrow(f);
+  }
+};
+template <typename T, int D>
+struct LaneDims<T, __nv_fp8_e4m3, D> {
+  static_assert(sizeof(T) == 2, "fp8 caches take 16-bit queries");
+  static constexpr int kParts = 1;
+  static constexpr int kPartElems = D / 8;         // 8 or 16 dims
+  static constexpr int kQChunks = kPartElems / 8;  // 16-byte chunks of T per lane
+  __device__ __forceinline__ static int dim(int sub, int, int e) { return sub * kPartElems + e; }
+  __device__ __forceinline__ static void kv(const unsigned char* row, int sub, int, float (&f)[kPartElems]) {
+    const uint2* r = reinterpret_cast<const uint2*>(row + sub * kPartElems);
+#pragma unroll
+    for (int c = 0; c < kPartElems / 8; ++c) {
+      float g[8];
+      widen_e4m3x8(r[c], g);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[8 * c + e] = g[e];
+    }
+  }
+  __device__ __forceinline__ static void q(const unsigned char* row, int sub, int, float (&f)[kPartElems]) {
+    const uint4* r = reinterpret_cast<const uint4*>(row + sub * kPartElems * 2);
+#pragma unroll
+    for (int c = 0; c < kQChunks; ++c) {
+      float g[8];
+      Chunk<T>::widen(r[c], g);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[8 * c + e] = g[e];
+    }
+  }
+  __device__ __forceinline__ static void out(unsigned char* row, int sub, int, const float (&f)[kPartElems]) {
+    uint4* r = reinterpret_cast<uint4*>(row + sub * kPartElems * 2);
+#pragma unroll
+    for (int c = 0; c < kQChunks; ++c) {
+      float g[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) g[e] = f[8 * c + e];
+      r[c] = Chunk<T>::narrow(g);
+    }
+  }
+};
+
+template <typename T, int D, int GPW, typename KT = T>
 struct DecodeShape {
   static constexpr int kElemBytes = sizeof(T);
-  static constexpr int kRowBytes = D * kElemBytes;
-  static constexpr int kTileBytes = kTileTokens * kRowBytes;             // K (or V) rows of one tile
+  static constexpr int kRowBytes = D * kElemBytes;                       // query / output row
+  static constexpr int kKvRowBytes = D * (int)sizeof(KT);                // cache row
+  static constexpr int kTileTokensT = tile_tokens_for<KT>();
+  static constexpr int kTileBytes = kTileTokensT * kKvRowBytes;          // K (or V) rows of one tile
   static constexpr int kStageBytes = 2 * kTileBytes + GPW * kRowBytes;   // K, V, query rows
   static constexpr int kRingBudget = 128 * 1024;
   static constexpr int kStagesRaw = kRingBudget / (kDecodeWarps * 2 * kTileBytes);
@@ -81,7 +152,7 @@ struct DecodeShape {
   static constexpr int kChunksPerRow = kRowBytes / 16;
   static constexpr int kChunksPerLane = kChunksPerRow / 8;
   static constexpr int kVec = Chunk<T>::kElems;
-  static constexpr int kDimsPerLane = kChunksPerLane * kVec;  // = D / 8
+  static constexpr int kDimsPerLane = D / 8;
   static constexpr int kRingBytes = kDecodeWarps * kStages * kStageBytes;
   static constexpr int kBarOff = kRingBytes;
   static constexpr int kBtOff = kBarOff + kDecodeWarps * kStages * 8;
@@ -90,10 +161,12 @@ struct DecodeShape {
   static constexpr int kSmemBytes = kStartOff + kDecodeWarps * 16;
   static_assert(kChunksPerRow % 8 == 0, "row must split into 8 lanes of 16-byte chunks");
   static_assert(kDimsPerLane * 8 == D, "lane mapping");
-  static_assert(kStageBytes % 16 == 0 && kRowBytes % 16 == 0, "bulk copy alignment");
+  static_assert(kStageBytes % 16 == 0 && kRowBytes % 16 == 0 && kTileBytes % 16 == 0, "bulk copy alignment");
 };
 
-__device__ __forceinline__ int tiles_of(int L) { return L > 0 ? (L + kTileTokens - 1) / kTileTokens : 1; }
+template <int TT>
+__device__ __forceinline__ int tiles_of_t(int L) { return L > 0 ? (L + TT - 1) / TT : 1; }
+__device__ __forceinline__ int tiles_of(int L) { return tiles_of_t<kTileTokens>(L); }
 
 // Context length of sequence s, clamped into [0, cap] (out-of-range lengths
 // are reported once, by block 0).
@@ -135,6 +208,7 @@ struct TileCursor {
   int s, hg, t, nt, L;
 };
 
+template <int TT>
 __device__ __forceinline__ void cursor_next(TileCursor& c, const DecodeParams& p, int cap) {
   ++c.g;
   if (++c.t < c.nt) return;
@@ -143,20 +217,25 @@ __device__ __forceinline__ void cursor_next(TileCursor& c, const DecodeParams& p
   c.hg = 0;
   if (++c.s < p.num_seqs) {
     c.L = load_len(p, c.s, cap);
-    c.nt = tiles_of(c.L);
+    c.nt = tiles_of_t<TT>(c.L);
   }
 }
 
-template <typename T, int D, int GPW>
+template <typename T, int D, int GPW, typename KT = T>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     pa_decode_kernel(const DecodeParams p) {
-  using S = DecodeShape<T, D, GPW>;
+  using S = DecodeShape<T, D, GPW, KT>;
+  using LD = LaneDims<T, KT, D>;
+  constexpr bool kQuant = !std::is_same<T, KT>::value;
+  constexpr int TT = S::kTileTokensT;  // tokens per tile
+  constexpr int RPG = TT / 4;          // rows of a tile per 8-lane group
   constexpr int NW = kDecodeWarps;
   constexpr int ST = S::kStages;
   constexpr int DPL = S::kDimsPerLane;
-  constexpr int CPL = S::kChunksPerLane;
-  constexpr int VEC = S::kVec;
-  constexpr int ROW = S::kRowBytes;
+  constexpr int CPL = LD::kParts;       // pieces of a row per lane
+  constexpr int VEC = LD::kPartElems;  // dims per piece
+  constexpr int ROW = S::kRowBytes;    // query / output row bytes
+  constexpr int KROW = S::kKvRowBytes; // cache row bytes
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
@@ -173,7 +252,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
   // ---- start-up: total tiles T, then each warp's first (sequence, offset) --
   long long mine = 0;
-  for (int s = threadIdx.x; s < p.num_seqs; s += NW * 32) mine += tiles_of(load_len(p, s, cap));
+  for (int s = threadIdx.x; s < p.num_seqs; s += NW * 32) mine += tiles_of_t<TT>(load_len(p, s, cap));
   long long Ttot;
   block_exclusive_scan(mine, scan, Ttot);
   Ttot *= HG;
@@ -187,7 +266,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   long long carry = 0;
   for (int base = 0; base < p.num_seqs; base += NW * 32) {
     const int s = base + threadIdx.x;
-    const long long cnt = s < p.num_seqs ? (long long)tiles_of(load_len(p, s, cap)) * HG : 0;
+    const long long cnt = s < p.num_seqs ? (long long)tiles_of_t<TT>(load_len(p, s, cap)) * HG : 0;
     long long chunk_total;
     const long long excl = carry + block_exclusive_scan(cnt, scan, chunk_total);
 #pragma unroll
@@ -219,7 +298,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     const longlong2 st0 = starts[warp];
     ci.s = static_cast<int>(st0.x);
     ci.L = load_len(p, ci.s, cap);
-    ci.nt = tiles_of(ci.L);
+    ci.nt = tiles_of_t<TT>(ci.L);
     ci.hg = static_cast<int>(st0.y / ci.nt);
     ci.t = static_cast<int>(st0.y % ci.nt);
     ci.g = a_begin;
@@ -230,13 +309,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const char* kbase = static_cast<const char*>(p.k_cache);
   const char* vbase = static_cast<const char*>(p.v_cache);
   const char* qbase = static_cast<const char*>(p.q);
-  const int seg = bs < kTileTokens ? bs : kTileTokens;  // rows per bulk copy
-  const int nseg = kTileTokens / seg;
+  const int seg = bs < TT ? bs : TT;  // rows per bulk copy
+  const int nseg = TT / seg;
 
   // Issue the copies of the tile under `c` into slot n % ST (warp-uniform call).
   auto issue = [&](const TileCursor& c, int n) {
-    const int t0 = c.t * kTileTokens;
-    const int nvalid = min(max(c.L - t0, 0), kTileTokens);
+    const int t0 = c.t * TT;
+    const int nvalid = min(max(c.L - t0, 0), TT);
     const bool with_q = (c.t == 0 || c.g == a_begin) && nvalid > 0;
     if (nvalid > 0) {
       const int j_first = t0 / bs;
@@ -269,16 +348,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       uint64_t* bar = my_bars + (n % ST);
       uint32_t bytes = with_q ? GPW * ROW : 0;
       for (int c2 = 0; c2 < nseg; ++c2)
-        if (t0 + c2 * seg < c.L) bytes += 2u * seg * ROW;
+        if (t0 + c2 * seg < c.L) bytes += 2u * seg * KROW;
       mbar_arrive_expect_tx(bar, bytes);
       const int kvh = (c.hg * GPW) / p.group;
       for (int c2 = 0; c2 < nseg; ++c2) {
         const int t = t0 + c2 * seg;
         if (t >= c.L) break;
         const size_t off =
-            (((size_t)my_bt[t / bs - bt_j0] * p.num_kv_heads + kvh) * bs + (t % bs)) * ROW;
-        bulk_copy_g2s(kdst + c2 * seg * ROW, kbase + off, seg * ROW, bar);
-        bulk_copy_g2s(vdst + c2 * seg * ROW, vbase + off, seg * ROW, bar);
+            (((size_t)my_bt[t / bs - bt_j0] * p.num_kv_heads + kvh) * bs + (t % bs)) * KROW;
+        bulk_copy_g2s(kdst + c2 * seg * KROW, kbase + off, seg * KROW, bar);
+        bulk_copy_g2s(vdst + c2 * seg * KROW, vbase + off, seg * KROW, bar);
       }
       if (with_q)
         bulk_copy_g2s(kdst + 2 * S::kTileBytes,
@@ -289,7 +368,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   int issued = 0;
   for (; issued < ST && ci.g < a_end; ++issued) {
     issue(ci, issued);
-    cursor_next(ci, p, cap);
+    cursor_next<TT>(ci, p, cap);
   }
 
   float qf[GPW][DPL];
@@ -307,8 +386,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     }
     const unsigned char* ks = my_ring + (n % ST) * S::kStageBytes;
     const unsigned char* vs = ks + S::kTileBytes;
-    const int t0 = cc.t * kTileTokens;
-    const int nvalid = min(max(cc.L - t0, 0), kTileTokens);
+    const int t0 = cc.t * TT;
+    const int nvalid = min(max(cc.L - t0, 0), TT);
     const bool first = cc.t == 0 || cc.g == a_begin;
     const bool last = cc.t == cc.nt - 1 || cc.g == a_end - 1;
 
@@ -325,11 +404,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         const unsigned char* qs = ks + 2 * S::kTileBytes;
 #pragma unroll
         for (int g = 0; g < GPW; ++g) {
-          const uint4* qrow = reinterpret_cast<const uint4*>(qs + g * ROW);
 #pragma unroll
           for (int k = 0; k < CPL; ++k) {
             float f[VEC];
-            Chunk<T>::widen(qrow[sub + 8 * k], f);
+            LD::q(qs + g * ROW, sub, k, f);
 #pragma unroll
             for (int e = 0; e < VEC; ++e) qf[g][k * VEC + e] = f[e] * p.scale_log2;
           }
@@ -339,18 +417,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
     if (nvalid > 0) {
       // logits of rows grp, grp+4, grp+8, grp+12
-      float x[GPW][4];
+      float x[GPW][RPG];
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
+      for (int it = 0; it < RPG; ++it) {
         const int r = it * 4 + grp;
-        const uint4* krow = reinterpret_cast<const uint4*>(ks + r * ROW);
+        const unsigned char* krow = ks + r * KROW;
         float acc[GPW];
 #pragma unroll
         for (int g = 0; g < GPW; ++g) acc[g] = 0.f;
 #pragma unroll
         for (int k = 0; k < CPL; ++k) {
           float f[VEC];
-          Chunk<T>::widen(krow[sub + 8 * k], f);
+          LD::kv(krow, sub, k, f);
 #pragma unroll
           for (int g = 0; g < GPW; ++g)
 #pragma unroll
@@ -366,17 +444,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         }
       }
       // online softmax update (base 2)
-      float pw[GPW][4];
+      float pw[GPW][RPG];
 #pragma unroll
       for (int g = 0; g < GPW; ++g) {
-        float mt = fmaxf(fmaxf(x[g][0], x[g][1]), fmaxf(x[g][2], x[g][3]));
+        float mt = x[g][0];
+#pragma unroll
+        for (int it = 1; it < RPG; ++it) mt = fmaxf(mt, x[g][it]);
         mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 8));
         mt = fmaxf(mt, __shfl_xor_sync(kFullMask, mt, 16));
         const float mn = fmaxf(m[g], mt);
         const float alpha = exp2f(m[g] - mn);  // 0 on the first tile (m = -inf)
         float ps = 0.f;
 #pragma unroll
-        for (int it = 0; it < 4; ++it) {
+        for (int it = 0; it < RPG; ++it) {
           pw[g][it] = exp2f(x[g][it] - mn);
           ps += pw[g][it];
         }
@@ -387,14 +467,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       }
       // o += p . V over the valid rows (masked rows may hold poison: skip them)
 #pragma unroll
-      for (int it = 0; it < 4; ++it) {
+      for (int it = 0; it < RPG; ++it) {
         const int r = it * 4 + grp;
         if (r < nvalid) {
-          const uint4* vrow = reinterpret_cast<const uint4*>(vs + r * ROW);
+          const unsigned char* vrow = vs + r * KROW;
 #pragma unroll
           for (int k = 0; k < CPL; ++k) {
             float f[VEC];
-            Chunk<T>::widen(vrow[sub + 8 * k], f);
+            LD::kv(vrow, sub, k, f);
 #pragma unroll
             for (int g = 0; g < GPW; ++g)
 #pragma unroll
@@ -406,7 +486,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     __syncwarp();  // every lane is done with this slot before it is refilled
     if (ci.g < a_end) {
       issue(ci, issued++);
-      cursor_next(ci, p, cap);
+      cursor_next<TT>(ci, p, cap);
     }
 
     if (last) {
@@ -427,14 +507,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         if (grp == 0) {
 #pragma unroll
           for (int g = 0; g < GPW; ++g) {
-            const float inv = cc.L > 0 ? 1.f / l[g] : 0.f;
-            uint4* orow = reinterpret_cast<uint4*>(static_cast<char*>(p.out) + (row0 + g) * ROW);
+            float inv = cc.L > 0 ? 1.f / l[g] : 0.f;
+            if constexpr (kQuant) inv *= p.v_scale;
+            unsigned char* orow = static_cast<unsigned char*>(p.out) + (row0 + g) * ROW;
 #pragma unroll
             for (int k = 0; k < CPL; ++k) {
               float f[VEC];
 #pragma unroll
               for (int e = 0; e < VEC; ++e) f[e] = o[g][k * VEC + e] * inv;
-              orow[sub + 8 * k] = Chunk<T>::narrow(f);
+              LD::out(orow, sub, k, f);
             }
           }
         }
@@ -451,7 +532,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
             for (int k = 0; k < CPL; ++k)
 #pragma unroll
               for (int e = 0; e < VEC; e += 4)
-                po[((sub + 8 * k) * VEC + e) / 4] =
+                po[LD::dim(sub, k, e) / 4] =
                     make_float4(o[g][k * VEC + e] * inv, o[g][k * VEC + e + 1] * inv,
                                 o[g][k * VEC + e + 2] * inv, o[g][k * VEC + e + 3] * inv);
           }
@@ -499,39 +580,46 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
             }
             T* orow = static_cast<T*>(p.out) + (row0 + g) * D + lane * DL;
 #pragma unroll
-            for (int e = 0; e < DL; ++e) store_elem(orow + e, O[e] / Ls);
+            if constexpr (kQuant) {
+              const float vs_l = p.v_scale / Ls;
+#pragma unroll
+              for (int e = 0; e < DL; ++e) store_elem(orow + e, O[e] * vs_l);
+            } else {
+#pragma unroll
+              for (int e = 0; e < DL; ++e) store_elem(orow + e, O[e] / Ls);
+            }
           }
         }
       }
     }
-    cursor_next(cc, p, cap);
+    cursor_next<TT>(cc, p, cap);
   }
 }
 
 // Launch one instantiation as a persistent grid sized to the device.
-template <typename T, int D, int GPW>
+template <typename T, int D, int GPW, typename KT = T>
 cudaError_t launch_pa_decode(const DecodeParams& p, cudaStream_t stream) {
-  using S = DecodeShape<T, D, GPW>;
+  using S = DecodeShape<T, D, GPW, KT>;
   static int grid_of_device[64] = {0};  // cached per device ordinal (0 = not yet known)
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   int grid = (dev >= 0 && dev < 64) ? __atomic_load_n(&grid_of_device[dev], __ATOMIC_ACQUIRE) : 0;
   if (grid == 0) {
-    e = cudaFuncSetAttribute(pa_decode_kernel<T, D, GPW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(pa_decode_kernel<T, D, GPW, KT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S::kSmemBytes);
     if (e != cudaSuccess) return e;
     int sms = 0, per_sm = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_decode_kernel<T, D, GPW>,
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_decode_kernel<T, D, GPW, KT>,
                                                       kDecodeWarps * 32, S::kSmemBytes);
     if (e != cudaSuccess) return e;
     grid = sms * (per_sm > 0 ? per_sm : 1);
     if (grid > kMaxDecodeWarps / kDecodeWarps) grid = kMaxDecodeWarps / kDecodeWarps;
     if (dev >= 0 && dev < 64) __atomic_store_n(&grid_of_device[dev], grid, __ATOMIC_RELEASE);
   }
-  pa_decode_kernel<T, D, GPW><<<grid, kDecodeWarps * 32, S::kSmemBytes, stream>>>(p);
+  pa_decode_kernel<T, D, GPW, KT><<<grid, kDecodeWarps * 32, S::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -541,5 +629,7 @@ using DecodeLauncher = cudaError_t (*)(const DecodeParams&, cudaStream_t);
 DecodeLauncher decode_launcher_f32(int head_dim, int gpw_index);
 DecodeLauncher decode_launcher_f16(int head_dim, int gpw_index);
 DecodeLauncher decode_launcher_bf16(int head_dim, int gpw_index);
+// fp8 e4m3 caches with 16-bit queries (decode_fp8.cu): q_is_bf16 0 -> fp16 queries.
+DecodeLauncher decode_launcher_fp8(int q_is_bf16, int head_dim, int gpw_index);
 
 }  // namespace pkv

@@ -15,7 +15,11 @@ AssertionError when the oracle disagrees with:
     same result as private copies;
   - the log-sum-exp combination of split contexts;
   - byte-level placement of cache writes and block copies, checked with numpy
-    indexing of the [num_blocks][kv_heads][block_size][head_dim] layout.
+    indexing of the [num_blocks][kv_heads][block_size][head_dim] layout;
+  - the fp8 (E4M3) cache: the code table and round-to-nearest-even of
+    PyTorch's float8_e4m3fn conversion (a library routine), saturation at
+    448, ties to the even code, and attention over E4M3 pools equal bit for
+    bit to the binary32 oracle over the exactly decoded values.
 
 tests/test_oracle_pins.py runs them on the oracle; tests/test_oracle_mutations.py
 runs them on copies with planted mistakes and expects each copy to fail one.
@@ -369,7 +373,96 @@ def pin_copy_blocks(L=None):
         assert np.array_equal(kc, ek) and np.array_equal(vc, ev), f"copy_blocks {dtype}"
 
 
+# ---------------------------------------------------------------- fp8 (E4M3) cache
+def _torch_e4m3_values():
+    """All 256 codes decoded by PyTorch's float8_e4m3fn (float64)."""
+    import torch
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def _torch_e4m3_encode(x32: np.ndarray) -> np.ndarray:
+    """binary32 values (|x| <= 448) -> codes by PyTorch's conversion."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x32, dtype=np.float32)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+
+
+@np.errstate(invalid="ignore")
+def pin_e4m3_codec(L=None):
+    ref = _torch_e4m3_values()
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.decode_e4m3(codes, L)
+    assert np.array_equal(got, ref, equal_nan=True), "e4m3 decode table"
+    finite = ~np.isnan(ref)
+    assert np.array_equal(oracle.encode_e4m3(ref[finite], L), codes[finite]), "e4m3 round trip"
+    rng = np.random.default_rng(31)
+    x = np.concatenate([rng.uniform(-448, 448, 4000), rng.standard_normal(4000) * 0.05,
+                        rng.uniform(-2.0 ** -6, 2.0 ** -6, 2000)]).astype(np.float32)
+    assert np.array_equal(oracle.encode_e4m3(x.astype(np.float64), L), _torch_e4m3_encode(x)), "e4m3 rounding"
+    # exact midpoints between neighbouring positive codes go to the even code
+    pos = [c for c in range(0x7e)]
+    mids = np.array([(ref[c] + ref[c + 1]) / 2 for c in pos])
+    want = np.array([c if c % 2 == 0 else c + 1 for c in pos], dtype=np.uint8)
+    assert np.array_equal(oracle.encode_e4m3(mids, L), want), "e4m3 ties to even"
+    assert np.array_equal(oracle.encode_e4m3(-mids, L), want | 0x80), "e4m3 negative ties"
+    sat = oracle.encode_e4m3(np.array([449.0, 1e6, np.inf, -460.0, -np.inf]), L)
+    assert np.array_equal(sat, np.array([0x7e, 0x7e, 0x7e, 0xfe, 0xfe], dtype=np.uint8)), "e4m3 saturation"
+
+
+def pin_fp8_attention(L=None):
+    """Power-of-two scales make scale * code exact in binary32, so attention
+    over E4M3 pools must equal, bit for bit, the binary32 oracle over pools
+    holding those values (and a binary32 copy of the binary16 queries)."""
+    rng = np.random.default_rng(33)
+    B, H_, Hkv, D, bs, NB = 3, 4, 2, 16, 4, 20
+    lens = np.array([1, 7, 13], dtype=np.int32)
+    _, kc16, vc16, bt, lens = _random_paged(rng, B, H_, Hkv, D, bs, NB, lens, "f16")
+    finite = np.flatnonzero(~np.isnan(_torch_e4m3_values()))
+    kc8 = rng.choice(finite, size=kc16.shape).astype(np.uint8)
+    vc8 = rng.choice(finite, size=vc16.shape).astype(np.uint8)
+    q = _rand_store(rng, (B, H_, D), "f16")
+    vals = _torch_e4m3_values()
+    for ks, vs in ((1.0, 1.0), (0.5, 2.0 ** -3)):
+        kc32 = (vals[kc8] * ks).astype(np.float32)
+        vc32 = (vals[vc8] * vs).astype(np.float32)
+        q32 = q.view(np.float16).astype(np.float32)
+        ref = oracle.paged_attention(q32, kc32, vc32, bt, lens, scale=0.3, num_heads=H_, num_kv_heads=Hkv,
+                                     head_dim=D, block_size=bs, dtype="f32", L=L)
+        got = oracle.paged_attention_fp8(q, kc8, vc8, bt, lens, scale=0.3, k_scale=ks, v_scale=vs, num_heads=H_,
+                                         num_kv_heads=Hkv, head_dim=D, block_size=bs, q_dtype="f16", L=L)
+        assert np.array_equal(got, ref), f"fp8 attention (scales {ks}, {vs})"
+
+
+def pin_fp8_cache_write(L=None):
+    """Each element lands at its slot as the E4M3 rounding of the binary32
+    quotient x / scale (numpy's float32 division, PyTorch's rounding)."""
+    rng = np.random.default_rng(35)
+    T, Hkv, D, bs, NB = 9, 2, 16, 4, 8
+    for dtype in ("f16", "bf16"):
+        k = _rand_store(rng, (T, Hkv, D), dtype)
+        v = _rand_store(rng, (T, Hkv, D), dtype)
+        slots = rng.permutation(NB * bs)[:T].astype(np.int64)
+        slots[2] = -1
+        kc = rng.integers(0, 256, (NB, Hkv, bs, D), dtype=np.uint8)
+        vc = kc.copy()
+        kc0, vc0 = kc.copy(), vc.copy()
+        ks, vs = np.float32(0.037), np.float32(0.011)
+        bad = oracle.reshape_and_cache_fp8(k, v, kc, vc, slots, num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                                           src_dtype=dtype, k_scale=float(ks), v_scale=float(vs), L=L)
+        assert bad == 0
+        ek, ev = kc0.copy(), vc0.copy()
+        for t in range(T):
+            if slots[t] < 0:
+                continue
+            b, r = slots[t] // bs, slots[t] % bs
+            ek[b, :, r, :] = _torch_e4m3_encode(_dec(k[t], dtype).astype(np.float32) / ks)
+            ev[b, :, r, :] = _torch_e4m3_encode(_dec(v[t], dtype).astype(np.float32) / vs)
+        assert np.array_equal(kc, ek) and np.array_equal(vc, ev), f"fp8 cache write ({dtype})"
+
+
 ALL_PINS = [pin_decoders, pin_context_one, pin_uniform_weights, pin_dominant_logit,
             pin_two_tokens, pin_gqa_mapping, pin_brute_force, pin_dense_equivalence,
             pin_placement_invariance, pin_copy_on_write, pin_split_merge,
-            pin_reshape_and_cache, pin_copy_blocks]
+            pin_reshape_and_cache, pin_copy_blocks, pin_e4m3_codec, pin_fp8_attention,
+            pin_fp8_cache_write]

@@ -115,6 +115,40 @@ def test_cache_op_host_checks(pkv):
     assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 2, 0, 128, 16, 10, 1, None, None) == INV
 
 
+def test_fp8_host_checks(pkv):
+    L = pkv.lib
+    INV, UNS, OK = pkv.PKV_ERR_INVALID_ARG, pkv.PKV_ERR_UNSUPPORTED, pkv.PKV_OK
+    # (k, v, k_cache, v_cache, slots, T, Hkv, D, bs, NB, src_dtype, k_scale, v_scale, err, stream)
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 3, 4, 128, 16, 10, 1, 0.5, 0.5, None, None]
+
+    def rc(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.pkv_reshape_and_cache_fp8(*a)
+    assert rc(a5=0) == OK
+    assert rc(a11=0.0) == INV and rc(a12=float("inf")) == INV and rc(a11=-1.0) == INV
+    assert rc(a10=0) == UNS            # binary32 rows: not taken
+    assert rc(a10=3) == UNS            # e4m3 rows: not a source type
+    assert rc(a0=None) == INV and rc(a4=FAKE + 4) == INV
+    # decode: (out, q, k, v, bt, cl, scale, k_scale, v_scale, H, Hkv, D, bs, B, MB, NB, mcl, dtype, ws, ws_bytes, err, s)
+    d = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, 0.5, 0.5, 8, 8, 128, 16, 4, 8, 100, 128, 1, None, 0, None, None]
+
+    def dc(**kw):
+        a = list(d)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.pkv_paged_attention_decode_fp8(*a)
+    assert dc(a13=0) == OK
+    assert dc(a7=0.0) == INV and dc(a8=float("nan")) == INV
+    assert dc(a17=0) == UNS            # binary32 queries: not taken
+    assert dc(a17=3) == UNS            # e4m3 queries: not taken
+    assert dc() == pkv.PKV_ERR_WORKSPACE
+    # block copies take the 1-byte element
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 0, 4, 128, 16, 10, 3, None, None) == OK
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 2, 4, 128, 16, 10, 4, None, None) == UNS
+
+
 def test_no_fallback_without_library(tmp_path):
     """A copy of the binding without its compiled library refuses to import."""
     import shutil

@@ -47,6 +47,11 @@ MUTATIONS = [
      "memmove((unsigned char*)k_cache + (size_t)src * block_bytes,\n            (const unsigned char*)k_cache + (size_t)dst * block_bytes, block_bytes);", 0),
     ("merge weight sign", "acc += cl[c] * exp(cm[c] - M) * co", "acc += cl[c] * exp(M - cm[c]) * co", 0),
     ("merge drops chunk exp-sum", "acc += cl[c] * exp(cm[c] - M) * co", "acc += exp(cm[c] - M) * co", 0),
+    ("e4m3 exponent bias", "ldexp((double)(m + 8), e - 10)", "ldexp((double)(m + 8), e - 9)", 0),
+    ("e4m3 ties away from zero", "(int)rint(ldexp(a, 3 - E))", "(int)floor(ldexp(a, 3 - E) + 0.5)", 0),
+    ("e4m3 no saturation", "if (a > 448.0) return sign | 0x7e;", "if (a > 480.0) return sign | 0x7f;", 0),
+    ("fp8 cache write skips the scale", "(float)elem(k, src, src_dtype) / k_scale", "(float)elem(k, src, src_dtype)", 0),
+    ("fp8 attention drops v_scale", "x[t] * (v_scale * orc_decode_e4m3(", "x[t] * (orc_decode_e4m3(", 0),
 ]
 
 
