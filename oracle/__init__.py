@@ -78,6 +78,8 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.orc_reshape_and_cache_fp8.restype = I
     L.orc_paged_attention_fp8.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, D, D, D, I, I]
     L.orc_paged_attention_fp8.restype = I
+    L.orc_paged_prefill.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, D, I, I]
+    L.orc_paged_prefill.restype = I
     return L
 
 
@@ -313,4 +315,35 @@ def paged_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, *, scal
         rcs = list(ex.map(lambda i: run(cuts[i], cuts[i + 1]), range(n)))
     if any(rc != 0 for rc in rcs):
         raise ValueError(f"orc_paged_attention_fp8 failed with codes {rcs}")
+    return out
+
+
+# ---- paged prefill -------------------------------------------------------------
+
+def paged_prefill(q, k_cache, v_cache, block_tables, context_lens, query_start, *, scale, num_heads,
+                  num_kv_heads, head_dim, block_size, dtype, threads: int = 1, L=None) -> np.ndarray:
+    """Causal attention of each sequence's last n = query_start[s+1] -
+    query_start[s] tokens over its paged context (query i at position
+    context_lens[s] - n + i sees tokens 0 .. that position). q is packed
+    [total_queries, num_heads, head_dim]; returns float64 of the same shape."""
+    L = L or lib()
+    for a, n in ((q, "q"), (k_cache, "k_cache"), (v_cache, "v_cache")):
+        _check_store(a, dtype, n)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    B = cl.shape[0]
+    out = np.zeros((q.shape[0], num_heads, head_dim), dtype=np.float64)
+
+    def run(lo, hi):
+        return L.orc_paged_prefill(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt), bt.shape[1], _ptr(cl),
+                                   _ptr(qs), B, num_heads, num_kv_heads, head_dim, block_size, k_cache.shape[0],
+                                   DTYPE_CODE[dtype], float(scale), lo, hi)
+
+    n = max(1, min(threads, B))
+    cuts = [B * i // n for i in range(n + 1)]
+    with ThreadPoolExecutor(max_workers=n) as ex:
+        rcs = list(ex.map(lambda i: run(cuts[i], cuts[i + 1]), range(n)))
+    if any(rc != 0 for rc in rcs):
+        raise ValueError(f"orc_paged_prefill failed with codes {rcs}")
     return out

@@ -550,3 +550,69 @@ int orc_paged_attention_fp8(double* out, const void* q, const uint8_t* k_cache, 
   free(row);
   return rc;
 }
+
+/* ---- paged prefill (multi-token causal queries) -------------------------- */
+/*
+ * [WL] "PagedAttention: the KV cache was the bottleneck all along", section
+ * "What is left": the wish for shared blocks for common system prompts
+ * across users, i.e. the prompt side over the same paged cache; [VM] for the
+ * paging. Reading taken: sequence s holds context_lens[s] = L tokens in the
+ * cache (its new tokens already written); its n = query_start[s+1] -
+ * query_start[s] queries are its last n tokens, and query i (at position
+ * L - n + i) attends to tokens 0 .. L - n + i (causal). q and out are packed
+ * [total_queries][num_heads][head_dim]. Returns 0 or a negative code.
+ */
+int orc_paged_prefill(double* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                      const int32_t* query_start, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                      int block_size, int num_blocks, int dtype, double scale, int seq_begin, int seq_end) {
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start) return -1;
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return -2;
+  if (head_dim <= 0 || block_size <= 0 || num_blocks <= 0 || !elem_bytes(dtype)) return -3;
+  if (seq_begin < 0 || seq_end > num_seqs || seq_begin > seq_end) return -4;
+  const int group = num_heads / num_kv_heads;
+  int max_len = 0;
+  for (int s = seq_begin; s < seq_end; ++s) {
+    const int L = context_lens[s], n = query_start[s + 1] - query_start[s];
+    if (L < 0 || L > max_blocks_per_seq * block_size || n < 0 || n > L) return -5;
+    if (L > max_len) max_len = L;
+  }
+  double* x = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+  size_t* row = (size_t*)malloc(sizeof(size_t) * (size_t)(max_len > 0 ? max_len : 1));
+  if (!x || !row) {
+    free(x);
+    free(row);
+    return -6;
+  }
+  int rc = 0;
+  for (int s = seq_begin; s < seq_end && rc == 0; ++s) {
+    const int L = context_lens[s], n = query_start[s + 1] - query_start[s];
+    for (int t = 0; t < L; ++t) {
+      const int32_t p = block_tables[(size_t)s * max_blocks_per_seq + t / block_size];
+      if (p < 0 || p >= num_blocks) {
+        rc = -7;
+        break;
+      }
+    }
+    if (rc) break;
+    for (int i = 0; i < n; ++i) {
+      const int pos = L - n + i; /* this query's own position */
+      const size_t qi = (size_t)query_start[s] + (size_t)i;
+      for (int h = 0; h < num_heads; ++h) {
+        const int g = h / group;
+        double* o = out + (qi * num_heads + h) * head_dim;
+        const size_t q_off = (qi * num_heads + h) * head_dim;
+        for (int t = 0; t <= pos; ++t) {
+          const int32_t p = block_tables[(size_t)s * max_blocks_per_seq + t / block_size];
+          row[t] = (((size_t)p * num_kv_heads + g) * block_size + (size_t)(t % block_size)) * head_dim;
+          x[t] = scale * dot_rows(q, q_off, k_cache, row[t], head_dim, dtype);
+        }
+        vrows V = {v_cache, row, dtype};
+        softmax_combine(o, x, pos + 1, V, head_dim);
+      }
+    }
+  }
+  free(x);
+  free(row);
+  return rc;
+}

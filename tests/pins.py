@@ -16,6 +16,9 @@ AssertionError when the oracle disagrees with:
   - the log-sum-exp combination of split contexts;
   - byte-level placement of cache writes and block copies, checked with numpy
     indexing of the [num_blocks][kv_heads][block_size][head_dim] layout;
+  - paged prefill (causal queries of a sequence's last tokens): one query
+    per sequence is decode; each query equals dense attention over exactly
+    its own prefix, gathered by numpy indexing;
   - the fp8 (E4M3) cache: the code table and round-to-nearest-even of
     PyTorch's float8_e4m3fn conversion (a library routine), saturation at
     448, ties to the even code, and attention over E4M3 pools equal bit for
@@ -461,8 +464,52 @@ def pin_fp8_cache_write(L=None):
         assert np.array_equal(kc, ek) and np.array_equal(vc, ev), f"fp8 cache write ({dtype})"
 
 
+# ---------------------------------------------------------------- paged prefill
+def _prefill_case(rng, dtype="f16"):
+    B, H_, Hkv, D, bs, NB = 3, 4, 2, 16, 4, 40
+    lens = np.array([1, 9, 22], dtype=np.int32)
+    q_unused, kc, vc, bt, lens = _random_paged(rng, B, H_, Hkv, D, bs, NB, lens, dtype)
+    return B, H_, Hkv, D, bs, kc, vc, bt, lens
+
+
+def pin_prefill_single_query_is_decode(L=None):
+    rng = np.random.default_rng(51)
+    B, H_, Hkv, D, bs, kc, vc, bt, lens = _prefill_case(rng)
+    q = _rand_store(rng, (B, H_, D), "f16")
+    qs = np.arange(B + 1, dtype=np.int32)
+    got = oracle.paged_prefill(q, kc, vc, bt, lens, qs, scale=0.4, num_heads=H_, num_kv_heads=Hkv, head_dim=D,
+                               block_size=bs, dtype="f16", L=L)
+    ref = _attn(L, q, kc, vc, bt, lens, H_, Hkv, D, bs, "f16", 0.4)
+    assert np.array_equal(got, ref), "one-query prefill == decode"
+
+
+def pin_prefill_prefix_dense(L=None):
+    """Query i of sequence s (context L_s, n_s queries) sits at position
+    L_s - n_s + i and must equal dense attention over exactly the tokens
+    0 .. that position, gathered with numpy from the block table."""
+    rng = np.random.default_rng(53)
+    B, H_, Hkv, D, bs, kc, vc, bt, lens = _prefill_case(rng)
+    n = np.array([1, 4, 22], dtype=np.int32)  # the last sequence is a full prompt
+    qs = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    q = _rand_store(rng, (int(qs[-1]), H_, D), "f16")
+    got = oracle.paged_prefill(q, kc, vc, bt, lens, qs, scale=0.4, num_heads=H_, num_kv_heads=Hkv, head_dim=D,
+                               block_size=bs, dtype="f16", L=L)
+    ks, vs, starts = [], [], [0]
+    for s in range(B):
+        for i in range(int(n[s])):
+            pos = int(lens[s]) - int(n[s]) + i
+            t = np.arange(pos + 1)
+            ks.append(kc[bt[s, t // bs], :, t % bs, :])
+            vs.append(vc[bt[s, t // bs], :, t % bs, :])
+            starts.append(starts[-1] + pos + 1)
+    ref = oracle.dense_attention(q, np.ascontiguousarray(np.concatenate(ks)), np.ascontiguousarray(np.concatenate(vs)),
+                                 np.array(starts, dtype=np.int64), scale=0.4, num_heads=H_, num_kv_heads=Hkv,
+                                 head_dim=D, dtype="f16", L=L)
+    assert np.array_equal(got, ref), "prefill query == dense attention over its prefix"
+
+
 ALL_PINS = [pin_decoders, pin_context_one, pin_uniform_weights, pin_dominant_logit,
             pin_two_tokens, pin_gqa_mapping, pin_brute_force, pin_dense_equivalence,
             pin_placement_invariance, pin_copy_on_write, pin_split_merge,
             pin_reshape_and_cache, pin_copy_blocks, pin_e4m3_codec, pin_fp8_attention,
-            pin_fp8_cache_write]
+            pin_fp8_cache_write, pin_prefill_single_query_is_decode, pin_prefill_prefix_dense]

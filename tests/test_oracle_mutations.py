@@ -52,6 +52,8 @@ MUTATIONS = [
     ("e4m3 no saturation", "if (a > 448.0) return sign | 0x7e;", "if (a > 480.0) return sign | 0x7f;", 0),
     ("fp8 cache write skips the scale", "(float)elem(k, src, src_dtype) / k_scale", "(float)elem(k, src, src_dtype)", 0),
     ("fp8 attention drops v_scale", "x[t] * (v_scale * orc_decode_e4m3(", "x[t] * (orc_decode_e4m3(", 0),
+    ("prefill causal off by one", "const int pos = L - n + i;", "const int pos = L - n + i - 1;", 0),
+    ("prefill positions from the start", "const int pos = L - n + i;", "const int pos = i;", 0),
 ]
 
 
