@@ -102,6 +102,17 @@ def peak_hbm() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "of fallback (6.8 TB/s)"
 
 
+def peak_bf16_tflops() -> tuple[float, str]:
+    """Dense bf16 tensor peak: the burst figure (the prefill kernel is timed
+    alone between L2 flushes)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "of measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "of fallback (1.9 PFLOP/s bf16)"
+
+
 def profiled_traffic() -> int | None:
     """DRAM bytes per launch of the decode kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -743,6 +754,189 @@ def run_beam(args, rank: int, world: int, local_rank: int) -> int:
     return 0
 
 
+def run_prefill(args, rank: int, world: int, local_rank: int) -> int:
+    """Prefill steps of users sharing a system prompt: the system prompt's
+    K/V is in the cache already (written once, its partly filled block copied
+    on write for the users); each step writes the users' own K/V rows and
+    runs the causal prefill attention of all their tokens."""
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_204_gb300 as pkv
+    import synth.prefill as SP
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    cfg = SP.get(args.workload)
+    if args.num_blocks:
+        cfg = cfg.replace(num_blocks=args.num_blocks)
+    if world > 1:
+        cfg = cfg.replace(seed=cfg.seed + rank)
+    lay = SP.build(cfg)
+    td = {"f16": torch.float16, "bf16": torch.bfloat16}[cfg.dtype]
+    H, Hkv, D = cfg.num_heads, cfg.num_kv_heads, cfg.head_dim
+    n = lay.total_queries
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg.seed * 1000003 + 31)
+    randn = lambda *shp: (torch.randn(shp, generator=gen, device=dev) * cfg.value_scale).to(td)
+    shape = (cfg.num_blocks, Hkv, cfg.block_size, D)
+    kc = torch.full(shape, float("nan"), dtype=td, device=dev)
+    vc = torch.full(shape, float("nan"), dtype=td, device=dev)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    if cfg.system_len:
+        pkv.reshape_and_cache(randn(cfg.system_len, Hkv, D), randn(cfg.system_len, Hkv, D), kc, vc,
+                              t(lay.system_slots), dev_err=err)
+    if lay.copy_pairs.size:
+        pkv.copy_blocks(kc, vc, t(lay.copy_pairs), dev_err=err)
+    uk, uv, q = randn(n, Hkv, D), randn(n, Hkv, D), randn(n, H, D)
+    slots, bt, cl, qs = t(lay.user_slots), t(lay.block_tables), t(lay.context_lens), t(lay.query_start)
+    out = torch.empty_like(q)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def write():
+        pkv.reshape_and_cache(uk, uv, kc, vc, slots, dev_err=err)
+
+    def attention():
+        pkv.paged_attention_prefill(out, q, kc, vc, bt, cl, qs, cfg.scale, lay.max_query_len, dev_err=err)
+
+    # algorithmic work: every query sees the system prompt and its own earlier tokens
+    visible = 0
+    for u in range(cfg.users):
+        nu = int(lay.query_start[u + 1] - lay.query_start[u])
+        L = int(lay.context_lens[u])
+        visible += sum(L - nu + i + 1 for i in range(nu))
+    flops = 4.0 * visible * H * D
+    warm = max(args.warmup, 3)
+    for _ in range(warm):
+        flush.fill_(1)
+        write()
+        attention()
+    torch.cuda.synchronize()
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x} during warm-up")
+    if not torch.isfinite(out.float()).all():
+        raise RuntimeError("non-finite prefill output")
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clocks:
+        t_wall0 = time.perf_counter()
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            write()
+            ev[i][1].record(stream)
+            attention()
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        wall = time.perf_counter() - t_wall0
+    step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / K
+    attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
+    write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    # end to end: the users' rows, queries and layout from pinned host memory,
+    # the step, the outputs back
+    host = [x.cpu().pin_memory() for x in (uk, uv, q, slots, bt, cl, qs)]
+    devs = [uk, uv, q, slots, bt, cl, qs]
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps, e2e_total = max(10, K // 4), 0.0
+    for i in range(e2e_steps + 3):
+        flush.fill_(i & 0xFF)
+        if i >= 3:
+            e0.record(stream)
+        for h_, d_ in zip(host, devs):
+            d_.copy_(h_, non_blocking=True)
+        write()
+        attention()
+        host_out.copy_(out, non_blocking=True)
+        if i >= 3:
+            e1.record(stream)
+            e1.synchronize()
+            e2e_total += e0.elapsed_time(e1)
+    e2e_ms = e2e_total / e2e_steps
+    agg = aggregate({"step_ms": step_ms, "attn_ms": attn_ms, "write_ms": write_ms, "e2e_ms": e2e_ms}, world,
+                    device=dev if world > 1 else None)
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_src = peak_bf16_tflops()
+    achieved = flops / (agg["attn_ms"] * 1e-3) / 1e12
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        from synth.device import to_storage
+        threads = len(os.sched_getaffinity(0))
+        u = 0
+        ids = np.unique(lay.block_tables[u][lay.block_tables[u] >= 0])
+        remap = np.full(cfg.num_blocks, -1, dtype=np.int32)
+        remap[ids] = np.arange(ids.size, dtype=np.int32)
+        bt_c = np.where(lay.block_tables[u:u + 1] >= 0, remap[np.maximum(lay.block_tables[u:u + 1], 0)], -1)
+        idx = torch.from_numpy(ids.astype(np.int64)).to(dev)
+        nu = int(lay.query_start[1])
+        hk = max(1, min(H, 2))  # a bounded sample: the first user's queries, first heads
+        q_h = to_storage(q[:nu, :hk].contiguous())
+        k_h = to_storage(kc[idx][:, :hk].contiguous()) if Hkv == H else to_storage(kc[idx])
+        v_h = to_storage(vc[idx][:, :hk].contiguous()) if Hkv == H else to_storage(vc[idx])
+        hkv = hk if Hkv == H else Hkv
+        L0 = int(lay.context_lens[0])
+        fl = 4.0 * sum(L0 - nu + i + 1 for i in range(nu)) * hk * D
+        times, t_start = [], time.perf_counter()
+        while True:
+            t0 = time.perf_counter()
+            oracle.paged_prefill(q_h, k_h, v_h, bt_c.astype(np.int32), lay.context_lens[:1],
+                                 np.array([0, nu], dtype=np.int32), scale=cfg.scale, num_heads=hk,
+                                 num_kv_heads=hkv, head_dim=D, block_size=cfg.block_size, dtype=cfg.dtype,
+                                 threads=threads)
+            times.append(time.perf_counter() - t0)
+            if time.perf_counter() - t_start >= args.cpu_seconds:
+                break
+        mean = sum(times) / len(times)
+        cpu = {"value": fl / mean / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+               "sample": (f"prefill of user 0 ({nu} queries over {L0} tokens) x {hk} of {H} heads, "
+                          f"{len(times)} run(s), {mean * 1e3:.1f} ms each; the oracle runs one thread per sequence")}
+    line = {
+        "metric": "prefill attention TFLOP/s (causal, users sharing a system prompt)",
+        "value": world * flops / (agg["step_ms"] * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world, "steps": K, "warmup": warm, "ms_per_step": agg["step_ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+        "config": {"workload": (f"prefill step: {cfg.users} users sharing a {cfg.system_len}-token system prompt "
+                                f"(its blocks shared, {lay.copy_pairs.shape[0]} copy-on-write copies), own prompts "
+                                f"{describe_lengths(cfg.user_len)} ({n} query tokens), {H} heads ({Hkv} kv), "
+                                f"head_dim {D}, block_size {cfg.block_size}, {cfg.dtype} with fp32 accumulation, "
+                                f"{cfg.num_blocks}-block pools"),
+                   "global_batch": n * world, "parallelism": "single GPU" if world == 1 else f"{world} replicas",
+                   "l2": "flushed between timed steps (256 MiB write)", "seed": cfg.seed},
+        "tokens_per_s": world * n / (agg["step_ms"] * 1e-3),
+        "attention_ms": agg["attn_ms"], "cache_write_ms": agg["write_ms"], "flops_per_step": flops,
+        "roofline": {"bound": "tensor", "kernel": "pa_prefill_kernel (mma.sync m16n8k16)", "achieved": achieved,
+                     "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": peak_src},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * flops / (agg["e2e_ms"] * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": agg["e2e_ms"],
+                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in host),
+                "d2h_bytes_per_step": host_out.numel() * host_out.element_size()},
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(),
+        "timed_region_wall_s": wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -768,6 +962,11 @@ def main() -> int:
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if world != args.gpus:
         print(f"warning: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    if args.workload.startswith("prefill"):
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the default workload"}))
+            return 0
+        return run_prefill(args, rank, world, local_rank)
     if args.workload.startswith("beam"):
         if args.impl == "reference":
             print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the default workload"}))

@@ -344,6 +344,40 @@ pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, const void* 
                                           void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                           pkv_stream_t stream);
 
+/* ----------------------------------------------------------------------
+ * Paged prefill
+ *
+ * [WL] "PagedAttention: the KV cache was the bottleneck all along", section
+ * "What is left": the wish for shared blocks for common system prompts
+ * across users, i.e. the prompt side running over the same paged cache. With
+ * the host block manager, users fork a sequence holding the system prompt,
+ * so the prompt's blocks are shared and its K/V is written once; each user's
+ * own tokens are then written with pkv_reshape_and_cache and attended with
+ * this call.
+ * ---------------------------------------------------------------------- */
+
+/* Causal attention of each sequence's newest tokens over its paged context
+ * ([WL], [VM]). Sequence s holds context_lens[s] = L tokens in the cache,
+ * its new ones included; its n = query_start[s+1] - query_start[s] queries
+ * (0 <= n <= L) are its last n tokens, and query i (position L - n + i)
+ * attends to tokens 0 .. L - n + i:
+ *     out[query_start[s] + i][h] = softmax_t(scale * q . K_t) . V_t.
+ * q, out: [query_start[num_seqs]][num_heads][head_dim], packed by sequence;
+ * query_start: int32 [num_seqs + 1], non-decreasing, query_start[0] = 0;
+ * max_query_len >= every n (it sizes the grid); caches, block tables and
+ * context lengths as in pkv_paged_attention_decode. dtype: PKV_F16 or
+ * PKV_BF16 (tensor-core path). No workspace. Host checks as in the decode
+ * call, plus PKV_ERR_INVALID_ARG for a NULL query_start or max_query_len < 0.
+ * Device: a sequence with n < 0, n > L or L out of range sets
+ * PKV_DEV_ERR_CONTEXT_LEN and is skipped; a bad block id sets
+ * PKV_DEV_ERR_BLOCK_ID (its rows read as zeros). */
+pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, const int32_t* context_lens,
+                                       const int32_t* query_start, float scale, int num_heads,
+                                       int num_kv_heads, int head_dim, int block_size, int num_seqs,
+                                       int max_blocks_per_seq, int num_blocks, int max_query_len,
+                                       pkv_dtype dtype, int32_t* dev_err, pkv_stream_t stream);
+
 /* Bytes of workspace pkv_paged_attention_decode needs for these sizes: the
  * segment counters (num_seqs * num_heads int32) plus a fixed area for the
  * partial results of the split segments (independent of the context lengths;

@@ -13,6 +13,7 @@ Functions mirror the C entry points:
   decode_workspace_bytes  -> pkv_decode_workspace_bytes
   paged_attention_decode_grouped  -> pkv_paged_attention_decode_grouped
   reshape_and_cache_fp8, paged_attention_decode_fp8  -> the fp8 (e4m3) cache entry points
+  paged_attention_prefill -> pkv_paged_attention_prefill
   decode_grouped_workspace_bytes  -> pkv_decode_grouped_workspace_bytes
   set_wait_timeout_ns / get_wait_timeout_ns, status_string, version
 The host block manager (include/pkv_block_manager.h) is wrapped by
@@ -70,6 +71,9 @@ lib.pkv_reshape_and_cache_fp8.restype = _I
 lib.pkv_paged_attention_decode_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _F, _F, _F, _I, _I, _I, _I, _I, _I, _I,
                                                _I, _I, _P, _SZ, _P, _P]
 lib.pkv_paged_attention_decode_fp8.restype = _I
+lib.pkv_paged_attention_prefill.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                              _P, _P]
+lib.pkv_paged_attention_prefill.restype = _I
 lib.pkv_paged_attention_decode_noalloc.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I,
                                                    _I, _I, _I, _P, _P]
 lib.pkv_paged_attention_decode_noalloc.restype = _I
@@ -205,6 +209,22 @@ def paged_attention_decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torc
         float(scale), float(k_scale), float(v_scale), H, Hkv, D, bs, B, block_tables.shape[1], nb,
         int(max_context_len), DTYPE_CODE[q.dtype], _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)),
         "pkv_paged_attention_decode_fp8")
+
+
+def paged_attention_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor, query_start: torch.Tensor,
+                            scale: float, max_query_len: int, dev_err: torch.Tensor | None = None,
+                            stream=None) -> None:
+    """Causal attention of each sequence's last n = query_start[s+1] -
+    query_start[s] tokens over its paged context. q, out [total_queries, H, D]
+    (fp16/bf16) packed by sequence; query_start int32 [B+1] (on the GPU)."""
+    _, H, D = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    B = context_lens.numel()
+    _check(lib.pkv_paged_attention_prefill(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens), _ptr(query_start),
+        float(scale), H, Hkv, D, bs, B, block_tables.shape[1], nb, int(max_query_len), DTYPE_CODE[q.dtype],
+        _ptr(dev_err), _stream(stream)), "pkv_paged_attention_prefill")
 
 
 def decode_grouped_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_context_len: int,

@@ -8,6 +8,7 @@
 #include "decode.cuh"
 #include "decode_grouped.cuh"
 #include "pkv.h"
+#include "prefill.cuh"
 
 namespace {
 
@@ -271,6 +272,42 @@ pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, const void* 
   p.ws_ml = reinterpret_cast<float2*>(wsb + ws.ml_off);
   p.ws_o = reinterpret_cast<float*>(wsb + ws.o_off);
   return launch_status(launch(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, const int32_t* context_lens,
+                                       const int32_t* query_start, float scale, int num_heads,
+                                       int num_kv_heads, int head_dim, int block_size, int num_seqs,
+                                       int max_blocks_per_seq, int num_blocks, int max_query_len,
+                                       pkv_dtype dtype, int32_t* dev_err, pkv_stream_t stream) {
+  if (max_query_len < 0) return PKV_ERR_INVALID_ARG;
+  if (dtype != PKV_F16 && dtype != PKV_BF16 && valid_dtype(dtype)) return PKV_ERR_UNSUPPORTED;
+  const pkv_status st = check_decode_args(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                          num_heads, num_kv_heads, head_dim, block_size, num_seqs,
+                                          max_blocks_per_seq, num_blocks, 0, dtype, dev_err);
+  if (st != PKV_OK || num_seqs == 0 || max_query_len == 0) return st;
+  if (!query_start || !aligned(query_start, 4)) return PKV_ERR_INVALID_ARG;
+  if (num_heads > 65535) return PKV_ERR_UNSUPPORTED;
+  pkv::PrefillLauncher launch = pkv::prefill_launcher(dtype == PKV_BF16 ? 1 : 0, head_dim);
+  if (!launch) return PKV_ERR_UNSUPPORTED;
+  pkv::PrefillParams p{};
+  p.out = out;
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.query_start = query_start;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.num_seqs = num_seqs;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = num_heads / num_kv_heads;
+  p.block_size = block_size;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.dev_err = dev_err;
+  return launch_status(launch(p, max_query_len, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t pkv_decode_grouped_workspace_bytes(int num_seqs, int num_heads, int head_dim, int max_context_len,

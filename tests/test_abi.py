@@ -149,6 +149,26 @@ def test_fp8_host_checks(pkv):
     assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 2, 4, 128, 16, 10, 4, None, None) == UNS
 
 
+def test_prefill_host_checks(pkv):
+    L = pkv.lib
+    INV, UNS, OK = pkv.PKV_ERR_INVALID_ARG, pkv.PKV_ERR_UNSUPPORTED, pkv.PKV_OK
+    # (out, q, k, v, bt, cl, query_start, scale, H, Hkv, D, bs, B, MB, NB, max_query_len, dtype, err, stream)
+    a = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, 8, 8, 128, 16, 4, 8, 100, 64, 2, None, None]
+
+    def rc(**kw):
+        b = list(a)
+        for i, v in kw.items():
+            b[int(i[1:])] = v
+        return L.pkv_paged_attention_prefill(*b)
+    assert rc(a12=0) == OK and rc(a15=0) == OK       # nothing to do
+    assert rc(a15=-1) == INV
+    assert rc(a6=None) == INV and rc(a6=FAKE + 2) == INV
+    assert rc(a16=0) == UNS                          # binary32: no tensor-core path
+    assert rc(a10=96) == UNS and rc(a11=64) == UNS
+    assert rc(a9=3) == INV                           # 8 % 3 != 0
+    assert rc(a1=FAKE + 8) == INV
+
+
 def test_no_fallback_without_library(tmp_path):
     """A copy of the binding without its compiled library refuses to import."""
     import shutil
