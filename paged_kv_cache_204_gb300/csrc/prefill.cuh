@@ -124,7 +124,7 @@ struct PrefillShape {
 };
 
 template <typename T, int D>
-__global__ void __launch_bounds__(kPfWarps * 32) pa_prefill_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kPfWarps * 32, 2) pa_prefill_kernel(const PrefillParams p) {
   using S = PrefillShape<T, D>;
   using M = PfMma<T>;
   constexpr int CH = D / 8;   // 16-byte chunks per row
@@ -190,7 +190,6 @@ __global__ void __launch_bounds__(kPfWarps * 32) pa_prefill_kernel(const Prefill
   // ---- per-warp state: rows w*16 + g and w*16 + g + 8 --------------------------
   const int wr = warp * 16;
   const int pos_a = first_pos + wr + g, pos_b = pos_a + 8;  // query positions of this thread's rows
-  uint32_t qa[KS][4];
   float o[NT][4];
 #pragma unroll
   for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
@@ -205,13 +204,7 @@ __global__ void __launch_bounds__(kPfWarps * 32) pa_prefill_kernel(const Prefill
       cp_async_wait<0>();
     }
     __syncthreads();
-    if (j == 0) {
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        const int r = wr + (lane & 15), c = 2 * kk + (lane >> 4);
-        ldsm_x4(qa[kk], qs + pf_off<D>(r, c));
-      }
-    }
+
     const unsigned char* ks = kv + (2 * (j & 1)) * S::kTileBytes;
     const unsigned char* vs = ks + S::kTileBytes;
     const int t0 = j * kPfTokens;
@@ -221,15 +214,21 @@ __global__ void __launch_bounds__(kPfWarps * 32) pa_prefill_kernel(const Prefill
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
 #pragma unroll
-    for (int kk = 0; kk < KS; ++kk)
+    for (int kk = 0; kk < KS; ++kk) {
+      uint32_t qa[4];  // this k-step's query fragment, reloaded per tile (keeps registers for occupancy)
+      {
+        const int r = wr + (lane & 15), c = 2 * kk + (lane >> 4);
+        ldsm_x4(qa, qs + pf_off<D>(r, c));
+      }
 #pragma unroll
       for (int np = 0; np < 4; ++np) {  // pairs of n-tiles
         uint32_t b[4];
         const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3), c = 2 * kk + ((lane >> 3) & 1);
         ldsm_x4(b, ks + pf_off<D>(r, c));
-        M::run(sc[2 * np], qa[kk], b[0], b[1]);
-        M::run(sc[2 * np + 1], qa[kk], b[2], b[3]);
+        M::run(sc[2 * np], qa, b[0], b[1]);
+        M::run(sc[2 * np + 1], qa, b[2], b[3]);
       }
+    }
     // scale, causal mask, running max
     float mx_a = -INFINITY, mx_b = -INFINITY;
 #pragma unroll
