@@ -74,6 +74,12 @@ constexpr int kTileTokens = 16;  // tokens of a tile of a 16- or 32-bit cache
 template <typename KT>
 constexpr int tile_tokens_for() { return sizeof(KT) == 1 ? 2 * kTileTokens : kTileTokens; }
 constexpr int kDecodeWarps = 8;  // one resident block of 8 warps per SM (measured best)
+// fp8 caches (1 or 2 query heads per warp): a warp's per-tile work is a
+// longer latency chain for half the bytes, so more warps share an SM (as many
+// as registers allow) with a larger ring budget.
+constexpr int kFp8Warps1 = 20;  // one query head per warp (measured: 16 -> 193 us, 20 -> 184 us, 24 -> 189 us)
+constexpr int kFp8Warps2 = 12;  // two query heads per warp (register limit)
+constexpr int kFp8RingBudget = 200 * 1024;
 constexpr int kMaxDecodeWarps = 4096;  // bound of the persistent grid (partial slots in the workspace)
 constexpr int kMaxGroupPerWarp = 4;    // query heads one warp serves against one kv head
 constexpr int kBtChunk = 128;          // block-table entries a warp keeps in shared memory
@@ -140,25 +146,27 @@ struct LaneDims<T, __nv_fp8_e4m3, D> {
 
 template <typename T, int D, int GPW, typename KT = T>
 struct DecodeShape {
+  static constexpr bool kFp8Wide = sizeof(KT) == 1 && GPW <= 2;
+  static constexpr int kWarps = kFp8Wide ? (GPW == 1 ? kFp8Warps1 : kFp8Warps2) : kDecodeWarps;
   static constexpr int kElemBytes = sizeof(T);
   static constexpr int kRowBytes = D * kElemBytes;                       // query / output row
   static constexpr int kKvRowBytes = D * (int)sizeof(KT);                // cache row
   static constexpr int kTileTokensT = tile_tokens_for<KT>();
   static constexpr int kTileBytes = kTileTokensT * kKvRowBytes;          // K (or V) rows of one tile
   static constexpr int kStageBytes = 2 * kTileBytes + GPW * kRowBytes;   // K, V, query rows
-  static constexpr int kRingBudget = 128 * 1024;
-  static constexpr int kStagesRaw = kRingBudget / (kDecodeWarps * 2 * kTileBytes);
+  static constexpr int kRingBudget = kFp8Wide ? kFp8RingBudget : 128 * 1024;
+  static constexpr int kStagesRaw = kRingBudget / (kWarps * 2 * kTileBytes);
   static constexpr int kStages = kStagesRaw < 1 ? 1 : (kStagesRaw > 4 ? 4 : kStagesRaw);
   static constexpr int kChunksPerRow = kRowBytes / 16;
   static constexpr int kChunksPerLane = kChunksPerRow / 8;
   static constexpr int kVec = Chunk<T>::kElems;
   static constexpr int kDimsPerLane = D / 8;
-  static constexpr int kRingBytes = kDecodeWarps * kStages * kStageBytes;
+  static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
   static constexpr int kBarOff = kRingBytes;
-  static constexpr int kBtOff = kBarOff + kDecodeWarps * kStages * 8;
-  static constexpr int kScanOff = kBtOff + kDecodeWarps * kBtChunk * 4;
-  static constexpr int kStartOff = kScanOff + kDecodeWarps * 8;
-  static constexpr int kSmemBytes = kStartOff + kDecodeWarps * 16;
+  static constexpr int kBtOff = kBarOff + kWarps * kStages * 8;
+  static constexpr int kScanOff = kBtOff + kWarps * kBtChunk * 4;
+  static constexpr int kStartOff = kScanOff + kWarps * 8;
+  static constexpr int kSmemBytes = kStartOff + kWarps * 16;
   static_assert(kChunksPerRow % 8 == 0, "row must split into 8 lanes of 16-byte chunks");
   static_assert(kDimsPerLane * 8 == D, "lane mapping");
   static_assert(kStageBytes % 16 == 0 && kRowBytes % 16 == 0 && kTileBytes % 16 == 0, "bulk copy alignment");
@@ -179,7 +187,9 @@ __device__ __forceinline__ int load_len(const DecodeParams& p, int s, int cap) {
   return L;
 }
 
-// Exclusive scan of one value per thread over the block; `total` gets the sum.
+// Exclusive scan of one value per thread over a block of NW warps; `total`
+// gets the sum.
+template <int NW = kDecodeWarps>
 __device__ __forceinline__ long long block_exclusive_scan(long long v, long long* scratch, long long& total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   long long x = v;
@@ -193,7 +203,7 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
   long long before = 0;
   total = 0;
 #pragma unroll
-  for (int i = 0; i < kDecodeWarps; ++i) {
+  for (int i = 0; i < NW; ++i) {
     const long long t = scratch[i];
     if (i < warp) before += t;
     total += t;
@@ -222,14 +232,14 @@ __device__ __forceinline__ void cursor_next(TileCursor& c, const DecodeParams& p
 }
 
 template <typename T, int D, int GPW, typename KT = T>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
+__global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
     pa_decode_kernel(const DecodeParams p) {
   using S = DecodeShape<T, D, GPW, KT>;
   using LD = LaneDims<T, KT, D>;
   constexpr bool kQuant = !std::is_same<T, KT>::value;
   constexpr int TT = S::kTileTokensT;  // tokens per tile
   constexpr int RPG = TT / 4;          // rows of a tile per 8-lane group
-  constexpr int NW = kDecodeWarps;
+  constexpr int NW = S::kWarps;
   constexpr int ST = S::kStages;
   constexpr int DPL = S::kDimsPerLane;
   constexpr int CPL = LD::kParts;       // pieces of a row per lane
@@ -254,7 +264,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   long long mine = 0;
   for (int s = threadIdx.x; s < p.num_seqs; s += NW * 32) mine += tiles_of_t<TT>(load_len(p, s, cap));
   long long Ttot;
-  block_exclusive_scan(mine, scan, Ttot);
+  block_exclusive_scan<NW>(mine, scan, Ttot);
   Ttot *= HG;
   const long long W = (long long)gridDim.x * NW;
   const long long Weff = W < Ttot ? W : Ttot;  // every active warp gets >= 1 tile
@@ -268,7 +278,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     const int s = base + threadIdx.x;
     const long long cnt = s < p.num_seqs ? (long long)tiles_of_t<TT>(load_len(p, s, cap)) * HG : 0;
     long long chunk_total;
-    const long long excl = carry + block_exclusive_scan(cnt, scan, chunk_total);
+    const long long excl = carry + block_exclusive_scan<NW>(cnt, scan, chunk_total);
 #pragma unroll
     for (int i = 0; i < NW; ++i) {
       const long long w = (long long)blockIdx.x * NW + i;
@@ -613,13 +623,13 @@ cudaError_t launch_pa_decode(const DecodeParams& p, cudaStream_t stream) {
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_decode_kernel<T, D, GPW, KT>,
-                                                      kDecodeWarps * 32, S::kSmemBytes);
+                                                      S::kWarps * 32, S::kSmemBytes);
     if (e != cudaSuccess) return e;
     grid = sms * (per_sm > 0 ? per_sm : 1);
-    if (grid > kMaxDecodeWarps / kDecodeWarps) grid = kMaxDecodeWarps / kDecodeWarps;
+    if (grid > kMaxDecodeWarps / S::kWarps) grid = kMaxDecodeWarps / S::kWarps;
     if (dev >= 0 && dev < 64) __atomic_store_n(&grid_of_device[dev], grid, __ATOMIC_RELEASE);
   }
-  pa_decode_kernel<T, D, GPW, KT><<<grid, kDecodeWarps * 32, S::kSmemBytes, stream>>>(p);
+  pa_decode_kernel<T, D, GPW, KT><<<grid, S::kWarps * 32, S::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
