@@ -144,17 +144,18 @@ struct LaneDims<T, __nv_fp8_e4m3, D> {
   }
 };
 
-template <typename T, int D, int GPW, typename KT = T>
+// NWO / BudgetO: explicit warps per block and ring budget (0: the defaults).
+template <typename T, int D, int GPW, typename KT = T, int NWO = 0, int BudgetO = 0>
 struct DecodeShape {
   static constexpr bool kFp8Wide = sizeof(KT) == 1 && GPW <= 2;
-  static constexpr int kWarps = kFp8Wide ? (GPW == 1 ? kFp8Warps1 : kFp8Warps2) : kDecodeWarps;
+  static constexpr int kWarps = NWO ? NWO : (kFp8Wide ? (GPW == 1 ? kFp8Warps1 : kFp8Warps2) : kDecodeWarps);
   static constexpr int kElemBytes = sizeof(T);
   static constexpr int kRowBytes = D * kElemBytes;                       // query / output row
   static constexpr int kKvRowBytes = D * (int)sizeof(KT);                // cache row
   static constexpr int kTileTokensT = tile_tokens_for<KT>();
   static constexpr int kTileBytes = kTileTokensT * kKvRowBytes;          // K (or V) rows of one tile
   static constexpr int kStageBytes = 2 * kTileBytes + GPW * kRowBytes;   // K, V, query rows
-  static constexpr int kRingBudget = kFp8Wide ? kFp8RingBudget : 128 * 1024;
+  static constexpr int kRingBudget = BudgetO ? BudgetO : (kFp8Wide ? kFp8RingBudget : 128 * 1024);
   static constexpr int kStagesRaw = kRingBudget / (kWarps * 2 * kTileBytes);
   static constexpr int kStages = kStagesRaw < 1 ? 1 : (kStagesRaw > 4 ? 4 : kStagesRaw);
   static constexpr int kChunksPerRow = kRowBytes / 16;

@@ -15,9 +15,9 @@
 //   tail segments (sequence s, head group hg): rows [S_g, L_s) of s's own
 //     blocks against its query heads, as in the plain kernel.
 // The prefix segments run first, balanced over all warps, then the tails,
-// balanced again; a grid-wide counter separates the two phases. A tail row of
-// a sequence with a shared prefix merges its prefix result (log-sum-exp) when
-// it writes the output. Pieces of a segment cut by warp range boundaries are
+// balanced again, as two launches in stream order. A tail row of a sequence
+// with a shared prefix merges its prefix result (log-sum-exp) when it writes
+// the output. Pieces of a segment cut by warp range boundaries are
 // merged as in the plain kernel.
 //
 // A prologue kernel checks the caller's grouping: group_start must partition
@@ -49,7 +49,7 @@ struct GroupedParams {
   const int32_t* shared_blocks;  // [num_groups]
   int num_groups;
   int32_t* ws_flag;     // [1] 1 = grouping rejected
-  int32_t* ws_sync;     // [2] phase arrivals, warps done (zero between launches)
+  int32_t* ws_sync;     // [2] reserved (unused)
   int32_t* ws_group_S;  // [num_groups] usable shared prefix tokens
   int32_t* ws_seq_P;    // [num_seqs] prefix tokens of the sequence's group
   int32_t* ws_seg_ctr;  // [2][num_seqs * num_heads] piece counters (prefix, tail)
@@ -506,47 +506,26 @@ __device__ __forceinline__ void core_tile(const unsigned char* ks, const unsigne
   }
 }
 
-// ---- grid-wide phase barrier (the grid is co-resident: cooperative launch) --
-// Called by the whole warp: the warp barrier orders every lane's earlier
-// writes before lane 0's release, which counts the warp in.
-__device__ __forceinline__ void arrive_gpu(int32_t* ctr) {
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ctr), "r"(1) : "memory");
+// Ring budget of a phase kernel of NW warps: two stages per warp for 16-bit
+// data while that fits (the default budget for 8 warps), at most 200 KB.
+template <typename T, int D, int NW>
+__host__ __device__ constexpr int grouped_ring_budget() {
+  return NW == kDecodeWarps ? 0
+                            : (NW * 4 * kTileTokens * D * (int)sizeof(T) < 200 * 1024
+                                   ? NW * 4 * kTileTokens * D * (int)sizeof(T)
+                                   : 200 * 1024);
 }
 
-__device__ __forceinline__ int load_acquire_gpu(const int32_t* ctr) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-  return v;
-}
-
-// Lane 0 waits until *ctr >= target, for at most limit_ns; false if it ran out.
-__device__ __forceinline__ bool wait_count(const int32_t* ctr, int target, uint64_t limit_ns) {
-  int ok = 1;
-  if ((threadIdx.x & 31) == 0 && load_acquire_gpu(ctr) < target) {
-    const uint64_t t0 = globaltimer_ns();
-    while (load_acquire_gpu(ctr) < target) {
-      if (globaltimer_ns() - t0 >= limit_ns) {
-        ok = 0;
-        break;
-      }
-      __nanosleep(256);
-    }
-  }
-  ok = __shfl_sync(kFullMask, ok, 0);
-  __syncwarp();  // every lane's later reads follow lane 0's acquire
-  return ok != 0;
-}
-
-// Two phases over the same persistent warps: first every prefix segment
-// (balanced over all warps), then every tail segment (balanced again). A
-// warp starts fetching its tail tiles before the phase barrier; only the end
-// of a tail visit — which needs the row's prefix result — waits for it.
-template <typename T, int D, int TG>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
+// One phase of the grouped decode over persistent warps: PH = 0 runs every
+// prefix segment, PH = 1 every tail segment, each balanced over all warps.
+// The two phases are two launches in stream order, so the tail phase sees
+// every prefix result (and the partial slots the prefix phase used are free);
+// the tail launch may start early (programmatic dependent launch) and waits
+// for the prefix grid right after issuing its first K/V copies.
+template <typename T, int D, int TG, int PH, int NW>
+__global__ void __launch_bounds__(NW * 32)
     pa_decode_grouped_kernel(const GroupedParams gp) {
-  using S = DecodeShape<T, D, kGroupRows>;
-  constexpr int NW = kDecodeWarps;
+  using S = DecodeShape<T, D, kGroupRows, T, NW, grouped_ring_budget<T, D, NW>()>;
   constexpr int R = kGroupRows;
   constexpr bool kMma = Mma16816<T>::kOk;
   constexpr int QR = kMma ? TG : R;  // query rows kept in fp32 registers
@@ -562,7 +541,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
   long long* scan = reinterpret_cast<long long*>(smem + S::kScanOff);
-  __shared__ longlong2 starts[2 * NW];  // per phase: (group or sequence, offset)
+  __shared__ longlong2 starts[NW];  // (group or sequence, offset) of each warp's first unit
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -586,50 +565,39 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   x.use_groups = __ldcg(gp.ws_flag) == 0;
   const int B = p.num_seqs, G = gp.num_groups, HG = p.head_groups, H = p.num_heads;
 
-  // ---- start-up: tiles of both phases, then each warp's first segment --------
-  long long mine = 0;
-  for (int g = threadIdx.x; g < G; g += NW * 32) mine += prefix_units(x, g);
-  long long TA;
-  block_exclusive_scan(mine, scan, TA);
-  mine = 0;
-  for (int s = threadIdx.x; s < B; s += NW * 32)
-    mine += (long long)HG * (tiles_of(ctx_len(x, s) - seq_prefix(x, s)) + kSegCostTail);
-  long long TB;
-  block_exclusive_scan(mine, scan, TB);
+  // ---- start-up: work units of this phase, then each warp's first segment ----
   const long long W = (long long)gridDim.x * NW;
-  const long long WA = W < TA ? W : TA;  // 0 when no group shares a prefix
-  const long long WB = W < TB ? W : TB;
   const long long wid = (long long)blockIdx.x * NW + warp;
-  if (threadIdx.x < 2 * NW) starts[threadIdx.x] = make_longlong2(-1, 0);
+  long long mine = 0, Ttot = 0;
+  if constexpr (PH == 0) {
+    for (int g = threadIdx.x; g < G; g += NW * 32) mine += prefix_units(x, g);
+  } else {
+    for (int s = threadIdx.x; s < B; s += NW * 32)
+      mine += (long long)HG * (tiles_of(ctx_len(x, s) - seq_prefix(x, s)) + kSegCostTail);
+  }
+  block_exclusive_scan<NW>(mine, scan, Ttot);
+  const long long Weff = W < Ttot ? W : Ttot;  // 0 when the phase has no work
+  if (threadIdx.x < NW) starts[threadIdx.x] = make_longlong2(-1, 0);
   __syncthreads();
   long long carry = 0;
-  for (int base = 0; base < G; base += NW * 32) {
-    const int g = base + threadIdx.x;
-    const long long cnt = g < G ? prefix_units(x, g) : 0;
-    long long tot;
-    const long long excl = carry + block_exclusive_scan(cnt, scan, tot);
-#pragma unroll
-    for (int i = 0; i < NW; ++i) {
-      const long long w = (long long)blockIdx.x * NW + i;
-      if (w < WA) {
-        const long long a = w * TA / WA;
-        if (cnt > 0 && a >= excl && a < excl + cnt) starts[i] = make_longlong2(g, a - excl);
-      }
+  const int nitems = PH == 0 ? G : B;
+  for (int base = 0; base < nitems; base += NW * 32) {
+    const int i0 = base + threadIdx.x;
+    long long cnt = 0;
+    if (i0 < nitems) {
+      if constexpr (PH == 0)
+        cnt = prefix_units(x, i0);
+      else
+        cnt = (long long)HG * (tiles_of(ctx_len(x, i0) - seq_prefix(x, i0)) + kSegCostTail);
     }
-    carry += tot;
-  }
-  carry = 0;
-  for (int base = 0; base < B; base += NW * 32) {
-    const int s = base + threadIdx.x;
-    const long long cnt = s < B ? (long long)HG * (tiles_of(ctx_len(x, s) - seq_prefix(x, s)) + kSegCostTail) : 0;
     long long tot;
-    const long long excl = carry + block_exclusive_scan(cnt, scan, tot);
+    const long long excl = carry + block_exclusive_scan<NW>(cnt, scan, tot);
 #pragma unroll
     for (int i = 0; i < NW; ++i) {
       const long long w = (long long)blockIdx.x * NW + i;
-      if (w < WB) {
-        const long long a = w * TB / WB;
-        if (cnt > 0 && a >= excl && a < excl + cnt) starts[NW + i] = make_longlong2(s, a - excl);
+      if (w < Weff) {
+        const long long a = w * Ttot / Weff;
+        if (cnt > 0 && a >= excl && a < excl + cnt) starts[i] = make_longlong2(i0, a - excl);
       }
     }
     carry += tot;
@@ -651,11 +619,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const char* qbase = static_cast<const char*>(p.q);
   const int seg = bs < kTileTokens ? bs : kTileTokens;
   const int nseg = kTileTokens / seg;
-  int32_t* sync_arrive = gp.ws_sync;
-  int32_t* sync_exit = gp.ws_sync + 1;
   int bt_s = -1, bt_j0 = 0;
   int ring = 0;  // tiles this warp has consumed so far (ring position)
-  bool failed = false, synced = false;
 
   float qf[QR][DPL];
   uint32_t qa[D / 32][2][2];        // prefix query rows as MMA A-operands (16-bit types)
@@ -663,15 +628,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   float pm = -INFINITY, pl = 0.f;   // tensor-core state of a prefix: row mg
   float po[D / 32][4][2];
 
-  for (int phase = 0; phase < 2; ++phase) {
-    const long long Tp = phase == 0 ? TA : TB, Wp = phase == 0 ? WA : WB;
+  {
+    constexpr int phase = PH;
+    const long long Tp = Ttot, Wp = Weff;
     const int E = phase == 0 ? kSegCostPrefix : kSegCostTail;
     const long long a_begin = wid < Wp ? wid * Tp / Wp : Tp;
     const long long a_end = wid < Wp ? (wid + 1) * Tp / Wp : Tp;
-    if (!failed && a_begin < a_end) {
+    if (a_begin < a_end) {
       GCursor ci;
       {
-        const longlong2 st0 = starts[phase * NW + warp];
+        const longlong2 st0 = starts[warp];
         ci.part = phase;
         ci.a = static_cast<int>(st0.x);
         ci.b = 0;
@@ -756,6 +722,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         issue(ci, issued);
         gcursor_next(ci, x);
       }
+      // the tail phase reads prefix results and reuses the partial slots:
+      // wait for the prefix grid (its first K/V copies are already in flight)
+      if constexpr (PH == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
       bool visit_from_start = true;
 
       for (; cc.g < a_end; ++ring) {
@@ -763,8 +732,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
           if (lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
           for (int k2 = ring; k2 < issued; ++k2)
             mbar_wait_bounded(my_bars + (k2 % ST), (k2 / ST) & 1, kDrainLimitNs);
-          failed = true;
-          break;
+          return;  // outputs of this call are not valid
         }
         const unsigned char* ks = my_ring + (ring % ST) * S::kStageBytes;
         const unsigned char* vs = ks + S::kTileBytes;
@@ -837,12 +805,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
         if (last) {
           // ---- end of this warp's visit of the segment under cc --------------
-          if (phase == 1 && !synced) {
-            // prefix results, and the partial slots phase 0 used, are settled
-            synced = wait_count(sync_arrive, (int)W, p.wait_limit_ns);
-            if (!synced && lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-            synced = true;
-          }
 #pragma unroll
           for (int g = 0; g < OR; ++g)
             if (!tc_prefix && g < nr) {
@@ -1021,51 +983,72 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         gcursor_next(cc, x);
       }
     }
-    if (phase == 0) arrive_gpu(sync_arrive);
-  }
-  // last warp out re-zeroes the phase counters for the next launch
-  __syncwarp();
-  if (lane == 0) {
-    const int prev = atomicAdd(sync_exit, 1);
-    if (prev == (int)W - 1) {
-      *sync_arrive = 0;
-      *sync_exit = 0;
-    }
   }
 }
 
-// Validation prologue, then the persistent grid sized to the device.
-template <typename T, int D, int TG>
-cudaError_t launch_pa_decode_grouped(const GroupedParams& gp, cudaStream_t stream) {
-  using S = DecodeShape<T, D, kGroupRows>;
+// Persistent grid of one phase kernel on the current device (cached).
+template <typename T, int D, int TG, int PH, int NW>
+cudaError_t grouped_grid(int& grid) {
+  using S = DecodeShape<T, D, kGroupRows, T, NW, grouped_ring_budget<T, D, NW>()>;
   static int grid_of_device[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  int grid = (dev >= 0 && dev < 64) ? __atomic_load_n(&grid_of_device[dev], __ATOMIC_ACQUIRE) : 0;
-  if (grid == 0) {
-    e = cudaFuncSetAttribute(pa_decode_grouped_kernel<T, D, TG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             S::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    int sms = 0, per_sm = 0;
-    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_decode_grouped_kernel<T, D, TG>,
-                                                      kDecodeWarps * 32, S::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    grid = sms * (per_sm > 0 ? per_sm : 1);
-    if (grid > kMaxDecodeWarps / kDecodeWarps) grid = kMaxDecodeWarps / kDecodeWarps;
-    if (dev >= 0 && dev < 64) __atomic_store_n(&grid_of_device[dev], grid, __ATOMIC_RELEASE);
-  }
+  grid = (dev >= 0 && dev < 64) ? __atomic_load_n(&grid_of_device[dev], __ATOMIC_ACQUIRE) : 0;
+  if (grid != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(pa_decode_grouped_kernel<T, D, TG, PH, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           S::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  int sms = 0, per_sm = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_decode_grouped_kernel<T, D, TG, PH, NW>, NW * 32,
+                                                    S::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  grid = sms * (per_sm > 0 ? per_sm : 1);
+  if (grid > kMaxDecodeWarps / NW) grid = kMaxDecodeWarps / NW;
+  if (dev >= 0 && dev < 64) __atomic_store_n(&grid_of_device[dev], grid, __ATOMIC_RELEASE);
+  return cudaSuccess;
+}
+
+// Warps per block of each phase kernel: the tail phase of 16-bit data runs
+// 12 warps (measured on the copy-on-write workload: prefix/tail warps 8/8
+// 160.1 us, 8/12 157.4 us, 12/8 167.9 us, 12/12 165.9 us, 12/16 168.3 us).
+template <typename T, int PH>
+__host__ __device__ constexpr int grouped_warps() { return sizeof(T) == 2 && PH == 1 ? 12 : kDecodeWarps; }
+
+// Validation prologue, the prefix phase, then the tail phase (launched as a
+// programmatic dependent of the prefix phase, so its start-up overlaps the
+// prefix phase's last blocks).
+template <typename T, int D, int TG>
+cudaError_t launch_pa_decode_grouped(const GroupedParams& gp, cudaStream_t stream) {
+  constexpr int NW0 = grouped_warps<T, 0>(), NW1 = grouped_warps<T, 1>();
+  using S0 = DecodeShape<T, D, kGroupRows, T, NW0, grouped_ring_budget<T, D, NW0>()>;
+  using S1 = DecodeShape<T, D, kGroupRows, T, NW1, grouped_ring_budget<T, D, NW1>()>;
+  int grid0 = 0, grid1 = 0;
+  cudaError_t e = grouped_grid<T, D, TG, 0, NW0>(grid0);
+  if (e != cudaSuccess) return e;
+  e = grouped_grid<T, D, TG, 1, NW1>(grid1);
+  if (e != cudaSuccess) return e;
   int pro = (gp.num_groups + 7) / 8;
   pro = pro < 1 ? 1 : (pro > 4096 ? 4096 : pro);
   pa_group_prologue_kernel<T><<<pro, 256, 0, stream>>>(gp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  // co-residency of every block is required by the phase barrier
-  void* args[] = {const_cast<GroupedParams*>(&gp)};
-  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(pa_decode_grouped_kernel<T, D, TG>), dim3(grid),
-                                  dim3(kDecodeWarps * 32), args, S::kSmemBytes, stream);
+  pa_decode_grouped_kernel<T, D, TG, 0, NW0><<<grid0, NW0 * 32, S0::kSmemBytes, stream>>>(gp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid1);
+  cfg.blockDim = dim3(NW1 * 32);
+  cfg.dynamicSmemBytes = S1::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, pa_decode_grouped_kernel<T, D, TG, 1, NW1>, gp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
