@@ -271,14 +271,12 @@ struct Mma16816<__nv_bfloat16> {
   // rows 0..7 only: accumulators of rows 8..15 are discarded
   __device__ __forceinline__ static void run2(float& c0, float& c1, uint32_t a_lo, uint32_t a_hi,
                                               uint32_t b_lo, uint32_t b_hi) {
-    float d2, d3;
+    [[maybe_unused]] float d2, d3;
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%10,%11,%12,%13};"
         : "=f"(c0), "=f"(c1), "=f"(d2), "=f"(d3)
         : "r"(a_lo), "r"(0u), "r"(a_hi), "r"(0u), "r"(b_lo), "r"(b_hi), "f"(c0), "f"(c1), "f"(0.f), "f"(0.f));
-    (void)d2;
-    (void)d3;
   }
   __device__ __forceinline__ static uint32_t pack(float x, float y) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
@@ -303,14 +301,12 @@ struct Mma16816<__half> {
   }
   __device__ __forceinline__ static void run2(float& c0, float& c1, uint32_t a_lo, uint32_t a_hi,
                                               uint32_t b_lo, uint32_t b_hi) {
-    float d2, d3;
+    [[maybe_unused]] float d2, d3;
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%10,%11,%12,%13};"
         : "=f"(c0), "=f"(c1), "=f"(d2), "=f"(d3)
         : "r"(a_lo), "r"(0u), "r"(a_hi), "r"(0u), "r"(b_lo), "r"(b_hi), "f"(c0), "f"(c1), "f"(0.f), "f"(0.f));
-    (void)d2;
-    (void)d3;
   }
   __device__ __forceinline__ static uint32_t pack(float x, float y) {
     const __half2 h = __floats2half2_rn(x, y);

@@ -117,3 +117,41 @@ def test_prefill_full_size_sampled():
                                scale=cfg.scale, num_heads=cfg.num_heads, num_kv_heads=cfg.num_kv_heads,
                                head_dim=cfg.head_dim, block_size=cfg.block_size, dtype=cfg.dtype, threads=3)
     assert_close(to_f64(out)[rows], ref, "full-size sampled")
+
+
+def test_prefill_device_errors_are_reported_and_skipped():
+    """A block id out of range sets PKV_DEV_ERR_BLOCK_ID (its rows read as
+    zeros, nothing faults); a sequence with more queries than tokens sets
+    PKV_DEV_ERR_CONTEXT_LEN and is skipped; the context stays usable."""
+    import paged_kv_cache_204_gb300 as pkv
+    cfg = SP.get("prefill_small")
+    lay = SP.build(cfg)
+    vals = SP.host_values(cfg, lay)
+    kc, vc = SP.host_pools(cfg)
+    kc_d, vc_d = up(kc, cfg.dtype), up(vc, cfg.dtype)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_prefill(cfg, lay, vals, kc_d, vc_d, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    bad_bt = lay.block_tables.copy()
+    bad_bt[1, 0] = cfg.num_blocks + 5
+    out2 = torch.empty_like(out)
+    pkv.paged_attention_prefill(out2, up(vals.q, cfg.dtype), kc_d, vc_d, t64(bad_bt), t64(lay.context_lens),
+                                t64(lay.query_start), cfg.scale, lay.max_query_len, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.DEV_ERR_BLOCK_ID
+    err.zero_()
+    bad_cl = lay.context_lens.copy()
+    bad_cl[0] = int(lay.query_start[1] - lay.query_start[0]) - 1  # fewer tokens than queries
+    pkv.paged_attention_prefill(out2, up(vals.q, cfg.dtype), kc_d, vc_d, t64(lay.block_tables), t64(bad_cl),
+                                t64(lay.query_start), cfg.scale, lay.max_query_len, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.DEV_ERR_CONTEXT_LEN
+    # the context is still fine: a normal call gives the same result as before
+    err.zero_()
+    out3 = torch.empty_like(out)
+    pkv.paged_attention_prefill(out3, up(vals.q, cfg.dtype), kc_d, vc_d, t64(lay.block_tables),
+                                t64(lay.context_lens), t64(lay.query_start), cfg.scale, lay.max_query_len,
+                                dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and torch.equal(out3, out)
