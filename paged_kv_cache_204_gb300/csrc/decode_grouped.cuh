@@ -98,13 +98,13 @@ __global__ void __launch_bounds__(256) pa_group_prologue_kernel(const GroupedPar
       minL = warp_min(minL);
       const int32_t* row0 = p.block_tables + (size_t)lo * MB;
       int first_bad = sb;
-      for (int j = lane; j < sb; j += 32) {
-        const int32_t id0 = __ldg(row0 + j);
-        for (int s = lo + 1; s < hi; ++s)
-          if (__ldg(p.block_tables + (size_t)s * MB + j) != id0) {
-            first_bad = min(first_bad, j);
-            break;
-          }
+      // every (member, entry) pair is an independent comparison: the lanes
+      // take them all at once, so the loads are in flight together
+      const int pairs = (hi - lo - 1) * sb;
+#pragma unroll 4
+      for (int i = lane; i < pairs; i += 32) {
+        const int m = i / sb, j = i - m * sb;
+        if (__ldg(p.block_tables + (size_t)(lo + 1 + m) * MB + j) != __ldg(row0 + j)) first_bad = min(first_bad, j);
       }
       first_bad = warp_min(first_bad);
       if (first_bad < sb) {
