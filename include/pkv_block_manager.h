@@ -134,6 +134,32 @@ pkv_status pkv_bm_beam_step(pkv_block_manager* bm, const int32_t* beams, const i
                             int32_t n_new, int32_t* new_beams, int64_t* slots, int64_t* cow_pairs,
                             int32_t* num_cow);
 
+/* One beam-search step of `requests` requests of `width` beams each, in one
+ * call (the host side of a batched beam-search decode step). beams and
+ * parents are [requests][width]; row r is one request's current beams and
+ * the parent index (in [0, width), within row r) of each of its new beams,
+ * as in pkv_bm_beam_step. The step runs in three passes over all requests:
+ * first every beam that no new beam continues is ended, then every new beam
+ * takes its sequence id (a parent's first child keeps the parent's id,
+ * further children are forks), then every new beam appends n_new tokens in
+ * row-major order (r, i), exactly as pkv_bm_append_batch over that order.
+ * Per request this gives the same tables as pkv_bm_beam_step; across
+ * requests the physical block and sequence ids handed out may differ from
+ * calling it once per request, because every request's ended blocks return
+ * before any request appends. new_beams is [requests][width]; slots
+ * ([requests * width * n_new], packed row-major), cow_pairs
+ * ([requests * width][2]) and num_cow as in pkv_bm_append_batch;
+ * shared_blocks ([requests]) receives, per request, the number of leading
+ * blocks its new beams all share (pkv_bm_common_prefix). Each output but
+ * new_beams may be NULL. All or nothing across all requests:
+ * PKV_ERR_OUT_OF_BLOCKS (nothing changed) when the whole step does not fit
+ * after the ended beams' blocks return; PKV_ERR_INVALID_ARG when
+ * requests < 0, width < 1, n_new < 0, a beam repeats anywhere in beams or is
+ * not live, or a parent index is out of range. requests = 0 is a no-op. */
+pkv_status pkv_bm_beam_step_many(pkv_block_manager* bm, const int32_t* beams, const int32_t* parents,
+                                 int32_t requests, int32_t width, int32_t n_new, int32_t* new_beams, int64_t* slots,
+                                 int64_t* cow_pairs, int32_t* num_cow, int32_t* shared_blocks);
+
 /* Length (tokens) and table length (blocks) of live sequence `seq`. */
 pkv_status pkv_bm_seq_info(const pkv_block_manager* bm, int32_t seq, int64_t* length, int32_t* num_blocks);
 

@@ -152,6 +152,34 @@ class BlockModel:
         self.__dict__.update(trial.__dict__)
         return new
 
+    def beam_step_many(self, rows, parent_rows, n_new: int = 1) -> list[list[int]]:
+        """The same step for several requests at once, in three passes over
+        all of them: every beam that no new beam of its own request continues
+        ends; then every new beam takes its sequence (first child keeps the
+        parent's, later ones fork it); then every new beam appends n_new
+        tokens, request by request and in order within a request. Raises
+        OutOfBlocks with nothing changed when the whole step does not fit."""
+        trial = copy.deepcopy(self)
+        for beams, parents in zip(rows, parent_rows):
+            for j, b in enumerate(beams):
+                if j not in parents:
+                    trial.free_seq(b)
+        out = []
+        for beams, parents in zip(rows, parent_rows):
+            new, kept = [], set()
+            for j in parents:
+                if j in kept:
+                    new.append(trial.fork(beams[j]))
+                else:
+                    kept.add(j)
+                    new.append(beams[j])
+            out.append(new)
+        for new in out:
+            for h in new:
+                trial.append(h, n_new)
+        self.__dict__.update(trial.__dict__)
+        return out
+
     def common_prefix(self, handles) -> int:
         ts = [self.tables[h] for h in handles]
         k = 0

@@ -96,23 +96,17 @@ class BeamDecoder:
     def plan(self, parents) -> StepPlan:
         """Host bookkeeping of one step: parents [R][W], entry (r, i) = the
         current beam of request r that new beam i continues."""
-        parents = np.asarray(parents, dtype=np.int32)
-        seqs, slots, pairs, shared = [], [], [], []
-        for r, beams in enumerate(self.requests):
-            new, sl, pr = self.manager.beam_step(beams, parents[r], 1)
-            self.requests[r] = [int(x) for x in new]
-            seqs.append(new)
-            slots.append(sl)
-            pairs.append(pr)
-        for beams in self.requests:
-            shared.append(self.manager.common_prefix(beams))
-        seqs = np.concatenate(seqs).astype(np.int32)
-        bt, cl = self.manager.export(seqs, self.max_blocks_per_seq)
         R = len(self.requests)
-        return StepPlan(seqs=seqs, slots=np.concatenate(slots), copy_pairs=np.concatenate(pairs).reshape(-1, 2),
+        parents = np.asarray(parents, dtype=np.int32).reshape(R, self.width)
+        beams = np.asarray(self.requests, dtype=np.int32).reshape(R, self.width)
+        new, slots, pairs, shared = self.manager.beam_step_many(beams, parents, 1)
+        self.requests = new.tolist()
+        seqs = new.reshape(-1)
+        bt, cl = self.manager.export(seqs, self.max_blocks_per_seq)
+        return StepPlan(seqs=seqs, slots=slots, copy_pairs=pairs,
                         block_tables=bt, context_lens=cl,
                         group_start=(np.arange(R + 1, dtype=np.int32) * self.width),
-                        shared_blocks=np.asarray(shared, dtype=np.int32),
+                        shared_blocks=shared,
                         max_context_len=int(cl.max()) if cl.size else 0)
 
     def _buffer(self, table: dict, name: str, nbytes: int, pinned: bool) -> torch.Tensor:

@@ -41,6 +41,8 @@ lib.pkv_bm_append_batch.argtypes = [_P, _P, _P, _I32, _P, _P, ctypes.POINTER(_I3
 lib.pkv_bm_append_batch.restype = ctypes.c_int
 lib.pkv_bm_beam_step.argtypes = [_P, _P, _P, _I32, _I32, _P, _P, _P, ctypes.POINTER(_I32)]
 lib.pkv_bm_beam_step.restype = ctypes.c_int
+lib.pkv_bm_beam_step_many.argtypes = [_P, _P, _P, _I32, _I32, _I32, _P, _P, _P, ctypes.POINTER(_I32), _P]
+lib.pkv_bm_beam_step_many.restype = ctypes.c_int
 lib.pkv_bm_seq_info.argtypes = [_P, _I32, ctypes.POINTER(_I64), ctypes.POINTER(_I32)]
 lib.pkv_bm_seq_info.restype = ctypes.c_int
 lib.pkv_bm_export.argtypes = [_P, _P, _I32, _I32, _P, _P]
@@ -142,6 +144,28 @@ class BlockManager:
         _check(lib.pkv_bm_beam_step(self._h, b.ctypes.data, p.ctypes.data, b.size, int(n_new), new.ctypes.data,
                                     slots.ctypes.data, pairs.ctypes.data, ctypes.byref(ncow)), "pkv_bm_beam_step")
         return new, slots, pairs[:ncow.value].copy()
+
+    def beam_step_many(self, beams, parents, n_new: int = 1
+                       ) -> tuple[np.ndarray, np.ndarray, np.ndarray, np.ndarray]:
+        """One beam-search step of R requests of W beams at once (beams and
+        parents int [R][W]; parents index within their own row). Every
+        request's ended beams are released before any request appends.
+        Returns (new beam sequence ids int32 [R][W], slots int64
+        [R * W * n_new] packed row-major, copy-on-write pairs int64 [k][2],
+        blocks shared by all new beams of each request int32 [R])."""
+        b, p = _i32(beams), _i32(parents)
+        if b.ndim != 2 or b.shape != p.shape:
+            raise ValueError("beams and parents must both be [requests][width]")
+        R, W = b.shape
+        new = np.empty((R, W), dtype=np.int32)
+        slots = np.empty(b.size * max(int(n_new), 0), dtype=np.int64)
+        pairs = np.empty((b.size, 2), dtype=np.int64)
+        shared = np.empty(R, dtype=np.int32)
+        ncow = _I32()
+        _check(lib.pkv_bm_beam_step_many(self._h, b.ctypes.data, p.ctypes.data, R, W, int(n_new), new.ctypes.data,
+                                         slots.ctypes.data, pairs.ctypes.data, ctypes.byref(ncow),
+                                         shared.ctypes.data), "pkv_bm_beam_step_many")
+        return new, slots, pairs[:ncow.value].copy(), shared
 
     def seq_info(self, seq: int) -> tuple[int, int]:
         """(length in tokens, table length in blocks) of seq."""

@@ -10,7 +10,6 @@
 #include <cstdint>
 #include <limits>
 #include <new>
-#include <unordered_map>
 #include <vector>
 
 #include "pkv_block_manager.h"
@@ -28,6 +27,45 @@ struct pkv_block_manager {
   std::vector<Seq> seqs;
   std::vector<int32_t> free_ids;    // ids of ended sequences, reused last-in first-out
   int64_t cow_copies = 0;
+
+  // Scratch of the batched pre-checks (sized on first use, all zero between
+  // calls): per-block reference changes and copies, the blocks touched, and
+  // per-sequence marks for duplicate detection.
+  std::vector<int32_t> blk_delta, blk_drop;
+  std::vector<uint8_t> blk_seen, seq_mark;
+  std::vector<int32_t> touched, marked;
+
+  void ensure_scratch() {
+    if (blk_delta.size() != (size_t)num_blocks) {
+      blk_delta.assign((size_t)num_blocks, 0);
+      blk_drop.assign((size_t)num_blocks, 0);
+      blk_seen.assign((size_t)num_blocks, 0);
+    }
+    if (seq_mark.size() < seqs.size()) seq_mark.resize(seqs.size(), 0);
+  }
+  void touch(int32_t b) {
+    if (!blk_seen[(size_t)b]) {
+      blk_seen[(size_t)b] = 1;
+      touched.push_back(b);
+    }
+  }
+  // false when `s` was marked already (a repeated id)
+  bool mark(int32_t s) {
+    if (seq_mark[(size_t)s]) return false;
+    seq_mark[(size_t)s] = 1;
+    marked.push_back(s);
+    return true;
+  }
+  void reset_scratch() {
+    for (int32_t b : touched) {
+      blk_delta[(size_t)b] = 0;
+      blk_drop[(size_t)b] = 0;
+      blk_seen[(size_t)b] = 0;
+    }
+    touched.clear();
+    for (int32_t q : marked) seq_mark[(size_t)q] = 0;
+    marked.clear();
+  }
 
   bool is_live(int32_t s) const { return s >= 0 && (size_t)s < seqs.size() && seqs[(size_t)s].live; }
 
@@ -206,30 +244,32 @@ pkv_status pkv_bm_append_batch(pkv_block_manager* bm, const int32_t* seqs, const
   if (n == 0) return PKV_OK;
   const int64_t bs = bm->block_size;
   int64_t need = 0;
+  pkv_status bad = PKV_OK;
   try {
-    std::vector<int32_t> ids(seqs, seqs + n);
-    std::sort(ids.begin(), ids.end());
-    if (std::adjacent_find(ids.begin(), ids.end()) != ids.end()) return PKV_ERR_INVALID_ARG;
+    bm->ensure_scratch();
     // blocks the batch takes, with the reference drops of earlier copies in it
-    std::unordered_map<int32_t, int32_t> dropped;
-    for (int32_t i = 0; i < n; ++i) {
-      if (!bm->is_live(seqs[i]) || counts[i] < 0) return PKV_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < n && bad == PKV_OK; ++i) {
+      if (!bm->is_live(seqs[i]) || counts[i] < 0 || !bm->mark(seqs[i])) {
+        bad = PKV_ERR_INVALID_ARG;
+        break;
+      }
       if (counts[i] == 0) continue;
       const pkv_block_manager::Seq& s = bm->seqs[(size_t)seqs[i]];
       if (s.len % bs != 0) {
         const int32_t last = s.table.back();
-        auto it = dropped.find(last);
-        const int32_t d = it == dropped.end() ? 0 : it->second;
-        if (bm->ref[(size_t)last] - d > 1) {
+        if (bm->ref[(size_t)last] - bm->blk_drop[(size_t)last] > 1) {
           ++need;
-          ++dropped[last];
+          bm->touch(last);
+          ++bm->blk_drop[(size_t)last];
         }
       }
       need += (s.len + counts[i] + bs - 1) / bs - (s.len + bs - 1) / bs;
     }
   } catch (...) {
-    return PKV_ERR_OUT_OF_BLOCKS;
+    bad = PKV_ERR_OUT_OF_BLOCKS;
   }
+  bm->reset_scratch();
+  if (bad != PKV_OK) return bad;
   if (need > (int64_t)bm->free_stack.size()) return PKV_ERR_OUT_OF_BLOCKS;
   int64_t at = 0;
   int32_t ncow = 0;
@@ -245,73 +285,107 @@ pkv_status pkv_bm_append_batch(pkv_block_manager* bm, const int32_t* seqs, const
   return PKV_OK;
 }
 
-pkv_status pkv_bm_beam_step(pkv_block_manager* bm, const int32_t* beams, const int32_t* parents, int32_t width,
-                            int32_t n_new, int32_t* new_beams, int64_t* slots, int64_t* cow_pairs,
-                            int32_t* num_cow) {
-  if (bm == nullptr || beams == nullptr || parents == nullptr || new_beams == nullptr || width < 1 || n_new < 0)
+pkv_status pkv_bm_beam_step_many(pkv_block_manager* bm, const int32_t* beams, const int32_t* parents,
+                                 int32_t requests, int32_t width, int32_t n_new, int32_t* new_beams, int64_t* slots,
+                                 int64_t* cow_pairs, int32_t* num_cow, int32_t* shared_blocks) {
+  if (bm == nullptr || beams == nullptr || parents == nullptr || new_beams == nullptr || requests < 0 ||
+      width < 1 || n_new < 0)
     return PKV_ERR_INVALID_ARG;
   if (num_cow != nullptr) *num_cow = 0;
+  if (requests == 0) return PKV_OK;
   const int64_t bs = bm->block_size;
-  std::vector<int32_t> children((size_t)width, 0);
+  const size_t total = (size_t)requests * (size_t)width;
+  std::vector<int32_t> children(total, 0);
+  pkv_status bad = PKV_OK;
+  int64_t need = 0, released = 0;
   try {
-    std::vector<int32_t> ids(beams, beams + width);
-    std::sort(ids.begin(), ids.end());
-    if (std::adjacent_find(ids.begin(), ids.end()) != ids.end()) return PKV_ERR_INVALID_ARG;
-    for (int32_t j = 0; j < width; ++j)
-      if (!bm->is_live(beams[j])) return PKV_ERR_INVALID_ARG;
-    for (int32_t i = 0; i < width; ++i) {
-      if (parents[i] < 0 || parents[i] >= width) return PKV_ERR_INVALID_ARG;
-      ++children[(size_t)parents[i]];
-    }
-    // reference counts after the step's forks and ends, for the blocks involved
-    std::unordered_map<int32_t, int32_t> delta;
-    for (int32_t j = 0; j < width; ++j) {
-      const int32_t d = children[(size_t)j] == 0 ? -1 : children[(size_t)j] - 1;
-      if (d == 0) continue;
-      for (int32_t b : bm->seqs[(size_t)beams[j]].table) delta[b] += d;
-    }
-    int64_t released = 0;
-    for (const auto& kv : delta)
-      if (bm->ref[(size_t)kv.first] + kv.second == 0) ++released;
-    // blocks the appends take (copies made earlier in the step counted)
-    int64_t need = 0;
-    std::unordered_map<int32_t, int32_t> dropped;
-    if (n_new > 0) {
-      for (int32_t i = 0; i < width; ++i) {
-        const pkv_block_manager::Seq& s = bm->seqs[(size_t)beams[parents[i]]];
-        if (s.len % bs != 0) {
-          const int32_t last = s.table.back();
-          auto it = delta.find(last);
-          const int32_t holders = bm->ref[(size_t)last] + (it == delta.end() ? 0 : it->second) - dropped[last];
-          if (holders > 1) {
-            ++need;
-            ++dropped[last];
-          }
-        }
-        need += (s.len + n_new + bs - 1) / bs - (s.len + bs - 1) / bs;
+    bm->ensure_scratch();
+    for (size_t k = 0; k < total; ++k)
+      if (!bm->is_live(beams[k]) || !bm->mark(beams[k])) {
+        bad = PKV_ERR_INVALID_ARG;
+        break;
       }
+    for (size_t k = 0; k < total && bad == PKV_OK; ++k) {
+      if (parents[k] < 0 || parents[k] >= width) {
+        bad = PKV_ERR_INVALID_ARG;
+        break;
+      }
+      ++children[k / (size_t)width * (size_t)width + (size_t)parents[k]];
     }
-    if (need > (int64_t)bm->free_stack.size() + released) return PKV_ERR_OUT_OF_BLOCKS;
-    bm->seqs.reserve(bm->seqs.size() + (size_t)width);
-    bm->free_ids.reserve(bm->free_ids.size() + (size_t)width);
+    if (bad == PKV_OK) {
+      // reference counts after every request's forks and ends
+      for (size_t k = 0; k < total; ++k) {
+        const int32_t d = children[k] == 0 ? -1 : children[k] - 1;
+        if (d == 0) continue;
+        for (int32_t b : bm->seqs[(size_t)beams[k]].table) {
+          bm->touch(b);
+          bm->blk_delta[(size_t)b] += d;
+        }
+      }
+      for (int32_t b : bm->touched)
+        if (bm->ref[(size_t)b] > 0 && bm->ref[(size_t)b] + bm->blk_delta[(size_t)b] == 0) ++released;
+      // blocks the appends take, in order (copies made earlier in the step counted)
+      if (n_new > 0)
+        for (size_t k = 0; k < total; ++k) {
+          const size_t r0 = k / (size_t)width * (size_t)width;
+          const pkv_block_manager::Seq& s = bm->seqs[(size_t)beams[r0 + (size_t)parents[k]]];
+          if (s.len % bs != 0) {
+            const int32_t last = s.table.back();
+            bm->touch(last);
+            if (bm->ref[(size_t)last] + bm->blk_delta[(size_t)last] - bm->blk_drop[(size_t)last] > 1) {
+              ++need;
+              ++bm->blk_drop[(size_t)last];
+            }
+          }
+          need += (s.len + n_new + bs - 1) / bs - (s.len + bs - 1) / bs;
+        }
+    }
+    if (bad == PKV_OK) {
+      bm->seqs.reserve(bm->seqs.size() + total);
+      bm->free_ids.reserve(bm->free_ids.size() + total);
+    }
   } catch (...) {
-    return PKV_ERR_OUT_OF_BLOCKS;
+    bad = PKV_ERR_OUT_OF_BLOCKS;
   }
-  // end the beams nobody continues, then hand out the survivors
-  for (int32_t j = 0; j < width; ++j)
-    if (children[(size_t)j] == 0) pkv_bm_free_seq(bm, beams[j]);
-  std::vector<char> taken((size_t)width, 0);
-  for (int32_t i = 0; i < width; ++i) {
-    const int32_t j = parents[i];
-    if (!taken[(size_t)j]) {
-      taken[(size_t)j] = 1;
-      new_beams[i] = beams[j];
-    } else if (pkv_bm_fork(bm, beams[j], &new_beams[i]) != PKV_OK) {
+  bm->reset_scratch();
+  if (bad != PKV_OK) return bad;
+  if (need > (int64_t)bm->free_stack.size() + released) return PKV_ERR_OUT_OF_BLOCKS;
+  // every request's ends, then its forks (a parent's first child keeps its id)
+  for (size_t k = 0; k < total; ++k)
+    if (children[k] == 0) pkv_bm_free_seq(bm, beams[k]);
+  std::vector<char> taken(total, 0);
+  for (size_t k = 0; k < total; ++k) {
+    const size_t j = k / (size_t)width * (size_t)width + (size_t)parents[k];
+    if (!taken[j]) {
+      taken[j] = 1;
+      new_beams[k] = beams[j];
+    } else if (pkv_bm_fork(bm, beams[j], &new_beams[k]) != PKV_OK) {
       return PKV_ERR_OUT_OF_BLOCKS;  // host memory ran out while copying a table
     }
   }
-  std::vector<int32_t> counts((size_t)width, n_new);
-  return pkv_bm_append_batch(bm, new_beams, counts.data(), width, slots, cow_pairs, num_cow);
+  // then every new beam's tokens, in order
+  int64_t at = 0;
+  int32_t ncow = 0;
+  if (n_new > 0)
+    for (size_t k = 0; k < total; ++k) {
+      int32_t c = 0;
+      const pkv_status st = pkv_bm_append(bm, new_beams[k], n_new, slots != nullptr ? slots + at : nullptr,
+                                          cow_pairs != nullptr ? cow_pairs + 2 * (size_t)ncow : nullptr, &c);
+      if (st != PKV_OK) return st;  // not reached: the step was checked to fit
+      ncow += c;
+      at += n_new;
+    }
+  if (num_cow != nullptr) *num_cow = ncow;
+  if (shared_blocks != nullptr)
+    for (int32_t r = 0; r < requests; ++r)
+      pkv_bm_common_prefix(bm, new_beams + (size_t)r * width, width, shared_blocks + r);
+  return PKV_OK;
+}
+
+pkv_status pkv_bm_beam_step(pkv_block_manager* bm, const int32_t* beams, const int32_t* parents, int32_t width,
+                            int32_t n_new, int32_t* new_beams, int64_t* slots, int64_t* cow_pairs,
+                            int32_t* num_cow) {
+  return pkv_bm_beam_step_many(bm, beams, parents, 1, width, n_new, new_beams, slots, cow_pairs, num_cow, nullptr);
 }
 
 pkv_status pkv_bm_seq_info(const pkv_block_manager* bm, int32_t seq, int64_t* length, int32_t* num_blocks) {

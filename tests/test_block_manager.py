@@ -541,3 +541,179 @@ def test_beam_step_host_checks(pb):
     with pytest.raises(pb.OutOfBlocks):
         m.beam_step([a, b], [0, 0], 100)
     assert m.stats()["live_seqs"] == 2 and m.seq_info(a) == (5, 2) and m.seq_info(b) == (5, 2)
+
+
+# ---- batched beam steps (all requests of a decode step in one call) ---------------------
+
+def beam_requests(rng, m, bs, n_req, share_prompt):
+    """Requests of 2-5 beams each. With share_prompt every request's root is a
+    fork of one common prompt, so blocks are shared across requests too."""
+    labels, reqs, nxt = {}, [], 0
+    common = None
+    if share_prompt:
+        common = m.add_seq()
+        P = int(rng.integers(1, 4 * bs))
+        m.append(common, P)
+        labels[common] = list(range(P))
+        nxt = P
+    for r in range(n_req):
+        if common is not None:
+            root = m.fork(common)
+            labels[root] = list(labels[common])
+        else:
+            root = m.add_seq()
+            labels[root] = []
+        P = int(rng.integers(1, 3 * bs))
+        m.append(root, P)
+        labels[root] += list(range(nxt, nxt + P))
+        nxt += P
+        beams = [root]
+        for _ in range(int(rng.integers(2, 6)) - 1):
+            c = m.fork(root)
+            labels[c] = list(labels[root])
+            beams.append(c)
+        reqs.append(beams)
+    return labels, reqs, nxt, common
+
+
+@pytest.mark.parametrize("share_prompt", [False, True])
+def test_model_beam_step_many_matches_brute_force_views(share_prompt):
+    rng = np.random.default_rng(12 + share_prompt)
+    for bs in (2, 4):
+        m = BlockModel(100000, bs)
+        labels, reqs, nxt, _ = beam_requests(rng, m, bs, 4, share_prompt)
+        for step in range(10):
+            parents = [draw_parents(rng, len(b)) for b in reqs]
+            old = {b: list(labels[b]) for beams in reqs for b in beams}
+            new = m.beam_step_many(reqs, parents, 2)
+            for beams in reqs:
+                for b in beams:
+                    labels.pop(b, None)
+            for beams, ps, nb in zip(reqs, parents, new):
+                for i, h in enumerate(nb):
+                    labels[h] = old[beams[ps[i]]] + [nxt, nxt + 1]
+                    nxt += 2
+            reqs = new
+            assert (m.used_blocks(), m.filled_slots()) == distinct_views(labels, bs)
+            assert m.logical_tokens() == sum(len(v) for v in labels.values())
+
+
+def test_model_beam_step_many_is_per_request_steps_without_sharing():
+    """Requests that share no block: the batched step leaves the same
+    counters and tables (up to block identity) as one step per request."""
+    rng = np.random.default_rng(21)
+    a = BlockModel(100000, 4)
+    _, reqs, _, _ = beam_requests(rng, a, 4, 3, False)
+    b = copy.deepcopy(a)
+    for step in range(8):
+        parents = [draw_parents(rng, len(x)) for x in reqs]
+        new_a = a.beam_step_many(reqs, parents, 1)
+        new_b = [b.beam_step(x, p, 1) for x, p in zip(reqs, parents)]
+        assert new_a == new_b and a.stats() == b.stats()
+        for row in new_a:
+            assert [a.lengths[h] for h in row] == [b.lengths[h] for h in row]
+            assert [a.tables[h] for h in row] == [b.tables[h] for h in row]
+        reqs = new_a
+
+
+@pytest.mark.parametrize("seed", range(5))
+@pytest.mark.parametrize("bs,num_blocks,share", [(4, 70, False), (4, 90, True), (16, 2000, True)])
+def test_manager_beam_step_many_matches_model(pb, seed, bs, num_blocks, share):
+    rng = np.random.default_rng(300 + seed)
+    prod = pb.BlockManager(num_blocks, bs, seed=seed + 7)
+    model = BlockModel(num_blocks, bs)
+    # build the same requests on both sides through the single-sequence calls
+    mrng = np.random.default_rng(400 + seed)
+    _, mreqs, _, mcommon = beam_requests(mrng, model, bs, 4, share)
+    handle_of = {}
+    prng = np.random.default_rng(400 + seed)
+    preqs = []
+    pcommon = None
+    if share:
+        pcommon = prod.add_seq()
+        prod.append(pcommon, int(prng.integers(1, 4 * bs)))
+        handle_of[pcommon] = mcommon
+    for mbeams in mreqs:
+        if pcommon is not None:
+            root = prod.fork(pcommon)
+        else:
+            root = prod.add_seq()
+        prod.append(root, int(prng.integers(1, 3 * bs)))
+        beams = [root]
+        for _ in range(int(prng.integers(2, 6)) - 1):
+            beams.append(prod.fork(root))
+        assert len(beams) == len(mbeams)
+        handle_of.update(zip(beams, mbeams))
+        preqs.append(beams)
+    assert prod.stats() == model.stats()
+    # one call per beam width (a call takes requests of equal width)
+    by_width = {}
+    for r, b in enumerate(preqs):
+        by_width.setdefault(len(b), []).append(r)
+    refused = 0
+    for step in range(40):
+        n_new = int(rng.integers(1, 4))
+        for width, rows in sorted(by_width.items()):
+            parents = [draw_parents(rng, width) for _ in rows]
+            try:
+                mnew = model.beam_step_many([[handle_of[b] for b in preqs[r]] for r in rows], parents, n_new)
+            except ModelOutOfBlocks:
+                before = prod.stats()
+                with pytest.raises(pb.OutOfBlocks):
+                    prod.beam_step_many([preqs[r] for r in rows], parents, n_new)
+                assert prod.stats() == before
+                refused += 1
+                continue
+            new, slots, pairs, shared = prod.beam_step_many([preqs[r] for r in rows], parents, n_new)
+            assert new.shape == (len(rows), width) and len(slots) == new.size * n_new
+            assert len(np.unique(slots)) == len(slots) and len(pairs) <= new.size
+            for k, r in enumerate(rows):  # ended ids may be reused by any request's forks
+                for j, b in enumerate(preqs[r]):
+                    if j not in parents[k]:
+                        handle_of.pop(b)
+            for k, r in enumerate(rows):
+                for pid, h in zip(new[k], mnew[k]):
+                    handle_of[int(pid)] = h
+                preqs[r] = [int(x) for x in new[k]]
+                assert shared[k] == model.common_prefix(mnew[k])
+            assert prod.stats() == model.stats(), step
+            check_relabelling(prod, model, handle_of)
+    if num_blocks < 100:
+        assert refused > 0  # the tight pools did run out at some step
+
+
+def test_beam_step_many_host_checks(pb):
+    m = pb.BlockManager(30, 4)
+    a = m.add_seq()
+    m.append(a, 5)
+    b, c, d = m.fork(a), m.fork(a), m.fork(a)
+    before = m.stats()
+    with pytest.raises(pb.PkvError):
+        m.beam_step_many([[a, b], [c, d]], [[0, 2], [0, 0]])  # parent out of range
+    with pytest.raises(pb.PkvError):
+        m.beam_step_many([[a, b], [c, a]], [[0, 1], [0, 1]])  # a beam in two requests
+    with pytest.raises(pb.PkvError):
+        m.beam_step_many([[a, b]], [[0, 1]], -1)
+    with pytest.raises(pb.OutOfBlocks):
+        m.beam_step_many([[a, b], [c, d]], [[0, 0], [1, 1]], 100)
+    assert m.stats() == before
+    new, slots, pairs, shared = m.beam_step_many(np.zeros((0, 2), dtype=np.int32), np.zeros((0, 2), dtype=np.int32))
+    assert new.shape == (0, 2) and slots.size == 0 and pairs.shape == (0, 2) and shared.size == 0
+    assert m.stats() == before
+    # a step that fits only because the other request's ended beams return their blocks
+    m2 = pb.BlockManager(6, 4)
+    x = m2.add_seq()
+    m2.append(x, 8)                      # 2 full blocks
+    y = m2.add_seq()
+    m2.append(y, 8)                      # 2 more; 2 free
+    x2, y2 = m2.fork(x), m2.fork(y)
+    # request 0 keeps x only (x2 ends, its blocks stay shared with x); request 1
+    # continues y twice and ends y2; 4 tokens each = 3 new blocks... needs 3 > 2 free
+    with pytest.raises(pb.OutOfBlocks):
+        m2.beam_step_many([[x, x2], [y, y2]], [[0, 1], [0, 0]], 4)
+    assert m2.stats()["free_blocks"] == 2
+    m2.free_seq(x2)
+    m2.free_seq(x)                       # 2 blocks return: 4 free
+    new, slots, pairs, shared = m2.beam_step_many([[y, y2]], [[0, 0]], 4)
+    assert new[0, 0] == y and len(set(new[0].tolist())) == 2 and shared[0] == 2
+    assert m2.stats()["free_blocks"] == 2
