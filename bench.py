@@ -403,7 +403,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         cache_ops()
         attention()
 
-    launches_per_step = int(has_copy) + int(has_new) + (2 if grouped else 1)
+    launches_per_step = int(has_copy) + int(has_new) + (3 if grouped else 1)  # grouped: prologue + two phases
 
     for _ in range(max(args.warmup, 3)):
         flush.fill_(1)
@@ -656,7 +656,7 @@ def run_beam(args, rank: int, world: int, local_rank: int) -> int:
             ev[i][0].record(stream)
             device_step(dp, ev[i][1])
             ev[i][2].record(stream)
-            launches += (1 if dp.copy_pairs.numel() else 0) + 1 + 2
+            launches += (1 if dp.copy_pairs.numel() else 0) + 1 + 3  # grouped: prologue + two phases
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()

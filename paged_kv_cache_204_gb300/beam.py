@@ -119,24 +119,34 @@ class BeamDecoder:
         return buf
 
     def upload(self, plan: StepPlan, stream=None) -> DevicePlan:
-        """Copy a plan to the device through reused pinned staging buffers."""
+        """Copy a plan to the device in one transfer: every array is packed
+        (16-byte aligned) into one reused pinned staging buffer, copied into
+        one reused device buffer, and returned as views of it. The views stay
+        valid until the next upload, which the stream orders after the work
+        already queued on them."""
         stream = torch.cuda.current_stream(self.k_cache.device) if stream is None else stream
         if self._staged is not None:
-            self._staged.synchronize()
+            self._staged.synchronize()  # the previous transfer has left the staging buffer
+        arrays, offsets, total = [], [], 0
+        for name in _FIELDS:
+            a = np.ascontiguousarray(getattr(plan, name))
+            arrays.append(a)
+            offsets.append(total)
+            total += (a.nbytes + 15) & ~15
+        host = self._buffer(self._pinned, "plan", total, pinned=True)
+        dev = self._buffer(self._dev, "plan", total, pinned=False)
+        hv = host.numpy()
+        for a, o in zip(arrays, offsets):
+            hv[o:o + a.nbytes] = a.view(np.uint8).reshape(-1)
         out = {}
         with torch.cuda.stream(stream):
-            for name in _FIELDS:
-                a = np.ascontiguousarray(getattr(plan, name))
-                nb = a.nbytes
-                host = self._buffer(self._pinned, name, nb, pinned=True)
-                dev = self._buffer(self._dev, name, nb, pinned=False)
-                if nb:
-                    host[:nb].numpy()[:] = a.view(np.uint8).reshape(-1)
-                    dev[:nb].copy_(host[:nb], non_blocking=True)
-                t = dev[:nb].view(torch.from_numpy(a[:0].reshape(-1)).dtype)
-                out[name] = t.view(a.shape)
+            if total:
+                dev[:total].copy_(host[:total], non_blocking=True)
             self._staged = torch.cuda.Event()
             self._staged.record(stream)
+        for name, a, o in zip(_FIELDS, arrays, offsets):
+            t = dev[o:o + a.nbytes].view(torch.from_numpy(a[:0].reshape(-1)).dtype)
+            out[name] = t.view(a.shape)
         return DevicePlan(max_context_len=plan.max_context_len, **out)
 
     def workspace(self, num_heads: int, head_dim: int) -> torch.Tensor:

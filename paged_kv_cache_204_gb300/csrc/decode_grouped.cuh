@@ -355,28 +355,33 @@ __device__ __forceinline__ void mma_prefix_tile(const unsigned char* ks, const u
   constexpr int ROW = D * (int)sizeof(T);
   const int lane = threadIdx.x & 31;
   const int mg = lane >> 2, mt = lane & 3;
-  float s[2][4];
+  // two independent accumulator chains per 8-token half (first and second
+  // k-step of each chunk), added at the end: half the dependent MMA latency
+  float s[2][2][2];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+    for (int h = 0; h < 2; ++h) s[nt][h][0] = s[nt][h][1] = 0.f;
 #pragma unroll
   for (int c = 0; c < D / 32; ++c)
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const uint4 kk = *reinterpret_cast<const uint4*>(ks + (mg + 8 * nt) * ROW + c * 64 + mt * 16);
-      Mma16816<T>::run(s[nt], qa[c][0][0], qa[c][0][1], kk.x, kk.y);
-      Mma16816<T>::run(s[nt], qa[c][1][0], qa[c][1][1], kk.z, kk.w);
+      Mma16816<T>::run2(s[nt][0][0], s[nt][0][1], qa[c][0][0], qa[c][0][1], kk.x, kk.y);
+      Mma16816<T>::run2(s[nt][1][0], s[nt][1][1], qa[c][1][0], qa[c][1][1], kk.z, kk.w);
     }
   float xs[4], tmax = -INFINITY;
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int tok = nt * 8 + 2 * mt + e;
-      xs[nt * 2 + e] = tok < nvalid ? s[nt][e] * scale_log2 : -INFINITY;
-      tmax = fmaxf(tmax, xs[nt * 2 + e]);
-    }
+    for (int e = 0; e < 2; ++e) xs[nt * 2 + e] = (s[nt][0][e] + s[nt][1][e]) * scale_log2;
+  if (nvalid < kTileTokens) {  // warp-uniform: only a segment's last tile can be partial
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if ((i >> 1) * 8 + 2 * mt + (i & 1) >= nvalid) xs[i] = -INFINITY;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) tmax = fmaxf(tmax, xs[i]);
   tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 1));
   tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 2));
   const float mn = fmaxf(pm, tmax);
@@ -408,8 +413,10 @@ __device__ __forceinline__ void mma_prefix_tile(const unsigned char* ks, const u
   for (int c = 0; c < D / 32; ++c) {
     uint4 v0 = *reinterpret_cast<const uint4*>(vs + mg * ROW + c * 64 + mt * 16);        // token mg
     uint4 v1 = *reinterpret_cast<const uint4*>(vs + (mg + 8) * ROW + c * 64 + mt * 16);  // token mg + 8
-    if (mg >= nvalid) v0 = make_uint4(0u, 0u, 0u, 0u);  // rows past the context may hold poison
-    if (mg + 8 >= nvalid) v1 = make_uint4(0u, 0u, 0u, 0u);
+    if (nvalid < kTileTokens) {  // rows past the context may hold poison
+      if (mg >= nvalid) v0 = make_uint4(0u, 0u, 0u, 0u);
+      if (mg + 8 >= nvalid) v1 = make_uint4(0u, 0u, 0u, 0u);
+    }
     const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
     const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
