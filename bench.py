@@ -919,7 +919,7 @@ def run_prefill(args, rank: int, world: int, local_rank: int) -> int:
                    "l2": "flushed between timed steps (256 MiB write)", "seed": cfg.seed},
         "tokens_per_s": world * n / (agg["step_ms"] * 1e-3),
         "attention_ms": agg["attn_ms"], "cache_write_ms": agg["write_ms"], "flops_per_step": flops,
-        "roofline": {"bound": "tensor", "kernel": "pa_prefill_kernel (mma.sync m16n8k16)", "achieved": achieved,
+        "roofline": {"bound": "tensor", "kernel": "pa_prefill_kernel (tcgen05.mma, TMEM accumulators, TMA-fed K/V)", "achieved": achieved,
                      "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
                      "peak_source": peak_src},
         "cpu_baseline": cpu,

@@ -11,24 +11,29 @@
 // 0 .. L - n + i. Sequences sharing a system prompt share its blocks, so the
 // prompt's K/V is written once.
 //
-// Work: one CTA of 8 warps per (128-query tile, sequence, query head); a warp
-// owns 16 query rows. K/V tiles of 64 tokens are gathered through the block
-// table with 16-byte cp.async copies into a double-buffered, XOR-swizzled
-// shared-memory layout (rows past the context are zero-filled without a
-// read) and fed to the tensor cores with ldmatrix:
-//   S = Q K^T   mma.sync m16n8k16, fp32 accumulation;
-//   online softmax in base 2 on the accumulators (causal mask by select);
-//   O += P V    P from the S accumulators as a high + low 16-bit pair (two
-//               MMAs) so that the probabilities keep fp32-level accuracy.
+// Work: one CTA per (128-query tile, sequence, query head) on the
+// fifth-generation tensor cores. K/V tiles of 64 tokens arrive by TMA, one box
+// per cache block found in the block table, in the 128-byte-swizzled layout
+// the MMAs read; S = Q K^T and O += P V accumulate in fp32 in tensor memory;
+// each query row's online softmax (base 2, causal mask by select) runs in
+// the thread that owns that row's tensor-memory lane. P is fed as a high and
+// a low 16-bit part (two MMAs) so that the probabilities keep ~16
+// significant bits.
 #pragma once
 
-#include "common.cuh"
+#include <type_traits>
+
+#include "tc.cuh"
 
 namespace pkv {
 
-constexpr int kPfRows = 128;   // query rows per CTA (8 warps x 16)
-constexpr int kPfTokens = 64;  // K/V tokens per tile
-constexpr int kPfWarps = 8;
+constexpr int kPfRows = 128;            // query rows per CTA = tensor-memory lanes
+constexpr int kPfTokens = 64;           // K/V tokens per tile
+constexpr int kPfThreads = 192;         // 4 softmax warps, 1 MMA warp, 1 TMA warp
+constexpr int kPfStages = 2;            // K and V tiles in flight
+constexpr uint32_t kPfTmemCols = 256;   // two S/P buffers (64 columns each) + O (up to 128)
+constexpr float kPfRescaleLog2 = 8.f;   // base of the running max moves only when it grows by more
+constexpr uint64_t kPfWaitNs = 2000000000ull;  // limit of every wait of the kernel
 
 struct PrefillParams {
   void* out;
@@ -43,17 +48,11 @@ struct PrefillParams {
   int32_t* dev_err;
 };
 
+// 16-bit packing of two fp32 values (round to nearest) and its exact inverse.
 template <typename T>
-struct PfMma;
+struct Pack16;
 template <>
-struct PfMma<__half> {
-  __device__ __forceinline__ static void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
+struct Pack16<__half> {
   __device__ __forceinline__ static uint32_t pack(float x, float y) {
     const __half2 h = __floats2half2_rn(x, y);
     uint32_t u;
@@ -67,14 +66,7 @@ struct PfMma<__half> {
   }
 };
 template <>
-struct PfMma<__nv_bfloat16> {
-  __device__ __forceinline__ static void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
+struct Pack16<__nv_bfloat16> {
   __device__ __forceinline__ static uint32_t pack(float x, float y) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
     uint32_t u;
@@ -86,57 +78,81 @@ struct PfMma<__nv_bfloat16> {
   }
 };
 
-__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* p) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(smem_u32(p)));
-}
 // 16-byte asynchronous copy; src_bytes 0 writes zeros and reads nothing.
 __device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, int src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem), "r"(src_bytes)
                : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// Byte offset of 16-byte chunk c of row r in a [rows][D] tile: chunks are
-// XOR-swizzled by the row's low 3 bits so that 8 consecutive rows at the same
-// chunk fall on different banks (ldmatrix reads them conflict-free).
+// Byte offset of 16-byte chunk c (0..7) of 128-byte row r in a tile with the
+// 128-byte swizzle.
+__device__ __forceinline__ int sw128_off(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
+// Shared memory of one CTA (offsets from a 1024-byte aligned base):
+//   Q      [2 or 1 column blocks][128 rows][128 B]          (K-major A operand)
+//   K, V   [2 stages][D/64 column blocks][64 tokens][128 B]  (K: K-major B of S;
+//                                                            V: MN-major B of O)
+//   mbarriers, tensor-memory address slot.
+// Tensor memory (256 columns, lanes = query rows): S/P buffers at columns 0
+// and 64 (S as fp32; P overwrites it as 16-bit hi / lo pairs in columns
+// +0..31 / +32..63), O (fp32, D columns) at column 128.
 template <int D>
-__device__ __forceinline__ int pf_off(int r, int c) {
-  return r * (D * 2) + ((c ^ (r & 7)) << 4);
-}
-
-template <typename T, int D>
 struct PrefillShape {
+  static constexpr int kBlocksD = D / 64;                 // 64-element column blocks of a row
+  static constexpr int kColBlock = kPfTokens * 128;       // bytes of one column block of a K/V tile
   static constexpr int kTileBytes = kPfTokens * D * 2;
-  static constexpr int kQBytes = kPfRows * D * 2;
-  static constexpr int kSmemBytes = kQBytes + 4 * kTileBytes;  // Q, then K and V for two stages
-  static_assert(D % 64 == 0, "head_dim 64 or 128");
+  static constexpr int kQColBlock = kPfRows * 128;
+  static constexpr int kQOff = 0;
+  static constexpr int kKOff = kPfRows * D * 2;
+  static constexpr int kVOff = kKOff + kPfStages * kTileBytes;
+  static constexpr int kBarOff = kVOff + kPfStages * kTileBytes;
+  static constexpr int kSlotOff = kBarOff + 13 * 8;
+  static constexpr int kUsed = kSlotOff + 16 + 1024;      // + alignment slack
+  // at least 80 KB, so that at most two CTAs share an SM and their tensor
+  // memory (2 x 256 columns) always fits
+  static constexpr int kSmemBytes = kUsed > 80 * 1024 ? kUsed : 80 * 1024;
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
 };
 
+// One CTA per (128-query tile, sequence, query head); 6 warps:
+//   warps 0-3  softmax: thread r owns query row r (tensor-memory lane r);
+//   warp 4     one thread issues the MMAs;
+//   warp 5     one thread issues the TMA loads of K and V tiles.
+// Per 64-token tile j (stage and S/P buffer j & 1):
+//   load:    K_j, V_j box by box (one box = one cache block of one kv head,
+//            64 head dims), through the block table;
+//   MMA:     S_j = Q K_j^T into buffer j & 1 (issued one tile ahead), then,
+//            once P_j is written, O += P_hi V_j and O += P_lo V_j;
+//   softmax: scale, causal mask, running max, P = 2^(s - m) as a high and a
+//            low 16-bit part (the two MMAs together keep P to ~16 bits); the
+//            running max is re-based (and O rescaled in tensor memory) only
+//            when it grows by more than kPfRescaleLog2, which leaves every
+//            P <= 2^kPfRescaleLog2 and the result exact (O and the row sum
+//            use the same base).
 template <typename T, int D>
-__global__ void __launch_bounds__(kPfWarps * 32, 2) pa_prefill_kernel(const PrefillParams p) {
-  using S = PrefillShape<T, D>;
-  using M = PfMma<T>;
-  constexpr int CH = D / 8;   // 16-byte chunks per row
-  constexpr int KS = D / 16;  // k-steps of q.k
-  constexpr int NT = D / 8;   // n-tiles of the output
-  extern __shared__ __align__(128) unsigned char smem[];
-  unsigned char* qs = smem;
-  unsigned char* kv = smem + S::kQBytes;  // stage s: K at kv + 2s*tile, V at kv + (2s+1)*tile
+__global__ void __launch_bounds__(kPfThreads, 2)
+    pa_prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                      const PrefillParams p) {
+  using S = PrefillShape<D>;
+  using P16 = Pack16<T>;
+  constexpr int kBf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBarOff);
+  uint64_t* full_k = bars;       // [2] K tile landed
+  uint64_t* full_v = bars + 2;   // [2] V tile landed
+  uint64_t* empty_k = bars + 4;  // [2] S MMA done with the K stage
+  uint64_t* empty_v = bars + 6;  // [2] O MMAs done with the V stage
+  uint64_t* s_full = bars + 8;   // [2] S of the buffer computed
+  uint64_t* p_full = bars + 10;  // [2] P of the buffer written (128 arrivals)
+  uint64_t* o_done = bars + 12;  // one phase per tile's O MMAs
+  uint32_t* slot = reinterpret_cast<uint32_t*>(sm + S::kSlotOff);
 
-  const int tile = blockIdx.x, s = blockIdx.y, h = blockIdx.z;
+  const int tile = gridDim.x - 1 - blockIdx.x;  // longest causal ranges first
+  const int s = blockIdx.y, h = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int g = lane >> 2, t4 = lane & 3;
   const int L = __ldg(p.context_lens + s);
   const int q0 = __ldg(p.query_start + s), n = __ldg(p.query_start + s + 1) - q0;
   if (L < 0 || L > p.max_blocks_per_seq * p.block_size || n < 0 || n > L) {
@@ -144,184 +160,299 @@ __global__ void __launch_bounds__(kPfWarps * 32, 2) pa_prefill_kernel(const Pref
     return;
   }
   const int row0 = tile * kPfRows;
-  if (row0 >= n) return;  // this tile has no queries
+  if (row0 >= n) return;  // this tile has no queries (before any allocation)
   const int rows = min(kPfRows, n - row0);
-  const int first_pos = L - n + row0;         // position of the tile's first query
-  const int kv_end = first_pos + rows;        // tokens the tile's queries can see
+  const int first_pos = L - n + row0;   // position of the tile's first query
+  const int kv_end = first_pos + rows;  // tokens the tile's queries can see
   const int ntiles = (kv_end + kPfTokens - 1) / kPfTokens;
   const int kvh = h / p.group;
-  const T* qg = static_cast<const T*>(p.q);
-  const T* kg = static_cast<const T*>(p.k_cache);
-  const T* vg = static_cast<const T*>(p.v_cache);
-  const int32_t* bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
   const int bs = p.block_size;
 
-  // ---- async loads -----------------------------------------------------------
-  for (int i = tid; i < kPfRows * CH; i += kPfWarps * 32) {
-    const int r = i / CH, c = i % CH;
-    const bool ok = r < rows;
-    const T* src = qg + ((size_t)(q0 + row0 + (ok ? r : 0)) * p.num_heads + h) * D + c * 8;
-    cp_async16_zfill(qs + pf_off<D>(r, c), src, ok ? 16 : 0);
+  // ---- set-up: Q rows, barriers, tensor memory --------------------------------
+  if (tid < kPfRows) {
+    const bool ok = tid < rows;
+    const T* src = static_cast<const T*>(p.q) + ((size_t)(q0 + row0 + (ok ? tid : 0)) * p.num_heads + h) * D;
+#pragma unroll
+    for (int c16 = 0; c16 < D / 8; ++c16)
+      cp_async16_zfill(sm + S::kQOff + (c16 >> 3) * S::kQColBlock + sw128_off(tid, c16 & 7), src + c16 * 8,
+                       ok ? 16 : 0);
+    cp_async_commit();
   }
-  auto load_kv = [&](int j, int stage) {
-    unsigned char* kd = kv + (2 * stage) * S::kTileBytes;
-    unsigned char* vd = kd + S::kTileBytes;
-    for (int i = tid; i < kPfTokens * CH; i += kPfWarps * 32) {
-      const int r = i / CH, c = i % CH;
-      const int t = j * kPfTokens + r;
-      int id = 0;
-      bool ok = t < kv_end;
-      if (ok) {
-        id = __ldg(bt + t / bs);
-        if (id < 0 || id >= p.num_blocks) {
-          set_err(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
+  if (tid == 0) {
+    for (int i = 0; i < 13; ++i) mbar_init(&bars[i], (i == 10 || i == 11) ? kPfRows : 1);
+    mbar_init_fence();
+  }
+  if (warp == 0) tmem_alloc(slot, kPfTmemCols);
+  if (tid < kPfRows) {
+    cp_async_wait_all();
+    fence_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *slot;
+
+  if (warp == 5) {
+    // ---- TMA producer ---------------------------------------------------------
+    if (lane == 0) {
+      const int32_t* bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+      const int per_tile = kPfTokens / bs;                        // cache blocks per tile
+      const int oob_row = p.num_blocks * p.num_kv_heads * bs;     // first row past the pool: reads zeros
+      const uint32_t box_bytes = (uint32_t)bs * 128u;
+      for (int j = 0; j < ntiles; ++j) {
+        const int st = j & 1;
+        const uint32_t prev = ((j >> 1) + 1) & 1;  // phase of the stage's previous use
+        const int t0 = j * kPfTokens;
+        const int nblk = min(per_tile, (kv_end - t0 + bs - 1) / bs);
+        int ys[kPfTokens / 8];
+        for (int b = 0; b < nblk; ++b) {
+          const int id = __ldg(bt + t0 / bs + b);
+          if (id < 0 || id >= p.num_blocks) {
+            set_err(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
+            ys[b] = oob_row;
+          } else {
+            ys[b] = (id * p.num_kv_heads + kvh) * bs;
+          }
+        }
+        const uint32_t bytes = (uint32_t)nblk * S::kBlocksD * box_bytes;
+        if (j >= 2 && !mbar_wait_bounded(&empty_k[st], prev, kPfWaitNs)) {
+          set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&full_k[st], bytes);
+        unsigned char* kd = sm + S::kKOff + st * S::kTileBytes;
+        for (int b = 0; b < nblk; ++b)
+#pragma unroll
+          for (int cb = 0; cb < S::kBlocksD; ++cb)
+            tma_load_2d(kd + cb * S::kColBlock + b * bs * 128, &kmap, cb * 64, ys[b], &full_k[st]);
+        if (j >= 2 && !mbar_wait_bounded(&empty_v[st], prev, kPfWaitNs)) {
+          set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&full_v[st], bytes);
+        unsigned char* vd = sm + S::kVOff + st * S::kTileBytes;
+        for (int b = 0; b < nblk; ++b)
+#pragma unroll
+          for (int cb = 0; cb < S::kBlocksD; ++cb)
+            tma_load_2d(vd + cb * S::kColBlock + b * bs * 128, &vmap, cb * 64, ys[b], &full_v[st]);
+      }
+    }
+  } else if (warp == 4) {
+    // ---- MMA issue ------------------------------------------------------------
+    if (lane == 0) {
+      constexpr uint32_t id_s = mma_idesc_f16(kPfRows, kPfTokens, kBf16, 0);
+      constexpr uint32_t id_o = mma_idesc_f16(kPfRows, D, kBf16, 1);
+      const uint32_t q_addr = smem_u32(sm + S::kQOff);
+      const uint32_t k_addr = smem_u32(sm + S::kKOff);
+      const uint32_t v_addr = smem_u32(sm + S::kVOff);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait_bounded(&full_k[st], (j >> 1) & 1, kPfWaitNs)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const int cb = ks >> 2, kk = ks & 3;
+          const uint64_t a = smem_desc_sw128(q_addr + cb * S::kQColBlock + kk * 32, 16, 1024);
+          const uint64_t b = smem_desc_sw128(k_addr + st * S::kTileBytes + cb * S::kColBlock + kk * 32, 16, 1024);
+          mma_ss(tbase + 64 * st, a, b, id_s, ks > 0);
+        }
+        mma_commit(&s_full[st]);
+        if (j + 2 < ntiles) mma_commit(&empty_k[st]);  // only commits that someone waits for
+        return true;
+      };
+      bool ok = issue_s(0);
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int b = j & 1;
+        if (j + 1 < ntiles && !issue_s(j + 1)) {
           ok = false;
-          id = 0;
+          break;
+        }
+        if (!mbar_wait_bounded(&p_full[b], (j >> 1) & 1, kPfWaitNs) ||
+            !mbar_wait_bounded(&full_v[b], (j >> 1) & 1, kPfWaitNs)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t pa = tbase + 64 * b;
+#pragma unroll
+        for (int part = 0; part < 2; ++part)  // high then low halves of P
+#pragma unroll
+          for (int ks = 0; ks < kPfTokens / 16; ++ks) {
+            const uint64_t vb = smem_desc_sw128(v_addr + b * S::kTileBytes + ks * 2048, S::kColBlock, 1024);
+            mma_ts(tbase + 128, pa + 32 * part + 8 * ks, vb, id_o, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
+          }
+        mma_commit(o_done);
+        if (j + 2 < ntiles) mma_commit(&empty_v[b]);
+      }
+      if (!ok) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+    }
+  } else {
+    // ---- softmax and output (thread = query row) ------------------------------
+    const int r = tid;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int pos = min(first_pos + r, kv_end - 1);  // rows past the last query: any finite result
+    float m_use = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int b = j & 1;
+      const uint32_t par = (j >> 1) & 1;
+      const int t0 = j * kPfTokens;
+      ok = __all_sync(kFullMask, mbar_wait_bounded(&s_full[b], par, kPfWaitNs));
+      if (!ok) break;
+      tc_fence_after();
+      float x[kPfTokens];
+      {
+        uint32_t u[32];
+        tmem_ld32(tbase + lane_base + 64 * b, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(u[i]) * p.scale_log2;
+        tmem_ld32(tbase + lane_base + 64 * b + 32, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) x[32 + i] = __uint_as_float(u[i]) * p.scale_log2;
+      }
+      const int vis = pos - t0 + 1;  // visible tokens of this tile for this row
+      if (vis < kPfTokens) {
+#pragma unroll
+        for (int i = 0; i < kPfTokens; ++i)
+          if (i >= vis) x[i] = -INFINITY;
+      }
+      float mt = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < kPfTokens; ++i) mt = fmaxf(mt, x[i]);
+      const bool grow = mt > m_use + kPfRescaleLog2;  // first visible tile: always (m_use = -inf)
+      float alpha = 1.f;
+      if (grow) {
+        alpha = exp2f(m_use - mt);  // 0 while nothing was visible
+        m_use = mt;
+      }
+      const float base = m_use == -INFINITY ? 0.f : m_use;
+      float ps = 0.f;
+      uint32_t hi[32], lo[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = exp2f(x[2 * i] - base), p1 = exp2f(x[2 * i + 1] - base);
+        ps += p0 + p1;
+        hi[i] = P16::pack(p0, p1);
+        const float2 hv = P16::unpack(hi[i]);
+        lo[i] = P16::pack(p0 - hv.x, p1 - hv.y);
+      }
+      l = l * alpha + ps;
+      if (j > 0 && __any_sync(kFullMask, grow)) {
+        // O holds the previous tiles' sums on the old base: rescale it once
+        // their MMAs are done (S_j completing implies those of tile j-2)
+        ok = __all_sync(kFullMask, mbar_wait_bounded(o_done, (j - 1) & 1, kPfWaitNs));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t w[32];
+          tmem_ld32(tbase + lane_base + 128 + 32 * c, w);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+          tmem_st32(tbase + lane_base + 128 + 32 * c, w);
         }
       }
-      const size_t off = (((size_t)id * p.num_kv_heads + kvh) * bs + (ok ? t % bs : 0)) * D + c * 8;
-      cp_async16_zfill(kd + pf_off<D>(r, c), kg + off, ok ? 16 : 0);
-      cp_async16_zfill(vd + pf_off<D>(r, c), vg + off, ok ? 16 : 0);
+      tmem_st32(tbase + lane_base + 64 * b, hi);
+      tmem_st32(tbase + lane_base + 64 * b + 32, lo);
+      tmem_wait_st();
+      if (j == ntiles - 1 && kv_end < t0 + kPfTokens) {
+        // V rows past the context may hold anything (a NaN would survive a
+        // zero probability): zero them once the tile has landed
+        ok = __all_sync(kFullMask, mbar_wait_bounded(&full_v[b], par, kPfWaitNs));
+        if (!ok) break;
+        const int z0 = kv_end - t0, per_row = S::kBlocksD * 8;
+        unsigned char* vd = sm + S::kVOff + b * S::kTileBytes;
+        for (int i = tid; i < (kPfTokens - z0) * per_row; i += kPfRows) {
+          const int row = z0 + i / per_row, rem = i % per_row;
+          *reinterpret_cast<uint4*>(vd + (rem >> 3) * S::kColBlock + row * 128 + (rem & 7) * 16) =
+              make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_async_smem();
+      }
+      tc_fence_before();
+      mbar_arrive(&p_full[b]);
     }
-  };
-  load_kv(0, 0);
-  cp_async_commit();
-
-  // ---- per-warp state: rows w*16 + g and w*16 + g + 8 --------------------------
-  const int wr = warp * 16;
-  const int pos_a = first_pos + wr + g, pos_b = pos_a + 8;  // query positions of this thread's rows
-  float o[NT][4];
-#pragma unroll
-  for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-
-  for (int j = 0; j < ntiles; ++j) {
-    if (j + 1 < ntiles) {
-      load_kv(j + 1, (j + 1) & 1);
-      cp_async_commit();
-      cp_async_wait<1>();
+    if (ok) {
+      // every tile's O MMAs done: wait the phases in order (a parity wait
+      // tells apart only adjacent phases)
+      if (ntiles >= 2) ok = __all_sync(kFullMask, mbar_wait_bounded(o_done, (ntiles - 2) & 1, kPfWaitNs));
+      if (ok) ok = __all_sync(kFullMask, mbar_wait_bounded(o_done, (ntiles - 1) & 1, kPfWaitNs));
+    }
+    if (!ok) {
+      if (lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
     } else {
-      cp_async_wait<0>();
-    }
-    __syncthreads();
-
-    const unsigned char* ks = kv + (2 * (j & 1)) * S::kTileBytes;
-    const unsigned char* vs = ks + S::kTileBytes;
-    const int t0 = j * kPfTokens;
-
-    // S = Q K^T over the tile's 64 tokens: 8 n-tiles of 8 tokens
-    float sc[8][4];
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      T* og = static_cast<T*>(p.out) + ((size_t)(q0 + row0 + r) * p.num_heads + h) * D;
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t w[32];
+        tmem_ld32(tbase + lane_base + 128 + 32 * c, w);
+        tmem_wait_ld();
+        if (r < rows) {
+          uint32_t pk[16];
 #pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-      uint32_t qa[4];  // this k-step's query fragment, reloaded per tile (keeps registers for occupancy)
-      {
-        const int r = wr + (lane & 15), c = 2 * kk + (lane >> 4);
-        ldsm_x4(qa, qs + pf_off<D>(r, c));
-      }
+          for (int i = 0; i < 16; ++i)
+            pk[i] = P16::pack(__uint_as_float(w[2 * i]) * inv, __uint_as_float(w[2 * i + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(og + 32 * c);
 #pragma unroll
-      for (int np = 0; np < 4; ++np) {  // pairs of n-tiles
-        uint32_t b[4];
-        const int r = np * 16 + (lane & 7) + ((lane >> 4) << 3), c = 2 * kk + ((lane >> 3) & 1);
-        ldsm_x4(b, ks + pf_off<D>(r, c));
-        M::run(sc[2 * np], qa, b[0], b[1]);
-        M::run(sc[2 * np + 1], qa, b[2], b[3]);
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
       }
     }
-    // scale, causal mask, running max
-    float mx_a = -INFINITY, mx_b = -INFINITY;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int t = t0 + nt * 8 + 2 * t4 + e;
-        sc[nt][e] = t <= pos_a ? sc[nt][e] * p.scale_log2 : -INFINITY;
-        sc[nt][2 + e] = t <= pos_b ? sc[nt][2 + e] * p.scale_log2 : -INFINITY;
-        mx_a = fmaxf(mx_a, sc[nt][e]);
-        mx_b = fmaxf(mx_b, sc[nt][2 + e]);
-      }
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(kFullMask, mx_a, 1));
-    mx_a = fmaxf(mx_a, __shfl_xor_sync(kFullMask, mx_a, 2));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(kFullMask, mx_b, 1));
-    mx_b = fmaxf(mx_b, __shfl_xor_sync(kFullMask, mx_b, 2));
-    const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
-    // a row with nothing visible yet keeps m = -inf: subtract 0 instead
-    const float base_a = mn_a == -INFINITY ? 0.f : mn_a, base_b = mn_b == -INFINITY ? 0.f : mn_b;
-    const float al_a = exp2f(m_a - base_a), al_b = exp2f(m_b - base_b);
-    m_a = mn_a;
-    m_b = mn_b;
-    float ps_a = 0.f, ps_b = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      sc[nt][0] = exp2f(sc[nt][0] - base_a);
-      sc[nt][1] = exp2f(sc[nt][1] - base_a);
-      sc[nt][2] = exp2f(sc[nt][2] - base_b);
-      sc[nt][3] = exp2f(sc[nt][3] - base_b);
-      ps_a += sc[nt][0] + sc[nt][1];
-      ps_b += sc[nt][2] + sc[nt][3];
-    }
-    l_a = l_a * al_a + ps_a;  // per-thread partial sums; the quad is summed at the end
-    l_b = l_b * al_b + ps_b;
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      o[nt][0] *= al_a;
-      o[nt][1] *= al_a;
-      o[nt][2] *= al_b;
-      o[nt][3] *= al_b;
-    }
-    // O += P V: k-steps of 16 tokens (n-tiles 2k, 2k+1 of S), P as hi + lo
-#pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2) {
-      uint32_t ph[4], pl[4];
-      const float* p0 = sc[2 * k2];
-      const float* p1 = sc[2 * k2 + 1];
-      const float src[4][2] = {{p0[0], p0[1]}, {p0[2], p0[3]}, {p1[0], p1[1]}, {p1[2], p1[3]}};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        ph[i] = M::pack(src[i][0], src[i][1]);
-        const float2 hv = M::unpack(ph[i]);
-        pl[i] = M::pack(src[i][0] - hv.x, src[i][1] - hv.y);
-      }
-#pragma unroll
-      for (int cp = 0; cp < NT / 2; ++cp) {  // pairs of output n-tiles (chunks 2cp, 2cp+1)
-        uint32_t b[4];
-        const int r = k2 * 16 + (lane & 7) + (((lane >> 3) & 1) << 3), c = 2 * cp + (lane >> 4);
-        ldsm_x4_trans(b, vs + pf_off<D>(r, c));
-        M::run(o[2 * cp], ph, b[0], b[1]);  // high halves first: dependent MMAs two apart
-        M::run(o[2 * cp + 1], ph, b[2], b[3]);
-        M::run(o[2 * cp], pl, b[0], b[1]);
-        M::run(o[2 * cp + 1], pl, b[2], b[3]);
-      }
-    }
-    __syncthreads();  // every warp is done with this stage before it is refilled
   }
 
-  // ---- normalise and store ---------------------------------------------------------
-  l_a += __shfl_xor_sync(kFullMask, l_a, 1);
-  l_a += __shfl_xor_sync(kFullMask, l_a, 2);
-  l_b += __shfl_xor_sync(kFullMask, l_b, 1);
-  l_b += __shfl_xor_sync(kFullMask, l_b, 2);
-  const float inv_a = l_a > 0.f ? 1.f / l_a : 0.f, inv_b = l_b > 0.f ? 1.f / l_b : 0.f;
-  const int ra = wr + g, rb = ra + 8;
-  T* og = static_cast<T*>(p.out);
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int d = nt * 8 + 2 * t4;
-    if (ra < rows) {
-      const uint32_t u = M::pack(o[nt][0] * inv_a, o[nt][1] * inv_a);
-      *reinterpret_cast<uint32_t*>(og + ((size_t)(q0 + row0 + ra) * p.num_heads + h) * D + d) = u;
-    }
-    if (rb < rows) {
-      const uint32_t u = M::pack(o[nt][2] * inv_b, o[nt][3] * inv_b);
-      *reinterpret_cast<uint32_t*>(og + ((size_t)(q0 + row0 + rb) * p.num_heads + h) * D + d) = u;
-    }
+  // ---- tear-down: every MMA has completed (or waits ran out) ------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kPfTmemCols);
   }
+}
+
+// cuTensorMapEncodeTiled, reached through the runtime (no driver library link).
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }
+  return fn;
+}
+
+// Rows of a cache pool [num_blocks][num_kv_heads][block_size][D] as a 2-D
+// tensor of 16-bit elements, read in boxes of {64 elements, block_size rows}
+// with the 128-byte swizzle.
+template <typename T, int D>
+cudaError_t encode_pool_map(CUtensorMap* map, const void* base, const PrefillParams& p) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.num_blocks * p.num_kv_heads * p.block_size};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * sizeof(T)};
+  const cuuint32_t box[2] = {64u, (cuuint32_t)p.block_size};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r =
+      enc(map, std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+          2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <typename T, int D>
 cudaError_t launch_pa_prefill(const PrefillParams& p, int max_query_len, cudaStream_t stream) {
-  using S = PrefillShape<T, D>;
+  using S = PrefillShape<D>;
+  // the TMA row coordinate (and one box past the pool) must fit in int32
+  if ((long long)p.num_blocks * p.num_kv_heads * p.block_size + kPfTokens > 0x7fffffffLL)
+    return cudaErrorNotSupported;
+  if (kPfTokens % p.block_size != 0) return cudaErrorNotSupported;
   static int configured[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -331,8 +462,13 @@ cudaError_t launch_pa_prefill(const PrefillParams& p, int max_query_len, cudaStr
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) __atomic_store_n(&configured[dev], 1, __ATOMIC_RELEASE);
   }
+  CUtensorMap kmap, vmap;
+  e = encode_pool_map<T, D>(&kmap, p.k_cache, p);
+  if (e != cudaSuccess) return e;
+  e = encode_pool_map<T, D>(&vmap, p.v_cache, p);
+  if (e != cudaSuccess) return e;
   const dim3 grid((max_query_len + kPfRows - 1) / kPfRows, p.num_seqs, p.num_heads);
-  pa_prefill_kernel<T, D><<<grid, kPfWarps * 32, S::kSmemBytes, stream>>>(p);
+  pa_prefill_kernel<T, D><<<grid, kPfThreads, S::kSmemBytes, stream>>>(kmap, vmap, p);
   return cudaGetLastError();
 }
 
