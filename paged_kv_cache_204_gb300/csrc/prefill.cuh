@@ -86,6 +86,15 @@ __device__ __forceinline__ void cp_async16_zfill(void* smem, const void* gmem, i
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx.ftz:
+// relative error about 2^-22, -inf -> +0); the probabilities it produces are
+// rounded to ~16 bits afterwards.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Byte offset of 16-byte chunk c (0..7) of 128-byte row r in a tile with the
 // 128-byte swizzle.
 __device__ __forceinline__ int sw128_off(int r, int c) { return r * 128 + ((c ^ (r & 7)) << 4); }
@@ -193,48 +202,47 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   const uint32_t tbase = *slot;
 
   if (warp == 5) {
-    // ---- TMA producer ---------------------------------------------------------
+    // ---- TMA producer: K and V tiles each issued as soon as their stage is free
     if (lane == 0) {
       const int32_t* bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-      const int per_tile = kPfTokens / bs;                        // cache blocks per tile
-      const int oob_row = p.num_blocks * p.num_kv_heads * bs;     // first row past the pool: reads zeros
+      const int per_tile = kPfTokens / bs;                     // cache blocks per tile
+      const int oob_row = p.num_blocks * p.num_kv_heads * bs;  // first row past the pool: reads zeros
       const uint32_t box_bytes = (uint32_t)bs * 128u;
-      for (int j = 0; j < ntiles; ++j) {
-        const int st = j & 1;
-        const uint32_t prev = ((j >> 1) + 1) & 1;  // phase of the stage's previous use
+      auto issue = [&](int j, const CUtensorMap* map, unsigned char* stage_base, uint64_t* full) {
         const int t0 = j * kPfTokens;
         const int nblk = min(per_tile, (kv_end - t0 + bs - 1) / bs);
-        int ys[kPfTokens / 8];
+        mbar_arrive_expect_tx(full, (uint32_t)nblk * S::kBlocksD * box_bytes);
         for (int b = 0; b < nblk; ++b) {
           const int id = __ldg(bt + t0 / bs + b);
+          int y = (id * p.num_kv_heads + kvh) * bs;
           if (id < 0 || id >= p.num_blocks) {
             set_err(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
-            ys[b] = oob_row;
-          } else {
-            ys[b] = (id * p.num_kv_heads + kvh) * bs;
+            y = oob_row;
           }
-        }
-        const uint32_t bytes = (uint32_t)nblk * S::kBlocksD * box_bytes;
-        if (j >= 2 && !mbar_wait_bounded(&empty_k[st], prev, kPfWaitNs)) {
-          set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-          break;
-        }
-        mbar_arrive_expect_tx(&full_k[st], bytes);
-        unsigned char* kd = sm + S::kKOff + st * S::kTileBytes;
-        for (int b = 0; b < nblk; ++b)
 #pragma unroll
           for (int cb = 0; cb < S::kBlocksD; ++cb)
-            tma_load_2d(kd + cb * S::kColBlock + b * bs * 128, &kmap, cb * 64, ys[b], &full_k[st]);
-        if (j >= 2 && !mbar_wait_bounded(&empty_v[st], prev, kPfWaitNs)) {
-          set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-          break;
+            tma_load_2d(stage_base + cb * S::kColBlock + b * bs * 128, map, cb * 64, y, full);
         }
-        mbar_arrive_expect_tx(&full_v[st], bytes);
-        unsigned char* vd = sm + S::kVOff + st * S::kTileBytes;
-        for (int b = 0; b < nblk; ++b)
-#pragma unroll
-          for (int cb = 0; cb < S::kBlocksD; ++cb)
-            tma_load_2d(vd + cb * S::kColBlock + b * bs * 128, &vmap, cb * 64, ys[b], &full_v[st]);
+      };
+      // order K_0, K_1, V_0, K_2, V_1, ...: K_{j+1} is needed (by S_{j+1})
+      // before V_j (by the O MMAs of tile j); each wait blocks in the barrier
+      int kj = 0, vj = 0;
+      while (kj < ntiles || vj < ntiles) {
+        if (kj < ntiles && kj <= vj + 1) {
+          if (kj >= 2 && !mbar_wait_bounded(&empty_k[kj & 1], ((kj >> 1) + 1) & 1, kPfWaitNs)) {
+            set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+            break;
+          }
+          issue(kj, &kmap, sm + S::kKOff + (kj & 1) * S::kTileBytes, &full_k[kj & 1]);
+          ++kj;
+        } else {
+          if (vj >= 2 && !mbar_wait_bounded(&empty_v[vj & 1], ((vj >> 1) + 1) & 1, kPfWaitNs)) {
+            set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+            break;
+          }
+          issue(vj, &vmap, sm + S::kVOff + (vj & 1) * S::kTileBytes, &full_v[vj & 1]);
+          ++vj;
+        }
       }
     }
   } else if (warp == 4) {
@@ -300,17 +308,25 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       ok = __all_sync(kFullMask, mbar_wait_bounded(&s_full[b], par, kPfWaitNs));
       if (!ok) break;
       tc_fence_after();
+      // raw scores; with a positive scale the maximum of the scaled scores is
+      // the scaled maximum, so scaling folds into the exponent's FFMA
       float x[kPfTokens];
       {
-        uint32_t u[32];
-        tmem_ld32(tbase + lane_base + 64 * b, u);
+        uint32_t u0[32], u1[32];
+        tmem_ld32(tbase + lane_base + 64 * b, u0);
+        tmem_ld32(tbase + lane_base + 64 * b + 32, u1);
         tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(u[i]) * p.scale_log2;
-        tmem_ld32(tbase + lane_base + 64 * b + 32, u);
-        tmem_wait_ld();
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(u0[i]);
+          x[32 + i] = __uint_as_float(u1[i]);
+        }
+      }
+      const bool pos_scale = p.scale_log2 > 0.f;
+      const float sc = pos_scale ? p.scale_log2 : 1.f;
+      if (!pos_scale) {  // rare: scale the scores first
 #pragma unroll
-        for (int i = 0; i < 32; ++i) x[32 + i] = __uint_as_float(u[i]) * p.scale_log2;
+        for (int i = 0; i < kPfTokens; ++i) x[i] *= p.scale_log2;
       }
       const int vis = pos - t0 + 1;  // visible tokens of this tile for this row
       if (vis < kPfTokens) {
@@ -318,27 +334,31 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         for (int i = 0; i < kPfTokens; ++i)
           if (i >= vis) x[i] = -INFINITY;
       }
-      float mt = -INFINITY;
+      float m8[8];  // eight independent partial maxima, then a tree
 #pragma unroll
-      for (int i = 0; i < kPfTokens; ++i) mt = fmaxf(mt, x[i]);
+      for (int k = 0; k < 8; ++k) m8[k] = x[k];
+#pragma unroll
+      for (int i = 8; i < kPfTokens; ++i) m8[i & 7] = fmaxf(m8[i & 7], x[i]);
+      const float mt = sc * fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                  fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
       const bool grow = mt > m_use + kPfRescaleLog2;  // first visible tile: always (m_use = -inf)
       float alpha = 1.f;
       if (grow) {
         alpha = exp2f(m_use - mt);  // 0 while nothing was visible
         m_use = mt;
       }
-      const float base = m_use == -INFINITY ? 0.f : m_use;
-      float ps = 0.f;
+      const float nbase = m_use == -INFINITY ? 0.f : -m_use;
+      float ps4[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t hi[32], lo[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const float p0 = exp2f(x[2 * i] - base), p1 = exp2f(x[2 * i + 1] - base);
-        ps += p0 + p1;
+        const float p0 = ex2_approx(fmaf(x[2 * i], sc, nbase)), p1 = ex2_approx(fmaf(x[2 * i + 1], sc, nbase));
+        ps4[i & 3] += p0 + p1;
         hi[i] = P16::pack(p0, p1);
         const float2 hv = P16::unpack(hi[i]);
         lo[i] = P16::pack(p0 - hv.x, p1 - hv.y);
       }
-      l = l * alpha + ps;
+      l = l * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
       if (j > 0 && __any_sync(kFullMask, grow)) {
         // O holds the previous tiles' sums on the old base: rescale it once
         // their MMAs are done (S_j completing implies those of tile j-2)
