@@ -29,7 +29,8 @@ namespace pkv {
 
 constexpr int kPfRows = 128;            // query rows per CTA = tensor-memory lanes
 constexpr int kPfTokens = 64;           // K/V tokens per tile
-constexpr int kPfThreads = 192;         // 4 softmax warps, 1 MMA warp, 1 TMA warp
+constexpr int kPfSoftThreads = 256;     // 8 softmax warps: 4 row quarters x 2 token halves
+constexpr int kPfThreads = 320;         // + 1 MMA warp + 1 TMA warp
 constexpr int kPfStages = 2;            // K and V tiles in flight
 constexpr uint32_t kPfTmemCols = 256;   // two S/P buffers (64 columns each) + O (up to 128)
 constexpr float kPfRescaleLog2 = 8.f;   // base of the running max moves only when it grows by more
@@ -117,7 +118,8 @@ struct PrefillShape {
   static constexpr int kKOff = kPfRows * D * 2;
   static constexpr int kVOff = kKOff + kPfStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kPfStages * kTileBytes;
-  static constexpr int kSlotOff = kBarOff + 13 * 8;
+  static constexpr int kXchOff = kBarOff + 16 * 8;         // softmax exchange: 6 x 128 floats
+  static constexpr int kSlotOff = kXchOff + 6 * kPfRows * 4;
   static constexpr int kUsed = kSlotOff + 16 + 1024;      // + alignment slack
   // at least 80 KB, so that at most two CTAs share an SM and their tensor
   // memory (2 x 256 columns) always fits
@@ -125,10 +127,11 @@ struct PrefillShape {
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
 };
 
-// One CTA per (128-query tile, sequence, query head); 6 warps:
-//   warps 0-3  softmax: thread r owns query row r (tensor-memory lane r);
-//   warp 4     one thread issues the MMAs;
-//   warp 5     one thread issues the TMA loads of K and V tiles.
+// One CTA per (128-query tile, sequence, query head); 10 warps:
+//   warps 0-7  softmax: warp w reads tensor-memory lanes (query rows)
+//              32 (w % 4) .. +31, token half w / 4 of each tile;
+//   warp 8     one thread issues the MMAs;
+//   warp 9     one thread issues the TMA loads of K and V tiles.
 // Per 64-token tile j (stage and S/P buffer j & 1):
 //   load:    K_j, V_j box by box (one box = one cache block of one kv head,
 //            64 head dims), through the block table;
@@ -155,8 +158,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   uint64_t* empty_k = bars + 4;  // [2] S MMA done with the K stage
   uint64_t* empty_v = bars + 6;  // [2] O MMAs done with the V stage
   uint64_t* s_full = bars + 8;   // [2] S of the buffer computed
-  uint64_t* p_full = bars + 10;  // [2] P of the buffer written (128 arrivals)
-  uint64_t* o_done = bars + 12;  // one phase per tile's O MMAs
+  uint64_t* p_full = bars + 10;  // [2] P of the buffer written (one arrival per softmax thread)
+  uint64_t* o_done = bars + 12;  // one phase per tile's O MMAs, all tiles but the last
+  uint64_t* o_last = bars + 13;  // the last tile's O MMAs: every MMA of the CTA done (one phase)
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + S::kSlotOff);
 
   const int tile = gridDim.x - 1 - blockIdx.x;  // longest causal ranges first
@@ -188,7 +192,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     cp_async_commit();
   }
   if (tid == 0) {
-    for (int i = 0; i < 13; ++i) mbar_init(&bars[i], (i == 10 || i == 11) ? kPfRows : 1);
+    for (int i = 0; i < 14; ++i) mbar_init(&bars[i], (i == 10 || i == 11) ? kPfSoftThreads : 1);
     mbar_init_fence();
   }
   if (warp == 0) tmem_alloc(slot, kPfTmemCols);
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   tc_fence_after();
   const uint32_t tbase = *slot;
 
-  if (warp == 5) {
+  if (warp == 9) {
     // ---- TMA producer: K and V tiles each issued as soon as their stage is free
     if (lane == 0) {
       const int32_t* bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         }
       }
     }
-  } else if (warp == 4) {
+  } else if (warp == 8) {
     // ---- MMA issue ------------------------------------------------------------
     if (lane == 0) {
       constexpr uint32_t id_s = mma_idesc_f16(kPfRows, kPfTokens, kBf16, 0);
@@ -289,128 +293,145 @@ __global__ void __launch_bounds__(kPfThreads, 2)
             const uint64_t vb = smem_desc_sw128(v_addr + b * S::kTileBytes + ks * 2048, S::kColBlock, 1024);
             mma_ts(tbase + 128, pa + 32 * part + 8 * ks, vb, id_o, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
           }
-        mma_commit(o_done);
+        // a separate barrier for the last tile: a parity wait tells apart only
+        // adjacent phases, and the final wait may come two phases late
+        mma_commit(j + 1 < ntiles ? o_done : o_last);
         if (j + 2 < ntiles) mma_commit(&empty_v[b]);
       }
       if (!ok) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
     }
   } else {
-    // ---- softmax and output (thread = query row) ------------------------------
-    const int r = tid;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    // ---- softmax and output --------------------------------------------------
+    // Warp w owns query rows 32 (w % 4) .. +31 (its tensor-memory lane
+    // quarter) and token half w / 4 of every tile (and that half of the O
+    // columns). The two warps of a row quarter exchange partial maxima through
+    // shared memory at one named barrier per tile; the barrier also ORs the
+    // threads' timeout flags, so that all softmax threads leave together.
+    const int r = 32 * (warp & 3) + lane;
+    const int ch = warp >> 2;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     const int pos = min(first_pos + r, kv_end - 1);  // rows past the last query: any finite result
+    float* xch = reinterpret_cast<float*>(sm + S::kXchOff);  // [2 tile parities][2 halves][128 rows]
+    float* lx = xch + 4 * kPfRows;                            // [2 halves][128 rows]
+    const bool pos_scale = p.scale_log2 > 0.f;
+    const float sc = pos_scale ? p.scale_log2 : 1.f;
     float m_use = -INFINITY, l = 0.f;
-    bool ok = true;
+    bool bad = false;
     for (int j = 0; j < ntiles; ++j) {
       const int b = j & 1;
       const uint32_t par = (j >> 1) & 1;
-      const int t0 = j * kPfTokens;
-      ok = __all_sync(kFullMask, mbar_wait_bounded(&s_full[b], par, kPfWaitNs));
-      if (!ok) break;
-      tc_fence_after();
-      // raw scores; with a positive scale the maximum of the scaled scores is
-      // the scaled maximum, so scaling folds into the exponent's FFMA
-      float x[kPfTokens];
-      {
-        uint32_t u0[32], u1[32];
-        tmem_ld32(tbase + lane_base + 64 * b, u0);
-        tmem_ld32(tbase + lane_base + 64 * b + 32, u1);
+      const int t0 = j * kPfTokens + 32 * ch;  // first token of this thread's half
+      float x[32];
+      float pm = -INFINITY;
+      // every wait is made warp-uniform before the warp-collective
+      // tensor-memory loads and stores that follow it
+      if (__all_sync(kFullMask, !bad && mbar_wait_bounded(&s_full[b], par, kPfWaitNs))) {
+        tc_fence_after();
+        uint32_t u[32];
+        tmem_ld32(tbase + lane_base + 64 * b + 32 * ch, u);
         tmem_wait_ld();
+        // raw scores: with a positive scale the maximum of the scaled scores
+        // is the scaled maximum, so scaling folds into the exponent's FFMA
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x[i] = __uint_as_float(u0[i]);
-          x[32 + i] = __uint_as_float(u1[i]);
+        for (int i = 0; i < 32; ++i) x[i] = pos_scale ? __uint_as_float(u[i]) : __uint_as_float(u[i]) * p.scale_log2;
+        const int vis = pos - t0 + 1;  // visible tokens of this half for this row
+        if (vis < 32) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (i >= vis) x[i] = -INFINITY;
         }
+        float m8[8];  // eight independent partial maxima, then a tree
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = x[k];
+#pragma unroll
+        for (int i = 8; i < 32; ++i) m8[i & 7] = fmaxf(m8[i & 7], x[i]);
+        pm = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      } else {
+        bad = true;
       }
-      const bool pos_scale = p.scale_log2 > 0.f;
-      const float sc = pos_scale ? p.scale_log2 : 1.f;
-      if (!pos_scale) {  // rare: scale the scores first
-#pragma unroll
-        for (int i = 0; i < kPfTokens; ++i) x[i] *= p.scale_log2;
+      xch[(b * 2 + ch) * kPfRows + r] = pm;
+      if (barrier_or(1, kPfSoftThreads, bad)) {
+        bad = true;
+        break;
       }
-      const int vis = pos - t0 + 1;  // visible tokens of this tile for this row
-      if (vis < kPfTokens) {
-#pragma unroll
-        for (int i = 0; i < kPfTokens; ++i)
-          if (i >= vis) x[i] = -INFINITY;
-      }
-      float m8[8];  // eight independent partial maxima, then a tree
-#pragma unroll
-      for (int k = 0; k < 8; ++k) m8[k] = x[k];
-#pragma unroll
-      for (int i = 8; i < kPfTokens; ++i) m8[i & 7] = fmaxf(m8[i & 7], x[i]);
-      const float mt = sc * fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                  fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      const float mt = sc * fmaxf(pm, xch[(b * 2 + (ch ^ 1)) * kPfRows + r]);
       const bool grow = mt > m_use + kPfRescaleLog2;  // first visible tile: always (m_use = -inf)
       float alpha = 1.f;
       if (grow) {
         alpha = exp2f(m_use - mt);  // 0 while nothing was visible
         m_use = mt;
       }
+      if (j > 0 && __any_sync(kFullMask, grow)) {
+        // O holds the previous tiles' sums on the old base: rescale this
+        // warp's half of its columns once their MMAs are done (S_j
+        // completing implies those of tile j-2)
+        if (__all_sync(kFullMask, mbar_wait_bounded(o_done, (j - 1) & 1, kPfWaitNs))) {
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t w[16];
+            const uint32_t a = tbase + lane_base + 128 + (D / 2) * ch + 16 * c;
+            tmem_ld16(a, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+            tmem_st16(a, w);
+          }
+        } else {
+          bad = true;
+        }
+      }
       const float nbase = m_use == -INFINITY ? 0.f : -m_use;
       float ps4[4] = {0.f, 0.f, 0.f, 0.f};
-      uint32_t hi[32], lo[32];
+      uint32_t hi[16], lo[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 16; ++i) {
         const float p0 = ex2_approx(fmaf(x[2 * i], sc, nbase)), p1 = ex2_approx(fmaf(x[2 * i + 1], sc, nbase));
         ps4[i & 3] += p0 + p1;
         hi[i] = P16::pack(p0, p1);
         const float2 hv = P16::unpack(hi[i]);
         lo[i] = P16::pack(p0 - hv.x, p1 - hv.y);
       }
-      l = l * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));
-      if (j > 0 && __any_sync(kFullMask, grow)) {
-        // O holds the previous tiles' sums on the old base: rescale it once
-        // their MMAs are done (S_j completing implies those of tile j-2)
-        ok = __all_sync(kFullMask, mbar_wait_bounded(o_done, (j - 1) & 1, kPfWaitNs));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t w[32];
-          tmem_ld32(tbase + lane_base + 128 + 32 * c, w);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
-          tmem_st32(tbase + lane_base + 128 + 32 * c, w);
-        }
-      }
-      tmem_st32(tbase + lane_base + 64 * b, hi);
-      tmem_st32(tbase + lane_base + 64 * b + 32, lo);
+      l = l * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));  // this half's share of the row sum
+      // P of this half: packed pairs at columns 16 ch .. (high) and 32 + 16 ch .. (low)
+      __syncwarp();
+      tmem_st16(tbase + lane_base + 64 * b + 16 * ch, hi);
+      tmem_st16(tbase + lane_base + 64 * b + 32 + 16 * ch, lo);
       tmem_wait_st();
-      if (j == ntiles - 1 && kv_end < t0 + kPfTokens) {
+      if (j == ntiles - 1 && kv_end < j * kPfTokens + kPfTokens) {
         // V rows past the context may hold anything (a NaN would survive a
         // zero probability): zero them once the tile has landed
-        ok = __all_sync(kFullMask, mbar_wait_bounded(&full_v[b], par, kPfWaitNs));
-        if (!ok) break;
-        const int z0 = kv_end - t0, per_row = S::kBlocksD * 8;
-        unsigned char* vd = sm + S::kVOff + b * S::kTileBytes;
-        for (int i = tid; i < (kPfTokens - z0) * per_row; i += kPfRows) {
-          const int row = z0 + i / per_row, rem = i % per_row;
-          *reinterpret_cast<uint4*>(vd + (rem >> 3) * S::kColBlock + row * 128 + (rem & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
+        if (__all_sync(kFullMask, mbar_wait_bounded(&full_v[b], par, kPfWaitNs))) {
+          const int z0 = kv_end - j * kPfTokens, per_row = S::kBlocksD * 8;
+          unsigned char* vd = sm + S::kVOff + b * S::kTileBytes;
+          for (int i = tid; i < (kPfTokens - z0) * per_row; i += kPfSoftThreads) {
+            const int row = z0 + i / per_row, rem = i % per_row;
+            *reinterpret_cast<uint4*>(vd + (rem >> 3) * S::kColBlock + row * 128 + (rem & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_async_smem();
+        } else {
+          bad = true;
         }
-        fence_async_smem();
       }
       tc_fence_before();
       mbar_arrive(&p_full[b]);
     }
-    if (ok) {
-      // every tile's O MMAs done: wait the phases in order (a parity wait
-      // tells apart only adjacent phases)
-      if (ntiles >= 2) ok = __all_sync(kFullMask, mbar_wait_bounded(o_done, (ntiles - 2) & 1, kPfWaitNs));
-      if (ok) ok = __all_sync(kFullMask, mbar_wait_bounded(o_done, (ntiles - 1) & 1, kPfWaitNs));
-    }
-    if (!ok) {
+    lx[ch * kPfRows + r] = l;
+    bad = barrier_or(1, kPfSoftThreads, bad);
+    if (!bad && !__all_sync(kFullMask, mbar_wait_bounded(o_last, 0, kPfWaitNs))) bad = true;
+    if (bad) {
       if (lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
     } else {
+      __syncwarp();
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      T* og = static_cast<T*>(p.out) + ((size_t)(q0 + row0 + r) * p.num_heads + h) * D;
+      const float lt = l + lx[(ch ^ 1) * kPfRows + r];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      T* og = static_cast<T*>(p.out) + ((size_t)(q0 + row0 + r) * p.num_heads + h) * D + (D / 2) * ch;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         uint32_t w[32];
-        tmem_ld32(tbase + lane_base + 128 + 32 * c, w);
+        tmem_ld32(tbase + lane_base + 128 + (D / 2) * ch + 32 * c, w);
         tmem_wait_ld();
         if (r < rows) {
           uint32_t pk[16];
