@@ -119,7 +119,8 @@ struct PrefillShape {
   static constexpr int kVOff = kKOff + kPfStages * kTileBytes;
   static constexpr int kBarOff = kVOff + kPfStages * kTileBytes;
   static constexpr int kXchOff = kBarOff + 16 * 8;         // softmax exchange: 6 x 128 floats
-  static constexpr int kSlotOff = kXchOff + 6 * kPfRows * 4;
+  static constexpr int kRingOff = kXchOff + 6 * kPfRows * 4;  // TMA rows of 8 tiles' blocks
+  static constexpr int kSlotOff = kRingOff + 8 * 8 * 4;
   static constexpr int kUsed = kSlotOff + 16 + 1024;      // + alignment slack
   // at least 80 KB, so that at most two CTAs share an SM and their tensor
   // memory (2 x 256 columns) always fits
@@ -206,49 +207,72 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   const uint32_t tbase = *slot;
 
   if (warp == 9) {
-    // ---- TMA producer: K and V tiles each issued as soon as their stage is free
-    if (lane == 0) {
-      const int32_t* bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
-      const int per_tile = kPfTokens / bs;                     // cache blocks per tile
-      const int oob_row = p.num_blocks * p.num_kv_heads * bs;  // first row past the pool: reads zeros
-      const uint32_t box_bytes = (uint32_t)bs * 128u;
-      auto issue = [&](int j, const CUtensorMap* map, unsigned char* stage_base, uint64_t* full) {
-        const int t0 = j * kPfTokens;
-        const int nblk = min(per_tile, (kv_end - t0 + bs - 1) / bs);
-        mbar_arrive_expect_tx(full, (uint32_t)nblk * S::kBlocksD * box_bytes);
-        for (int b = 0; b < nblk; ++b) {
-          const int id = __ldg(bt + t0 / bs + b);
-          int y = (id * p.num_kv_heads + kvh) * bs;
-          if (id < 0 || id >= p.num_blocks) {
-            set_err(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
-            y = oob_row;
-          }
-#pragma unroll
-          for (int cb = 0; cb < S::kBlocksD; ++cb)
-            tma_load_2d(stage_base + cb * S::kColBlock + b * bs * 128, map, cb * 64, y, full);
-        }
-      };
-      // order K_0, K_1, V_0, K_2, V_1, ...: K_{j+1} is needed (by S_{j+1})
-      // before V_j (by the O MMAs of tile j); each wait blocks in the barrier
-      int kj = 0, vj = 0;
-      while (kj < ntiles || vj < ntiles) {
-        if (kj < ntiles && kj <= vj + 1) {
-          if (kj >= 2 && !mbar_wait_bounded(&empty_k[kj & 1], ((kj >> 1) + 1) & 1, kPfWaitNs)) {
-            set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-            break;
-          }
-          issue(kj, &kmap, sm + S::kKOff + (kj & 1) * S::kTileBytes, &full_k[kj & 1]);
-          ++kj;
-        } else {
-          if (vj >= 2 && !mbar_wait_bounded(&empty_v[vj & 1], ((vj >> 1) + 1) & 1, kPfWaitNs)) {
-            set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
-            break;
-          }
-          issue(vj, &vmap, sm + S::kVOff + (vj & 1) * S::kTileBytes, &full_v[vj & 1]);
-          ++vj;
-        }
+    // ---- TMA producer ----------------------------------------------------------
+    // The warp fetches block-table entries four tiles ahead (lane 8 t + b holds
+    // block b of tile t of a group of four) into a shared ring of TMA row
+    // coordinates, so that no global load sits between a free stage and its
+    // copies. Order K_0, K_1, V_0, K_2, V_1, ...:
+    // K_{j+1} is needed (by S_{j+1}) before V_j (by the O MMAs of tile j).
+    const int32_t* bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
+    const int per_tile = kPfTokens / bs;                     // cache blocks per tile (<= 8)
+    const int oob_row = p.num_blocks * p.num_kv_heads * bs;  // first row past the pool: reads zeros
+    const uint32_t box_bytes = (uint32_t)bs * 128u;
+    int* ring = reinterpret_cast<int*>(sm + S::kRingOff);    // [8 tiles][8 blocks]
+    auto nblk_of = [&](int j) { return min(per_tile, (kv_end - j * kPfTokens + bs - 1) / bs); };
+    const int gt = lane >> 3, gb = lane & 7;  // this lane's tile in a group of four, block in the tile
+    auto fetch_group = [&](int g) -> int {    // issues the load only
+      const int t = 4 * g + gt;
+      return (t < ntiles && gb < nblk_of(t)) ? __ldg(bt + t * per_tile + gb) : 0;
+    };
+    auto store_group = [&](int g, int id) {
+      const int t = 4 * g + gt;
+      if (t < ntiles && gb < nblk_of(t)) {
+        int y = oob_row;
+        if (id >= 0 && id < p.num_blocks)
+          y = (id * p.num_kv_heads + kvh) * bs;
+        else
+          set_err(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
+        ring[(t & 7) * 8 + gb] = y;
       }
+    };
+    // all lanes: lane 0 posts the tile's bytes, then lane 2 b + cb issues the
+    // box of block b, column block cb (boxes from one lane issue ~100 cycles apart)
+    auto issue = [&](int j, const CUtensorMap* map, unsigned char* stage_base, uint64_t* full) {
+      const int nblk = nblk_of(j);
+      if (lane == 0) mbar_arrive_expect_tx(full, (uint32_t)nblk * S::kBlocksD * box_bytes);
+      __syncwarp();
+      if (lane < nblk * S::kBlocksD) {
+        const int b = lane / S::kBlocksD, cb = lane % S::kBlocksD;
+        tma_load_2d(stage_base + cb * S::kColBlock + b * bs * 128, map, cb * 64, ring[(j & 7) * 8 + b], full);
+      }
+    };
+    auto wait_free = [&](uint64_t* bar, uint32_t parity) -> bool {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_bounded(bar, parity, kPfWaitNs);
+      return __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+    };
+    store_group(0, fetch_group(0));  // the first group waits for its loads
+    int pending = fetch_group(1);
+    int kj = 0, vj = 0;
+    bool ok = true;
+    while (ok && (kj < ntiles || vj < ntiles)) {
+      if (kj < ntiles && kj <= vj + 1) {
+        if (kj > 0 && (kj & 3) == 0) {  // tiles kj .. kj+3 into the ring, the next group requested
+          store_group(kj >> 2, pending);
+          pending = fetch_group((kj >> 2) + 1);
+        }
+        __syncwarp();
+        ok = kj < 2 || wait_free(&empty_k[kj & 1], ((kj >> 1) + 1) & 1);
+        if (ok) issue(kj, &kmap, sm + S::kKOff + (kj & 1) * S::kTileBytes, &full_k[kj & 1]);
+        ++kj;
+      } else {
+        ok = vj < 2 || wait_free(&empty_v[vj & 1], ((vj >> 1) + 1) & 1);
+        if (ok) issue(vj, &vmap, sm + S::kVOff + (vj & 1) * S::kTileBytes, &full_v[vj & 1]);
+        ++vj;
+      }
+      __syncwarp();
     }
+    if (!ok && lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
   } else if (warp == 8) {
     // ---- MMA issue ------------------------------------------------------------
     if (lane == 0) {
