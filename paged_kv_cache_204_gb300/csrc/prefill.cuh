@@ -164,8 +164,10 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   uint64_t* o_last = bars + 13;  // the last tile's O MMAs: every MMA of the CTA done (one phase)
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + S::kSlotOff);
 
-  const int tile = gridDim.x - 1 - blockIdx.x;  // longest causal ranges first
-  const int s = blockIdx.y, h = blockIdx.z;
+  // blocks launch in x order: every (sequence, head)'s last query tile (the
+  // longest causal range) before any earlier tile
+  const int tile = gridDim.y - 1 - blockIdx.y;
+  const int s = blockIdx.x / p.num_heads, h = blockIdx.x % p.num_heads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int L = __ldg(p.context_lens + s);
   const int q0 = __ldg(p.query_start + s), n = __ldg(p.query_start + s + 1) - q0;
@@ -532,7 +534,8 @@ cudaError_t launch_pa_prefill(const PrefillParams& p, int max_query_len, cudaStr
   if (e != cudaSuccess) return e;
   e = encode_pool_map<T, D>(&vmap, p.v_cache, p);
   if (e != cudaSuccess) return e;
-  const dim3 grid((max_query_len + kPfRows - 1) / kPfRows, p.num_seqs, p.num_heads);
+  if ((max_query_len + kPfRows - 1) / kPfRows > 65535) return cudaErrorNotSupported;
+  const dim3 grid(p.num_seqs * p.num_heads, (max_query_len + kPfRows - 1) / kPfRows);
   pa_prefill_kernel<T, D><<<grid, kPfThreads, S::kSmemBytes, stream>>>(kmap, vmap, p);
   return cudaGetLastError();
 }
