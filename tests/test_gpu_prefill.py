@@ -155,3 +155,55 @@ def test_prefill_device_errors_are_reported_and_skipped():
                                 dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0 and torch.equal(out3, out)
+
+
+def _ramp_values(cfg, lay, growth, seed):
+    """Keys that point more and more along one direction u as their position
+    grows, and queries near u: every query's scores rise steadily along the
+    context, so the running maximum keeps moving by more than the kernel's
+    re-basing threshold and the tensor-memory rescale of O runs on most
+    tiles."""
+    import synth.host as H
+    rng = np.random.default_rng(seed)
+    Hkv, D = cfg.num_kv_heads, cfg.head_dim
+    u = rng.standard_normal(D)
+    sys_pos = np.arange(cfg.system_len, dtype=float)
+    user_pos = np.concatenate([np.arange(int(lay.query_start[i + 1] - lay.query_start[i]), dtype=float)
+                               + cfg.system_len for i in range(cfg.users)])
+    keys = lambda pos: growth * pos[:, None, None] * u[None, None, :] + rng.standard_normal((pos.size, Hkv, D))
+    nrm = lambda shape: rng.standard_normal(shape)
+    st = lambda x: H.round_to_storage(x, cfg.dtype)
+    n = lay.total_queries
+    return SP.PrefillValues(system_k=st(keys(sys_pos)), system_v=st(nrm((cfg.system_len, Hkv, D))),
+                            user_k=st(keys(user_pos)), user_v=st(nrm((n, Hkv, D))),
+                            q=st(u[None, None, :] + 0.3 * nrm((n, cfg.num_heads, D))))
+
+
+SCALE_CASES = {
+    # scores rising ~10 (base 2) per 64-token tile: O is re-based on most tiles
+    "rising_scores": dict(growth=0.01, scale=None),
+    # a negative scale: the kernel scales before the maximum instead of after
+    "negative_scale": dict(growth=0.0, scale=-0.125),
+    # scale 0: every visible token weighs the same (the mean of the visible V rows)
+    "zero_scale": dict(growth=0.0, scale=0.0),
+}
+
+
+@pytest.mark.parametrize("name", list(SCALE_CASES))
+def test_prefill_rescale_and_scale_sign(name):
+    case = SCALE_CASES[name]
+    cfg = SP.get("prefill_small").replace(dtype="bf16", head_dim=128, block_size=16, num_heads=4, num_kv_heads=2,
+                                          system_len=100, user_len=("uniform", 150, 300), users=3, num_blocks=300,
+                                          seed=2101)
+    if case["scale"] is not None:
+        cfg = cfg.replace(scale=case["scale"])
+    lay = SP.build(cfg)
+    vals = _ramp_values(cfg, lay, case["growth"], seed=2102)
+    kc, vc = SP.host_pools(cfg)
+    kc_d, vc_d = up(kc, cfg.dtype), up(vc, cfg.dtype)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_prefill(cfg, lay, vals, kc_d, vc_d, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref, rows = oracle_prefill(cfg, lay, vals)
+    assert_close(to_f64(out)[rows], ref, name)
