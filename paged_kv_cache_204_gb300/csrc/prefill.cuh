@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   uint64_t* p_full = bars + 10;  // [2] P of the buffer written (one arrival per softmax thread)
   uint64_t* o_done = bars + 12;  // one phase per tile's O MMAs, all tiles but the last
   uint64_t* o_last = bars + 13;  // the last tile's O MMAs: every MMA of the CTA done (one phase)
+  uint64_t* q_full = bars + 14;  // Q rows landed (one arrival per loading thread)
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + S::kSlotOff);
 
   // blocks launch in x order: every (sequence, head)'s last query tile (the
@@ -195,14 +196,10 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     cp_async_commit();
   }
   if (tid == 0) {
-    for (int i = 0; i < 14; ++i) mbar_init(&bars[i], (i == 10 || i == 11) ? kPfSoftThreads : 1);
+    for (int i = 0; i < 15; ++i) mbar_init(&bars[i], (i == 10 || i == 11) ? kPfSoftThreads : (i == 14 ? kPfRows : 1));
     mbar_init_fence();
   }
   if (warp == 0) tmem_alloc(slot, kPfTmemCols);
-  if (tid < kPfRows) {
-    cp_async_wait_all();
-    fence_async_smem();
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -298,7 +295,12 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         if (j + 2 < ntiles) mma_commit(&empty_k[st]);  // only commits that someone waits for
         return true;
       };
-      bool ok = issue_s(0);
+      // Q (loaded by the first four warps) before the first S
+      bool ok = mbar_wait_bounded(q_full, 0, kPfWaitNs);
+      if (ok) {
+        tc_fence_after();
+        ok = issue_s(0);
+      }
       for (int j = 0; j < ntiles && ok; ++j) {
         const int b = j & 1;
         if (j + 1 < ntiles && !issue_s(j + 1)) {
@@ -333,6 +335,11 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     // columns). The two warps of a row quarter exchange partial maxima through
     // shared memory at one named barrier per tile; the barrier also ORs the
     // threads' timeout flags, so that all softmax threads leave together.
+    if (tid < kPfRows) {  // the Q rows this thread copied, made visible to the MMAs
+      cp_async_wait_all();
+      fence_async_smem();
+      mbar_arrive(q_full);
+    }
     const int r = 32 * (warp & 3) + lane;
     const int ch = warp >> 2;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
