@@ -104,7 +104,8 @@ __device__ __forceinline__ int sw128_off(int r, int c) { return r * 128 + ((c ^ 
 //   Q      [2 or 1 column blocks][128 rows][128 B]          (K-major A operand)
 //   K, V   [2 stages][D/64 column blocks][64 tokens][128 B]  (K: K-major B of S;
 //                                                            V: MN-major B of O)
-//   mbarriers, tensor-memory address slot.
+//   mbarriers, softmax exchange (row maxima and sums), ring of TMA row
+//   coordinates, tensor-memory address slot.
 // Tensor memory (256 columns, lanes = query rows): S/P buffers at columns 0
 // and 64 (S as fp32; P overwrites it as 16-bit hi / lo pairs in columns
 // +0..31 / +32..63), O (fp32, D columns) at column 128.
@@ -132,7 +133,8 @@ struct PrefillShape {
 //   warps 0-7  softmax: warp w reads tensor-memory lanes (query rows)
 //              32 (w % 4) .. +31, token half w / 4 of each tile;
 //   warp 8     one thread issues the MMAs;
-//   warp 9     one thread issues the TMA loads of K and V tiles.
+//   warp 9     the TMA loads of K and V tiles (block-table entries fetched
+//              ahead by the whole warp, a tile's boxes issued by parallel lanes).
 // Per 64-token tile j (stage and S/P buffer j & 1):
 //   load:    K_j, V_j box by box (one box = one cache block of one kv head,
 //            64 head dims), through the block table;
