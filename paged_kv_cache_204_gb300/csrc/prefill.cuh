@@ -212,8 +212,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     // The warp fetches block-table entries four tiles ahead (lane 8 t + b holds
     // block b of tile t of a group of four) into a shared ring of TMA row
     // coordinates, so that no global load sits between a free stage and its
-    // copies. Order K_0, K_1, V_0, K_2, V_1, ...:
-    // K_{j+1} is needed (by S_{j+1}) before V_j (by the O MMAs of tile j).
+    // copies.
     const int32_t* bt = p.block_tables + (size_t)s * p.max_blocks_per_seq;
     const int per_tile = kPfTokens / bs;                     // cache blocks per tile (<= 8)
     const int oob_row = p.num_blocks * p.num_kv_heads * bs;  // first row past the pool: reads zeros
@@ -247,31 +246,54 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         tma_load_2d(stage_base + cb * S::kColBlock + b * bs * 128, map, cb * 64, ring[(j & 7) * 8 + b], full);
       }
     };
-    auto wait_free = [&](uint64_t* bar, uint32_t parity) -> bool {
-      bool ok = true;
-      if (lane == 0) ok = mbar_wait_bounded(bar, parity, kPfWaitNs);
-      return __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
-    };
     store_group(0, fetch_group(0));  // the first group waits for its loads
     int pending = fetch_group(1);
+    // K and V tiles go as soon as their own stage is free (a K tile is
+    // needed by S two tiles before the V tile of the same stage frees); V_j
+    // after K_j, whose step wrote tile j's rows into the ring
     int kj = 0, vj = 0;
     bool ok = true;
-    while (ok && (kj < ntiles || vj < ntiles)) {
-      if (kj < ntiles && kj <= vj + 1) {
+    uint64_t t_last = 0;
+    while (kj < ntiles || vj < ntiles) {
+      bool k_go = false, v_go = false;
+      if (lane == 0) {
+        k_go = kj < ntiles && (kj < 2 || mbar_test_wait(&empty_k[kj & 1], ((kj >> 1) + 1) & 1));
+        v_go = vj < kj && (vj < 2 || mbar_test_wait(&empty_v[vj & 1], ((vj >> 1) + 1) & 1));
+      }
+      k_go = __shfl_sync(kFullMask, k_go ? 1 : 0, 0) != 0;
+      v_go = __shfl_sync(kFullMask, v_go ? 1 : 0, 0) != 0;
+      if (k_go) {
         if (kj > 0 && (kj & 3) == 0) {  // tiles kj .. kj+3 into the ring, the next group requested
           store_group(kj >> 2, pending);
           pending = fetch_group((kj >> 2) + 1);
         }
         __syncwarp();
-        ok = kj < 2 || wait_free(&empty_k[kj & 1], ((kj >> 1) + 1) & 1);
-        if (ok) issue(kj, &kmap, sm + S::kKOff + (kj & 1) * S::kTileBytes, &full_k[kj & 1]);
+        issue(kj, &kmap, sm + S::kKOff + (kj & 1) * S::kTileBytes, &full_k[kj & 1]);
         ++kj;
-      } else {
-        ok = vj < 2 || wait_free(&empty_v[vj & 1], ((vj >> 1) + 1) & 1);
-        if (ok) issue(vj, &vmap, sm + S::kVOff + (vj & 1) * S::kTileBytes, &full_v[vj & 1]);
+      }
+      if (v_go) {
+        issue(vj, &vmap, sm + S::kVOff + (vj & 1) * S::kTileBytes, &full_v[vj & 1]);
         ++vj;
       }
-      __syncwarp();
+      if (k_go || v_go) {
+        t_last = 0;
+        continue;
+      }
+      // nothing free: sleep in the barrier of the tile needed first (K while
+      // it is not ahead of V by two, else V), with the overall limit
+      if (lane == 0) {
+        const uint64_t now = globaltimer_ns();
+        if (t_last == 0) t_last = now;
+        if (now - t_last >= kPfWaitNs) {
+          ok = false;
+        } else if (kj < ntiles && kj <= vj + 1) {
+          mbar_try_wait(&empty_k[kj & 1], ((kj >> 1) + 1) & 1);
+        } else if (vj < kj) {
+          mbar_try_wait(&empty_v[vj & 1], ((vj >> 1) + 1) & 1);
+        }
+      }
+      ok = __shfl_sync(kFullMask, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
     }
     if (!ok && lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
   } else if (warp == 8) {
