@@ -301,19 +301,24 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     if (lane == 0) {
       constexpr uint32_t id_s = mma_idesc_f16(kPfRows, kPfTokens, kBf16, 0);
       constexpr uint32_t id_o = mma_idesc_f16(kPfRows, D, kBf16, 1);
-      const uint32_t q_addr = smem_u32(sm + S::kQOff);
-      const uint32_t k_addr = smem_u32(sm + S::kKOff);
-      const uint32_t v_addr = smem_u32(sm + S::kVOff);
+      // descriptors built once; a k-step only moves the start address, whose
+      // field (address / 16, low bits of the descriptor) never carries here
+      // (shared addresses stay below 256 KB)
+      const uint64_t q_desc = smem_desc_sw128(smem_u32(sm + S::kQOff), 16, 1024);
+      const uint64_t k_desc0 = smem_desc_sw128(smem_u32(sm + S::kKOff), 16, 1024);
+      const uint64_t k_desc1 = smem_desc_sw128(smem_u32(sm + S::kKOff + S::kTileBytes), 16, 1024);
+      const uint64_t v_desc0 = smem_desc_sw128(smem_u32(sm + S::kVOff), S::kColBlock, 1024);
+      const uint64_t v_desc1 = smem_desc_sw128(smem_u32(sm + S::kVOff + S::kTileBytes), S::kColBlock, 1024);
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
         if (!mbar_wait_bounded(&full_k[st], (j >> 1) & 1, kPfWaitNs)) return false;
         tc_fence_after();
+        const uint64_t kd = st ? k_desc1 : k_desc0;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const int cb = ks >> 2, kk = ks & 3;
-          const uint64_t a = smem_desc_sw128(q_addr + cb * S::kQColBlock + kk * 32, 16, 1024);
-          const uint64_t b = smem_desc_sw128(k_addr + st * S::kTileBytes + cb * S::kColBlock + kk * 32, 16, 1024);
-          mma_ss(tbase + 64 * st, a, b, id_s, ks > 0);
+          mma_ss(tbase + 64 * st, q_desc + (uint64_t)((cb * S::kQColBlock + kk * 32) >> 4),
+                 kd + (uint64_t)((cb * S::kColBlock + kk * 32) >> 4), id_s, ks > 0);
         }
         mma_commit(&s_full[st]);
         if (j + 2 < ntiles) mma_commit(&empty_k[st]);  // only commits that someone waits for
@@ -338,13 +343,13 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         }
         tc_fence_after();
         const uint32_t pa = tbase + 64 * b;
+        const uint64_t vd = b ? v_desc1 : v_desc0;
 #pragma unroll
         for (int part = 0; part < 2; ++part)  // high then low halves of P
 #pragma unroll
-          for (int ks = 0; ks < kPfTokens / 16; ++ks) {
-            const uint64_t vb = smem_desc_sw128(v_addr + b * S::kTileBytes + ks * 2048, S::kColBlock, 1024);
-            mma_ts(tbase + 128, pa + 32 * part + 8 * ks, vb, id_o, (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
-          }
+          for (int ks = 0; ks < kPfTokens / 16; ++ks)
+            mma_ts(tbase + 128, pa + 32 * part + 8 * ks, vd + (uint64_t)((ks * 2048) >> 4), id_o,
+                   (j > 0 || part > 0 || ks > 0) ? 1u : 0u);
         // a separate barrier for the last tile: a parity wait tells apart only
         // adjacent phases, and the final wait may come two phases late
         mma_commit(j + 1 < ntiles ? o_done : o_last);

@@ -69,6 +69,8 @@ CASES = {
                            user_len=("uniform", 60, 140), users=4, seed=2093),
     "short_users": dict(user_len=("uniform", 1, 3), users=5, system_len=16, seed=2094),
     "tile_edges": dict(user_len=("fixed", (63, 64, 65, 128, 129)), users=5, system_len=0, num_blocks=400, seed=2095),
+    # users with no new tokens (n = 0) between users with some: their tiles do nothing
+    "zero_query_users": dict(user_len=("fixed", (0, 70, 1, 0)), users=4, system_len=20, seed=2096),
 }
 
 
