@@ -295,10 +295,13 @@ pkv_status pkv_bm_beam_step_many(pkv_block_manager* bm, const int32_t* beams, co
   if (requests == 0) return PKV_OK;
   const int64_t bs = bm->block_size;
   const size_t total = (size_t)requests * (size_t)width;
-  std::vector<int32_t> children(total, 0);
+  std::vector<int32_t> children;
+  std::vector<char> taken;  // a parent's first child already placed
   pkv_status bad = PKV_OK;
   int64_t need = 0, released = 0;
-  try {
+  try {  // every allocation of the call happens here, before anything changes
+    children.assign(total, 0);
+    taken.assign(total, 0);
     bm->ensure_scratch();
     for (size_t k = 0; k < total; ++k)
       if (!bm->is_live(beams[k]) || !bm->mark(beams[k])) {
@@ -353,7 +356,6 @@ pkv_status pkv_bm_beam_step_many(pkv_block_manager* bm, const int32_t* beams, co
   // every request's ends, then its forks (a parent's first child keeps its id)
   for (size_t k = 0; k < total; ++k)
     if (children[k] == 0) pkv_bm_free_seq(bm, beams[k]);
-  std::vector<char> taken(total, 0);
   for (size_t k = 0; k < total; ++k) {
     const size_t j = k / (size_t)width * (size_t)width + (size_t)parents[k];
     if (!taken[j]) {
