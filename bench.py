@@ -5,7 +5,7 @@ One step = one layer's decode step of the workload: reshape_and_cache of the
 128 new K/V rows into their cache slots, then paged decode attention of the
 128 query tokens (40 heads, head_dim 128, bf16) over their 16..2048-token
 contexts scattered through a 40 000-block pool. Inputs are seeded synthetic
-data resident in HBM; L2 is flushed (256 MiB write) between timed steps and
+data resident in HBM; L2 is flushed (256 MiB written, another 256 MiB read) between timed steps and
 each step is timed with CUDA events on the launching stream.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
@@ -64,7 +64,15 @@ def describe_lengths(spec) -> str:
     return f"fixed {list(spec[1])}"
 
 
-def config_json(cfg, st, world: int, attention: str = "plain", kv: str | None = None) -> dict:
+def flush_desc(mode: str = "write+read") -> str:
+    if mode == "write+read":
+        return (f"flushed between timed steps: {FLUSH_BYTES >> 20} MiB written, then another "
+                f"{FLUSH_BYTES >> 20} MiB read (the flush's dirty lines reach HBM before the step)")
+    return f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write)"
+
+
+def config_json(cfg, st, world: int, attention: str = "plain", kv: str | None = None,
+                flush: str = "write+read") -> dict:
     parts = [f"{cfg.name}-shaped decode step: {st.num_seqs} seqs, {cfg.num_heads} heads "
              f"({cfg.num_kv_heads} kv), head_dim {cfg.head_dim}, block_size {cfg.block_size}, "
              f"{cfg.dtype} storage with fp32 accumulation"]
@@ -87,7 +95,7 @@ def config_json(cfg, st, world: int, attention: str = "plain", kv: str | None = 
         "global_batch": st.num_seqs * world,
         "seq_len": int(st.max_context_len),
         "parallelism": "single GPU" if world == 1 else f"{world} independent replicas",
-        "l2": f"flushed between timed steps ({FLUSH_BYTES >> 20} MiB write); step inputs "
+        "l2": f"{flush_desc(flush)}; step inputs "
               f"{workload_bytes(st, 1 if kv else None)['step'] / 1e9:.2f} GB",
         "seed": cfg.seed,
     }
@@ -129,97 +137,205 @@ def profiled_traffic() -> int | None:
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock, power and clock-event reasons of the GPU, polled from a
+    background thread through NVML (read-only queries, by ctypes) every
+    `period_s`; nvidia-smi polling when NVML cannot be loaded. Start it before
+    the warm-up and call `mark_timed(t0, t1)` with the timed region's wall
+    clock: the summary covers the samples inside it."""
+    # clock-event reason bits of nvmlDeviceGetCurrentClocksEventReasons
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, device_index: int):
-        self.proc = None
-        self.lines: list[str] = []
-        sel = []
+    def __init__(self, device_index: int, period_s: float = 0.001):
+        self.device_index = device_index
+        self.period = period_s
+        self.samples: list[tuple[float, float, float, float, int]] = []  # (t, sm, max, watts, reasons)
+        self.source = None
+        self.window = None
+        self._stop = None
+        self._thread = None
+        self._proc = None
+        self._uuid = None
         try:
             import torch
-            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
-            sel = ["-i", uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"]
+            u = str(torch.cuda.get_device_properties(device_index).uuid)
+            self._uuid = u if u.startswith("GPU-") else f"GPU-{u}"
         except Exception:
-            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
-            if vis.split(",")[0].strip().isdigit():
-                sel = ["-i", vis.split(",")[0].strip()]
-        self.cmd = ["nvidia-smi", *sel, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                    "-lms", "20"]
+            pass
+
+    # -- NVML ------------------------------------------------------------
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        h = ctypes.c_void_p()
+        if self._uuid is None or lib.nvmlDeviceGetHandleByUUID(self._uuid.encode(), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle for the device")
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        sm, mx, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+
+        def read():
+            lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm))      # NVML_CLOCK_SM
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(mw))
+            reasons_fn(h, ctypes.byref(rs))
+            return float(sm.value), float(mx.value), mw.value / 1000.0, int(rs.value)
+        read()
+        return lib, read
+
+    def _poll(self, read):
+        while not self._stop.is_set():
+            try:
+                s = read()
+            except Exception:
+                break
+            self.samples.append((time.perf_counter(), *s))
+            self._stop.wait(self.period)
 
     def __enter__(self):
+        import threading
+        self._stop = threading.Event()
         try:
-            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            self._lib, read = self._nvml()
+            self.source = "nvml"
+            self._thread = threading.Thread(target=self._poll, args=(read,), daemon=True)
+            self._thread.start()
+        except Exception:
+            sel = ["-i", self._uuid] if self._uuid else []
+            try:
+                self._proc = subprocess.Popen(
+                    ["nvidia-smi", *sel, f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
+                     "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi"
+                self._t_smi = time.perf_counter()
+            except OSError:
+                self._proc = None
         return self
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        if self._thread is not None:
+            self._stop.set()
+            self._thread.join(timeout=5)
             try:
-                out, _ = self.proc.communicate(timeout=5)
+                self._lib.nvmlShutdown()
+            except Exception:
+                pass
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                out, _ = self._proc.communicate(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-                out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+                self._proc.kill()
+                out, _ = self._proc.communicate()
+            lines = [l for l in out.splitlines() if l.strip()]
+            t_end = time.perf_counter()
+            names = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+                     "sw_power_cap": 0x4}
+            for k, line in enumerate(lines):  # spread evenly over the polling time (no timestamps)
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    sm, mx = float(parts[0]), float(parts[1])
+                    w = float(parts[2]) if parts[2].replace(".", "", 1).isdigit() else 0.0
+                except (ValueError, IndexError):
+                    continue
+                bits = 0
+                for (name, bit), val in zip(names.items(), parts[4:8]):
+                    if val.lower() == "active":
+                        bits |= bit
+                t = self._t_smi + (t_end - self._t_smi) * (k + 0.5) / max(1, len(lines))
+                self.samples.append((t, sm, mx, w, bits))
+
+    def mark_timed(self, t0: float, t1: float) -> None:
+        self.window = (t0, t1)
 
     def summary(self) -> dict:
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
-            try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
-                    "note": "no nvidia-smi samples"}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source,
+                    "note": "no clock samples"}
+        sel, where = self.samples, "whole run (warm-up, timed region, end-to-end steps)"
+        if self.window is not None:
+            inside = [s for s in self.samples if self.window[0] <= s[0] <= self.window[1]]
+            if inside:
+                sel, where = inside, "timed region"
+        reasons = sorted({name for s in sel for bit, name in self.REASON_BITS.items() if s[4] & bit})
+        return {"sm_mhz": statistics.median(s[1] for s in sel), "sm_max_mhz": max(s[2] for s in sel),
+                "sm_mhz_min": min(s[1] for s in sel), "power_w_max": max(s[3] for s in sel),
+                "reasons": reasons, "samples": len(sel), "samples_total": len(self.samples),
+                "window": where, "source": self.source}
+
+
+class L2Flush:
+    """Evicts the previous step's lines from L2 between timed steps: writes a
+    buffer twice the L2's size and, in mode "write+read", then reads another
+    buffer of that size, so that the written lines are back in HBM before
+    the timed region starts and no write-back of the flush lands inside it."""
+
+    def __init__(self, device, mode: str = "write+read"):
+        import torch
+        self.mode = mode
+        self.wbuf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.rbuf = torch.zeros(FLUSH_BYTES // 8, dtype=torch.int64, device=device) if mode == "write+read" else None
+
+    def __call__(self, i: int) -> None:
+        self.wbuf.fill_(i & 0xFF)
+        if self.rbuf is not None:
+            self.rbuf.amax()
+
+    def describe(self) -> str:
+        return flush_desc(self.mode)
+
+    @property
+    def launches(self) -> int:
+        return 2 if self.rbuf is not None else 1
 
 
 def cpu_sample(cfg, n_seqs: int):
     """The first n_seqs sequences of the workload (same length draws), on the host."""
     import synth.host as H
-    n_seqs = max(cfg.samples, n_seqs // cfg.samples * cfg.samples)
+    n_seqs = max(cfg.samples, min(n_seqs, cfg.num_seqs) // cfg.samples * cfg.samples)
     hw = H.generate(cfg, num_seqs=n_seqs)
     return hw, H.compact_pools(hw)
 
 
 def time_oracle(cfg, min_seconds: float, n_seqs: int, max_runs: int | None = None) -> dict:
-    n_seqs = max(cfg.samples, n_seqs // cfg.samples * cfg.samples)
     """The fp64 oracle, as it stands, on the host cores: one step (new rows
-    written, then attention) over a bounded sample of the workload."""
+    written, then attention) over a bounded sample of the workload, with one
+    thread per core of the affinity mask and then with a single thread (on a
+    quarter of the sample)."""
     import oracle
     import synth.host as H
     threads = len(os.sched_getaffinity(0))
-    hw, hp0 = cpu_sample(cfg, n_seqs)
-    nbytes = workload_bytes(hw.st)["step"]
-    times = []
-    t_start = time.perf_counter()
-    while True:
-        hp = H.HostPools(hp0.k_cache.copy(), hp0.v_cache.copy(), hp0.block_tables, hp0.slot_mapping,
-                         hp0.copy_pairs, hp0.ids, hp0.seqs, hp0.prefix_tables)
-        t0 = time.perf_counter()
-        oracle.decode_step(hp, hw, threads=threads)
-        times.append(time.perf_counter() - t0)
-        if time.perf_counter() - t_start >= min_seconds or (max_runs and len(times) >= max_runs):
-            break
-    mean = sum(times) / len(times)
-    return {"value": nbytes / mean / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": (f"first {n_seqs} of {cfg.num_seqs} sequences of the same workload "
-                       f"({int(hw.st.context_lens.sum())} tokens x {cfg.num_heads} heads), "
-                       f"{len(times)} run(s) of one step, {mean * 1e3:.1f} ms each"),
+
+    def timed(n, nthreads, seconds):
+        hw, hp0 = cpu_sample(cfg, n)
+        nbytes = workload_bytes(hw.st)["step"]
+        times = []
+        t_start = time.perf_counter()
+        while True:
+            hp = H.HostPools(hp0.k_cache.copy(), hp0.v_cache.copy(), hp0.block_tables, hp0.slot_mapping,
+                             hp0.copy_pairs, hp0.ids, hp0.seqs, hp0.prefix_tables)
+            t0 = time.perf_counter()
+            oracle.decode_step(hp, hw, threads=nthreads)
+            times.append(time.perf_counter() - t0)
+            if time.perf_counter() - t_start >= seconds or (max_runs and len(times) >= max_runs):
+                break
+        mean = sum(times) / len(times)
+        desc = (f"first {hw.st.num_seqs} of {cfg.num_seqs} sequences of the same workload "
+                f"({int(hw.st.context_lens.sum())} tokens x {cfg.num_heads} heads), "
+                f"{len(times)} run(s) of one step, {mean * 1e3:.1f} ms each")
+        return nbytes / mean / 1e9, mean, nbytes, desc
+
+    n_seqs = max(cfg.samples, min(n_seqs, cfg.num_seqs) // cfg.samples * cfg.samples)
+    value, mean, nbytes, desc = timed(n_seqs, threads, min_seconds)
+    n1 = max(cfg.samples, n_seqs // 4 // cfg.samples * cfg.samples)
+    v1, _, _, desc1 = timed(n1, 1, min_seconds / 2)
+    return {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
+            "single_thread": {"value": v1, "unit": "GB/s", "cores": 1, "sample": desc1},
             "ms_per_step": mean * 1e3, "bytes_per_step": nbytes}
 
 
@@ -374,7 +490,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         ws = pkv.new_workspace(B, H, D, mcl, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     out = torch.empty_like(dw.q)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, args.flush)
     stream = torch.cuda.current_stream(dev)
     has_copy, has_new = dw.copy_pairs.numel() > 0, dw.slot_mapping.numel() > 0
 
@@ -405,8 +521,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
 
     launches_per_step = int(has_copy) + int(has_new) + (3 if grouped else 1)  # grouped: prologue + two phases
 
+    clocks = ClockSampler(local_rank).__enter__()  # sampled from the warm-up on
     for _ in range(max(args.warmup, 3)):
-        flush.fill_(1)
+        flush(1)
         step()
     torch.cuda.synchronize()
     if int(err.item()) != 0:
@@ -419,19 +536,19 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clocks:
-        t_wall0 = time.perf_counter()
-        for i in range(K):
-            flush.fill_(i & 0xFF)        # evict the previous step's lines from L2
-            ev[i][0].record(stream)
-            cache_ops()
-            ev[i][1].record(stream)
-            attention()
-            ev[i][2].record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        wall = time.perf_counter() - t_wall0
+    t_wall0 = time.perf_counter()
+    for i in range(K):
+        flush(i)  # evict the previous step's lines from L2
+        ev[i][0].record(stream)
+        cache_ops()
+        ev[i][1].record(stream)
+        attention()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall0
+    clocks.mark_timed(t_wall0, t_wall0 + wall)
     step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / K
     decode_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     cache_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
@@ -452,7 +569,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_total = 0.0
     for i in range(e2e_steps + 3):
-        flush.fill_(i & 0xFF)
+        flush(i)
         if i >= 3:
             e0.record(stream)
         for h, d in zip(host_in, dev_in):
@@ -464,6 +581,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
             e1.synchronize()
             e2e_total += e0.elapsed_time(e1)
     e2e_ms = e2e_total / e2e_steps
+    clocks.__exit__(None, None, None)
 
     agg = aggregate({"step_ms": step_ms, "decode_ms": decode_ms, "cache_ms": cache_ms, "e2e_ms": e2e_ms},
                     world, device=dev if world > 1 else None)
@@ -482,7 +600,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
                                              fp8_scales=(FP8_SCALE, FP8_SCALE))
         else:
             cpu = time_oracle(cfg, args.cpu_seconds, args.cpu_seqs)
-            cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+            cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample", "single_thread")}
     line = {
         "metric": METRIC,
         "value": world * nbytes["step"] / (agg["step_ms"] * 1e-3) / 1e9,
@@ -491,7 +609,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         "ms_per_step": agg["step_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": f"{cfg.dtype} queries, fp8_e4m3 K/V" if fp8 else cfg.dtype, "data": "synthetic",
-        "config": config_json(cfg, st, world, args.attention, kv_desc),
+        "config": config_json(cfg, st, world, args.attention, kv_desc, args.flush),
         "seqs_per_s": world * B / (agg["step_ms"] * 1e-3),
         "attention_ms": agg["decode_ms"], "cache_ops_ms": agg["cache_ms"],
         "bytes_per_step": nbytes["step"], "roofline_frac_step": nbytes["step"] / (agg["step_ms"] * 1e-3) / 1e9 / peak,
@@ -625,7 +743,7 @@ def run_beam(args, rank: int, world: int, local_rank: int) -> int:
             name: torch.from_numpy(np.ascontiguousarray(getattr(plan, name))).to(dev)
             for name in ("slots", "copy_pairs", "block_tables", "context_lens", "group_start", "shared_blocks")}))
     ws = dec.workspace(H, D)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, args.flush)
     stream = torch.cuda.current_stream(dev)
 
     def device_step(dp, e_write=None):
@@ -637,8 +755,9 @@ def run_beam(args, rank: int, world: int, local_rank: int) -> int:
         pkv.paged_attention_decode_grouped(out, q, kc, vc, dp.block_tables, dp.context_lens, cfg.scale,
                                            dp.max_context_len, dp.group_start, dp.shared_blocks, ws, dev_err=err)
 
+    clocks = ClockSampler(local_rank).__enter__()  # sampled from the warm-up on
     for i in range(warm):
-        flush.fill_(1)
+        flush(1)
         device_step(dplans[i])
     torch.cuda.synchronize()
     if int(err.item()) != 0:
@@ -648,19 +767,19 @@ def run_beam(args, rank: int, world: int, local_rank: int) -> int:
         dist.barrier()
     torch.cuda.synchronize()
     launches = 0
-    with ClockSampler(local_rank) as clocks:
-        t_wall0 = time.perf_counter()
-        for i in range(K):
-            dp = dplans[warm + i]
-            flush.fill_(i & 0xFF)
-            ev[i][0].record(stream)
-            device_step(dp, ev[i][1])
-            ev[i][2].record(stream)
-            launches += (1 if dp.copy_pairs.numel() else 0) + 1 + 3  # grouped: prologue + two phases
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        wall = time.perf_counter() - t_wall0
+    t_wall0 = time.perf_counter()
+    for i in range(K):
+        dp = dplans[warm + i]
+        flush(i)
+        ev[i][0].record(stream)
+        device_step(dp, ev[i][1])
+        ev[i][2].record(stream)
+        launches += (1 if dp.copy_pairs.numel() else 0) + 1 + 3  # grouped: prologue + two phases
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall0
+    clocks.mark_timed(t_wall0, t_wall0 + wall)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item()):#x} in the timed region")
     step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / K
@@ -677,7 +796,7 @@ def run_beam(args, rank: int, world: int, local_rank: int) -> int:
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_bytes = 0
     for i in range(e2e_steps + 3):
-        flush.fill_(i & 0xFF)
+        flush(i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         plan = dec.plan(next(parents_of))
@@ -697,6 +816,7 @@ def run_beam(args, rank: int, world: int, local_rank: int) -> int:
                                                          "group_start", "shared_blocks"))
             h2d += sum(t.numel() * t.element_size() for t in (host_k, host_v, host_q))
     e2e_ms = e2e_total / e2e_steps * 1e3
+    clocks.__exit__(None, None, None)
     if int(err.item()) != 0:
         raise RuntimeError(f"device error word {int(err.item()):#x} in the end-to-end steps")
 
@@ -729,7 +849,7 @@ def run_beam(args, rank: int, world: int, local_rank: int) -> int:
                                 f"[{cfg.prompt[1]}, {cfg.prompt[2]}], parents drawn with rank weights (W-j)^2, "
                                 f"{cfg.num_blocks}-block pools, grouped attention (one group per request)"),
                    "global_batch": B, "parallelism": "single GPU" if world == 1 else f"{world} replicas",
-                   "l2": "flushed between timed steps (256 MiB write)", "seed": cfg.seed,
+                   "l2": flush.describe(), "seed": cfg.seed,
                    "copies_per_step": n_copies / (warm + K)},
         "seqs_per_s": world * B / (agg["step_ms"] * 1e-3),
         "attention_ms": agg["attn_ms"], "cache_ops_ms": agg["cache_ms"],
@@ -795,7 +915,7 @@ def run_prefill(args, rank: int, world: int, local_rank: int) -> int:
     uk, uv, q = randn(n, Hkv, D), randn(n, Hkv, D), randn(n, H, D)
     slots, bt, cl, qs = t(lay.user_slots), t(lay.block_tables), t(lay.context_lens), t(lay.query_start)
     out = torch.empty_like(q)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, args.flush)
     stream = torch.cuda.current_stream(dev)
 
     def write():
@@ -812,8 +932,9 @@ def run_prefill(args, rank: int, world: int, local_rank: int) -> int:
         visible += sum(L - nu + i + 1 for i in range(nu))
     flops = 4.0 * visible * H * D
     warm = max(args.warmup, 3)
+    clocks = ClockSampler(local_rank).__enter__()  # sampled from the warm-up on
     for _ in range(warm):
-        flush.fill_(1)
+        flush(1)
         write()
         attention()
     torch.cuda.synchronize()
@@ -826,19 +947,19 @@ def run_prefill(args, rank: int, world: int, local_rank: int) -> int:
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local_rank) as clocks:
-        t_wall0 = time.perf_counter()
-        for i in range(K):
-            flush.fill_(i & 0xFF)
-            ev[i][0].record(stream)
-            write()
-            ev[i][1].record(stream)
-            attention()
-            ev[i][2].record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            dist.barrier()
-        wall = time.perf_counter() - t_wall0
+    t_wall0 = time.perf_counter()
+    for i in range(K):
+        flush(i)
+        ev[i][0].record(stream)
+        write()
+        ev[i][1].record(stream)
+        attention()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall0
+    clocks.mark_timed(t_wall0, t_wall0 + wall)
     step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / K
     attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
@@ -850,7 +971,7 @@ def run_prefill(args, rank: int, world: int, local_rank: int) -> int:
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_steps, e2e_total = max(10, K // 4), 0.0
     for i in range(e2e_steps + 3):
-        flush.fill_(i & 0xFF)
+        flush(i)
         if i >= 3:
             e0.record(stream)
         for h_, d_ in zip(host, devs):
@@ -863,6 +984,7 @@ def run_prefill(args, rank: int, world: int, local_rank: int) -> int:
             e1.synchronize()
             e2e_total += e0.elapsed_time(e1)
     e2e_ms = e2e_total / e2e_steps
+    clocks.__exit__(None, None, None)
     agg = aggregate({"step_ms": step_ms, "attn_ms": attn_ms, "write_ms": write_ms, "e2e_ms": e2e_ms}, world,
                     device=dev if world > 1 else None)
     if rank != 0:
@@ -916,7 +1038,7 @@ def run_prefill(args, rank: int, world: int, local_rank: int) -> int:
                                 f"head_dim {D}, block_size {cfg.block_size}, {cfg.dtype} with fp32 accumulation, "
                                 f"{cfg.num_blocks}-block pools"),
                    "global_batch": n * world, "parallelism": "single GPU" if world == 1 else f"{world} replicas",
-                   "l2": "flushed between timed steps (256 MiB write)", "seed": cfg.seed},
+                   "l2": flush.describe(), "seed": cfg.seed},
         "tokens_per_s": world * n / (agg["step_ms"] * 1e-3),
         "attention_ms": agg["attn_ms"], "cache_write_ms": agg["write_ms"], "flops_per_step": flops,
         "roofline": {"bound": "tensor", "kernel": "pa_prefill_kernel (tcgen05.mma, TMEM accumulators, TMA-fed K/V)", "achieved": achieved,
@@ -950,6 +1072,10 @@ def main() -> int:
                     help="fp8: K/V pools of e4m3 codes with one scale per pool (plain attention)")
     ap.add_argument("--attention", choices=("plain", "grouped"), default="plain",
                     help="grouped: siblings read shared prefix blocks once (copy-on-write workloads)")
+    ap.add_argument("--flush", choices=("write+read", "write"), default="write+read",
+                    help="L2 flush between timed steps: write 256 MiB and then read another 256 MiB "
+                         "(default), or only write (its dirty lines are then written back inside the "
+                         "next timed kernel)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="minimum time of the CPU baseline")
     ap.add_argument("--cpu-seqs", type=int, default=32, help="sequences in the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
