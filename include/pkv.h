@@ -285,6 +285,10 @@ size_t pkv_decode_grouped_workspace_bytes(int num_seqs, int num_heads, int head_
  *  - The first call on a device looks up the array's device address once for
  *    that device (with that device current); make that first call before any
  *    stream capture begins.
+ *  - The address found then is kept for the life of the process. Do not use
+ *    this entry point on a device after cudaDeviceReset() (or any other
+ *    teardown of its primary context): the library's module is loaded again
+ *    there and the array may move, so the kept address would be stale.
  *  - Every call on a device shares the same array and leaves its last
  *    contents in it. Each call first clears the segment counters it needs
  *    (an asynchronous memset on `stream`; this happens even when the call

@@ -40,8 +40,9 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim) {
   return w;
 }
 
-// Grouped decode: grouping scratch and phase counters, piece counters, each
-// row's prefix result, then the warps' partial slots.
+// Grouped decode: the grouping flag, usable prefix per group and per
+// sequence, piece counters, each row's prefix result, then the warps'
+// partial slots.
 struct GroupedLayout {
   size_t flag = 0, group_S = 0, seq_P = 0, seg_ctr = 0, row_ml = 0, row_o = 0;
   size_t slot_ml = 0, slot_o = 0, total = 0;
@@ -51,9 +52,9 @@ GroupedLayout grouped_layout(int num_seqs, int num_heads, int head_dim, int num_
   GroupedLayout w;
   if (num_seqs <= 0 || num_heads <= 0 || head_dim <= 0 || num_groups <= 0) return w;
   const size_t rows = (size_t)num_seqs * num_heads;
-  const size_t slots = (size_t)pkv::kMaxDecodeWarps * 2 * pkv::kMaxGroupPerWarp;
+  const size_t slots = (size_t)pkv::kMaxDecodeWarps * 2 * pkv::kMaxPrefixRows;
   size_t off = 0;
-  w.flag = off;  // flag word, then the two phase counters
+  w.flag = off;  // flag word (1 = grouping rejected)
   off += 256;
   w.group_S = off;
   off += align_up((size_t)num_groups * 4, 256);
@@ -307,6 +308,7 @@ pkv_status pkv_paged_attention_prefill(void* out, const void* q, const void* k_c
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.num_blocks = num_blocks;
   p.dev_err = dev_err;
+  p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
   return launch_status(launch(p, max_query_len, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -335,6 +337,10 @@ pkv_status pkv_paged_attention_decode_grouped(void* out, const void* q, const vo
   const GroupedLayout ws = grouped_layout(num_seqs, num_heads, head_dim, num_groups);
   if (!workspace || workspace_bytes < ws.total) return PKV_ERR_WORKSPACE;
   if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
+  // 16-bit pools are read by TMA as rows of head_dim elements: the row index
+  // (one past the pool included) must fit in int32
+  if (dtype != PKV_F32 && (int64_t)num_blocks * num_kv_heads * block_size + 16 > 0x7fffffffLL)
+    return PKV_ERR_UNSUPPORTED;
 
   const int gpw = heads_per_warp(num_heads / num_kv_heads);
   const int gpw_index = gpw == 4 ? 2 : (gpw == 2 ? 1 : 0);
@@ -353,7 +359,6 @@ pkv_status pkv_paged_attention_decode_grouped(void* out, const void* q, const vo
   gp.shared_blocks = shared_blocks;
   gp.num_groups = num_groups;
   gp.ws_flag = reinterpret_cast<int32_t*>(wsb + ws.flag);
-  gp.ws_sync = reinterpret_cast<int32_t*>(wsb + ws.flag) + 1;
   gp.ws_group_S = reinterpret_cast<int32_t*>(wsb + ws.group_S);
   gp.ws_seq_P = reinterpret_cast<int32_t*>(wsb + ws.seq_P);
   gp.ws_seg_ctr = reinterpret_cast<int32_t*>(wsb + ws.seg_ctr);

@@ -590,7 +590,6 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
               for (int e = 0; e < DL; ++e) O[e] += __ldcg(po + e) * wt;
             }
             T* orow = static_cast<T*>(p.out) + (row0 + g) * D + lane * DL;
-#pragma unroll
             if constexpr (kQuant) {
               const float vs_l = p.v_scale / Ls;
 #pragma unroll

@@ -10,8 +10,8 @@
 // Work: the same persistent, balanced streaming as the plain kernel, over two
 // kinds of segments laid end to end:
 //   prefix segments (group g, head h, row group c): K/V rows [0, S_g) of the
-//     group's shared blocks against the query rows of up to kGroupRows
-//     siblings (head h of members 4c .. 4c+3);
+//     group's shared blocks against the query rows of up to prefix_rows<T>()
+//     siblings (head h of members R c .. R c + R - 1, R = prefix_rows<T>());
 //   tail segments (sequence s, head group hg): rows [S_g, L_s) of s's own
 //     blocks against its query heads, as in the plain kernel.
 // The prefix segments run first, balanced over all warps, then the tails,
@@ -29,11 +29,20 @@
 // wrong answer silently.
 #pragma once
 
+#include <cstring>
+#include <type_traits>
+
 #include "decode.cuh"
+#include "tc.cuh"
 
 namespace pkv {
 
-constexpr int kGroupRows = 4;  // query rows one warp serves against one K/V tile
+// Query rows one warp serves against each shared K/V tile of a prefix
+// segment: 16-bit data, the N = 8 columns of an m16n8k16 MMA whose M is the
+// tile's 16 tokens; fp32 data, 4 rows on CUDA cores.
+template <typename T>
+__host__ __device__ constexpr int prefix_rows() { return sizeof(T) == 2 ? 8 : 4; }
+constexpr int kMaxPrefixRows = 8;
 
 // The work split charges every segment a fixed cost, in tile units, on top of
 // its tiles: entering a segment (metadata, query rows) and finishing it
@@ -49,7 +58,6 @@ struct GroupedParams {
   const int32_t* shared_blocks;  // [num_groups]
   int num_groups;
   int32_t* ws_flag;     // [1] 1 = grouping rejected
-  int32_t* ws_sync;     // [2] reserved (unused)
   int32_t* ws_group_S;  // [num_groups] usable shared prefix tokens
   int32_t* ws_seq_P;    // [num_seqs] prefix tokens of the sequence's group
   int32_t* ws_seg_ctr;  // [2][num_seqs * num_heads] piece counters (prefix, tail)
@@ -67,6 +75,7 @@ __device__ __forceinline__ int warp_min(int v) {
 // (A template only so that every element-type unit owns its own copy.)
 template <typename T>
 __global__ void __launch_bounds__(256) pa_group_prologue_kernel(const GroupedParams gp) {
+  grid_launch_dependents();  // the prefix launch may start; it waits for these results
   const DecodeParams& p = gp.base;
   const int B = p.num_seqs, G = gp.num_groups, bs = p.block_size, MB = p.max_blocks_per_seq;
   const int cap = min(p.max_context_len, MB * bs);
@@ -142,6 +151,7 @@ struct GCtx {
   const int32_t* context_lens;
   int32_t* dev_err;
   int num_groups, num_seqs, num_heads, head_groups, group, cap, gpw;
+  int rows;  // query rows of a prefix segment
   bool use_groups;
 };
 
@@ -154,30 +164,30 @@ __device__ __forceinline__ int ctx_len(const GCtx& x, int s) {
   return L;
 }
 
-__device__ __forceinline__ int group_rows(int M) { return (M + kGroupRows - 1) / kGroupRows; }
+__device__ __forceinline__ int group_rows(int M, int rows) { return (M + rows - 1) / rows; }
 
 // Work units of group g's prefix segments: tiles plus the per-segment cost
 // (0 when the group has no usable shared prefix).
 __device__ __forceinline__ long long prefix_units(const GCtx& x, int g) {
   if (!x.use_groups) return 0;
   const int M = __ldg(x.group_start + g + 1) - __ldg(x.group_start + g);
-  const int S = x.group_S[g];
+  const int S = __ldcg(x.group_S + g);
   if (M < 2 || S <= 0) return 0;
-  return (long long)x.num_heads * group_rows(M) * (S / kTileTokens + kSegCostPrefix);
+  return (long long)x.num_heads * group_rows(M, x.rows) * (S / kTileTokens + kSegCostPrefix);
 }
 
-__device__ __forceinline__ int seq_prefix(const GCtx& x, int s) { return x.use_groups ? x.seq_P[s] : 0; }
+__device__ __forceinline__ int seq_prefix(const GCtx& x, int s) { return x.use_groups ? __ldcg(x.seq_P + s) : 0; }
 
 __device__ __forceinline__ void gseg_enter(GCursor& c, const GCtx& x) {
   if (c.part == 0) {
     c.lo = __ldg(x.group_start + c.a);
     c.M = __ldg(x.group_start + c.a + 1) - c.lo;
     c.tok0 = 0;
-    c.tok_end = x.group_S[c.a];
+    c.tok_end = __ldcg(x.group_S + c.a);
     c.sbt = c.lo;
     c.sbt_len = ctx_len(x, c.lo);
     c.kvh = c.b / x.group;
-    c.nrows = min(kGroupRows, c.M - kGroupRows * c.c);
+    c.nrows = min(x.rows, c.M - x.rows * c.c);
     c.nt = c.tok_end / kTileTokens;
   } else {
     const int L = ctx_len(x, c.a);
@@ -209,7 +219,7 @@ __device__ __forceinline__ void gseek_prefix(GCursor& c, const GCtx& x) {
 // Next segment (c.t is 0).
 __device__ __forceinline__ void gseg_next(GCursor& c, const GCtx& x) {
   if (c.part == 0) {
-    if (++c.c < group_rows(c.M)) {
+    if (++c.c < group_rows(c.M, x.rows)) {
       gseg_enter(c, x);
       return;
     }
@@ -240,43 +250,34 @@ __device__ __forceinline__ void gcursor_next(GCursor& c, const GCtx& x) {
 }
 
 // (sequence, head) of row r of the segment under c.
-__device__ __forceinline__ int row_seq(const GCursor& c, int r) { return c.part == 0 ? c.lo + kGroupRows * c.c + r : c.a; }
+__device__ __forceinline__ int row_seq(const GCursor& c, const GCtx& x, int r) {
+  return c.part == 0 ? c.lo + x.rows * c.c + r : c.a;
+}
 __device__ __forceinline__ int row_head(const GCursor& c, const GCtx& x, int r) {
   return c.part == 0 ? c.b : c.b * x.gpw + r;
 }
 
-// ---- tensor-core q.k for prefix tiles ---------------------------------------
-// m16n8k16 MMA with fp32 accumulation. Only query rows 0..7 are used, so the
-// A registers of rows 8..15 are zero. a_lo / a_hi hold row g's k-positions
-// 2t, 2t+1 and 2t+8, 2t+9; b_lo / b_hi the same k-positions of column g.
+// ---- tensor-core prefix tiles ------------------------------------------------
+// m16n8k16 MMA with fp32 accumulation, D += A B: A 16x16 (four registers of
+// 16-bit pairs), B 16x8 (two), D 16x8 (four fp32). Lane 4g + t holds
+// A rows g and g+8, k-pairs 2t and 2t+8; B column g, k-pairs 2t and 2t+8;
+// D rows g and g+8, columns 2t and 2t+1.
 template <typename T>
 struct Mma16816 {
   static constexpr bool kOk = false;
-  __device__ __forceinline__ static void run(float (&)[4], uint32_t, uint32_t, uint32_t, uint32_t) {}
-  __device__ __forceinline__ static void run2(float&, float&, uint32_t, uint32_t, uint32_t, uint32_t) {}
+  __device__ __forceinline__ static void run(float (&)[4], const uint32_t (&)[4], uint32_t, uint32_t) {}
   __device__ __forceinline__ static uint32_t pack(float, float) { return 0u; }
   __device__ __forceinline__ static float2 unpack(uint32_t) { return make_float2(0.f, 0.f); }
 };
 template <>
 struct Mma16816<__nv_bfloat16> {
   static constexpr bool kOk = true;
-  __device__ __forceinline__ static void run(float (&d)[4], uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
-                                             uint32_t b_hi) {
+  __device__ __forceinline__ static void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a_lo), "r"(0u), "r"(a_hi), "r"(0u), "r"(b_lo), "r"(b_hi));
-  }
-  // rows 0..7 only: accumulators of rows 8..15 are discarded
-  __device__ __forceinline__ static void run2(float& c0, float& c1, uint32_t a_lo, uint32_t a_hi,
-                                              uint32_t b_lo, uint32_t b_hi) {
-    [[maybe_unused]] float d2, d3;
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};"
-        : "=f"(c0), "=f"(c1), "=f"(d2), "=f"(d3)
-        : "r"(a_lo), "r"(0u), "r"(a_hi), "r"(0u), "r"(b_lo), "r"(b_hi), "f"(c0), "f"(c1), "f"(0.f), "f"(0.f));
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
   __device__ __forceinline__ static uint32_t pack(float x, float y) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
@@ -291,22 +292,12 @@ struct Mma16816<__nv_bfloat16> {
 template <>
 struct Mma16816<__half> {
   static constexpr bool kOk = true;
-  __device__ __forceinline__ static void run(float (&d)[4], uint32_t a_lo, uint32_t a_hi, uint32_t b_lo,
-                                             uint32_t b_hi) {
+  __device__ __forceinline__ static void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
         "{%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a_lo), "r"(0u), "r"(a_hi), "r"(0u), "r"(b_lo), "r"(b_hi));
-  }
-  __device__ __forceinline__ static void run2(float& c0, float& c1, uint32_t a_lo, uint32_t a_hi,
-                                              uint32_t b_lo, uint32_t b_hi) {
-    [[maybe_unused]] float d2, d3;
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};"
-        : "=f"(c0), "=f"(c1), "=f"(d2), "=f"(d3)
-        : "r"(a_lo), "r"(0u), "r"(a_hi), "r"(0u), "r"(b_lo), "r"(b_hi), "f"(c0), "f"(c1), "f"(0.f), "f"(0.f));
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
   }
   __device__ __forceinline__ static uint32_t pack(float x, float y) {
     const __half2 h = __floats2half2_rn(x, y);
@@ -329,103 +320,102 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
   return d;
 }
 
-// q.k is a sum over head dims, so any permutation of the dims applied to both
-// operands leaves it unchanged. Within each 32-dim chunk, lane t of an MMA
-// group feeds dims [8t, 8t+4) to k-step 0 and [8t+4, 8t+8) to k-step 1, so
-// its K operand for both k-steps of a chunk is one 16-byte shared-memory load
-// of one token row. The query operand uses the same mapping.
+// Shared-memory stage of the tensor-core prefix phase: the K and then the V
+// rows of one 16-token tile, each as D/64 column blocks of 16 rows x 128 bytes
+// with the 128-byte swizzle (16-byte chunk c of row r at position c ^ (r & 7)),
+// exactly as TMA boxes of {64 elements, up to 16 rows} land in 1024-byte
+// aligned memory; then the segment's query rows (plain, D elements each).
+template <int D>
+struct PrefixStage {
+  static constexpr int kColBytes = kTileTokens * 128;
+  static constexpr int kTensorBytes = (D / 64) * kColBytes;
+  static constexpr int kQOff = 2 * kTensorBytes;
+  static constexpr int kBytes = kQOff + kMaxPrefixRows * D * 2;
+  static_assert(kBytes % 1024 == 0, "stages stay 1024-byte aligned");
+};
 
-// One 16-token tile of a prefix segment, entirely on tensor cores. The query
-// rows (rows < nr of the MMA's M = 16; only rows 0..7 are ever used) are the
-// siblings' queries against one K/V tile.
-//   S = Q K^T: K operand from token rows, head dims permuted as above.
-//   Online softmax on the S accumulators: lane 4r + t holds row r, tokens
-//   2t, 2t+1, 2t+8, 2t+9, so a row's max and sum reduce over its 4 lanes.
-//   O += P V: the S accumulators are already P's A-operand layout (k =
-//   tokens). P is fed as a hi + lo pair of 16-bit values (two MMAs) so that
-//   it keeps ~16 significant bits; V's B operand comes from one 16-byte load
-//   per lane per 32-dim chunk and 16-token half, cut into four 8x8 blocks
-//   over a permutation of the head dims and transposed with movmatrix.
-//   Lane 4r + t ends up with row r, dims [32c + 8t, 32c + 8t + 8) of chunk c
-//   in po[c][0..3][0..1].
+// Byte offset of 16-byte chunk `ch` (0 .. D/8 - 1) of token row `tok` in a
+// swizzled K or V tile.
+__device__ __forceinline__ uint32_t sw_tile_off(int tok, int ch) {
+  return (uint32_t)((ch >> 3) * (kTileTokens * 128) + tok * 128 + (((ch & 7) ^ (tok & 7)) << 4));
+}
+
+// One 16-token tile of a prefix segment on tensor cores, with the tile's
+// tokens as the MMA's M and the segment's query rows (up to 8) as its N:
+//   S^T = K Q^T   (A = K rows from shared memory by ldmatrix; B = Q^T, the
+//                  query rows' fragments qb, fixed for the segment);
+//   online softmax of each query row (a column of S^T): lane 4g + t holds
+//     rows 2t and 2t+1 for tokens g and g+8, so a row's maximum reduces over
+//     the 8 lanes of equal t; the row sums stay per lane until the segment
+//     ends;
+//   O^T += V^T P^T (A = V^T by transposed ldmatrix of the V rows; B = P^T,
+//     the S^T accumulators as 16-bit pairs transposed by movmatrix). P goes
+//     in as a high and a low 16-bit part (two MMAs), so the probabilities
+//     keep about 16 significant bits.
+// acc[mb] holds O^T rows (head dims) 16 mb + g and 16 mb + g + 8 for query
+// rows 2t, 2t+1. Prefix tiles are always full (16 valid tokens).
 template <typename T, int D>
-__device__ __forceinline__ void mma_prefix_tile(const unsigned char* ks, const unsigned char* vs,
-                                                const uint32_t (&qa)[D / 32][2][2], float (&po)[D / 32][4][2],
-                                                float& pm, float& pl, int nvalid, float scale_log2) {
-  constexpr int ROW = D * (int)sizeof(T);
+__device__ __forceinline__ void mma_prefix_tile(uint32_t stage, const uint32_t (&qb)[D / 16][2],
+                                                float (&acc)[D / 16][4], float (&pm)[2], float (&pl)[2],
+                                                float scale_log2) {
+  using M = Mma16816<T>;
   const int lane = threadIdx.x & 31;
-  const int mg = lane >> 2, mt = lane & 3;
-  // two independent accumulator chains per 8-token half (first and second
-  // k-step of each chunk), added at the end: half the dependent MMA latency
-  float s[2][2][2];
+  // K: lane i addresses token (i & 7) + 8 ((i >> 3) & 1), chunk 2 ks + (i >> 4)
+  const int ktok = (lane & 7) + (((lane >> 3) & 1) << 3);
+  const int khi = lane >> 4;
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};  // even / odd k-steps
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int h = 0; h < 2; ++h) s[nt][h][0] = s[nt][h][1] = 0.f;
-#pragma unroll
-  for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const uint4 kk = *reinterpret_cast<const uint4*>(ks + (mg + 8 * nt) * ROW + c * 64 + mt * 16);
-      Mma16816<T>::run2(s[nt][0][0], s[nt][0][1], qa[c][0][0], qa[c][0][1], kk.x, kk.y);
-      Mma16816<T>::run2(s[nt][1][0], s[nt][1][1], qa[c][1][0], qa[c][1][1], kk.z, kk.w);
-    }
-  float xs[4], tmax = -INFINITY;
-#pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-    for (int e = 0; e < 2; ++e) xs[nt * 2 + e] = (s[nt][0][e] + s[nt][1][e]) * scale_log2;
-  if (nvalid < kTileTokens) {  // warp-uniform: only a segment's last tile can be partial
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      if ((i >> 1) * 8 + 2 * mt + (i & 1) >= nvalid) xs[i] = -INFINITY;
+  for (int ks = 0; ks < D / 16; ++ks) {
+    uint32_t a[4];
+    ldsm_x4(stage + sw_tile_off(ktok, 2 * ks + khi), a);
+    M::run((ks & 1) ? s1 : s0, a, qb[ks][0], qb[ks][1]);
   }
+  float x[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) tmax = fmaxf(tmax, xs[i]);
-  tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 1));
-  tmax = fmaxf(tmax, __shfl_xor_sync(kFullMask, tmax, 2));
-  const float mn = fmaxf(pm, tmax);
-  const float alpha = exp2f(pm - mn);  // 0 on the segment's first tile (pm = -inf)
-  float pe[4], psum = 0.f;
+  for (int i = 0; i < 4; ++i) x[i] = (s0[i] + s1[i]) * scale_log2;
+  float mt[2] = {fmaxf(x[0], x[2]), fmaxf(x[1], x[3])};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    pe[i] = exp2f(xs[i] - mn);
-    psum += pe[i];
+  for (int o = 4; o < 32; o <<= 1) {
+    mt[0] = fmaxf(mt[0], __shfl_xor_sync(kFullMask, mt[0], o));
+    mt[1] = fmaxf(mt[1], __shfl_xor_sync(kFullMask, mt[1], o));
   }
-  psum += __shfl_xor_sync(kFullMask, psum, 1);
-  psum += __shfl_xor_sync(kFullMask, psum, 2);
-  pl = pl * alpha + psum;
-  pm = mn;
+  float alpha[2];
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c)
+  for (int e = 0; e < 2; ++e) {
+    const float mn = fmaxf(pm[e], mt[e]);
+    alpha[e] = exp2f(pm[e] - mn);  // 0 on the segment's first tile (pm = -inf)
+    pm[e] = mn;
+  }
+  float pe[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      po[c][q][0] *= alpha;
-      po[c][q][1] *= alpha;
+  for (int i = 0; i < 4; ++i) pe[i] = exp2f(x[i] - pm[i & 1]);
+  pl[0] = pl[0] * alpha[0] + (pe[0] + pe[2]);
+  pl[1] = pl[1] * alpha[1] + (pe[1] + pe[3]);
+  if (!__all_sync(kFullMask, alpha[0] == 1.f && alpha[1] == 1.f)) {
+#pragma unroll
+    for (int mb = 0; mb < D / 16; ++mb) {
+      acc[mb][0] *= alpha[0];
+      acc[mb][1] *= alpha[1];
+      acc[mb][2] *= alpha[0];
+      acc[mb][3] *= alpha[1];
     }
-  // P (k = tokens 2t, 2t+1 | 2t+8, 2t+9) as hi + lo 16-bit pairs
-  const uint32_t hi0 = Mma16816<T>::pack(pe[0], pe[1]);
-  const uint32_t hi1 = Mma16816<T>::pack(pe[2], pe[3]);
-  const float2 h0 = Mma16816<T>::unpack(hi0), h1 = Mma16816<T>::unpack(hi1);
-  const uint32_t lo0 = Mma16816<T>::pack(pe[0] - h0.x, pe[1] - h0.y);
-  const uint32_t lo1 = Mma16816<T>::pack(pe[2] - h1.x, pe[3] - h1.y);
+  }
+  // P^T fragments: (token g | g+8) x (rows 2t, 2t+1) pairs, transposed
+  const uint32_t h0 = M::pack(pe[0], pe[1]), h1 = M::pack(pe[2], pe[3]);
+  const float2 u0 = M::unpack(h0), u1 = M::unpack(h1);
+  const uint32_t l0 = M::pack(pe[0] - u0.x, pe[1] - u0.y), l1 = M::pack(pe[2] - u1.x, pe[3] - u1.y);
+  const uint32_t bh0 = movmatrix_trans(h0), bh1 = movmatrix_trans(h1);
+  const uint32_t bl0 = movmatrix_trans(l0), bl1 = movmatrix_trans(l1);
+  // V: lane i addresses token (i & 7) + 8 (i >> 4), chunk 2 mb + ((i >> 3) & 1)
+  const int vtok = (lane & 7) + ((lane >> 4) << 3);
+  const int vhi = (lane >> 3) & 1;
+  const uint32_t vstage = stage + PrefixStage<D>::kTensorBytes;
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
-    uint4 v0 = *reinterpret_cast<const uint4*>(vs + mg * ROW + c * 64 + mt * 16);        // token mg
-    uint4 v1 = *reinterpret_cast<const uint4*>(vs + (mg + 8) * ROW + c * 64 + mt * 16);  // token mg + 8
-    if (nvalid < kTileTokens) {  // rows past the context may hold poison
-      if (mg >= nvalid) v0 = make_uint4(0u, 0u, 0u, 0u);
-      if (mg + 8 >= nvalid) v1 = make_uint4(0u, 0u, 0u, 0u);
-    }
-    const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
-    const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint32_t b_lo = movmatrix_trans(w0[q]);
-      const uint32_t b_hi = movmatrix_trans(w1[q]);
-      Mma16816<T>::run2(po[c][q][0], po[c][q][1], hi0, hi1, b_lo, b_hi);
-      Mma16816<T>::run2(po[c][q][0], po[c][q][1], lo0, lo1, b_lo, b_hi);
-    }
+  for (int mb = 0; mb < D / 16; ++mb) {
+    uint32_t a[4];
+    ldsm_x4_trans(vstage + sw_tile_off(vtok, 2 * mb + vhi), a);
+    M::run(acc[mb], a, bh0, bh1);
+    M::run(acc[mb], a, bl0, bl1);
   }
 }
 
@@ -519,18 +509,47 @@ __host__ __device__ constexpr int grouped_ring_budget() {
                                    : 200 * 1024);
 }
 
+// Shared memory of the tensor-core prefix phase (16-bit data): two
+// PrefixStage stages per warp from a 1024-byte aligned base, then the
+// warps' mbarriers, block-table chunks and the start-up scan's scratch.
+template <int D, int NW>
+struct PrefixShape {
+  static constexpr int kStages = 2;
+  static constexpr int kStageBytes = PrefixStage<D>::kBytes;
+  static constexpr int kBarOff = NW * kStages * kStageBytes;
+  static constexpr int kBtOff = kBarOff + NW * kStages * 8;
+  static constexpr int kScanOff = kBtOff + NW * kBtChunk * 4;
+  static constexpr int kSmemBytes = kScanOff + NW * 8 + 1024;  // + alignment of the base
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int kTileBytes = PrefixStage<D>::kTensorBytes;
+  static constexpr int kDimsPerLane = D / 8;
+  static constexpr int kChunksPerLane = kRowBytes / 16 / 8;
+  static constexpr int kVec = 8;
+};
+
+template <typename T, int D, int NW, int PH>
+using GroupedShape = typename std::conditional<Mma16816<T>::kOk && PH == 0, PrefixShape<D, NW>,
+                                               DecodeShape<T, D, kMaxGroupPerWarp, T, NW,
+                                                           grouped_ring_budget<T, D, NW>()>>::type;
+
 // One phase of the grouped decode over persistent warps: PH = 0 runs every
 // prefix segment, PH = 1 every tail segment, each balanced over all warps.
 // The two phases are two launches in stream order, so the tail phase sees
 // every prefix result (and the partial slots the prefix phase used are free);
 // the tail launch may start early (programmatic dependent launch) and waits
 // for the prefix grid right after issuing its first K/V copies.
+// The prefix phase of 16-bit data loads K/V tiles by TMA (kmap, vmap: the
+// pools as rows of head_dim elements, boxes of {64, min(block_size, 16)}
+// rows, 128-byte swizzle) and runs them on tensor cores; the tail phase and
+// fp32 data use 1-D bulk copies (the maps are then unused).
 template <typename T, int D, int TG, int PH, int NW>
 __global__ void __launch_bounds__(NW * 32)
-    pa_decode_grouped_kernel(const GroupedParams gp) {
-  using S = DecodeShape<T, D, kGroupRows, T, NW, grouped_ring_budget<T, D, NW>()>;
-  constexpr int R = kGroupRows;
+    pa_decode_grouped_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                             const GroupedParams gp) {
+  using S = GroupedShape<T, D, NW, PH>;
+  constexpr int R = prefix_rows<T>();
   constexpr bool kMma = Mma16816<T>::kOk;
+  constexpr bool kTma = kMma && PH == 0;  // tensor-core prefix tiles, TMA-fed
   constexpr int QR = kMma ? TG : R;  // query rows kept in fp32 registers
   constexpr int OR = kMma ? TG : R;  // rows of the CUDA-core accumulators
   constexpr int ST = S::kStages;
@@ -541,7 +560,8 @@ __global__ void __launch_bounds__(NW * 32)
   constexpr int DL = D / 32;  // dims per lane in merges
   const DecodeParams& p = gp.base;
 
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = kTma ? smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) : smem_raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
   long long* scan = reinterpret_cast<long long*>(smem + S::kScanOff);
   __shared__ longlong2 starts[NW];  // (group or sequence, offset) of each warp's first unit
@@ -565,6 +585,11 @@ __global__ void __launch_bounds__(NW * 32)
   x.group = p.group;
   x.cap = min(p.max_context_len, p.max_blocks_per_seq * bs);
   x.gpw = p.num_heads / p.head_groups;
+  x.rows = R;
+  // the prefix launch is a programmatic dependent of the grouping check:
+  // wait for its results (the tail launch may read them at once: its primary,
+  // the prefix grid, started its work only after the check completed)
+  if constexpr (PH == 0) grid_dependency_wait();
   x.use_groups = __ldcg(gp.ws_flag) == 0;
   const int B = p.num_seqs, G = gp.num_groups, HG = p.head_groups, H = p.num_heads;
 
@@ -626,10 +651,13 @@ __global__ void __launch_bounds__(NW * 32)
   int ring = 0;  // tiles this warp has consumed so far (ring position)
 
   float qf[QR][DPL];
-  uint32_t qa[D / 32][2][2];        // prefix query rows as MMA A-operands (16-bit types)
   float m[OR], l[OR], o[OR][DPL];   // CUDA-core state (tails; prefixes of fp32 data)
-  float pm = -INFINITY, pl = 0.f;   // tensor-core state of a prefix: row mg
-  float po[D / 32][4][2];
+  // tensor-core state of a prefix segment (see mma_prefix_tile): query rows
+  // as B fragments, O^T accumulators, running max and per-lane row sums of
+  // rows 2t and 2t+1
+  uint32_t qb[D / 16][2];
+  float acc[D / 16][4];
+  float tm[2] = {-INFINITY, -INFINITY}, tl[2] = {0.f, 0.f};
 
   {
     constexpr int phase = PH;
@@ -652,8 +680,8 @@ __global__ void __launch_bounds__(NW * 32)
         ci.t = r < 0 ? 0 : r;  // a range that starts on charged units starts at tile 0
         ci.g = a_begin + (ci.t - r);
         if (phase == 0) {
-          ci.b = static_cast<int>(seg_idx / group_rows(ci.M));
-          ci.c = static_cast<int>(seg_idx % group_rows(ci.M));
+          ci.b = static_cast<int>(seg_idx / group_rows(ci.M, R));
+          ci.c = static_cast<int>(seg_idx % group_rows(ci.M, R));
         } else {
           ci.b = static_cast<int>(seg_idx);
         }
@@ -692,7 +720,31 @@ __global__ void __launch_bounds__(NW * 32)
             bt_j0 = j_first;
           }
         }
-        if (lane == 0) {
+        if constexpr (kTma) {
+          // prefix tiles are whole (the usable prefix is cut to whole tiles):
+          // the K and V rows as TMA boxes of {64 dims, rb rows} into the
+          // swizzled stage, from parallel lanes; the query rows by lane 0
+          unsigned char* st = my_ring + (n % ST) * S::kStageBytes;
+          uint64_t* bar = my_bars + (n % ST);
+          if (lane == 0) mbar_arrive_expect_tx(bar, 2u * kTileTokens * ROW + (with_q ? c.nrows * ROW : 0u));
+          __syncwarp();
+          const int rb = bs < kTileTokens ? bs : kTileTokens;
+          constexpr int CB = D / 64;
+          const int per = (kTileTokens / rb) * CB;  // boxes per tensor
+          if (lane < 2 * per) {
+            const int tsr = lane / per, rem = lane - tsr * per;
+            const int b = rem / CB, cb = rem - b * CB;
+            const int t = t0 + b * rb;
+            const int y = (my_bt[t / bs - bt_j0] * p.num_kv_heads + c.kvh) * bs + (t % bs);
+            tma_load_2d(st + tsr * PrefixStage<D>::kTensorBytes + cb * PrefixStage<D>::kColBytes + b * rb * 128,
+                        tsr ? &vmap : &kmap, cb * 64, y, bar);
+          }
+          if (with_q && lane == 0) {
+            for (int r = 0; r < c.nrows; ++r)
+              bulk_copy_g2s(st + PrefixStage<D>::kQOff + r * ROW,
+                            qbase + ((size_t)row_seq(c, x, r) * H + c.b) * ROW, ROW, bar);
+          }
+        } else if (lane == 0) {
           unsigned char* kdst = my_ring + (n % ST) * S::kStageBytes;
           unsigned char* vdst = kdst + S::kTileBytes;
           unsigned char* qdst = kdst + 2 * S::kTileBytes;
@@ -714,7 +766,7 @@ __global__ void __launch_bounds__(NW * 32)
               bulk_copy_g2s(qdst, qbase + ((size_t)c.a * H + (size_t)c.b * c.nrows) * ROW, c.nrows * ROW, bar);
             } else {
               for (int r = 0; r < c.nrows; ++r)
-                bulk_copy_g2s(qdst + r * ROW, qbase + ((size_t)row_seq(c, r) * H + c.b) * ROW, ROW, bar);
+                bulk_copy_g2s(qdst + r * ROW, qbase + ((size_t)row_seq(c, x, r) * H + c.b) * ROW, ROW, bar);
             }
           }
         }
@@ -727,7 +779,7 @@ __global__ void __launch_bounds__(NW * 32)
       }
       // the tail phase reads prefix results and reuses the partial slots:
       // wait for the prefix grid (its first K/V copies are already in flight)
-      if constexpr (PH == 1) asm volatile("griddepcontrol.wait;" ::: "memory");
+      if constexpr (PH == 1) grid_dependency_wait();
       bool visit_from_start = true;
 
       for (; cc.g < a_end; ++ring) {
@@ -744,16 +796,15 @@ __global__ void __launch_bounds__(NW * 32)
         const bool first = cc.t == 0 || cc.g == g_first;
         const bool last = cc.t == cc.nt - 1 || cc.g == a_end - 1;
         const int nr = cc.nrows;
-        const bool tc_prefix = kMma && phase == 0;  // state in the tensor-core layout
 
         if (first) {
           visit_from_start = cc.t == 0;
-          pm = -INFINITY;
-          pl = 0.f;
+          if constexpr (kTma) {
+            tm[0] = tm[1] = -INFINITY;
+            tl[0] = tl[1] = 0.f;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) po[c][q][0] = po[c][q][1] = 0.f;
+            for (int mb = 0; mb < D / 16; ++mb) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.f;
+          }
 #pragma unroll
           for (int g = 0; g < OR; ++g) {
             m[g] = -INFINITY;
@@ -762,17 +813,16 @@ __global__ void __launch_bounds__(NW * 32)
             for (int e = 0; e < DPL; ++e) o[g][e] = 0.f;
           }
           if (nvalid > 0) {
-            const unsigned char* qs = ks + 2 * S::kTileBytes;
-            if (tc_prefix) {
+            const unsigned char* qs = ks + (kTma ? PrefixStage<D>::kQOff : 2 * S::kTileBytes);
+            if constexpr (kTma) {
+              // B fragments of Q^T: lane 4g + t holds query row g, dims
+              // 16 ks + 2t, +1 and 16 ks + 2t + 8, +9 (rows past nr: zero)
+              const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qs + mg * ROW);
 #pragma unroll
-              for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                  const int d0 = c * 32 + 8 * mt + 4 * j;  // dims d0, d0+1 | d0+2, d0+3 (see Mma16816)
-                  const uint32_t* qrow = reinterpret_cast<const uint32_t*>(qs + mg * ROW);
-                  qa[c][j][0] = mg < nr ? qrow[d0 / 2] : 0u;
-                  qa[c][j][1] = mg < nr ? qrow[d0 / 2 + 1] : 0u;
-                }
+              for (int ks2 = 0; ks2 < D / 16; ++ks2) {
+                qb[ks2][0] = mg < nr ? qrow[8 * ks2 + mt] : 0u;
+                qb[ks2][1] = mg < nr ? qrow[8 * ks2 + mt + 4] : 0u;
+              }
             } else {
 #pragma unroll
               for (int g = 0; g < QR; ++g) {
@@ -794,8 +844,8 @@ __global__ void __launch_bounds__(NW * 32)
         if (nvalid > 0) {
           if (phase == 1) {
             core_tile<T, D, QR, TG, false, OR>(ks, vs, qf, o, m, l, nvalid, TG);
-          } else if constexpr (kMma) {
-            mma_prefix_tile<T, D>(ks, vs, qa, po, pm, pl, nvalid, p.scale_log2);
+          } else if constexpr (kTma) {
+            mma_prefix_tile<T, D>(smem_u32(ks), qb, acc, tm, tl, p.scale_log2);
           } else {
             core_tile<T, D, QR, R, true, OR>(ks, vs, qf, o, m, l, nvalid, nr);
           }
@@ -810,7 +860,7 @@ __global__ void __launch_bounds__(NW * 32)
           // ---- end of this warp's visit of the segment under cc --------------
 #pragma unroll
           for (int g = 0; g < OR; ++g)
-            if (!tc_prefix && g < nr) {
+            if (!kTma && g < nr) {
               l[g] += __shfl_xor_sync(kFullMask, l[g], 8);
               l[g] += __shfl_xor_sync(kFullMask, l[g], 16);
 #pragma unroll
@@ -822,26 +872,42 @@ __global__ void __launch_bounds__(NW * 32)
           // phase 1 rows of a sequence with a shared prefix merge with its result
           const bool with_prefix = phase == 1 && cc.tok0 > 0;
           const bool whole = visit_from_start && cc.t == cc.nt - 1;
-          if (whole && tc_prefix) {
-            // prefix result of each sibling row (rows are quads of lanes)
-            if (mg < nr) {
-              const size_t row = (size_t)row_seq(cc, mg) * H + row_head(cc, x, mg);
-              const float inv = 1.f / pl;
-              float4* dst = reinterpret_cast<float4*>(gp.ws_row_o + row * D);
+          if constexpr (kTma) {
+            // row sums: per-lane shares of rows 2t, 2t+1 over the 8 lanes of equal t
 #pragma unroll
-              for (int c = 0; c < D / 32; ++c) {
-                dst[(c * 32 + 8 * mt) / 4] = make_float4(po[c][0][0] * inv, po[c][0][1] * inv,
-                                                         po[c][1][0] * inv, po[c][1][1] * inv);
-                dst[(c * 32 + 8 * mt) / 4 + 1] = make_float4(po[c][2][0] * inv, po[c][2][1] * inv,
-                                                             po[c][3][0] * inv, po[c][3][1] * inv);
-              }
-              if (mt == 0) gp.ws_row_ml[row] = make_float2(pm, pl);
+            for (int e = 0; e < 2; ++e) {
+              tl[e] += __shfl_xor_sync(kFullMask, tl[e], 4);
+              tl[e] += __shfl_xor_sync(kFullMask, tl[e], 8);
+              tl[e] += __shfl_xor_sync(kFullMask, tl[e], 16);
             }
+          }
+          // (m, l, o / l) of query rows 2t and 2t+1 of a tensor-core prefix
+          // segment: into the rows' prefix results, or into partial slot `base`
+          auto store_tc_rows = [&](bool prefix_result, size_t base) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int r = 2 * mt + e;
+              if (r < nr) {
+                const size_t dst = prefix_result ? (size_t)row_seq(cc, x, r) * H + row_head(cc, x, r) : base + r;
+                float2* ml = prefix_result ? gp.ws_row_ml : p.ws_ml;
+                float* orow = (prefix_result ? gp.ws_row_o : p.ws_o) + dst * D + mg;
+                const float inv = 1.f / tl[e];
+#pragma unroll
+                for (int mb = 0; mb < D / 16; ++mb) {
+                  orow[16 * mb] = acc[mb][e] * inv;
+                  orow[16 * mb + 8] = acc[mb][e + 2] * inv;
+                }
+                if (mg == 0) ml[dst] = make_float2(tm[e], tl[e]);
+              }
+            }
+          };
+          if (whole && kTma) {
+            store_tc_rows(true, 0);  // the prefix result of each sibling row
           } else if (whole) {
 #pragma unroll
             for (int g = 0; g < OR; ++g) {
               if (g >= nr) continue;
-              const size_t row = (size_t)row_seq(cc, g) * H + row_head(cc, x, g);
+              const size_t row = (size_t)row_seq(cc, x, g) * H + row_head(cc, x, g);
               if (phase == 0) {  // prefix result (fp32 data)
                 const float inv = 1.f / l[g];
                 if (grp == 0) {
@@ -888,19 +954,8 @@ __global__ void __launch_bounds__(NW * 32)
             // in this segment, charged units included); slot 1: its last piece
             const int slot = cc.g - cc.t - E <= a_begin ? 0 : 1;
             const size_t base = ((size_t)wid * 2 + slot) * R;
-            if (tc_prefix) {
-              if (mg < nr) {
-                const float inv = 1.f / pl;
-                float4* dst = reinterpret_cast<float4*>(p.ws_o + (base + mg) * D);
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                  dst[(c * 32 + 8 * mt) / 4] = make_float4(po[c][0][0] * inv, po[c][0][1] * inv,
-                                                           po[c][1][0] * inv, po[c][1][1] * inv);
-                  dst[(c * 32 + 8 * mt) / 4 + 1] = make_float4(po[c][2][0] * inv, po[c][2][1] * inv,
-                                                               po[c][3][0] * inv, po[c][3][1] * inv);
-                }
-                if (mt == 0) p.ws_ml[base + mg] = make_float2(pm, pl);
-              }
+            if constexpr (kTma) {
+              store_tc_rows(false, base);
             } else {
 #pragma unroll
               for (int g = 0; g < OR; ++g) {
@@ -927,7 +982,7 @@ __global__ void __launch_bounds__(NW * 32)
             const long long w_last = (seg_end * Wq + Tq - 1) / Tq - 1;
             int is_last = 0;
             if (lane == 0) {
-              const size_t ci_idx = phase == 0 ? (size_t)(cc.lo + kGroupRows * cc.c) * H + cc.b
+              const size_t ci_idx = phase == 0 ? (size_t)(cc.lo + R * cc.c) * H + cc.b
                                                : (size_t)B * H + (size_t)cc.a * HG + cc.b;
               int32_t* ctr = gp.ws_seg_ctr + ci_idx;
               const int prev = atomic_add_acq_rel_gpu(ctr, 1);
@@ -938,7 +993,7 @@ __global__ void __launch_bounds__(NW * 32)
             if (is_last) {
               __syncwarp();  // the other pieces' partials, acquired by lane 0, are visible to all lanes
               for (int g = 0; g < nr; ++g) {
-                const size_t row = (size_t)row_seq(cc, g) * H + row_head(cc, x, g);
+                const size_t row = (size_t)row_seq(cc, x, g) * H + row_head(cc, x, g);
                 float M = -INFINITY;
                 for (long long w = w_first; w <= w_last; ++w) {
                   const int sl = (w == w_first && w * Tq / Wq < seg_units0) ? 1 : 0;
@@ -992,7 +1047,7 @@ __global__ void __launch_bounds__(NW * 32)
 // Persistent grid of one phase kernel on the current device (cached).
 template <typename T, int D, int TG, int PH, int NW>
 cudaError_t grouped_grid(int& grid) {
-  using S = DecodeShape<T, D, kGroupRows, T, NW, grouped_ring_budget<T, D, NW>()>;
+  using S = GroupedShape<T, D, NW, PH>;
   static int grid_of_device[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1020,40 +1075,59 @@ cudaError_t grouped_grid(int& grid) {
 template <typename T, int PH>
 __host__ __device__ constexpr int grouped_warps() { return sizeof(T) == 2 && PH == 1 ? 12 : kDecodeWarps; }
 
-// Validation prologue, the prefix phase, then the tail phase (launched as a
-// programmatic dependent of the prefix phase, so its start-up overlaps the
-// prefix phase's last blocks).
-template <typename T, int D, int TG>
-cudaError_t launch_pa_decode_grouped(const GroupedParams& gp, cudaStream_t stream) {
-  constexpr int NW0 = grouped_warps<T, 0>(), NW1 = grouped_warps<T, 1>();
-  using S0 = DecodeShape<T, D, kGroupRows, T, NW0, grouped_ring_budget<T, D, NW0>()>;
-  using S1 = DecodeShape<T, D, kGroupRows, T, NW1, grouped_ring_budget<T, D, NW1>()>;
-  int grid0 = 0, grid1 = 0;
-  cudaError_t e = grouped_grid<T, D, TG, 0, NW0>(grid0);
-  if (e != cudaSuccess) return e;
-  e = grouped_grid<T, D, TG, 1, NW1>(grid1);
-  if (e != cudaSuccess) return e;
-  int pro = (gp.num_groups + 7) / 8;
-  pro = pro < 1 ? 1 : (pro > 4096 ? 4096 : pro);
-  pa_group_prologue_kernel<T><<<pro, 256, 0, stream>>>(gp);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  pa_decode_grouped_kernel<T, D, TG, 0, NW0><<<grid0, NW0 * 32, S0::kSmemBytes, stream>>>(gp);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+// Launch of a phase kernel as a programmatic dependent of the kernel before
+// it in the stream: its launch overlaps that kernel, and it waits for that
+// kernel's results at griddepcontrol.wait.
+template <typename T, int D, int TG, int PH, int NW>
+cudaError_t launch_phase(int grid, const CUtensorMap& kmap, const CUtensorMap& vmap, const GroupedParams& gp,
+                         cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid1);
-  cfg.blockDim = dim3(NW1 * 32);
-  cfg.dynamicSmemBytes = S1::kSmemBytes;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = GroupedShape<T, D, NW, PH>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, pa_decode_grouped_kernel<T, D, TG, 1, NW1>, gp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, pa_decode_grouped_kernel<T, D, TG, PH, NW>, kmap, vmap, gp);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// Validation prologue, then the prefix phase and the tail phase, each
+// launched as a programmatic dependent of the launch before it. For 16-bit
+// data the pools' tensor maps (boxes of {64, min(block_size, 16)} rows) feed
+// the prefix phase's TMA loads.
+template <typename T, int D, int TG>
+cudaError_t launch_pa_decode_grouped(const GroupedParams& gp, cudaStream_t stream) {
+  constexpr int NW0 = grouped_warps<T, 0>(), NW1 = grouped_warps<T, 1>();
+  int grid0 = 0, grid1 = 0;
+  cudaError_t e = grouped_grid<T, D, TG, 0, NW0>(grid0);
   if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  e = grouped_grid<T, D, TG, 1, NW1>(grid1);
+  if (e != cudaSuccess) return e;
+  CUtensorMap kmap, vmap;
+  memset(&kmap, 0, sizeof(kmap));
+  memset(&vmap, 0, sizeof(vmap));
+  if constexpr (Mma16816<T>::kOk) {
+    const DecodeParams& p = gp.base;
+    const uint64_t rows = (uint64_t)p.num_blocks * p.num_kv_heads * p.block_size;
+    const int box_rows = p.block_size < kTileTokens ? p.block_size : kTileTokens;
+    const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
+    e = encode_pool_rows_map(&kmap, p.k_cache, rows, D, box_rows, bf16);
+    if (e != cudaSuccess) return e;
+    e = encode_pool_rows_map(&vmap, p.v_cache, rows, D, box_rows, bf16);
+    if (e != cudaSuccess) return e;
+  }
+  int pro = (gp.num_groups + 7) / 8;
+  pro = pro < 1 ? 1 : (pro > 4096 ? 4096 : pro);
+  pa_group_prologue_kernel<T><<<pro, 256, 0, stream>>>(gp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = launch_phase<T, D, TG, 0, NW0>(grid0, kmap, vmap, gp, stream);
+  if (e != cudaSuccess) return e;
+  return launch_phase<T, D, TG, 1, NW1>(grid1, kmap, vmap, gp, stream);
 }
 
 using GroupedLauncher = cudaError_t (*)(const GroupedParams&, cudaStream_t);

@@ -34,7 +34,6 @@ constexpr int kPfThreads = 320;         // + 1 MMA warp + 1 TMA warp
 constexpr int kPfStages = 2;            // K and V tiles in flight
 constexpr uint32_t kPfTmemCols = 256;   // two S/P buffers (64 columns each) + O (up to 128)
 constexpr float kPfRescaleLog2 = 8.f;   // base of the running max moves only when it grows by more
-constexpr uint64_t kPfWaitNs = 2000000000ull;  // limit of every wait of the kernel
 
 struct PrefillParams {
   void* out;
@@ -47,6 +46,7 @@ struct PrefillParams {
   float scale_log2;  // scale * log2(e)
   int num_seqs, num_heads, num_kv_heads, group, block_size, max_blocks_per_seq, num_blocks;
   int32_t* dev_err;
+  uint64_t wait_limit_ns;  // limit of every wait on another role's progress
 };
 
 // 16-bit packing of two fp32 values (round to nearest) and its exact inverse.
@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   uint64_t* o_done = bars + 12;  // one phase per tile's O MMAs, all tiles but the last
   uint64_t* o_last = bars + 13;  // the last tile's O MMAs: every MMA of the CTA done (one phase)
   uint64_t* q_full = bars + 14;  // Q rows landed (one arrival per loading thread)
+  uint64_t* drained = bars + 15; // every MMA the issuing thread started has completed (tear-down)
   uint32_t* slot = reinterpret_cast<uint32_t*>(sm + S::kSlotOff);
 
   // blocks launch in x order: every (sequence, head)'s last query tile (the
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     cp_async_commit();
   }
   if (tid == 0) {
-    for (int i = 0; i < 15; ++i) mbar_init(&bars[i], (i == 10 || i == 11) ? kPfSoftThreads : (i == 14 ? kPfRows : 1));
+    for (int i = 0; i < 16; ++i) mbar_init(&bars[i], (i == 10 || i == 11) ? kPfSoftThreads : (i == 14 ? kPfRows : 1));
     mbar_init_fence();
   }
   if (warp == 0) tmem_alloc(slot, kPfTmemCols);
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       if (lane == 0) {
         const uint64_t now = globaltimer_ns();
         if (t_last == 0) t_last = now;
-        if (now - t_last >= kPfWaitNs) {
+        if (now - t_last >= p.wait_limit_ns) {
           ok = false;
         } else if (kj < ntiles && kj <= vj + 1) {
           mbar_try_wait(&empty_k[kj & 1], ((kj >> 1) + 1) & 1);
@@ -296,6 +297,23 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       if (!ok) break;
     }
     if (!ok && lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+    // Every box this warp issued must land before the CTA can leave (its
+    // shared memory would otherwise be written after exit). Per stage only
+    // the latest tile's phase can still be open: a stage is reissued only
+    // after its previous tile was consumed, which needed that tile's bytes.
+    if (lane == 0) {
+      for (int st = 0; st < kPfStages; ++st) {
+        if (kj > st) {
+          const int j = st + kPfStages * ((kj - 1 - st) / kPfStages);
+          mbar_wait_bounded(&full_k[st], (j >> 1) & 1, kDrainLimitNs);
+        }
+        if (vj > st) {
+          const int j = st + kPfStages * ((vj - 1 - st) / kPfStages);
+          mbar_wait_bounded(&full_v[st], (j >> 1) & 1, kDrainLimitNs);
+        }
+      }
+    }
+    __syncwarp();
   } else if (warp == 8) {
     // ---- MMA issue ------------------------------------------------------------
     if (lane == 0) {
@@ -311,7 +329,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       const uint64_t v_desc1 = smem_desc_sw128(smem_u32(sm + S::kVOff + S::kTileBytes), S::kColBlock, 1024);
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
-        if (!mbar_wait_bounded(&full_k[st], (j >> 1) & 1, kPfWaitNs)) return false;
+        if (!mbar_wait_bounded(&full_k[st], (j >> 1) & 1, p.wait_limit_ns)) return false;
         tc_fence_after();
         const uint64_t kd = st ? k_desc1 : k_desc0;
 #pragma unroll
@@ -325,7 +343,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         return true;
       };
       // Q (loaded by the first four warps) before the first S
-      bool ok = mbar_wait_bounded(q_full, 0, kPfWaitNs);
+      bool ok = mbar_wait_bounded(q_full, 0, p.wait_limit_ns);
       if (ok) {
         tc_fence_after();
         ok = issue_s(0);
@@ -336,8 +354,8 @@ __global__ void __launch_bounds__(kPfThreads, 2)
           ok = false;
           break;
         }
-        if (!mbar_wait_bounded(&p_full[b], (j >> 1) & 1, kPfWaitNs) ||
-            !mbar_wait_bounded(&full_v[b], (j >> 1) & 1, kPfWaitNs)) {
+        if (!mbar_wait_bounded(&p_full[b], (j >> 1) & 1, p.wait_limit_ns) ||
+            !mbar_wait_bounded(&full_v[b], (j >> 1) & 1, p.wait_limit_ns)) {
           ok = false;
           break;
         }
@@ -356,7 +374,13 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         if (j + 2 < ntiles) mma_commit(&empty_v[b]);
       }
       if (!ok) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+      // A commit tracks every MMA this thread issued before it: once it
+      // arrives, nothing of the CTA reads shared memory or writes tensor
+      // memory any more (after a timeout, MMAs may still be running here).
+      mma_commit(drained);
+      mbar_wait_bounded(drained, 0, kDrainLimitNs);
     }
+    __syncwarp();
   } else {
     // ---- softmax and output --------------------------------------------------
     // Warp w owns query rows 32 (w % 4) .. +31 (its tensor-memory lane
@@ -387,7 +411,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       float pm = -INFINITY;
       // every wait is made warp-uniform before the warp-collective
       // tensor-memory loads and stores that follow it
-      if (__all_sync(kFullMask, !bad && mbar_wait_bounded(&s_full[b], par, kPfWaitNs))) {
+      if (__all_sync(kFullMask, !bad && mbar_wait_bounded(&s_full[b], par, p.wait_limit_ns))) {
         tc_fence_after();
         uint32_t u[32];
         tmem_ld32(tbase + lane_base + 64 * b + 32 * ch, u);
@@ -427,7 +451,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         // O holds the previous tiles' sums on the old base: rescale this
         // warp's half of its columns once their MMAs are done (S_j
         // completing implies those of tile j-2)
-        if (__all_sync(kFullMask, mbar_wait_bounded(o_done, (j - 1) & 1, kPfWaitNs))) {
+        if (__all_sync(kFullMask, mbar_wait_bounded(o_done, (j - 1) & 1, p.wait_limit_ns))) {
           tc_fence_after();
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -463,7 +487,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
       if (j == ntiles - 1 && kv_end < j * kPfTokens + kPfTokens) {
         // V rows past the context may hold anything (a NaN would survive a
         // zero probability): zero them once the tile has landed
-        if (__all_sync(kFullMask, mbar_wait_bounded(&full_v[b], par, kPfWaitNs))) {
+        if (__all_sync(kFullMask, mbar_wait_bounded(&full_v[b], par, p.wait_limit_ns))) {
           const int z0 = kv_end - j * kPfTokens, per_row = S::kBlocksD * 8;
           unsigned char* vd = sm + S::kVOff + b * S::kTileBytes;
           for (int i = tid; i < (kPfTokens - z0) * per_row; i += kPfSoftThreads) {
@@ -481,7 +505,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     }
     lx[ch * kPfRows + r] = l;
     bad = barrier_or(1, kPfSoftThreads, bad);
-    if (!bad && !__all_sync(kFullMask, mbar_wait_bounded(o_last, 0, kPfWaitNs))) bad = true;
+    if (!bad && !__all_sync(kFullMask, mbar_wait_bounded(o_last, 0, p.wait_limit_ns))) bad = true;
     if (bad) {
       if (lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
     } else {
@@ -508,7 +532,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
     }
   }
 
-  // ---- tear-down: every MMA has completed (or waits ran out) ------------------
+  // ---- tear-down: the TMA warp's boxes have landed and the MMA thread's
+  // MMAs have completed (each drain bounded by kDrainLimitNs; if one ran
+  // out, the error word already marks this call's outputs as invalid) -----
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -517,37 +543,12 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   }
 }
 
-// cuTensorMapEncodeTiled, reached through the runtime (no driver library
-// link); looked up once, thread-safely, on first use.
-inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static const PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      return nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }();
-  return fn;
-}
-
-// Rows of a cache pool [num_blocks][num_kv_heads][block_size][D] as a 2-D
-// tensor of 16-bit elements, read in boxes of {64 elements, block_size rows}
-// with the 128-byte swizzle.
+// Rows of a cache pool as a 2-D tensor of 16-bit elements, read in boxes of
+// {64 elements, block_size rows} with the 128-byte swizzle.
 template <typename T, int D>
 cudaError_t encode_pool_map(CUtensorMap* map, const void* base, const PrefillParams& p) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (enc == nullptr) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.num_blocks * p.num_kv_heads * p.block_size};
-  const cuuint64_t strides[1] = {(cuuint64_t)D * sizeof(T)};
-  const cuuint32_t box[2] = {64u, (cuuint32_t)p.block_size};
-  const cuuint32_t estr[2] = {1u, 1u};
-  const CUresult r =
-      enc(map, std::is_same<T, __nv_bfloat16>::value ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-          2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  return encode_pool_rows_map(map, base, (uint64_t)p.num_blocks * p.num_kv_heads * p.block_size, D, p.block_size,
+                              std::is_same<T, __nv_bfloat16>::value);
 }
 
 template <typename T, int D>

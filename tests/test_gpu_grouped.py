@@ -110,3 +110,37 @@ def test_workspace_reuse_and_plain_agreement():
                                                            st.max_context_len))
     for o in outs:
         assert_close(o, to_f64(plain), "grouped vs plain")
+
+
+def test_wait_timeout_is_reported_and_context_survives():
+    """With a wait limit of 0 the prefix and tail launches give up at their
+    first wait that is not already complete: they report PKV_DEV_ERR_TIMEOUT
+    (and nothing else), let their own copies land and return. After the
+    workspace is cleared, the next call with the default limit matches the
+    oracle."""
+    import paged_kv_cache_204_gb300 as pkv
+    cfg = synth.get("cow").replace(num_heads=8, num_kv_heads=8, num_blocks=4000)
+    st = synth.build(cfg, num_seqs=24)
+    hw = H.generate(cfg, st=st)
+    hp = H.compact_pools(hw)
+    dw = SD.from_host(hw)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = pkv.new_grouped_workspace(st.num_seqs, cfg.num_heads, cfg.head_dim, st.max_context_len,
+                                   len(st.shared_blocks))
+    old = pkv.get_wait_timeout_ns()
+    try:
+        pkv.set_wait_timeout_ns(0)
+        _run_grouped(dw, st.group_start, st.shared_blocks, err, ws=ws)
+        code = device_error(err)
+    finally:
+        pkv.set_wait_timeout_ns(old)
+    assert code & pkv.DEV_ERR_TIMEOUT
+    assert code & ~pkv.DEV_ERR_TIMEOUT == 0
+    # the cache writes ran before the timed-out attention: restart from fresh pools
+    dw = SD.from_host(hw)
+    err.zero_()
+    ws.zero_()  # a call that reported a device error may leave piece counters set
+    out = _run_grouped(dw, st.group_start, st.shared_blocks, err, ws=ws)
+    assert device_error(err) == 0
+    ref, _, _ = oracle.decode_step(hp, hw, threads=8)
+    assert_close(to_f64(out), ref, "grouped after timeout")

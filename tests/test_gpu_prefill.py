@@ -209,3 +209,42 @@ def test_prefill_rescale_and_scale_sign(name):
     assert int(err.item()) == 0
     ref, rows = oracle_prefill(cfg, lay, vals)
     assert_close(to_f64(out)[rows], ref, name)
+
+
+def test_prefill_wait_timeout_is_reported_and_context_survives():
+    """With a wait limit of 0 the prefill's roles (TMA loads, MMA issue,
+    softmax) give up at their first wait that is not already complete: the
+    call reports PKV_DEV_ERR_TIMEOUT and nothing else, and every CTA lets its
+    own TMA loads land and its MMAs complete before it frees its tensor
+    memory. The next call with the default limit matches the oracle."""
+    import paged_kv_cache_204_gb300 as pkv
+    cfg = SP.get("prefill_small").replace(dtype="bf16", block_size=16, head_dim=128, num_heads=4,
+                                          num_kv_heads=4, system_len=100, user_len=("uniform", 100, 300),
+                                          seed=2097)
+    lay = SP.build(cfg)
+    vals = SP.host_values(cfg, lay)
+    kc, vc = SP.host_pools(cfg)
+    kc_d, vc_d = up(kc, cfg.dtype), up(vc, cfg.dtype)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_prefill(cfg, lay, vals, kc_d, vc_d, err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    q, bt, cl, qs = up(vals.q, cfg.dtype), t64(lay.block_tables), t64(lay.context_lens), t64(lay.query_start)
+    old = pkv.get_wait_timeout_ns()
+    try:
+        pkv.set_wait_timeout_ns(0)
+        pkv.paged_attention_prefill(torch.empty_like(out), q, kc_d, vc_d, bt, cl, qs, cfg.scale,
+                                    lay.max_query_len, dev_err=err)
+        torch.cuda.synchronize()
+        code = int(err.item())
+    finally:
+        pkv.set_wait_timeout_ns(old)
+    assert code & pkv.DEV_ERR_TIMEOUT
+    assert code & ~pkv.DEV_ERR_TIMEOUT == 0
+    err.zero_()
+    out2 = torch.empty_like(out)
+    pkv.paged_attention_prefill(out2, q, kc_d, vc_d, bt, cl, qs, cfg.scale, lay.max_query_len, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref, rows = oracle_prefill(cfg, lay, vals)
+    assert_close(to_f64(out2)[rows], ref, "prefill after timeout")
