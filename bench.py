@@ -39,21 +39,35 @@ FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 
 
-def workload_bytes(st, kv_elem_bytes: int | None = None) -> dict:
+def workload_bytes(st, kv_elem_bytes: int | None = None, new_rows: int | None = None,
+                   copy_pairs: int | None = None) -> dict:
     """Algorithmic bytes of one step: attention reads each distinct cached
     (block, row) once for K and once for V plus q, and writes out; the cache
     write reads the new rows and writes them into the pools; each
-    copy-on-write pair reads and writes one whole block of both pools."""
+    copy-on-write pair reads and writes one whole block of both pools.
+    new_rows / copy_pairs: the step's counts when they differ from the
+    structure's (a copy-on-write decode step writes one row per sample)."""
     cfg = st.cfg
     es = cfg.elem_bytes
     kes = es if kv_elem_bytes is None else kv_elem_bytes  # cached element (1 for fp8 pools)
     row = cfg.num_kv_heads * cfg.head_dim * kes          # one token, one of K/V, all kv heads, as cached
     qo = st.num_seqs * cfg.num_heads * cfg.head_dim * es
     attn = 2 * st.unique_kv_tokens() * row + 2 * qo
-    cache_write = 2 * st.num_new_tokens * (row // kes * es + row)  # read the new rows, write them cached
-    copies = 2 * 2 * st.copy_pairs.shape[0] * cfg.block_size * row
+    n_new = st.num_new_tokens if new_rows is None else new_rows
+    n_pairs = st.copy_pairs.shape[0] if copy_pairs is None else copy_pairs
+    cache_write = 2 * n_new * (row // kes * es + row)  # read the new rows, write them cached
+    copies = 2 * 2 * n_pairs * cfg.block_size * row
     return {"attention": attn, "cache_write": cache_write, "copy": copies,
             "step": attn + cache_write + copies}
+
+
+def step_counts(cfg, st) -> dict:
+    """New rows and copy pairs of one timed step: a copy-on-write decode step
+    writes each sample's newest row (its tail and the copies at divergence
+    are history); other workloads write the structure's new rows."""
+    if cfg.samples > 1:
+        return {"new_rows": st.num_seqs, "copy_pairs": 0}
+    return {}
 
 
 def describe_lengths(spec) -> str:
@@ -79,8 +93,10 @@ def config_json(cfg, st, world: int, attention: str = "plain", kv: str | None = 
     if cfg.samples > 1:
         parts.append(f"{st.num_seqs // cfg.samples} prompts x {cfg.samples} samples sharing "
                      f"ref-counted prompt blocks, prompt lengths {describe_lengths(cfg.lengths)}, "
-                     f"divergent tails {describe_lengths(cfg.tail)}, {st.copy_pairs.shape[0]} "
-                     f"copy-on-write block copies and {st.num_new_tokens} tail rows written per step")
+                     f"divergent tails {describe_lengths(cfg.tail)} already cached (written before "
+                     f"the timed steps, after {st.copy_pairs.shape[0]} copy-on-write block copies at "
+                     f"divergence); each step writes every sample's newest K/V row "
+                     f"({st.num_seqs} rows), then attends")
     else:
         parts.append(f"context lengths {describe_lengths(cfg.lengths)} "
                      f"(mean {st.context_lens.mean():.0f})")
@@ -96,7 +112,7 @@ def config_json(cfg, st, world: int, attention: str = "plain", kv: str | None = 
         "seq_len": int(st.max_context_len),
         "parallelism": "single GPU" if world == 1 else f"{world} independent replicas",
         "l2": f"{flush_desc(flush)}; step inputs "
-              f"{workload_bytes(st, 1 if kv else None)['step'] / 1e9:.2f} GB",
+              f"{workload_bytes(st, 1 if kv else None, **step_counts(cfg, st))['step'] / 1e9:.2f} GB",
         "seed": cfg.seed,
     }
 
@@ -468,6 +484,33 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         cfg = cfg.replace(seed=cfg.seed + rank)
     dw = SD.generate(cfg, device=dev)
     st = dw.st
+    cow = cfg.samples > 1
+    cow_copy_us = None
+    if cow:
+        # Copy-on-write history: the copies at divergence and the samples'
+        # tails are written once here (copy_blocks timed on its own); a timed
+        # step then writes each sample's newest row (its last tail token,
+        # the same values again) and attends.
+        err0 = torch.zeros(1, dtype=torch.int32, device=dev)
+        flush0 = L2Flush(dev, args.flush)
+        copy_times = []
+        for i in range(8):  # the copies, then the tails (which rewrite the copied blocks' tail rows)
+            flush0(i)
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            c0.record()
+            pkv.copy_blocks(dw.k_cache, dw.v_cache, dw.copy_pairs, dev_err=err0)
+            c1.record()
+            pkv.reshape_and_cache(dw.new_k, dw.new_v, dw.k_cache, dw.v_cache, dw.slot_mapping, dev_err=err0)
+            torch.cuda.synchronize()
+            copy_times.append(c0.elapsed_time(c1) * 1e3)
+        del flush0
+        if int(err0.item()) != 0:
+            raise RuntimeError(f"device error word {int(err0.item()):#x} while writing the tails")
+        cow_copy_us = statistics.median(copy_times[3:])  # warm launches, L2 flushed before each
+        last = torch.from_numpy(st.new_start[1:] - 1).to(dev)
+        dw.new_k, dw.new_v = dw.new_k[last].contiguous(), dw.new_v[last].contiguous()
+        dw.slot_mapping = dw.slot_mapping[last].contiguous()
+        dw.copy_pairs = dw.copy_pairs[:0]
     fp8 = args.kv == "fp8"
     if fp8:
         if args.attention != "plain" or cfg.dtype == "f32":
@@ -476,7 +519,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         dw.v_cache = fp8_pool(dw.v_cache, FP8_SCALE)
         torch.cuda.empty_cache()
     kv_desc = (f"fp8 e4m3 K/V pools (per-pool scale {FP8_SCALE:.6g}; new rows rounded on write)" if fp8 else None)
-    nbytes = workload_bytes(st, 1 if fp8 else None)
+    nbytes = workload_bytes(st, 1 if fp8 else None, new_rows=int(dw.slot_mapping.numel()),
+                            copy_pairs=int(dw.copy_pairs.shape[0]))
     B, H, D = st.num_seqs, cfg.num_heads, cfg.head_dim
     mcl = st.max_context_len
     grouped = args.attention == "grouped"
@@ -598,6 +642,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
             cpu = sampled_attention_baseline(cfg, dw.k_cache, dw.v_cache, st.block_tables, st.context_lens, dw.q,
                                              args.cpu_seconds, args.cpu_seqs, "sequences (fp8 pools)",
                                              fp8_scales=(FP8_SCALE, FP8_SCALE))
+        elif cow:
+            cpu = sampled_attention_baseline(cfg, dw.k_cache, dw.v_cache, st.block_tables, st.context_lens, dw.q,
+                                             args.cpu_seconds, args.cpu_seqs, "samples (plain paged attention)")
         else:
             cpu = time_oracle(cfg, args.cpu_seconds, args.cpu_seqs)
             cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample", "single_thread")}
@@ -624,6 +671,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         "e2e": {"value": world * nbytes["step"] / (agg["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
                 "ms_per_step": agg["e2e_ms"], "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * K,
+        **({"cow_copy_blocks_us": cow_copy_us, "cow_copy_pairs": int(st.copy_pairs.shape[0])} if cow else {}),
         "clocks": clocks.summary(),
         "timed_region_wall_s": wall,
         "kv_memory": kv_memory(cfg),

@@ -41,10 +41,11 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim) {
 }
 
 // Grouped decode: the grouping flag, usable prefix per group and per
-// sequence, piece counters, each row's prefix result, then the warps'
-// partial slots.
+// sequence, piece counters, each row's prefix result, the row counters and
+// tail results of the single-launch kernel, then the warps' partial slots.
 struct GroupedLayout {
   size_t flag = 0, group_S = 0, seq_P = 0, seg_ctr = 0, row_ml = 0, row_o = 0;
+  size_t row_ctr = 0, tail_ml = 0, tail_o = 0;
   size_t slot_ml = 0, slot_o = 0, total = 0;
 };
 
@@ -65,6 +66,12 @@ GroupedLayout grouped_layout(int num_seqs, int num_heads, int head_dim, int num_
   w.row_ml = off;
   off += align_up(rows * sizeof(float2), 256);
   w.row_o = off;
+  off += align_up(rows * head_dim * sizeof(float), 256);
+  w.row_ctr = off;
+  off += align_up(rows * 4, 256);
+  w.tail_ml = off;
+  off += align_up(rows * sizeof(float2), 256);
+  w.tail_o = off;
   off += align_up(rows * head_dim * sizeof(float), 256);
   w.slot_ml = off;
   off += align_up(slots * sizeof(float2), 256);
@@ -364,6 +371,9 @@ pkv_status pkv_paged_attention_decode_grouped(void* out, const void* q, const vo
   gp.ws_seg_ctr = reinterpret_cast<int32_t*>(wsb + ws.seg_ctr);
   gp.ws_row_ml = reinterpret_cast<float2*>(wsb + ws.row_ml);
   gp.ws_row_o = reinterpret_cast<float*>(wsb + ws.row_o);
+  gp.ws_row_ctr = reinterpret_cast<int32_t*>(wsb + ws.row_ctr);
+  gp.ws_tail_ml = reinterpret_cast<float2*>(wsb + ws.tail_ml);
+  gp.ws_tail_o = reinterpret_cast<float*>(wsb + ws.tail_o);
   return launch_status(launch(gp, reinterpret_cast<cudaStream_t>(stream)));
 }
 

@@ -63,6 +63,11 @@ struct GroupedParams {
   int32_t* ws_seg_ctr;  // [2][num_seqs * num_heads] piece counters (prefix, tail)
   float2* ws_row_ml;    // [num_seqs * num_heads] (m, l) of each row's prefix result
   float* ws_row_o;      // [num_seqs * num_heads][head_dim] o / l of each row's prefix result
+  // single-launch kernel (16-bit data): the tail part of rows whose parts meet
+  // through the workspace, and each row's count of arrived parts
+  float2* ws_tail_ml;   // [num_seqs * num_heads]
+  float* ws_tail_o;     // [num_seqs * num_heads][head_dim]
+  int32_t* ws_row_ctr;  // [num_seqs * num_heads]
 };
 
 __device__ __forceinline__ int warp_min(int v) {
@@ -1044,6 +1049,696 @@ __global__ void __launch_bounds__(NW * 32)
   }
 }
 
+// ---- single-launch grouped decode (16-bit data) ------------------------------
+//
+// One persistent launch after the grouping check. Work units, laid end to
+// end: for every group, for every head group hg, the group's prefix
+// segments for the heads of hg (rows [0, S_g) of the shared blocks against up
+// to 8 siblings' query rows, on tensor cores), then the tail segment of every
+// member (rows [S_g, L_s) of its own blocks, CUDA cores). A row (member s,
+// head h) of a group with a shared prefix has two parts, each merged over
+// its pieces when warp ranges cut its segment (as in the plain kernel). The
+// two parts of a row meet
+//   - in the warp's shared memory, when one warp's range holds the row's
+//     whole prefix segment and whole tail segment (the prefix results wait in
+//     the warp's buffer until its tails end; nothing goes through global
+//     memory);
+//   - through the workspace otherwise: each part stores its (m, l, o / l)
+//     and counts itself on the row's counter; the part that arrives second
+//     merges both by the log-sum-exp rule, writes the output and clears the
+//     counter.
+// Sequences of rejected or single-member groups have tails only.
+
+struct SCursor {
+  long long g;        // unit of the current tile
+  int grp, hg, part, j, t, nt;
+  int lo, M, S, nch;  // group: members [lo, lo + M), usable prefix S (0: none), row chunks of 8
+  int h, c;           // prefix segment: query head and row chunk
+  int tok0, tok_end, sbt, sbt_len, kvh, nrows;
+};
+
+// Groups the work runs over: the caller's groups, or one per sequence when the
+// grouping was rejected.
+__device__ __forceinline__ int sgroup_count(const GCtx& x) { return x.use_groups ? x.num_groups : x.num_seqs; }
+
+__device__ __forceinline__ void sgroup_load(SCursor& c, const GCtx& x) {
+  if (x.use_groups) {
+    c.lo = __ldg(x.group_start + c.grp);
+    c.M = __ldg(x.group_start + c.grp + 1) - c.lo;
+    c.S = c.M >= 2 ? __ldcg(x.group_S + c.grp) : 0;
+  } else {
+    c.lo = c.grp;
+    c.M = 1;
+    c.S = 0;
+  }
+  c.nch = (c.M + kMaxPrefixRows - 1) / kMaxPrefixRows;
+}
+
+// Units of one prefix segment and of one head group of the loaded group.
+__device__ __forceinline__ long long sprefix_seg_units(const SCursor& c) {
+  return c.S / kTileTokens + kSegCostPrefix;
+}
+__device__ __forceinline__ long long shg_units(const SCursor& c, const GCtx& x) {
+  long long u = c.S > 0 ? (long long)x.gpw * c.nch * sprefix_seg_units(c) : 0;
+  for (int k = 0; k < c.M; ++k) u += tiles_of(ctx_len(x, c.lo + k) - c.S) + kSegCostTail;
+  return u;
+}
+
+__device__ __forceinline__ void sseg_enter(SCursor& c, const GCtx& x) {
+  if (c.part == 0) {
+    const int hi = c.j / c.nch;
+    c.c = c.j - hi * c.nch;
+    c.h = c.hg * x.gpw + hi;
+    c.nrows = min(kMaxPrefixRows, c.M - kMaxPrefixRows * c.c);
+    c.tok0 = 0;
+    c.tok_end = c.S;
+    c.sbt = c.lo;
+    c.sbt_len = ctx_len(x, c.lo);
+    c.kvh = c.h / x.group;
+    c.nt = c.S / kTileTokens;
+  } else {
+    const int s = c.lo + c.j;
+    const int L = ctx_len(x, s);
+    c.tok0 = c.S;
+    c.tok_end = L;
+    c.sbt = s;
+    c.sbt_len = L;
+    c.kvh = (c.hg * x.gpw) / x.group;
+    c.nrows = x.gpw;
+    c.nt = tiles_of(L - c.S);
+  }
+}
+
+// Next segment (c.t is 0); past the last group the cursor stops changing.
+__device__ __forceinline__ void sseg_next(SCursor& c, const GCtx& x, int NG) {
+  if (c.part == 0) {
+    if (++c.j < x.gpw * c.nch) {
+      sseg_enter(c, x);
+      return;
+    }
+    c.part = 1;
+    c.j = 0;
+    sseg_enter(c, x);
+    return;
+  }
+  if (++c.j < c.M) {
+    sseg_enter(c, x);
+    return;
+  }
+  c.j = 0;
+  if (++c.hg >= x.head_groups) {
+    c.hg = 0;
+    do {
+      if (++c.grp >= NG) return;
+      sgroup_load(c, x);
+    } while (c.M == 0);
+  }
+  c.part = c.S > 0 ? 0 : 1;
+  sseg_enter(c, x);
+}
+
+// Next tile: c.g is its unit (the next segment's charged units skipped).
+__device__ __forceinline__ void scursor_next(SCursor& c, const GCtx& x, int NG) {
+  ++c.g;
+  if (++c.t < c.nt) return;
+  c.t = 0;
+  sseg_next(c, x, NG);
+  c.g += c.part == 0 ? kSegCostPrefix : kSegCostTail;
+}
+
+// Shared memory of the single-launch kernel: two stages per warp (a prefix
+// tile as swizzled TMA boxes, or a tail tile as plain rows at the same
+// offsets), then per warp the prefix results of its latest prefix segment
+// (8 rows of o / l, m, l) and the results of its current tail segment (4
+// rows), then mbarriers, block-table chunks and the start-up scan.
+template <int D, int NW>
+struct SharedShape {
+  static constexpr int kStages = 2;
+  static constexpr int kStageBytes = PrefixStage<D>::kBytes;
+  static constexpr int kRowFloats = D + 4;  // o / l, then m and l
+  static constexpr int kPbufOff = NW * kStages * kStageBytes;
+  static constexpr int kTbufOff = kPbufOff + NW * kMaxPrefixRows * kRowFloats * 4;
+  static constexpr int kBarOff = kTbufOff + NW * kMaxGroupPerWarp * kRowFloats * 4;
+  static constexpr int kBtOff = kBarOff + NW * kStages * 8;
+  static constexpr int kScanOff = kBtOff + NW * kBtChunk * 4;
+  static constexpr int kSmemBytes = kScanOff + NW * 8 + 1024;  // + alignment of the base
+};
+
+// out = (a.o a.l 2^(a.m - M) + b.o b.l 2^(b.m - M)) / (a.l 2^(a.m - M) + b.l 2^(b.m - M)),
+// M = max(a.m, b.m), for this lane's DL dims; a, b hold normalised o (o / l).
+template <int DL>
+__device__ __forceinline__ void lse_combine(float am, float al, const float (&ao)[DL], float bm, float bl,
+                                            const float (&bo)[DL], float (&out)[DL]) {
+  const float M = fmaxf(am, bm);
+  const float wa = am == -INFINITY ? 0.f : al * exp2f(am - M);
+  const float wb = bm == -INFINITY ? 0.f : bl * exp2f(bm - M);
+  const float den = wa + wb;
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+  for (int e = 0; e < DL; ++e) out[e] = (ao[e] * wa + bo[e] * wb) * inv;
+}
+
+template <typename T, int D, int TG>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+    pa_decode_shared_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                            const GroupedParams gp) {
+  constexpr int NW = kDecodeWarps;
+  using S = SharedShape<D, NW>;
+  using St = PrefixStage<D>;
+  constexpr int R = kMaxPrefixRows;
+  constexpr int ST = S::kStages;
+  constexpr int ROW = D * 2;
+  constexpr int VEC = 8;
+  constexpr int CPL = ROW / 16 / 8;
+  constexpr int DPL = D / 8;
+  constexpr int DL = D / 32;  // dims per lane in merges and combines
+  constexpr int RF = S::kRowFloats;
+  const DecodeParams& p = gp.base;
+
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
+  long long* scan = reinterpret_cast<long long*>(smem + S::kScanOff);
+  __shared__ longlong2 starts[NW];  // (group, offset) of each warp's first unit
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int grp = lane >> 3;
+  const int sub = lane & 7;
+  const int mg = lane >> 2, mt = lane & 3;
+  const int bs = p.block_size;
+  GCtx x;
+  x.group_start = gp.group_start;
+  x.group_S = gp.ws_group_S;
+  x.seq_P = gp.ws_seq_P;
+  x.context_lens = p.context_lens;
+  x.dev_err = p.dev_err;
+  x.num_groups = gp.num_groups;
+  x.num_seqs = p.num_seqs;
+  x.num_heads = p.num_heads;
+  x.head_groups = p.head_groups;
+  x.group = p.group;
+  x.cap = min(p.max_context_len, p.max_blocks_per_seq * bs);
+  x.gpw = p.num_heads / p.head_groups;
+  x.rows = R;
+  grid_dependency_wait();  // the grouping check's results
+  x.use_groups = __ldcg(gp.ws_flag) == 0;
+  const int NG = sgroup_count(x);
+  const int H = p.num_heads, HG = p.head_groups;
+
+  // ---- start-up: units of every group, then each warp's first segment -------
+  const long long W = (long long)gridDim.x * NW;
+  const long long wid = (long long)blockIdx.x * NW + warp;
+  auto group_units = [&](int gi) -> long long {
+    SCursor c;
+    c.grp = gi;
+    sgroup_load(c, x);
+    return (long long)HG * shg_units(c, x);
+  };
+  long long mine = 0, Ttot = 0;
+  for (int gi = threadIdx.x; gi < NG; gi += NW * 32) mine += group_units(gi);
+  block_exclusive_scan<NW>(mine, scan, Ttot);
+  const long long Weff = W < Ttot ? W : Ttot;
+  if (threadIdx.x < NW) starts[threadIdx.x] = make_longlong2(-1, 0);
+  __syncthreads();
+  long long carry = 0;
+  for (int base = 0; base < NG; base += NW * 32) {
+    const int i0 = base + threadIdx.x;
+    const long long cnt = i0 < NG ? group_units(i0) : 0;
+    long long tot;
+    const long long excl = carry + block_exclusive_scan<NW>(cnt, scan, tot);
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      const long long w = (long long)blockIdx.x * NW + i;
+      if (w < Weff) {
+        const long long a = w * Ttot / Weff;
+        if (cnt > 0 && a >= excl && a < excl + cnt) starts[i] = make_longlong2(i0, a - excl);
+      }
+    }
+    carry += tot;
+  }
+  __syncthreads();  // the last block-wide barrier
+
+  const long long a_begin = wid < Weff ? wid * Ttot / Weff : Ttot;
+  const long long a_end = wid < Weff ? (wid + 1) * Ttot / Weff : Ttot;
+  if (a_begin >= a_end) return;
+
+  unsigned char* my_ring = smem + warp * ST * S::kStageBytes;
+  float* pbuf = reinterpret_cast<float*>(smem + S::kPbufOff) + warp * R * RF;
+  float* tbuf = reinterpret_cast<float*>(smem + S::kTbufOff) + warp * kMaxGroupPerWarp * RF;
+  uint64_t* my_bars = bars + warp * ST;
+  int32_t* my_bt = reinterpret_cast<int32_t*>(smem + S::kBtOff) + warp * kBtChunk;
+  if (lane == 0) {
+#pragma unroll
+    for (int i = 0; i < ST; ++i) mbar_init(&my_bars[i], 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+
+  // ---- this warp's first segment ----------------------------------------------
+  SCursor ci;
+  {
+    const longlong2 st0 = starts[warp];
+    ci.grp = static_cast<int>(st0.x);
+    sgroup_load(ci, x);
+    const long long uhg = shg_units(ci, x);
+    ci.hg = static_cast<int>(st0.y / uhg);
+    long long r = st0.y - ci.hg * uhg;
+    const long long pseg = sprefix_seg_units(ci);
+    const long long pu = ci.S > 0 ? (long long)x.gpw * ci.nch * pseg : 0;
+    int r2;
+    if (r < pu) {
+      ci.part = 0;
+      ci.j = static_cast<int>(r / pseg);
+      r2 = static_cast<int>(r - ci.j * pseg) - kSegCostPrefix;
+    } else {
+      r -= pu;
+      ci.part = 1;
+      int k = 0;
+      for (;;) {
+        const long long uk = tiles_of(ctx_len(x, ci.lo + k) - ci.S) + kSegCostTail;
+        if (r < uk || k == ci.M - 1) break;
+        r -= uk;
+        ++k;
+      }
+      ci.j = k;
+      r2 = static_cast<int>(r) - kSegCostTail;
+    }
+    ci.t = 0;
+    sseg_enter(ci, x);
+    ci.t = r2 < 0 ? 0 : r2;  // a range that starts on charged units starts at tile 0
+    ci.g = a_begin + (ci.t - r2);
+  }
+  SCursor cc = ci;
+  const long long g_first = ci.g;
+
+  const char* kbase = static_cast<const char*>(p.k_cache);
+  const char* vbase = static_cast<const char*>(p.v_cache);
+  const char* qbase = static_cast<const char*>(p.q);
+  const int seg = bs < kTileTokens ? bs : kTileTokens;
+  const int nseg = kTileTokens / seg;
+  int bt_s = -1, bt_j0 = 0;
+
+  auto issue = [&](const SCursor& c, int n) {
+    const int t0 = c.tok0 + c.t * kTileTokens;
+    const int nvalid = min(max(c.tok_end - t0, 0), kTileTokens);
+    const bool with_q = (c.t == 0 || c.g == g_first) && nvalid > 0;
+    if (nvalid > 0) {
+      const int j_first = t0 / bs;
+      const int j_last = (t0 + nvalid - 1) / bs;
+      if (c.sbt != bt_s || j_first < bt_j0 || j_last >= bt_j0 + kBtChunk) {
+        const int nblk = (c.sbt_len + bs - 1) / bs;
+        const int32_t* row = p.block_tables + (size_t)c.sbt * p.max_blocks_per_seq;
+        __syncwarp();
+        for (int i = lane; i < kBtChunk; i += 32) {
+          const int j = j_first + i;
+          int id = 0;
+          if (j < nblk) {
+            id = __ldg(row + j);
+            if (id < 0 || id >= p.num_blocks) {
+              set_err(p.dev_err, PKV_DEV_ERR_BLOCK_ID);
+              id = 0;
+            }
+          }
+          my_bt[i] = id;
+        }
+        __syncwarp();
+        bt_s = c.sbt;
+        bt_j0 = j_first;
+      }
+    }
+    unsigned char* st = my_ring + (n % ST) * S::kStageBytes;
+    uint64_t* bar = my_bars + (n % ST);
+    if (c.part == 0) {
+      // a whole prefix tile: K and V as TMA boxes of {64 dims, rb rows} into
+      // the swizzled stage, from parallel lanes; the siblings' query rows
+      if (lane == 0) mbar_arrive_expect_tx(bar, 2u * kTileTokens * ROW + (with_q ? c.nrows * ROW : 0u));
+      __syncwarp();
+      const int rb = bs < kTileTokens ? bs : kTileTokens;
+      constexpr int CB = D / 64;
+      const int per = (kTileTokens / rb) * CB;
+      if (lane < 2 * per) {
+        const int tsr = lane / per, rem = lane - tsr * per;
+        const int b = rem / CB, cb = rem - b * CB;
+        const int t = t0 + b * rb;
+        const int y = (my_bt[t / bs - bt_j0] * p.num_kv_heads + c.kvh) * bs + (t % bs);
+        tma_load_2d(st + tsr * St::kTensorBytes + cb * St::kColBytes + b * rb * 128, tsr ? &vmap : &kmap, cb * 64, y,
+                    bar);
+      }
+      if (with_q && lane == 0) {
+        for (int r = 0; r < c.nrows; ++r)
+          bulk_copy_g2s(st + St::kQOff + r * ROW,
+                        qbase + ((size_t)(c.lo + R * c.c + r) * H + c.h) * ROW, ROW, bar);
+      }
+    } else if (lane == 0) {
+      // a tail tile: plain K and V rows by 1-D bulk copies, the query rows
+      uint32_t bytes = with_q ? c.nrows * ROW : 0;
+      for (int c2 = 0; c2 < nseg; ++c2)
+        if (t0 + c2 * seg < c.tok_end) bytes += 2u * seg * ROW;
+      mbar_arrive_expect_tx(bar, bytes);
+      for (int c2 = 0; c2 < nseg; ++c2) {
+        const int t = t0 + c2 * seg;
+        if (t >= c.tok_end) break;
+        const size_t off = (((size_t)my_bt[t / bs - bt_j0] * p.num_kv_heads + c.kvh) * bs + (t % bs)) * ROW;
+        bulk_copy_g2s(st + c2 * seg * ROW, kbase + off, seg * ROW, bar);
+        bulk_copy_g2s(st + St::kTensorBytes + c2 * seg * ROW, vbase + off, seg * ROW, bar);
+      }
+      if (with_q)
+        bulk_copy_g2s(st + St::kQOff, qbase + ((size_t)(c.lo + c.j) * H + (size_t)c.hg * c.nrows) * ROW,
+                      c.nrows * ROW, bar);
+    }
+  };
+
+  int issued = 0;
+  for (; issued < ST && ci.g < a_end; ++issued) {
+    issue(ci, issued);
+    scursor_next(ci, x, NG);
+  }
+
+  // prefix state (tensor-core layout, see mma_prefix_tile) and tail state
+  uint32_t qb[D / 16][2];
+  float acc[D / 16][4];
+  float tm[2] = {-INFINITY, -INFINITY}, tl[2] = {0.f, 0.f};
+  float qf[TG][DPL];
+  float m[TG], l[TG], o[TG][DPL];
+  bool visit_from_start = true;
+  // the prefix results in pbuf: group, head group and the members (bits)
+  // whose rows meet their tails there
+  int pb_grp = -1, pb_hg = -1;
+  unsigned pb_local = 0u;
+
+  // Second part of a row to arrive: merge with the other part's stored
+  // result and write the output. `mine` is this part's row in shared memory.
+  auto write_out = [&](size_t row, const float* mine, float om, float ol, const float* other_o, float other_m,
+                       float other_l, bool other_global) {
+    float a[DL], b[DL], r[DL];
+#pragma unroll
+    for (int e = 0; e < DL; ++e) {
+      a[e] = mine[lane * DL + e];
+      b[e] = other_global ? __ldcg(other_o + lane * DL + e) : other_o[lane * DL + e];
+    }
+    lse_combine<DL>(om, ol, a, other_m, other_l, b, r);
+    T* orow = static_cast<T*>(p.out) + row * D + lane * DL;
+#pragma unroll
+    for (int e = 0; e < DL; ++e) store_elem(orow + e, r[e]);
+  };
+
+  // The prefix part of rows [0, nr) of segment c is complete in pbuf.
+  auto complete_prefix = [&](const SCursor& c, bool whole) {
+    unsigned local = 0u;
+    if (whole && x.gpw == 1 && c.nch == 1) {
+      // member k's tail ends at unit c.g + sum_{i <= k} (charge + tiles_i):
+      // its row stays local when that is still inside this warp's range
+      long long u = lane < c.M ? tiles_of(ctx_len(x, c.lo + lane) - c.S) + kSegCostTail : 0;
+#pragma unroll
+      for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const long long y = __shfl_up_sync(kFullMask, u, o2);
+        if (lane >= o2) u += y;
+      }
+      local = __ballot_sync(kFullMask, lane < c.M && c.g + u <= a_end - 1);
+      pb_grp = c.grp;
+      pb_hg = c.hg;
+    } else {
+      pb_grp = -1;
+    }
+    pb_local = local;
+    const int nr = c.nrows;
+    // rows that do not stay local: publish, count, merge when second
+    unsigned pub = __ballot_sync(kFullMask, lane < nr && !((local >> lane) & 1u)) & ((1u << nr) - 1u);
+    if (pub == 0u) return;
+    for (unsigned q = pub; q; q &= q - 1) {
+      const int r = __ffs(q) - 1;
+      const size_t row = (size_t)(c.lo + R * c.c + r) * H + c.h;
+      const float* src = pbuf + r * RF;
+#pragma unroll
+      for (int e = 0; e < DL; ++e) gp.ws_row_o[row * D + lane * DL + e] = src[lane * DL + e];
+      if (lane == 0) gp.ws_row_ml[row] = make_float2(src[D], src[D + 1]);
+    }
+    __syncwarp();  // the rows' stores precede the releases below
+    int prev = 0;
+    if ((pub >> lane) & 1u) {
+      const size_t row = (size_t)(c.lo + R * c.c + lane) * H + c.h;
+      prev = atomic_add_acq_rel_gpu(gp.ws_row_ctr + row, 1);
+      if (prev == 1) gp.ws_row_ctr[row] = 0;
+    }
+    const unsigned second = __ballot_sync(kFullMask, prev == 1);
+    __syncwarp();
+    for (unsigned q = second; q; q &= q - 1) {
+      const int r = __ffs(q) - 1;
+      const size_t row = (size_t)(c.lo + R * c.c + r) * H + c.h;
+      const float* src = pbuf + r * RF;
+      const float2 tml = __ldcg(gp.ws_tail_ml + row);
+      write_out(row, src, src[D], src[D + 1], gp.ws_tail_o + row * D, tml.x, tml.y, true);
+    }
+  };
+
+  // The tail part of rows [0, gpw) of segment c is complete in tbuf.
+  auto complete_tail = [&](const SCursor& c, bool whole) {
+    const int s = c.lo + c.j;
+    const int nr = c.nrows;
+    if (c.S == 0) {  // no shared prefix: the tail is the whole row
+      for (int r = 0; r < nr; ++r) {
+        const size_t row = (size_t)s * H + (size_t)c.hg * nr + r;
+        const float* src = tbuf + r * RF;
+        T* orow = static_cast<T*>(p.out) + row * D + lane * DL;
+#pragma unroll
+        for (int e = 0; e < DL; ++e) store_elem(orow + e, src[lane * DL + e]);
+      }
+      return;
+    }
+    if (whole && pb_grp == c.grp && pb_hg == c.hg && ((pb_local >> c.j) & 1u)) {
+      // the prefix result waits in this warp's buffer (gpw 1, one row chunk)
+      const size_t row = (size_t)s * H + c.hg;
+      const float* src = tbuf;
+      const float* pre = pbuf + c.j * RF;
+      write_out(row, src, src[D], src[D + 1], pre, pre[D], pre[D + 1], false);
+      return;
+    }
+    for (int r = 0; r < nr; ++r) {
+      const size_t row = (size_t)s * H + (size_t)c.hg * nr + r;
+      const float* src = tbuf + r * RF;
+#pragma unroll
+      for (int e = 0; e < DL; ++e) gp.ws_tail_o[row * D + lane * DL + e] = src[lane * DL + e];
+      if (lane == 0) gp.ws_tail_ml[row] = make_float2(src[D], src[D + 1]);
+    }
+    __syncwarp();
+    int prev = 0;
+    if (lane < nr) {
+      const size_t row = (size_t)s * H + (size_t)c.hg * nr + lane;
+      prev = atomic_add_acq_rel_gpu(gp.ws_row_ctr + row, 1);
+      if (prev == 1) gp.ws_row_ctr[row] = 0;
+    }
+    const unsigned second = __ballot_sync(kFullMask, prev == 1);
+    __syncwarp();
+    for (unsigned q = second; q; q &= q - 1) {
+      const int r = __ffs(q) - 1;
+      const size_t row = (size_t)s * H + (size_t)c.hg * nr + r;
+      const float* src = tbuf + r * RF;
+      const float2 pml = __ldcg(gp.ws_row_ml + row);
+      write_out(row, src, src[D], src[D + 1], gp.ws_row_o + row * D, pml.x, pml.y, true);
+    }
+  };
+
+  for (int ring = 0; cc.g < a_end; ++ring) {
+    if (!__all_sync(kFullMask, mbar_wait_bounded(my_bars + (ring % ST), (ring / ST) & 1, p.wait_limit_ns))) {
+      if (lane == 0) set_err(p.dev_err, PKV_DEV_ERR_TIMEOUT);
+      for (int k2 = ring; k2 < issued; ++k2) mbar_wait_bounded(my_bars + (k2 % ST), (k2 / ST) & 1, kDrainLimitNs);
+      return;  // outputs of this call are not valid
+    }
+    const unsigned char* ks = my_ring + (ring % ST) * S::kStageBytes;
+    const int t0 = cc.tok0 + cc.t * kTileTokens;
+    const int nvalid = min(max(cc.tok_end - t0, 0), kTileTokens);
+    const bool first = cc.t == 0 || cc.g == g_first;
+    const bool last = cc.t == cc.nt - 1 || cc.g == a_end - 1;
+    const int nr = cc.nrows;
+
+    if (cc.part == 0) {
+      if (first) {
+        visit_from_start = cc.t == 0;
+        tm[0] = tm[1] = -INFINITY;
+        tl[0] = tl[1] = 0.f;
+#pragma unroll
+        for (int mb = 0; mb < D / 16; ++mb) acc[mb][0] = acc[mb][1] = acc[mb][2] = acc[mb][3] = 0.f;
+        // B fragments of Q^T: lane 4g + t holds query row g, dims 16 k + 2t,
+        // +1 and 16 k + 2t + 8, +9 (rows past nr: zero)
+        const uint32_t* qrow = reinterpret_cast<const uint32_t*>(ks + St::kQOff + mg * ROW);
+#pragma unroll
+        for (int k2 = 0; k2 < D / 16; ++k2) {
+          qb[k2][0] = mg < nr ? qrow[8 * k2 + mt] : 0u;
+          qb[k2][1] = mg < nr ? qrow[8 * k2 + mt + 4] : 0u;
+        }
+      }
+      mma_prefix_tile<T, D>(smem_u32(ks), qb, acc, tm, tl, p.scale_log2);
+    } else {
+      if (first) {
+        visit_from_start = cc.t == 0;
+#pragma unroll
+        for (int g = 0; g < TG; ++g) {
+          m[g] = -INFINITY;
+          l[g] = 0.f;
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) o[g][e] = 0.f;
+        }
+        if (nvalid > 0) {
+#pragma unroll
+          for (int g = 0; g < TG; ++g) {
+            const uint4* qrow = reinterpret_cast<const uint4*>(ks + St::kQOff + g * ROW);
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) {
+              float f[VEC];
+              Chunk<T>::widen(qrow[sub + 8 * k], f);
+#pragma unroll
+              for (int e = 0; e < VEC; ++e) qf[g][k * VEC + e] = f[e] * p.scale_log2;
+            }
+          }
+        }
+      }
+      if (nvalid > 0) core_tile<T, D, TG, TG, false, TG>(ks, ks + St::kTensorBytes, qf, o, m, l, nvalid, TG);
+    }
+    __syncwarp();
+    if (ci.g < a_end) {
+      issue(ci, issued++);
+      scursor_next(ci, x, NG);
+    }
+
+    if (last) {
+      // ---- end of this warp's visit of the segment under cc ------------------
+      const bool whole = visit_from_start && cc.t == cc.nt - 1;
+      float* rows_buf = cc.part == 0 ? pbuf : tbuf;
+      if (cc.part == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          tl[e] += __shfl_xor_sync(kFullMask, tl[e], 4);
+          tl[e] += __shfl_xor_sync(kFullMask, tl[e], 8);
+          tl[e] += __shfl_xor_sync(kFullMask, tl[e], 16);
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < TG; ++g) {
+          l[g] += __shfl_xor_sync(kFullMask, l[g], 8);
+          l[g] += __shfl_xor_sync(kFullMask, l[g], 16);
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) {
+            o[g][e] += __shfl_xor_sync(kFullMask, o[g][e], 8);
+            o[g][e] += __shfl_xor_sync(kFullMask, o[g][e], 16);
+          }
+        }
+      }
+      // this warp's (m, l, o / l) of the segment's rows: into the row buffer
+      // (whole segment) or into a partial slot (one piece)
+      const int slot = cc.g - cc.t - (cc.part == 0 ? kSegCostPrefix : kSegCostTail) <= a_begin ? 0 : 1;
+      const size_t base = ((size_t)wid * 2 + slot) * R;
+      float* o_dst = whole ? rows_buf : p.ws_o + base * D;
+      const int o_stride = whole ? RF : D;
+      if (cc.part == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int r = 2 * mt + e;
+          if (r < nr) {
+            const float inv = 1.f / tl[e];
+            float* orow = o_dst + r * o_stride + mg;
+#pragma unroll
+            for (int mb = 0; mb < D / 16; ++mb) {
+              orow[16 * mb] = acc[mb][e] * inv;
+              orow[16 * mb + 8] = acc[mb][e + 2] * inv;
+            }
+            if (mg == 0) {
+              if (whole) {
+                rows_buf[r * RF + D] = tm[e];
+                rows_buf[r * RF + D + 1] = tl[e];
+              } else {
+                p.ws_ml[base + r] = make_float2(tm[e], tl[e]);
+              }
+            }
+          }
+        }
+      } else {
+#pragma unroll
+        for (int g = 0; g < TG; ++g) {
+          const float inv = l[g] > 0.f ? 1.f / l[g] : 0.f;
+          if (grp == 0) {
+            float* orow = o_dst + g * o_stride;
+#pragma unroll
+            for (int k = 0; k < CPL; ++k)
+#pragma unroll
+              for (int e = 0; e < VEC; ++e) orow[(sub + 8 * k) * VEC + e] = o[g][k * VEC + e] * inv;
+          }
+          if (lane == 0) {
+            if (whole) {
+              rows_buf[g * RF + D] = m[g];
+              rows_buf[g * RF + D + 1] = l[g];
+            } else {
+              p.ws_ml[base + g] = make_float2(m[g], l[g]);
+            }
+          }
+        }
+      }
+      __syncwarp();  // the rows (shared) or the partial (global, before the release below)
+      bool done = whole;
+      if (!whole) {
+        // one piece of a segment shared with neighbouring warps: the last
+        // piece to arrive merges all pieces into the row buffer
+        const long long E = cc.part == 0 ? kSegCostPrefix : kSegCostTail;
+        const long long seg_start = cc.g - cc.t;
+        const long long seg_end = seg_start + cc.nt;
+        const long long seg_units0 = seg_start - E;
+        const long long w_first = ((seg_start + 1) * Weff + Ttot - 1) / Ttot - 1;
+        const long long w_last = (seg_end * Weff + Ttot - 1) / Ttot - 1;
+        int is_last = 0;
+        if (lane == 0) {
+          const size_t ci_idx = cc.part == 0 ? (size_t)(cc.lo + R * cc.c) * H + cc.h
+                                             : (size_t)x.num_seqs * H + (size_t)(cc.lo + cc.j) * HG + cc.hg;
+          int32_t* ctr = gp.ws_seg_ctr + ci_idx;
+          const int prev = atomic_add_acq_rel_gpu(ctr, 1);
+          is_last = prev == (int)(w_last - w_first);
+          if (is_last) *ctr = 0;
+        }
+        is_last = __shfl_sync(kFullMask, is_last, 0);
+        if (is_last) {
+          __syncwarp();
+          for (int r = 0; r < nr; ++r) {
+            float Mx = -INFINITY;
+            for (long long w = w_first; w <= w_last; ++w) {
+              const int sl = (w == w_first && w * Ttot / Weff < seg_units0) ? 1 : 0;
+              Mx = fmaxf(Mx, __ldcg(p.ws_ml + ((size_t)w * 2 + sl) * R + r).x);
+            }
+            float Ls = 0.f, O[DL];
+#pragma unroll
+            for (int e = 0; e < DL; ++e) O[e] = 0.f;
+            for (long long w = w_first; w <= w_last; ++w) {
+              const int sl = (w == w_first && w * Ttot / Weff < seg_units0) ? 1 : 0;
+              const size_t idx = ((size_t)w * 2 + sl) * R + r;
+              const float2 v = __ldcg(p.ws_ml + idx);
+              const float wt = v.x == -INFINITY ? 0.f : v.y * exp2f(v.x - Mx);
+              Ls += wt;
+              const float* src = p.ws_o + idx * D + lane * DL;
+#pragma unroll
+              for (int e = 0; e < DL; ++e) O[e] += __ldcg(src + e) * wt;
+            }
+            float* dst = rows_buf + r * RF;
+            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+#pragma unroll
+            for (int e = 0; e < DL; ++e) dst[lane * DL + e] = O[e] * inv;
+            if (lane == 0) {
+              dst[D] = Mx;
+              dst[D + 1] = Ls;
+            }
+          }
+          __syncwarp();
+          done = true;
+        }
+      }
+      if (done) {
+        if (cc.part == 0)
+          complete_prefix(cc, whole);
+        else
+          complete_tail(cc, whole);
+      }
+    }
+    scursor_next(cc, x, NG);
+  }
+}
+
 // Persistent grid of one phase kernel on the current device (cached).
 template <typename T, int D, int TG, int PH, int NW>
 cudaError_t grouped_grid(int& grid) {
@@ -1095,22 +1790,46 @@ cudaError_t launch_phase(int grid, const CUtensorMap& kmap, const CUtensorMap& v
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// Validation prologue, then the prefix phase and the tail phase, each
-// launched as a programmatic dependent of the launch before it. For 16-bit
-// data the pools' tensor maps (boxes of {64, min(block_size, 16)} rows) feed
-// the prefix phase's TMA loads.
+// Persistent grid of the single-launch kernel on the current device (cached).
+template <typename T, int D, int TG>
+cudaError_t shared_grid(int& grid) {
+  using S = SharedShape<D, kDecodeWarps>;
+  static int grid_of_device[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  grid = (dev >= 0 && dev < 64) ? __atomic_load_n(&grid_of_device[dev], __ATOMIC_ACQUIRE) : 0;
+  if (grid != 0) return cudaSuccess;
+  e = cudaFuncSetAttribute(pa_decode_shared_kernel<T, D, TG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           S::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  int sms = 0, per_sm = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_decode_shared_kernel<T, D, TG>,
+                                                    kDecodeWarps * 32, S::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  grid = sms * (per_sm > 0 ? per_sm : 1);
+  if (grid > kMaxDecodeWarps / kDecodeWarps) grid = kMaxDecodeWarps / kDecodeWarps;
+  if (dev >= 0 && dev < 64) __atomic_store_n(&grid_of_device[dev], grid, __ATOMIC_RELEASE);
+  return cudaSuccess;
+}
+
+// Validation prologue, then the work as a programmatic dependent of it: for
+// 16-bit data one single-launch kernel (the pools' tensor maps, boxes of
+// {64, min(block_size, 16)} rows, feed its prefix tiles); for fp32 data the
+// prefix phase and then the tail phase.
 template <typename T, int D, int TG>
 cudaError_t launch_pa_decode_grouped(const GroupedParams& gp, cudaStream_t stream) {
-  constexpr int NW0 = grouped_warps<T, 0>(), NW1 = grouped_warps<T, 1>();
-  int grid0 = 0, grid1 = 0;
-  cudaError_t e = grouped_grid<T, D, TG, 0, NW0>(grid0);
-  if (e != cudaSuccess) return e;
-  e = grouped_grid<T, D, TG, 1, NW1>(grid1);
-  if (e != cudaSuccess) return e;
   CUtensorMap kmap, vmap;
   memset(&kmap, 0, sizeof(kmap));
   memset(&vmap, 0, sizeof(vmap));
+  int pro = (gp.num_groups + 7) / 8;
+  pro = pro < 1 ? 1 : (pro > 4096 ? 4096 : pro);
   if constexpr (Mma16816<T>::kOk) {
+    int grid = 0;
+    cudaError_t e = shared_grid<T, D, TG>(grid);
+    if (e != cudaSuccess) return e;
     const DecodeParams& p = gp.base;
     const uint64_t rows = (uint64_t)p.num_blocks * p.num_kv_heads * p.block_size;
     const int box_rows = p.block_size < kTileTokens ? p.block_size : kTileTokens;
@@ -1119,15 +1838,35 @@ cudaError_t launch_pa_decode_grouped(const GroupedParams& gp, cudaStream_t strea
     if (e != cudaSuccess) return e;
     e = encode_pool_rows_map(&vmap, p.v_cache, rows, D, box_rows, bf16);
     if (e != cudaSuccess) return e;
+    pa_group_prologue_kernel<T><<<pro, 256, 0, stream>>>(gp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kDecodeWarps * 32);
+    cfg.dynamicSmemBytes = SharedShape<D, kDecodeWarps>::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, pa_decode_shared_kernel<T, D, TG>, kmap, vmap, gp);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  } else {
+    constexpr int NW0 = grouped_warps<T, 0>(), NW1 = grouped_warps<T, 1>();
+    int grid0 = 0, grid1 = 0;
+    cudaError_t e = grouped_grid<T, D, TG, 0, NW0>(grid0);
+    if (e != cudaSuccess) return e;
+    e = grouped_grid<T, D, TG, 1, NW1>(grid1);
+    if (e != cudaSuccess) return e;
+    pa_group_prologue_kernel<T><<<pro, 256, 0, stream>>>(gp);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    e = launch_phase<T, D, TG, 0, NW0>(grid0, kmap, vmap, gp, stream);
+    if (e != cudaSuccess) return e;
+    return launch_phase<T, D, TG, 1, NW1>(grid1, kmap, vmap, gp, stream);
   }
-  int pro = (gp.num_groups + 7) / 8;
-  pro = pro < 1 ? 1 : (pro > 4096 ? 4096 : pro);
-  pa_group_prologue_kernel<T><<<pro, 256, 0, stream>>>(gp);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  e = launch_phase<T, D, TG, 0, NW0>(grid0, kmap, vmap, gp, stream);
-  if (e != cudaSuccess) return e;
-  return launch_phase<T, D, TG, 1, NW1>(grid1, kmap, vmap, gp, stream);
 }
 
 using GroupedLauncher = cudaError_t (*)(const GroupedParams&, cudaStream_t);
