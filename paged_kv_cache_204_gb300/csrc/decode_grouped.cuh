@@ -1069,8 +1069,21 @@ __global__ void __launch_bounds__(NW * 32)
 //     counter.
 // Sequences of rejected or single-member groups have tails only.
 
+// Work units of the single-launch kernel, in eighths of a prefix tile's
+// time (measured per warp on the copy-on-write step): a prefix tile 8, a
+// tail tile 10 (one query row on CUDA cores, its last tile often partly
+// filled), the end of a prefix segment 28 and of a tail segment 25
+// (reductions, and the two parts of each row meeting in shared memory or
+// through the workspace). A tile belongs to the warp whose unit range holds
+// its first unit; ranges are at least kUnitMax long, so every warp between
+// the first and the last of a segment's warps gets some of its tiles.
+constexpr int kUnitP = 8, kUnitT = 10, kChargeP = 28, kChargeT = 25, kUnitMax = 10;
+
+__device__ __forceinline__ int sunit(int part) { return part == 0 ? kUnitP : kUnitT; }
+__device__ __forceinline__ int scharge(int part) { return part == 0 ? kChargeP : kChargeT; }
+
 struct SCursor {
-  long long g;        // unit of the current tile
+  long long g;        // first unit of the current tile
   int grp, hg, part, j, t, nt;
   int lo, M, S, nch;  // group: members [lo, lo + M), usable prefix S (0: none), row chunks of 8
   int h, c;           // prefix segment: query head and row chunk
@@ -1096,11 +1109,11 @@ __device__ __forceinline__ void sgroup_load(SCursor& c, const GCtx& x) {
 
 // Units of one prefix segment and of one head group of the loaded group.
 __device__ __forceinline__ long long sprefix_seg_units(const SCursor& c) {
-  return c.S / kTileTokens + kSegCostPrefix;
+  return (long long)(c.S / kTileTokens) * kUnitP + kChargeP;
 }
 __device__ __forceinline__ long long shg_units(const SCursor& c, const GCtx& x) {
   long long u = c.S > 0 ? (long long)x.gpw * c.nch * sprefix_seg_units(c) : 0;
-  for (int k = 0; k < c.M; ++k) u += tiles_of(ctx_len(x, c.lo + k) - c.S) + kSegCostTail;
+  for (int k = 0; k < c.M; ++k) u += (long long)tiles_of(ctx_len(x, c.lo + k) - c.S) * kUnitT + kChargeT;
   return u;
 }
 
@@ -1157,13 +1170,13 @@ __device__ __forceinline__ void sseg_next(SCursor& c, const GCtx& x, int NG) {
   sseg_enter(c, x);
 }
 
-// Next tile: c.g is its unit (the next segment's charged units skipped).
+// Next tile: c.g is its first unit (the next segment's charge skipped).
 __device__ __forceinline__ void scursor_next(SCursor& c, const GCtx& x, int NG) {
-  ++c.g;
+  c.g += sunit(c.part);
   if (++c.t < c.nt) return;
   c.t = 0;
   sseg_next(c, x, NG);
-  c.g += c.part == 0 ? kSegCostPrefix : kSegCostTail;
+  c.g += scharge(c.part);
 }
 
 // Shared memory of the single-launch kernel: two stages per warp (a prefix
@@ -1258,7 +1271,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   long long mine = 0, Ttot = 0;
   for (int gi = threadIdx.x; gi < NG; gi += NW * 32) mine += group_units(gi);
   block_exclusive_scan<NW>(mine, scan, Ttot);
-  const long long Weff = W < Ttot ? W : Ttot;
+  const long long Weff = W < Ttot / kUnitMax ? W : Ttot / kUnitMax;
   if (threadIdx.x < NW) starts[threadIdx.x] = make_longlong2(-1, 0);
   __syncthreads();
   long long carry = 0;
@@ -1306,28 +1319,37 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     long long r = st0.y - ci.hg * uhg;
     const long long pseg = sprefix_seg_units(ci);
     const long long pu = ci.S > 0 ? (long long)x.gpw * ci.nch * pseg : 0;
-    int r2;
+    long long r2;  // the range's start relative to the segment's first tile
     if (r < pu) {
       ci.part = 0;
       ci.j = static_cast<int>(r / pseg);
-      r2 = static_cast<int>(r - ci.j * pseg) - kSegCostPrefix;
+      r2 = r - ci.j * pseg - kChargeP;
     } else {
       r -= pu;
       ci.part = 1;
       int k = 0;
       for (;;) {
-        const long long uk = tiles_of(ctx_len(x, ci.lo + k) - ci.S) + kSegCostTail;
+        const long long uk = (long long)tiles_of(ctx_len(x, ci.lo + k) - ci.S) * kUnitT + kChargeT;
         if (r < uk || k == ci.M - 1) break;
         r -= uk;
         ++k;
       }
       ci.j = k;
-      r2 = static_cast<int>(r) - kSegCostTail;
+      r2 = r - kChargeT;
     }
     ci.t = 0;
     sseg_enter(ci, x);
-    ci.t = r2 < 0 ? 0 : r2;  // a range that starts on charged units starts at tile 0
-    ci.g = a_begin + (ci.t - r2);
+    // the first tile whose first unit is inside the range
+    const int w = sunit(ci.part);
+    const long long t = r2 <= 0 ? 0 : (r2 + w - 1) / w;
+    if (t < ci.nt) {
+      ci.t = static_cast<int>(t);
+      ci.g = a_begin - r2 + t * w;
+    } else {  // the segment's last tile began before the range: start at the next one
+      ci.g = a_begin - r2 + (long long)ci.nt * w;
+      sseg_next(ci, x, NG);
+      ci.g += scharge(ci.part);
+    }
   }
   SCursor cc = ci;
   const long long g_first = ci.g;
@@ -1449,13 +1471,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     if (whole && x.gpw == 1 && c.nch == 1) {
       // member k's tail ends at unit c.g + sum_{i <= k} (charge + tiles_i):
       // its row stays local when that is still inside this warp's range
-      long long u = lane < c.M ? tiles_of(ctx_len(x, c.lo + lane) - c.S) + kSegCostTail : 0;
+      // member k's tail: its last tile starts at c.g + kUnitP - kUnitT +
+      // sum_{i <= k} (kChargeT + kUnitT tiles_i); the row stays local when
+      // that tile is still inside this warp's range
+      long long u = lane < c.M ? (long long)tiles_of(ctx_len(x, c.lo + lane) - c.S) * kUnitT + kChargeT : 0;
 #pragma unroll
       for (int o2 = 1; o2 < 32; o2 <<= 1) {
         const long long y = __shfl_up_sync(kFullMask, u, o2);
         if (lane >= o2) u += y;
       }
-      local = __ballot_sync(kFullMask, lane < c.M && c.g + u <= a_end - 1);
+      local = __ballot_sync(kFullMask, lane < c.M && c.g + kUnitP - kUnitT + u <= a_end - 1);
       pb_grp = c.grp;
       pb_hg = c.hg;
     } else {
@@ -1549,7 +1574,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     const int t0 = cc.tok0 + cc.t * kTileTokens;
     const int nvalid = min(max(cc.tok_end - t0, 0), kTileTokens);
     const bool first = cc.t == 0 || cc.g == g_first;
-    const bool last = cc.t == cc.nt - 1 || cc.g == a_end - 1;
+    const bool last = cc.t == cc.nt - 1 || cc.g + sunit(cc.part) >= a_end;
     const int nr = cc.nrows;
 
     if (cc.part == 0) {
@@ -1626,7 +1651,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       }
       // this warp's (m, l, o / l) of the segment's rows: into the row buffer
       // (whole segment) or into a partial slot (one piece)
-      const int slot = cc.g - cc.t - (cc.part == 0 ? kSegCostPrefix : kSegCostTail) <= a_begin ? 0 : 1;
+      const int slot = cc.g - (long long)cc.t * sunit(cc.part) - scharge(cc.part) <= a_begin ? 0 : 1;
       const size_t base = ((size_t)wid * 2 + slot) * R;
       float* o_dst = whole ? rows_buf : p.ws_o + base * D;
       const int o_stride = whole ? RF : D;
@@ -1678,12 +1703,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       if (!whole) {
         // one piece of a segment shared with neighbouring warps: the last
         // piece to arrive merges all pieces into the row buffer
-        const long long E = cc.part == 0 ? kSegCostPrefix : kSegCostTail;
-        const long long seg_start = cc.g - cc.t;
-        const long long seg_end = seg_start + cc.nt;
-        const long long seg_units0 = seg_start - E;
+        // the warps holding the first units of the segment's first and last tiles
+        const long long seg_start = cc.g - (long long)cc.t * sunit(cc.part);
+        const long long seg_last = seg_start + (long long)(cc.nt - 1) * sunit(cc.part);
+        const long long seg_units0 = seg_start - scharge(cc.part);
         const long long w_first = ((seg_start + 1) * Weff + Ttot - 1) / Ttot - 1;
-        const long long w_last = (seg_end * Weff + Ttot - 1) / Ttot - 1;
+        const long long w_last = ((seg_last + 1) * Weff + Ttot - 1) / Ttot - 1;
         int is_last = 0;
         if (lane == 0) {
           const size_t ci_idx = cc.part == 0 ? (size_t)(cc.lo + R * cc.c) * H + cc.h
