@@ -71,6 +71,11 @@ CASES = {
     "tile_edges": dict(user_len=("fixed", (63, 64, 65, 128, 129)), users=5, system_len=0, num_blocks=400, seed=2095),
     # users with no new tokens (n = 0) between users with some: their tiles do nothing
     "zero_query_users": dict(user_len=("fixed", (0, 70, 1, 0)), users=4, system_len=20, seed=2096),
+    # head_dim 64 over long contexts: one query tile per user (every K/V tile's S issued two tiles
+    # ahead), and pairs of query tiles whose second tile reads K/V tiles past the first's causal end
+    "d64_long_single_tile": dict(system_len=300, user_len=("uniform", 60, 120), users=3, num_blocks=400,
+                                 seed=2098),
+    "d64_long_pairs": dict(system_len=200, user_len=("uniform", 130, 250), users=3, num_blocks=400, seed=2099),
 }
 
 
