@@ -1079,6 +1079,12 @@ __global__ void __launch_bounds__(NW * 32)
 // the first and the last of a segment's warps gets some of its tiles.
 constexpr int kUnitP = 8, kUnitT = 10, kChargeP = 28, kChargeT = 25, kUnitMax = 10;
 
+// Warps per block and ring stages per warp of the single-launch kernel
+// (measured on the copy-on-write step, attention: 8 x 2 139.6 us, 6 x 3 164.9
+// us, 4 x 3 213.4 us, 4 x 4 214.1 us; registers (244 per thread) and shared
+// memory leave no room for more warps).
+constexpr int kSharedWarps = 8, kSharedStages = 2;
+
 __device__ __forceinline__ int sunit(int part) { return part == 0 ? kUnitP : kUnitT; }
 __device__ __forceinline__ int scharge(int part) { return part == 0 ? kChargeP : kChargeT; }
 
@@ -1186,7 +1192,7 @@ __device__ __forceinline__ void scursor_next(SCursor& c, const GCtx& x, int NG) 
 // rows), then mbarriers, block-table chunks and the start-up scan.
 template <int D, int NW>
 struct SharedShape {
-  static constexpr int kStages = 2;
+  static constexpr int kStages = kSharedStages;
   static constexpr int kStageBytes = PrefixStage<D>::kBytes;
   static constexpr int kRowFloats = D + 4;  // o / l, then m and l
   static constexpr int kPbufOff = NW * kStages * kStageBytes;
@@ -1212,10 +1218,10 @@ __device__ __forceinline__ void lse_combine(float am, float al, const float (&ao
 }
 
 template <typename T, int D, int TG>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
+__global__ void __launch_bounds__(kSharedWarps * 32)
     pa_decode_shared_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                             const GroupedParams gp) {
-  constexpr int NW = kDecodeWarps;
+  constexpr int NW = kSharedWarps;
   using S = SharedShape<D, NW>;
   using St = PrefixStage<D>;
   constexpr int R = kMaxPrefixRows;
@@ -1818,7 +1824,7 @@ cudaError_t launch_phase(int grid, const CUtensorMap& kmap, const CUtensorMap& v
 // Persistent grid of the single-launch kernel on the current device (cached).
 template <typename T, int D, int TG>
 cudaError_t shared_grid(int& grid) {
-  using S = SharedShape<D, kDecodeWarps>;
+  using S = SharedShape<D, kSharedWarps>;
   static int grid_of_device[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1832,10 +1838,10 @@ cudaError_t shared_grid(int& grid) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pa_decode_shared_kernel<T, D, TG>,
-                                                    kDecodeWarps * 32, S::kSmemBytes);
+                                                    kSharedWarps * 32, S::kSmemBytes);
   if (e != cudaSuccess) return e;
   grid = sms * (per_sm > 0 ? per_sm : 1);
-  if (grid > kMaxDecodeWarps / kDecodeWarps) grid = kMaxDecodeWarps / kDecodeWarps;
+  if (grid > kMaxDecodeWarps / kSharedWarps) grid = kMaxDecodeWarps / kSharedWarps;
   if (dev >= 0 && dev < 64) __atomic_store_n(&grid_of_device[dev], grid, __ATOMIC_RELEASE);
   return cudaSuccess;
 }
@@ -1868,8 +1874,8 @@ cudaError_t launch_pa_decode_grouped(const GroupedParams& gp, cudaStream_t strea
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kDecodeWarps * 32);
-    cfg.dynamicSmemBytes = SharedShape<D, kDecodeWarps>::kSmemBytes;
+    cfg.blockDim = dim3(kSharedWarps * 32);
+    cfg.dynamicSmemBytes = SharedShape<D, kSharedWarps>::kSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
