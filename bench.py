@@ -661,7 +661,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         "attention_ms": agg["decode_ms"], "cache_ops_ms": agg["cache_ms"],
         "bytes_per_step": nbytes["step"], "roofline_frac_step": nbytes["step"] / (agg["step_ms"] * 1e-3) / 1e9 / peak,
         "roofline": {"bound": "hbm",
-                     "kernel": ("pa_group_prologue + pa_decode_grouped_kernel" if grouped else
+                     "kernel": ("pa_group_prologue + pa_decode_shared_kernel" if grouped else
                                 "pa_decode_kernel<fp8 e4m3 cache>" if fp8 else "pa_decode_kernel"),
                      "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
@@ -902,7 +902,7 @@ def run_beam(args, rank: int, world: int, local_rank: int) -> int:
         "seqs_per_s": world * B / (agg["step_ms"] * 1e-3),
         "attention_ms": agg["attn_ms"], "cache_ops_ms": agg["cache_ms"],
         "bytes_per_step": bytes_step,
-        "roofline": {"bound": "hbm", "kernel": "pa_group_prologue + pa_decode_grouped_kernel",
+        "roofline": {"bound": "hbm", "kernel": "pa_group_prologue + pa_decode_shared_kernel",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None, "algorithmic_bytes_per_launch": bytes_attn, "peak_source": peak_src},
         "cpu_baseline": cpu,

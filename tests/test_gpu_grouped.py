@@ -113,7 +113,7 @@ def test_workspace_reuse_and_plain_agreement():
 
 
 def test_wait_timeout_is_reported_and_context_survives():
-    """With a wait limit of 0 the prefix and tail launches give up at their
+    """With a wait limit of 0 the grouped kernel's warps give up at their
     first wait that is not already complete: they report PKV_DEV_ERR_TIMEOUT
     (and nothing else), let their own copies land and return. After the
     workspace is cleared, the next call with the default limit matches the
