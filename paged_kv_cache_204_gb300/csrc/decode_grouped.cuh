@@ -1085,6 +1085,12 @@ constexpr int kUnitP = 8, kUnitT = 10, kChargeP = 28, kChargeT = 25, kUnitMax = 
 // memory leave no room for more warps).
 constexpr int kSharedWarps = 8, kSharedStages = 2;
 
+// Rows whose pieces one warp loads together when it merges a segment cut by
+// warp ranges (fewer where more query heads per warp leave fewer registers
+// free).
+template <int TG>
+__host__ __device__ constexpr int merge_rows() { return TG == 1 ? 4 : TG == 2 ? 2 : 1; }
+
 __device__ __forceinline__ int sunit(int part) { return part == 0 ? kUnitP : kUnitT; }
 __device__ __forceinline__ int scharge(int part) { return part == 0 ? kChargeP : kChargeT; }
 
@@ -1232,6 +1238,7 @@ __global__ void __launch_bounds__(kSharedWarps * 32)
   constexpr int DPL = D / 8;
   constexpr int DL = D / 32;  // dims per lane in merges and combines
   constexpr int RF = S::kRowFloats;
+  constexpr int kMergeRows = merge_rows<TG>();
   const DecodeParams& p = gp.base;
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -1727,32 +1734,56 @@ __global__ void __launch_bounds__(kSharedWarps * 32)
         is_last = __shfl_sync(kFullMask, is_last, 0);
         if (is_last) {
           __syncwarp();
-          for (int r = 0; r < nr; ++r) {
-            float Mx = -INFINITY;
+          // kMergeRows rows at a time, their pieces' loads in flight together;
+          // each piece folds in by the running-maximum rule
+          for (int r0 = 0; r0 < nr; r0 += kMergeRows) {
+            float Mx[kMergeRows], Ls[kMergeRows], O[kMergeRows][DL];
+#pragma unroll
+            for (int i = 0; i < kMergeRows; ++i) {
+              Mx[i] = -INFINITY;
+              Ls[i] = 0.f;
+#pragma unroll
+              for (int e = 0; e < DL; ++e) O[i][e] = 0.f;
+            }
             for (long long w = w_first; w <= w_last; ++w) {
               const int sl = (w == w_first && w * Ttot / Weff < seg_units0) ? 1 : 0;
-              Mx = fmaxf(Mx, __ldcg(p.ws_ml + ((size_t)w * 2 + sl) * R + r).x);
+              const size_t idx0 = ((size_t)w * 2 + sl) * R + r0;
+              float2 v[kMergeRows];
+              float ov[kMergeRows][DL];
+#pragma unroll
+              for (int i = 0; i < kMergeRows; ++i) {
+                v[i] = make_float2(-INFINITY, 0.f);
+                if (r0 + i < nr) {
+                  v[i] = __ldcg(p.ws_ml + idx0 + i);
+#pragma unroll
+                  for (int e = 0; e < DL; ++e) ov[i][e] = __ldcg(p.ws_o + (idx0 + i) * D + lane * DL + e);
+                }
+              }
+#pragma unroll
+              for (int i = 0; i < kMergeRows; ++i) {
+                if (v[i].x != -INFINITY) {  // an empty piece adds nothing
+                  const float Mn = fmaxf(Mx[i], v[i].x);
+                  const float a = exp2f(Mx[i] - Mn);  // 0 while nothing was folded in
+                  const float b = v[i].y * exp2f(v[i].x - Mn);
+                  Ls[i] = Ls[i] * a + b;
+#pragma unroll
+                  for (int e = 0; e < DL; ++e) O[i][e] = O[i][e] * a + ov[i][e] * b;
+                  Mx[i] = Mn;
+                }
+              }
             }
-            float Ls = 0.f, O[DL];
 #pragma unroll
-            for (int e = 0; e < DL; ++e) O[e] = 0.f;
-            for (long long w = w_first; w <= w_last; ++w) {
-              const int sl = (w == w_first && w * Ttot / Weff < seg_units0) ? 1 : 0;
-              const size_t idx = ((size_t)w * 2 + sl) * R + r;
-              const float2 v = __ldcg(p.ws_ml + idx);
-              const float wt = v.x == -INFINITY ? 0.f : v.y * exp2f(v.x - Mx);
-              Ls += wt;
-              const float* src = p.ws_o + idx * D + lane * DL;
+            for (int i = 0; i < kMergeRows; ++i) {
+              if (r0 + i < nr) {
+                float* dst = rows_buf + (r0 + i) * RF;
+                const float inv = Ls[i] > 0.f ? 1.f / Ls[i] : 0.f;
 #pragma unroll
-              for (int e = 0; e < DL; ++e) O[e] += __ldcg(src + e) * wt;
-            }
-            float* dst = rows_buf + r * RF;
-            const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
-#pragma unroll
-            for (int e = 0; e < DL; ++e) dst[lane * DL + e] = O[e] * inv;
-            if (lane == 0) {
-              dst[D] = Mx;
-              dst[D + 1] = Ls;
+                for (int e = 0; e < DL; ++e) dst[lane * DL + e] = O[i][e] * inv;
+                if (lane == 0) {
+                  dst[D] = Mx[i];
+                  dst[D + 1] = Ls[i];
+                }
+              }
             }
           }
           __syncwarp();
