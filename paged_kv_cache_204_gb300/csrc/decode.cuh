@@ -32,7 +32,9 @@
 // lanes of a group with shuffles; the running max m, exp-sum l and output o
 // follow the online softmax in base 2 (q is pre-scaled by scale * log2(e));
 // tokens past the context are masked by select, never by multiplication, so
-// poisoned rows never reach the result.
+// poisoned rows never reach the result. An fp8 cache read with one query head
+// per warp takes the tensor-core tile instead (FpMma below): same ring,
+// segments and merges, q.K^T and P.V of each 32-token tile as MMAs.
 #pragma once
 
 #include <type_traits>
@@ -77,8 +79,13 @@ constexpr int kDecodeWarps = 8;  // one resident block of 8 warps per SM (measur
 // fp8 caches (1 or 2 query heads per warp): a warp's per-tile work is a
 // longer latency chain for half the bytes, so more warps share an SM (as many
 // as registers allow) with a larger ring budget.
-constexpr int kFp8Warps1 = 20;  // one query head per warp (measured: 16 -> 193 us, 20 -> 184 us, 24 -> 189 us)
-constexpr int kFp8Warps2 = 12;  // two query heads per warp (register limit)
+constexpr int kFp8Warps2 = 12;  // two query heads per warp, CUDA cores (register limit)
+// One query head per warp: q.K^T and P.V of a tile on tensor cores (FpMma
+// below), one 32-token stage per warp. Measured on the LLaMA-13B-shaped step
+// (attention, 200 steps): 12 warps (two stages each) 176.7 us, 16 warps
+// 170.6 us, 20 warps 182.5 us (registers capped at 96: spills); 16-token
+// tiles with three stages per warp 191.2 us at 16 warps.
+constexpr int kFp8MmaWarps = 16;
 constexpr int kFp8RingBudget = 200 * 1024;
 constexpr int kMaxDecodeWarps = 4096;  // bound of the persistent grid (partial slots in the workspace)
 constexpr int kMaxGroupPerWarp = 4;    // query heads one warp serves against one kv head
@@ -144,11 +151,78 @@ struct LaneDims<T, __nv_fp8_e4m3, D> {
   }
 };
 
+// Tensor-core tile of an fp8 cache with one query head per warp (m16n8k16,
+// binary16 operands, fp32 accumulation). Every e4m3 value is exactly a
+// binary16 value, so K and V enter the MMAs exactly; the query row enters as
+// binary16 after scaling by a power of two that brings its largest element
+// into [2^14, 2^15) (exact for every element within 2^28 of the largest; the
+// power of two is taken back out of the scores), and P as a binary16 high
+// part plus a binary16 remainder, about 22 significant bits.
+//
+// Scores, S^T = K q^T: the tile's tokens are M (two 16-token halves), the
+// head dims K, and q fills every column of N, so every lane holds scores.
+// The head dims are permuted consistently in K and q (which leaves the dot
+// product unchanged) so that lane (g, t) = (lane / 4, lane % 4) finds every A
+// element it needs in bytes [t D/4, (t+1) D/4) of its two token rows: k-step
+// kk, MMA column 2t + u + 8v is byte t D/4 + 4 kk + 2 v + u. Lane (g, t) holds
+// the scores of tokens g and g + 8 of each half.
+//
+// Output, O^T += V^T P^T: the head dims are M (D / 16 tiles), the tokens K,
+// P_hi and P_lo columns 0 and 1 of N (the rest zero). The B fragments of P^T
+// are the transposes (movmatrix) of the 8 x 8 matrices [token][column] that
+// the score layout gives. MMA row 16 m + g + 8 v is head dim (D/8) g + 2 m + v,
+// so lane (g, t) reads bytes [g D/8, (g+1) D/8) of its four token rows 2t,
+// 2t + 1, 2t + 8, 2t + 9, and lane 4g ends with the head dims (D/8) g .. + D/8:
+// the same dims lane g holds in the CUDA-core layout.
+struct FpMma {
+  __device__ __forceinline__ static void mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+  // the two e4m3 codes in the low (high) 16 bits of w as a binary16 pair,
+  // the lower byte in the lower half
+  __device__ __forceinline__ static uint32_t lo2(uint32_t w) {
+    uint32_t r;
+    asm("{.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, l;}" : "=r"(r) : "r"(w));
+    return r;
+  }
+  __device__ __forceinline__ static uint32_t hi2(uint32_t w) {
+    uint32_t r;
+    asm("{.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, h;}" : "=r"(r) : "r"(w));
+    return r;
+  }
+  __device__ __forceinline__ static uint32_t pack(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    uint32_t u;
+    memcpy(&u, &h, 4);
+    return u;
+  }
+  __device__ __forceinline__ static float2 unpack(uint32_t u) {
+    __half2 h;
+    memcpy(&h, &u, 4);
+    return __half22float2(h);
+  }
+  // transpose of an 8 x 8 matrix of 16-bit elements in fragment layout
+  __device__ __forceinline__ static uint32_t trans(uint32_t a) {
+    uint32_t d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+  }
+  // 2^k with k in [-126, 127]
+  __device__ __forceinline__ static float pow2(int k) { return __int_as_float((k + 127) << 23); }
+};
+
 // NWO / BudgetO: explicit warps per block and ring budget (0: the defaults).
 template <typename T, int D, int GPW, typename KT = T, int NWO = 0, int BudgetO = 0>
 struct DecodeShape {
   static constexpr bool kFp8Wide = sizeof(KT) == 1 && GPW <= 2;
-  static constexpr int kWarps = NWO ? NWO : (kFp8Wide ? (GPW == 1 ? kFp8Warps1 : kFp8Warps2) : kDecodeWarps);
+  static constexpr bool kFp8Mma = sizeof(KT) == 1 && GPW == 1;
+  static constexpr int kWarps =
+      NWO ? NWO : (kFp8Mma ? kFp8MmaWarps : kFp8Wide ? kFp8Warps2 : kDecodeWarps);
   static constexpr int kElemBytes = sizeof(T);
   static constexpr int kRowBytes = D * kElemBytes;                       // query / output row
   static constexpr int kKvRowBytes = D * (int)sizeof(KT);                // cache row
@@ -238,6 +312,8 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
   using S = DecodeShape<T, D, GPW, KT>;
   using LD = LaneDims<T, KT, D>;
   constexpr bool kQuant = !std::is_same<T, KT>::value;
+  constexpr bool kMma = S::kFp8Mma;    // fp8 cache, one query head per warp: tensor-core tiles
+  constexpr int NKS = D / 16;          // MMA k-steps of the scores, m-tiles of the output
   constexpr int TT = S::kTileTokensT;  // tokens per tile
   constexpr int RPG = TT / 4;          // rows of a tile per 8-lane group
   constexpr int NW = S::kWarps;
@@ -384,6 +460,11 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
 
   float qf[GPW][DPL];
   float m[GPW], l[GPW], o[GPW][DPL];
+  // tensor-core state (kMma): the scaled query as B fragments, O^T
+  // accumulators, and the scale of the scores
+  uint32_t qb[NKS][2];
+  float oa[NKS][4];
+  float sc_q = 0.f;
   bool visit_from_start = true;
   const size_t H = p.num_heads;
 
@@ -402,7 +483,46 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
     const bool first = cc.t == 0 || cc.g == a_begin;
     const bool last = cc.t == cc.nt - 1 || cc.g == a_end - 1;
 
-    if (first) {
+    if constexpr (kMma) {
+      if (first) {
+        visit_from_start = cc.t == 0;
+        m[0] = -INFINITY;
+        l[0] = 0.f;
+#pragma unroll
+        for (int mm = 0; mm < NKS; ++mm) oa[mm][0] = oa[mm][1] = oa[mm][2] = oa[mm][3] = 0.f;
+        if (nvalid > 0) {
+          // lane (g, t) takes query dims [t D/4, (t+1) D/4); lanes 0-3 (g = 0)
+          // hold them as the B column, the others zeros
+          constexpr int QPL = D / 4;
+          const int t = lane & 3;
+          const uint4* qr = reinterpret_cast<const uint4*>(ks + 2 * S::kTileBytes + t * QPL * (int)sizeof(T));
+          float qv[QPL];
+#pragma unroll
+          for (int c = 0; c < QPL / 8; ++c) {
+            float f8[8];
+            Chunk<T>::widen(qr[c], f8);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) qv[8 * c + e] = f8[e];
+          }
+          float amax = 0.f;
+#pragma unroll
+          for (int e = 0; e < QPL; ++e) amax = fmaxf(amax, fabsf(qv[e]));
+          amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+          // largest element times 2^k in [2^14, 2^15)
+          int k = 0;
+          if (amax > 0.f) k = min(141 - ((__float_as_int(amax) >> 23) & 0xff), 127);
+          const float sig = FpMma::pow2(max(k, -126));
+          sc_q = ldexpf(p.scale_log2, -max(k, -126));
+#pragma unroll
+          for (int kk = 0; kk < NKS; ++kk) {  // the same query in every column
+            qb[kk][0] = FpMma::pack(qv[4 * kk] * sig, qv[4 * kk + 1] * sig);
+            qb[kk][1] = FpMma::pack(qv[4 * kk + 2] * sig, qv[4 * kk + 3] * sig);
+          }
+        }
+      }
+    }
+    if (first && !kMma) {
       visit_from_start = cc.t == 0;
 #pragma unroll
       for (int g = 0; g < GPW; ++g) {
@@ -426,7 +546,109 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
       }
     }
 
-    if (nvalid > 0) {
+    if constexpr (kMma) {
+      if (nvalid > 0) {
+        // ---- tensor-core tile (layouts: FpMma) --------------------------------
+        const int g = lane >> 2, t = lane & 3;
+        constexpr int MT = TT / 16;  // 16-token row blocks of the tile
+        float sacc[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
+          // bytes [t D/4, (t+1) D/4) of token rows 16 mt + g and 16 mt + g + 8
+          uint32_t w0[NKS], w1[NKS];
+          const uint4* r0 = reinterpret_cast<const uint4*>(ks + (16 * mt + g) * KROW + t * (D / 4));
+          const uint4* r1 = reinterpret_cast<const uint4*>(ks + (16 * mt + g + 8) * KROW + t * (D / 4));
+#pragma unroll
+          for (int c = 0; c < NKS / 4; ++c) {
+            const uint4 a = r0[c], b = r1[c];
+            w0[4 * c] = a.x, w0[4 * c + 1] = a.y, w0[4 * c + 2] = a.z, w0[4 * c + 3] = a.w;
+            w1[4 * c] = b.x, w1[4 * c + 1] = b.y, w1[4 * c + 2] = b.z, w1[4 * c + 3] = b.w;
+          }
+#pragma unroll
+          for (int kk = 0; kk < NKS; ++kk)
+            FpMma::mma(sacc[mt], FpMma::lo2(w0[kk]), FpMma::lo2(w1[kk]), FpMma::hi2(w0[kk]),
+                       FpMma::hi2(w1[kk]), qb[kk][0], qb[kk][1]);
+        }
+        // every lane (g, t) holds the scores of tokens 16 mt + g + 8 v (all
+        // columns are equal)
+        float x[MT][2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            const int tok = 16 * mt + g + 8 * v;
+            x[mt][v] = tok < nvalid ? sacc[mt][2 * v] * sc_q : -INFINITY;
+            mx = fmaxf(mx, x[mt][v]);
+          }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, off));
+        const float mn = fmaxf(m[0], mx);
+        const float alpha = exp2f(m[0] - mn);  // 0 on the first tile (m = -inf)
+        m[0] = mn;
+        float pv[MT][2], ps = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            pv[mt][v] = exp2f(x[mt][v] - mn);
+            ps += pv[mt][v];
+          }
+        l[0] = l[0] * alpha + ps;  // this lane's tokens (each counted by the 4 lanes of its row)
+        if (alpha != 1.f) {        // warp-uniform
+#pragma unroll
+          for (int mm = 0; mm < NKS; ++mm)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oa[mm][e] *= alpha;
+        }
+        // O^T += V^T P^T, one 16-token k-step at a time
+#pragma unroll
+        for (int ks2 = 0; ks2 < MT; ++ks2) {
+          // P of tokens 16 ks2 + g (+ 8) as a binary16 high part and remainder,
+          // as the 8 x 8 matrices M[token][column] (column 0 P_hi, 1 P_lo, the
+          // rest 0) in MMA fragment layout; transposed, they are the B fragments
+          // of P^T (lane (g, t): column g, tokens 2t, 2t + 1)
+          uint32_t mv[2];
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            const float ph = __half2float(__float2half_rn(pv[ks2][v]));
+            mv[v] = t == 0 ? FpMma::pack(ph, pv[ks2][v] - ph) : 0u;
+          }
+          const uint32_t b0 = FpMma::trans(mv[0]), b1 = FpMma::trans(mv[1]);
+          // bytes [g D/8, (g+1) D/8) of token rows 2t, 2t + 1, 2t + 8, 2t + 9; rows
+          // past the context may hold anything (NaN codes): zeros instead
+          constexpr int VW = D / 32;  // words per row
+          uint32_t vr[4][VW];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tok = 16 * ks2 + 2 * t + (i & 1) + 8 * (i >> 1);
+            const unsigned char* vrow = vs + tok * KROW + g * (D / 8);
+            if constexpr (VW == 4) {
+              const uint4 a = *reinterpret_cast<const uint4*>(vrow);
+              vr[i][0] = a.x, vr[i][1] = a.y, vr[i][2] = a.z, vr[i][3] = a.w;
+            } else {
+              const uint2 a = *reinterpret_cast<const uint2*>(vrow);
+              vr[i][0] = a.x, vr[i][1] = a.y;
+            }
+            if (tok >= nvalid) {
+#pragma unroll
+              for (int w = 0; w < VW; ++w) vr[i][w] = 0u;
+            }
+          }
+#pragma unroll
+          for (int mm = 0; mm < NKS; ++mm) {
+            // head dim bytes 2 mm, 2 mm + 1 of the token pairs, interleaved by token
+            const uint32_t sel = (mm & 1) ? 0x7362u : 0x5140u;
+            const uint32_t u01 = __byte_perm(vr[0][mm >> 1], vr[1][mm >> 1], sel);
+            const uint32_t u23 = __byte_perm(vr[2][mm >> 1], vr[3][mm >> 1], sel);
+            FpMma::mma(oa[mm], FpMma::lo2(u01), FpMma::hi2(u01), FpMma::lo2(u23), FpMma::hi2(u23), b0, b1);
+          }
+        }
+      }
+    }
+
+    if (!kMma && nvalid > 0) {
       // logits of rows grp, grp+4, grp+8, grp+12
       float x[GPW][RPG];
 #pragma unroll
@@ -502,6 +724,20 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
 
     if (last) {
       // ---- end of this warp's visit of segment (cc.s, cc.hg) -----------
+      if constexpr (kMma) {
+        // into the CUDA-core layout: lane g < 8 holds the row sum and head
+        // dims (D/8) g .. + D/8 (lane 4g's columns 0 + 1), the other lanes zeros
+        float lt = l[0];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) lt += __shfl_xor_sync(kFullMask, lt, off);
+        l[0] = lane < 8 ? lt : 0.f;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) {
+          const float v = oa[e >> 1][2 * (e & 1)] + oa[e >> 1][2 * (e & 1) + 1];
+          const float w = __shfl_sync(kFullMask, v, 4 * (lane & 7));
+          o[0][e] = lane < 8 ? w : 0.f;
+        }
+      }
 #pragma unroll
       for (int g = 0; g < GPW; ++g) {
         l[g] += __shfl_xor_sync(kFullMask, l[g], 8);

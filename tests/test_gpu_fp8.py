@@ -80,6 +80,10 @@ CASES = [
     ("f16", 8, 2, 128, 32, [3000, 1, 64, 333]),
     ("bf16", 4, 1, 128, 16, [2500, 2500, 7]),
     ("f16", 4, 4, 64, 16, [0, 9, 1000]),
+    # one query head per kv head (the tensor-core tile): bf16 queries, small
+    # and large blocks, ragged last tiles
+    ("bf16", 8, 8, 64, 8, [5, 129, 1500, 40]),
+    ("bf16", 4, 4, 128, 32, [2500, 31, 33, 1, 64]),
 ]
 
 
@@ -115,6 +119,55 @@ def test_fp8_decode_matches_oracle(qd, H_, Hkv, D, bs, lens):
         ref = oracle.paged_attention_fp8(q, kc, vc, bt, lens, scale=scale, k_scale=ks, v_scale=vs, num_heads=H_,
                                          num_kv_heads=Hkv, head_dim=D, block_size=bs, q_dtype=qd, threads=8)
         assert_close(to_f64(out), ref, f"fp8 decode rep {rep}")
+
+
+@pytest.mark.parametrize("qd,D", [("bf16", 128), ("f16", 128), ("bf16", 64)])
+def test_fp8_decode_poison_and_query_range(qd, D):
+    """Every cache byte outside the sequences' tokens is a NaN code (0x7f or
+    0xff), so a kernel that lets a masked key or value reach the arithmetic
+    gives NaN. Query rows span 2^-20 .. 2^20 times N(0, 1) (bf16) or
+    2^-8 .. 2^8 (f16), so a query path that loses range or precision on the
+    way into 16-bit operands shows up against the oracle."""
+    import paged_kv_cache_204_gb300 as pkv
+    rng = np.random.default_rng(4099 + D)
+    H_, bs = 6, 16
+    lens = np.asarray([1, 15, 16, 17, 31, 32, 33, 700, 0, 95], dtype=np.int32)
+    B = lens.size
+    MB = max(1, int(-(-lens.max() // bs)))
+    nblk = [-(-int(L) // bs) for L in lens]
+    NB = sum(nblk) + 5
+    perm = rng.permutation(NB)
+    bt = np.full((B, MB), -1, dtype=np.int32)
+    kc = np.where(rng.random((NB, H_, bs, D)) < 0.5, 0x7f, 0xff).astype(np.uint8)
+    vc = np.where(rng.random((NB, H_, bs, D)) < 0.5, 0x7f, 0xff).astype(np.uint8)
+    k = 0
+    for s in range(B):
+        bt[s, :nblk[s]] = perm[k:k + nblk[s]]
+        for j in range(nblk[s]):
+            n = min(bs, int(lens[s]) - j * bs)
+            kc[bt[s, j], :, :n] = finite_codes(rng, (H_, n, D))
+            vc[bt[s, j], :, :n] = finite_codes(rng, (H_, n, D))
+        k += nblk[s]
+    span = 20 if qd == "bf16" else 8
+    row_scale = np.exp2(rng.integers(-span, span + 1, size=(B, H_, 1)).astype(np.float64))
+    q = rng.standard_normal((B, H_, D)) * row_scale
+    q[0, 0, 0] *= 2.0**(span if qd == "bf16" else 4)  # one element far above the rest of its row
+    q = H.round_to_storage(q, qd)
+    scale, ks, vs = 1.0 / np.sqrt(D), 0.0123, 0.0311
+    out = torch.empty((B, H_, D), dtype=TD[qd], device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mcl = int(lens.max())
+    ws = pkv.new_workspace(B, H_, D, mcl, device=DEV)
+    pkv.paged_attention_decode_fp8(out, up16(q, qd), torch.from_numpy(kc).to(DEV), torch.from_numpy(vc).to(DEV),
+                                   torch.from_numpy(bt).to(DEV), torch.from_numpy(lens).to(DEV), scale, ks, vs, mcl,
+                                   workspace=ws, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = to_f64(out)
+    assert np.isfinite(got).all()
+    ref = oracle.paged_attention_fp8(q, kc, vc, bt, lens, scale=scale, k_scale=ks, v_scale=vs, num_heads=H_,
+                                     num_kv_heads=H_, head_dim=D, block_size=bs, q_dtype=qd, threads=8)
+    assert_close(got, ref, "fp8 decode, poison and query range")
 
 
 def test_fp8_decode_full_size_sampled():
