@@ -44,7 +44,7 @@ WorkspaceLayout workspace_layout(int num_seqs, int num_heads, int head_dim) {
 // sequence, piece counters, each row's prefix result, the row counters and
 // tail results of the single-launch kernel, then the warps' partial slots.
 struct GroupedLayout {
-  size_t flag = 0, group_S = 0, seq_P = 0, seg_ctr = 0, row_ml = 0, row_o = 0;
+  size_t flag = 0, group_S = 0, group_units = 0, seq_P = 0, seg_ctr = 0, row_ml = 0, row_o = 0;
   size_t row_ctr = 0, tail_ml = 0, tail_o = 0;
   size_t slot_ml = 0, slot_o = 0, total = 0;
 };
@@ -59,6 +59,8 @@ GroupedLayout grouped_layout(int num_seqs, int num_heads, int head_dim, int num_
   off += 256;
   w.group_S = off;
   off += align_up((size_t)num_groups * 4, 256);
+  w.group_units = off;
+  off += align_up((size_t)num_groups * 8, 256);
   w.seq_P = off;
   off += align_up((size_t)num_seqs * 4, 256);
   w.seg_ctr = off;
@@ -367,6 +369,7 @@ pkv_status pkv_paged_attention_decode_grouped(void* out, const void* q, const vo
   gp.num_groups = num_groups;
   gp.ws_flag = reinterpret_cast<int32_t*>(wsb + ws.flag);
   gp.ws_group_S = reinterpret_cast<int32_t*>(wsb + ws.group_S);
+  gp.ws_group_units = reinterpret_cast<long long*>(wsb + ws.group_units);
   gp.ws_seq_P = reinterpret_cast<int32_t*>(wsb + ws.seq_P);
   gp.ws_seg_ctr = reinterpret_cast<int32_t*>(wsb + ws.seg_ctr);
   gp.ws_row_ml = reinterpret_cast<float2*>(wsb + ws.row_ml);

@@ -59,6 +59,7 @@ struct GroupedParams {
   int num_groups;
   int32_t* ws_flag;     // [1] 1 = grouping rejected
   int32_t* ws_group_S;  // [num_groups] usable shared prefix tokens
+  long long* ws_group_units;  // [num_groups] work units of the group (single-launch kernel)
   int32_t* ws_seq_P;    // [num_seqs] prefix tokens of the sequence's group
   int32_t* ws_seg_ctr;  // [2][num_seqs * num_heads] piece counters (prefix, tail)
   float2* ws_row_ml;    // [num_seqs * num_heads] (m, l) of each row's prefix result
@@ -69,6 +70,16 @@ struct GroupedParams {
   float* ws_tail_o;     // [num_seqs * num_heads][head_dim]
   int32_t* ws_row_ctr;  // [num_seqs * num_heads]
 };
+
+// Work units of the single-launch kernel, in eighths of a prefix tile's
+// time (measured per warp on the copy-on-write step): a prefix tile 8, a
+// tail tile 10 (one query row on CUDA cores, its last tile often partly
+// filled), the end of a prefix segment 28 and of a tail segment 25
+// (reductions, and the two parts of each row meeting in shared memory or
+// through the workspace). A tile belongs to the warp whose unit range holds
+// its first unit; ranges are at least kUnitMax long, so every warp between
+// the first and the last of a segment's warps gets some of its tiles.
+constexpr int kUnitP = 8, kUnitT = 10, kChargeP = 28, kChargeT = 25, kUnitMax = 10;
 
 __device__ __forceinline__ int warp_min(int v) {
 #pragma unroll
@@ -127,7 +138,21 @@ __global__ void __launch_bounds__(256) pa_group_prologue_kernel(const GroupedPar
       }
       S = min(sb * bs, minL) / unit * unit;
     }
-    if (lane == 0) gp.ws_group_S[g] = S;
+    // the group's work units (head groups x (prefix segments + member tails)),
+    // read by the single-launch kernel's start-up instead of recomputing them
+    const int HG = p.head_groups, gpw = p.num_heads / p.head_groups;
+    long long u = 0;
+    for (int s = lo + lane; s < hi; s += 32) {
+      u += (long long)tiles_of(load_len(p, s, cap) - S) * kUnitT + kChargeT;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) u += __shfl_xor_sync(kFullMask, u, o);
+    if (S > 0) u += (long long)gpw * ((hi - lo + kMaxPrefixRows - 1) / kMaxPrefixRows) *
+                    ((long long)(S / kTileTokens) * kUnitP + kChargeP);
+    if (lane == 0) {
+      gp.ws_group_S[g] = S;
+      gp.ws_group_units[g] = (long long)HG * u;
+    }
     for (int s = lo + lane; s < hi; s += 32) gp.ws_seq_P[s] = S;
   }
 }
@@ -1069,15 +1094,6 @@ __global__ void __launch_bounds__(NW * 32)
 //     counter.
 // Sequences of rejected or single-member groups have tails only.
 
-// Work units of the single-launch kernel, in eighths of a prefix tile's
-// time (measured per warp on the copy-on-write step): a prefix tile 8, a
-// tail tile 10 (one query row on CUDA cores, its last tile often partly
-// filled), the end of a prefix segment 28 and of a tail segment 25
-// (reductions, and the two parts of each row meeting in shared memory or
-// through the workspace). A tile belongs to the warp whose unit range holds
-// its first unit; ranges are at least kUnitMax long, so every warp between
-// the first and the last of a segment's warps gets some of its tiles.
-constexpr int kUnitP = 8, kUnitT = 10, kChargeP = 28, kChargeT = 25, kUnitMax = 10;
 
 // Warps per block and ring stages per warp of the single-launch kernel
 // (measured on the copy-on-write step, attention: 8 x 2 139.6 us, 6 x 3 164.9
@@ -1276,6 +1292,7 @@ __global__ void __launch_bounds__(kSharedWarps * 32)
   const long long W = (long long)gridDim.x * NW;
   const long long wid = (long long)blockIdx.x * NW + warp;
   auto group_units = [&](int gi) -> long long {
+    if (x.use_groups) return __ldcg(gp.ws_group_units + gi);  // from the grouping check
     SCursor c;
     c.grp = gi;
     sgroup_load(c, x);
@@ -1327,7 +1344,7 @@ __global__ void __launch_bounds__(kSharedWarps * 32)
     const longlong2 st0 = starts[warp];
     ci.grp = static_cast<int>(st0.x);
     sgroup_load(ci, x);
-    const long long uhg = shg_units(ci, x);
+    const long long uhg = x.use_groups ? __ldcg(gp.ws_group_units + ci.grp) / HG : shg_units(ci, x);
     ci.hg = static_cast<int>(st0.y / uhg);
     long long r = st0.y - ci.hg * uhg;
     const long long pseg = sprefix_seg_units(ci);
