@@ -40,6 +40,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "tc.cuh"
 
 namespace pkv {
 
@@ -228,7 +229,12 @@ struct DecodeShape {
   static constexpr int kKvRowBytes = D * (int)sizeof(KT);                // cache row
   static constexpr int kTileTokensT = tile_tokens_for<KT>();
   static constexpr int kTileBytes = kTileTokensT * kKvRowBytes;          // K (or V) rows of one tile
-  static constexpr int kStageBytes = 2 * kTileBytes + GPW * kRowBytes;   // K, V, query rows
+  // the tensor-core fp8 tile at head_dim 128 takes its K and V rows by 2-D
+  // TMA with the 128-byte swizzle (conflict-free reads of its fragments):
+  // stages start on 1024-byte boundaries
+  static constexpr bool kTma = kFp8Mma && D == 128;
+  static constexpr int kStageRaw = 2 * kTileBytes + GPW * kRowBytes;     // K, V, query rows
+  static constexpr int kStageBytes = kTma ? (kStageRaw + 1023) / 1024 * 1024 : kStageRaw;
   static constexpr int kRingBudget = BudgetO ? BudgetO : (kFp8Wide ? kFp8RingBudget : 128 * 1024);
   static constexpr int kStagesRaw = kRingBudget / (kWarps * 2 * kTileBytes);
   static constexpr int kStages = kStagesRaw < 1 ? 1 : (kStagesRaw > 4 ? 4 : kStagesRaw);
@@ -241,7 +247,7 @@ struct DecodeShape {
   static constexpr int kBtOff = kBarOff + kWarps * kStages * 8;
   static constexpr int kScanOff = kBtOff + kWarps * kBtChunk * 4;
   static constexpr int kStartOff = kScanOff + kWarps * 8;
-  static constexpr int kSmemBytes = kStartOff + kWarps * 16;
+  static constexpr int kSmemBytes = kStartOff + kWarps * 16 + (kTma ? 1024 : 0);  // + alignment of the base
   static_assert(kChunksPerRow % 8 == 0, "row must split into 8 lanes of 16-byte chunks");
   static_assert(kDimsPerLane * 8 == D, "lane mapping");
   static_assert(kStageBytes % 16 == 0 && kRowBytes % 16 == 0 && kTileBytes % 16 == 0, "bulk copy alignment");
@@ -308,7 +314,8 @@ __device__ __forceinline__ void cursor_next(TileCursor& c, const DecodeParams& p
 
 template <typename T, int D, int GPW, typename KT = T>
 __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
-    pa_decode_kernel(const DecodeParams p) {
+    pa_decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                     const DecodeParams p) {
   using S = DecodeShape<T, D, GPW, KT>;
   using LD = LaneDims<T, KT, D>;
   constexpr bool kQuant = !std::is_same<T, KT>::value;
@@ -324,7 +331,8 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
   constexpr int ROW = S::kRowBytes;    // query / output row bytes
   constexpr int KROW = S::kKvRowBytes; // cache row bytes
 
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = S::kTma ? smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u) : smem_raw;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::kBarOff);
   long long* scan = reinterpret_cast<long long*>(smem + S::kScanOff);
   longlong2* starts = reinterpret_cast<longlong2*>(smem + S::kStartOff);
@@ -441,10 +449,16 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
       for (int c2 = 0; c2 < nseg; ++c2) {
         const int t = t0 + c2 * seg;
         if (t >= c.L) break;
-        const size_t off =
-            (((size_t)my_bt[t / bs - bt_j0] * p.num_kv_heads + kvh) * bs + (t % bs)) * KROW;
-        bulk_copy_g2s(kdst + c2 * seg * KROW, kbase + off, seg * KROW, bar);
-        bulk_copy_g2s(vdst + c2 * seg * KROW, vbase + off, seg * KROW, bar);
+        if constexpr (S::kTma) {  // boxes of {128 bytes, seg rows}, swizzled
+          const int y = (my_bt[t / bs - bt_j0] * p.num_kv_heads + kvh) * bs + (t % bs);
+          tma_load_2d(kdst + c2 * seg * KROW, &kmap, 0, y, bar);
+          tma_load_2d(vdst + c2 * seg * KROW, &vmap, 0, y, bar);
+        } else {
+          const size_t off =
+              (((size_t)my_bt[t / bs - bt_j0] * p.num_kv_heads + kvh) * bs + (t % bs)) * KROW;
+          bulk_copy_g2s(kdst + c2 * seg * KROW, kbase + off, seg * KROW, bar);
+          bulk_copy_g2s(vdst + c2 * seg * KROW, vbase + off, seg * KROW, bar);
+        }
       }
       if (with_q)
         bulk_copy_g2s(kdst + 2 * S::kTileBytes,
@@ -557,11 +571,16 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
           sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
           // bytes [t D/4, (t+1) D/4) of token rows 16 mt + g and 16 mt + g + 8
           uint32_t w0[NKS], w1[NKS];
-          const uint4* r0 = reinterpret_cast<const uint4*>(ks + (16 * mt + g) * KROW + t * (D / 4));
-          const uint4* r1 = reinterpret_cast<const uint4*>(ks + (16 * mt + g + 8) * KROW + t * (D / 4));
+          const unsigned char* r0 = ks + (16 * mt + g) * KROW;
+          const unsigned char* r1 = ks + (16 * mt + g + 8) * KROW;
 #pragma unroll
           for (int c = 0; c < NKS / 4; ++c) {
-            const uint4 a = r0[c], b = r1[c];
+            // 16-byte chunk (D/64) t + c of the rows (stored at chunk ^ (row & 7)
+            // when the tile came by swizzled TMA; rows g and g + 8 share row & 7)
+            const int ch = (D / 64) * t + c;
+            const int pc = S::kTma ? (ch ^ g) : ch;
+            const uint4 a = *reinterpret_cast<const uint4*>(r0 + 16 * pc);
+            const uint4 b = *reinterpret_cast<const uint4*>(r1 + 16 * pc);
             w0[4 * c] = a.x, w0[4 * c + 1] = a.y, w0[4 * c + 2] = a.z, w0[4 * c + 3] = a.w;
             w1[4 * c] = b.x, w1[4 * c + 1] = b.y, w1[4 * c + 2] = b.z, w1[4 * c + 3] = b.w;
           }
@@ -625,7 +644,9 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
             const int tok = 16 * ks2 + 2 * t + (i & 1) + 8 * (i >> 1);
             const unsigned char* vrow = vs + tok * KROW + g * (D / 8);
             if constexpr (VW == 4) {
-              const uint4 a = *reinterpret_cast<const uint4*>(vrow);
+              // chunk g of the row (at chunk g ^ (tok & 7) when swizzled)
+              const uint4 a = *reinterpret_cast<const uint4*>(
+                  S::kTma ? vs + tok * KROW + 16 * (g ^ (tok & 7)) : vrow);
               vr[i][0] = a.x, vr[i][1] = a.y, vr[i][2] = a.z, vr[i][3] = a.w;
             } else {
               const uint2 a = *reinterpret_cast<const uint2*>(vrow);
@@ -865,7 +886,20 @@ cudaError_t launch_pa_decode(const DecodeParams& p, cudaStream_t stream) {
     if (grid > kMaxDecodeWarps / S::kWarps) grid = kMaxDecodeWarps / S::kWarps;
     if (dev >= 0 && dev < 64) __atomic_store_n(&grid_of_device[dev], grid, __ATOMIC_RELEASE);
   }
-  pa_decode_kernel<T, D, GPW, KT><<<grid, S::kWarps * 32, S::kSmemBytes, stream>>>(p);
+  CUtensorMap kmap, vmap;
+  memset(&kmap, 0, sizeof(kmap));
+  memset(&vmap, 0, sizeof(vmap));
+  if constexpr (S::kTma) {
+    const uint64_t rows = (uint64_t)p.num_blocks * p.num_kv_heads * p.block_size;
+    // the TMA row coordinate (one box past the pool included) must fit in int32
+    if (rows + S::kTileTokensT > 0x7fffffffull) return cudaErrorNotSupported;
+    const int box_rows = p.block_size < S::kTileTokensT ? p.block_size : S::kTileTokensT;
+    e = encode_pool_bytes_map(&kmap, p.k_cache, rows, box_rows);
+    if (e != cudaSuccess) return e;
+    e = encode_pool_bytes_map(&vmap, p.v_cache, rows, box_rows);
+    if (e != cudaSuccess) return e;
+  }
+  pa_decode_kernel<T, D, GPW, KT><<<grid, S::kWarps * 32, S::kSmemBytes, stream>>>(kmap, vmap, p);
   return cudaGetLastError();
 }
 

@@ -216,4 +216,21 @@ inline cudaError_t encode_pool_rows_map(CUtensorMap* map, const void* base, uint
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// A pool of one-byte codes [num_blocks][num_kv_heads][block_size][128] seen
+// as `rows` rows of 128 bytes, read in boxes of {128 bytes, box_rows rows}
+// with the 128-byte swizzle (chunk c of box row r at chunk c ^ (r & 7)).
+// Rows past the pool read as zeros.
+inline cudaError_t encode_pool_bytes_map(CUtensorMap* map, const void* base, uint64_t rows, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[2] = {128u, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {128u};
+  const cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1u, 1u};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace pkv
