@@ -563,7 +563,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         cache_ops()
         attention()
 
-    launches_per_step = int(has_copy) + int(has_new) + (3 if grouped else 1)  # grouped: prologue + two phases
+    # grouped: the grouping check, then one kernel (16-bit data) or a prefix and a tail phase (fp32)
+    launches_per_step = int(has_copy) + int(has_new) + ((3 if cfg.dtype == "f32" else 2) if grouped else 1)
 
     clocks = ClockSampler(local_rank).__enter__()  # sampled from the warm-up on
     for _ in range(max(args.warmup, 3)):
@@ -822,7 +823,9 @@ def run_beam(args, rank: int, world: int, local_rank: int) -> int:
         ev[i][0].record(stream)
         device_step(dp, ev[i][1])
         ev[i][2].record(stream)
-        launches += (1 if dp.copy_pairs.numel() else 0) + 1 + 3  # grouped: prologue + two phases
+        # copies, the row writes, the grouping check and the grouped kernel (16-bit data) or its
+        # prefix and tail phases (fp32)
+        launches += (1 if dp.copy_pairs.numel() else 0) + 1 + (3 if cfg.dtype == "f32" else 2)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
