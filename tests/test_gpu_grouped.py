@@ -71,6 +71,22 @@ def test_group_shapes(dtype, D, bs, Hkv, G):
     assert _check(st, cfg) == 0
 
 
+@pytest.mark.parametrize("groups", [128, 129, 150])
+def test_many_groups_both_check_paths(groups):
+    """Up to 128 groups the grouped kernel checks the grouping itself, in
+    every block; beyond that a separate check launch runs first. Both paths
+    give the oracle's result, and both flag a wrong shared-blocks promise."""
+    import paged_kv_cache_204_gb300 as pkv
+    cfg = synth.get("cow").replace(samples=2, num_heads=4, num_kv_heads=4, num_blocks=6000,
+                                   lengths=("uniform", 16, 160), tail=("uniform", 1, 40))
+    st = synth.build(cfg, num_seqs=2 * groups)
+    assert len(st.shared_blocks) == groups
+    assert _check(st, cfg) == 0
+    lie = st.shared_blocks.copy()
+    lie[groups // 2] += 2                              # one group promises blocks that differ
+    assert _check(st, cfg, sb=lie) == pkv.DEV_ERR_GROUP
+
+
 def test_wrong_shared_blocks_promise_is_flagged_and_still_correct():
     import paged_kv_cache_204_gb300 as pkv
     cfg = synth.get("cow").replace(num_heads=4, num_kv_heads=4, num_blocks=3000,
