@@ -72,10 +72,10 @@ def test_group_shapes(dtype, D, bs, Hkv, G):
 
 
 @pytest.mark.parametrize("groups", [128, 129, 150])
-def test_many_groups_both_check_paths(groups):
-    """Up to 128 groups the grouped kernel checks the grouping itself, in
-    every block; beyond that a separate check launch runs first. Both paths
-    give the oracle's result, and both flag a wrong shared-blocks promise."""
+def test_many_groups(groups):
+    """More groups than the grouping check's blocks hold warps (8 per block):
+    the check still covers every group, the result is the oracle's, and a
+    wrong shared-blocks promise in one group among many is flagged."""
     import paged_kv_cache_204_gb300 as pkv
     cfg = synth.get("cow").replace(samples=2, num_heads=4, num_kv_heads=4, num_blocks=6000,
                                    lengths=("uniform", 16, 160), tail=("uniform", 1, 40))
