@@ -14,11 +14,14 @@
 //     siblings (head h of members R c .. R c + R - 1, R = prefix_rows<T>());
 //   tail segments (sequence s, head group hg): rows [S_g, L_s) of s's own
 //     blocks against its query heads, as in the plain kernel.
-// The prefix segments run first, balanced over all warps, then the tails,
-// balanced again, as two launches in stream order. A tail row of a sequence
-// with a shared prefix merges its prefix result (log-sum-exp) when it writes
-// the output. Pieces of a segment cut by warp range boundaries are
-// merged as in the plain kernel.
+// 16-bit data: one persistent launch (pa_decode_shared_kernel) walks, per
+// (group, head group), the prefix segment and then the members' tails, all
+// balanced over the warps by cost units; a row's prefix and tail results meet
+// by the log-sum-exp rule in the warp's shared memory or through the
+// workspace. fp32 data: the prefix segments run first, balanced over all
+// warps, then the tails, balanced again, as two launches in stream order; a
+// tail row merges its prefix result when it writes the output. Pieces of a
+// segment cut by warp range boundaries are merged as in the plain kernel.
 //
 // A prologue kernel checks the caller's grouping: group_start must partition
 // [0, num_seqs) and the first shared_blocks[g] block-table entries of every
