@@ -210,3 +210,51 @@ def test_fp8_decode_full_size_sampled():
                                      num_heads=H_, num_kv_heads=Hkv, head_dim=D, block_size=bs, q_dtype="bf16",
                                      threads=8)
     assert_close(to_f64(out)[seqs], ref, "fp8 full-size sampled")
+
+
+def test_fp8_decode_wait_timeout_is_reported_and_context_survives():
+    """The tensor-core fp8 tile (one query head per kv head, TMA loads at head
+    dim 128) under a wait limit of 0: PKV_DEV_ERR_TIMEOUT and nothing else,
+    then a call with the default limit (workspace cleared) matches the oracle."""
+    import paged_kv_cache_204_gb300 as pkv
+    rng = np.random.default_rng(4242)
+    H_, D, bs = 8, 128, 16
+    lens = np.asarray([700, 33, 1200, 5, 64, 900], dtype=np.int32)
+    B = lens.size
+    MB = int(-(-lens.max() // bs))
+    nblk = [-(-int(L) // bs) for L in lens]
+    NB = sum(nblk) + 3
+    perm = rng.permutation(NB)
+    bt = np.full((B, MB), -1, dtype=np.int32)
+    k = 0
+    for s in range(B):
+        bt[s, :nblk[s]] = perm[k:k + nblk[s]]
+        k += nblk[s]
+    kc = finite_codes(rng, (NB, H_, bs, D))
+    vc = finite_codes(rng, (NB, H_, bs, D))
+    q = H.round_to_storage(rng.standard_normal((B, H_, D)), "bf16")
+    scale, ks, vs = 1.0 / np.sqrt(D), 0.02, 0.03
+    out = torch.empty((B, H_, D), dtype=torch.bfloat16, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    mcl = int(lens.max())
+    ws = pkv.new_workspace(B, H_, D, mcl, device=DEV)
+    args = (up16(q, "bf16"), torch.from_numpy(kc).to(DEV), torch.from_numpy(vc).to(DEV),
+            torch.from_numpy(bt).to(DEV), torch.from_numpy(lens).to(DEV))
+    old = pkv.get_wait_timeout_ns()
+    try:
+        pkv.set_wait_timeout_ns(0)
+        pkv.paged_attention_decode_fp8(out, *args, scale, ks, vs, mcl, workspace=ws, dev_err=err)
+        torch.cuda.synchronize()
+        code = int(err.item())
+    finally:
+        pkv.set_wait_timeout_ns(old)
+    assert code & pkv.DEV_ERR_TIMEOUT
+    assert code & ~pkv.DEV_ERR_TIMEOUT == 0
+    err.zero_()
+    ws.zero_()
+    pkv.paged_attention_decode_fp8(out, *args, scale, ks, vs, mcl, workspace=ws, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = oracle.paged_attention_fp8(q, kc, vc, bt, lens, scale=scale, k_scale=ks, v_scale=vs, num_heads=H_,
+                                     num_kv_heads=H_, head_dim=D, block_size=bs, q_dtype="bf16", threads=8)
+    assert_close(to_f64(out), ref, "fp8 decode after timeout")
