@@ -33,8 +33,14 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode attention KV GB/s and % of HBM roofline; sequences/s per decode step"
 WORKLOAD = "llama13b"
-PROFILE = os.path.join(ROOT, "profiles", "pa_decode_llama13b.md")
-DECODE_SOURCE = os.path.join(ROOT, "paged_kv_cache_204_gb300", "csrc", "decode.cuh")
+CSRC = os.path.join(ROOT, "paged_kv_cache_204_gb300", "csrc")
+# committed ncu summaries that record a kernel's DRAM bytes per launch, keyed by
+# a hash of the kernel sources they were taken on
+PROFILES = {
+    "plain": (os.path.join(ROOT, "profiles", "pa_decode_llama13b.md"), ("decode.cuh",)),
+    "fp8": (os.path.join(ROOT, "profiles", "pa_decode_fp8_llama13b.md"), ("decode.cuh",)),
+    "grouped": (os.path.join(ROOT, "profiles", "pa_decode_grouped_cow.md"), ("decode.cuh", "decode_grouped.cuh")),
+}
 FLUSH_BYTES = 256 << 20
 FALLBACK_HBM_GBS = 6800.0
 
@@ -137,17 +143,24 @@ def peak_bf16_tflops() -> tuple[float, str]:
         return 1900.0, "of fallback (1.9 PFLOP/s bf16)"
 
 
-def profiled_traffic() -> int | None:
-    """DRAM bytes per launch of the decode kernel from the committed ncu
-    summary, if it was taken on the current kernel source."""
+def source_hash(files) -> str:
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(CSRC, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kind: str = "plain") -> int | None:
+    """DRAM bytes per launch of a kernel from its committed ncu summary, if
+    the summary was taken on the current kernel sources."""
+    path, files = PROFILES[kind]
     try:
-        text = open(PROFILE).read()
+        text = open(path).read()
     except OSError:
         return None
-    src_hash = hashlib.sha256(open(DECODE_SOURCE, "rb").read()).hexdigest()[:16]
-    m_hash = re.search(r"decode_source_sha256_16:\s*([0-9a-f]+)", text)
+    m_hash = re.search(r"source_sha256_16:\s*([0-9a-f]+)", text)
     m_traffic = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
-    if not m_hash or not m_traffic or m_hash.group(1) != src_hash:
+    if not m_hash or not m_traffic or m_hash.group(1) != source_hash(files):
         return None
     return int(m_traffic.group(1))
 
@@ -690,7 +703,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
                                 "pa_decode_kernel<fp8 e4m3 cache>" if fp8 else "pa_decode_kernel"),
                      "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": profiled_traffic() if (cfg.name == WORKLOAD and not grouped and not fp8) else None,
+                     "traffic": (profiled_traffic("fp8") if fp8 else profiled_traffic("plain"))
+                     if (cfg.name == WORKLOAD and not grouped) else
+                     profiled_traffic("grouped") if (cfg.name == "cow" and grouped) else None,
                      "algorithmic_bytes_per_launch": nbytes["attention"], "peak_source": peak_src},
         "cpu_baseline": cpu,
         "e2e": {"value": world * nbytes["step"] / (agg["e2e_ms"] * 1e-3) / 1e9, "unit": "GB/s",
