@@ -505,8 +505,8 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
 #pragma unroll
         for (int mm = 0; mm < NKS; ++mm) oa[mm][0] = oa[mm][1] = oa[mm][2] = oa[mm][3] = 0.f;
         if (nvalid > 0) {
-          // lane (g, t) takes query dims [t D/4, (t+1) D/4); lanes 0-3 (g = 0)
-          // hold them as the B column, the others zeros
+          // lane (g, t) takes query dims [t D/4, (t+1) D/4) as its B
+          // fragments (the query fills every column of N)
           constexpr int QPL = D / 4;
           const int t = lane & 3;
           const uint4* qr = reinterpret_cast<const uint4*>(ks + 2 * S::kTileBytes + t * QPL * (int)sizeof(T));
