@@ -1058,6 +1058,8 @@ def run_prefill(args, rank: int, world: int, local_rank: int) -> int:
     step_ms = sum(e[0].elapsed_time(e[2]) for e in ev) / K
     attn_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / K
     write_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / K
+    if int(err.item()) != 0:
+        raise RuntimeError(f"device error word {int(err.item()):#x} in the timed region")
     # end to end: the users' rows, queries and layout from pinned host memory,
     # the step, the outputs back
     dbuf, hbuf, views = pack_inputs([uk, uv, q, slots, bt, cl, qs], dev)
