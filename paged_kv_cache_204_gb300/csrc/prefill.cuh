@@ -16,9 +16,9 @@
 // per cache block found in the block table, in the 128-byte-swizzled layout
 // the MMAs read; S = Q K^T and O += P V accumulate in fp32 in tensor memory;
 // each query row's online softmax (base 2, causal mask by select) runs in
-// the thread that owns that row's tensor-memory lane. P is fed as a high and
-// a low 16-bit part (two MMAs) so that the probabilities keep ~16
-// significant bits.
+// the thread that owns that row's tensor-memory lane. For bfloat16 data P
+// is fed as a high and a low 16-bit part (two MMAs) so that the
+// probabilities keep ~16 significant bits; binary16 P (11 bits) goes as one.
 #pragma once
 
 #include <type_traits>
@@ -107,7 +107,7 @@ __device__ __forceinline__ int sw128_off(int r, int c) { return r * 128 + ((c ^ 
 //   mbarriers, softmax exchange (row maxima and sums), ring of TMA row
 //   coordinates, tensor-memory address slot.
 // Tensor memory (256 columns, lanes = query rows): S/P buffers at columns 0
-// and 64 (S as fp32; P overwrites it as 16-bit hi / lo pairs in columns
+// and 64 (S as fp32; P overwrites it as 16-bit hi (/ lo, bfloat16) pairs in columns
 // +0..31 / +32..63), O (fp32, D columns) at column 128.
 template <int D>
 struct PrefillShape {
@@ -140,8 +140,8 @@ struct PrefillShape {
 //            64 head dims), through the block table;
 //   MMA:     S_j = Q K_j^T into buffer j & 1 (issued one tile ahead), then,
 //            once P_j is written, O += P_hi V_j and O += P_lo V_j;
-//   softmax: scale, causal mask, running max, P = 2^(s - m) as a high and a
-//            low 16-bit part (the two MMAs together keep P to ~16 bits); the
+//   softmax: scale, causal mask, running max, P = 2^(s - m) (bfloat16: as a
+//            high and a low part, the two MMAs together keep ~16 bits); the
 //            running max is re-based (and O rescaled in tensor memory) only
 //            when it grows by more than kPfRescaleLog2, which leaves every
 //            P <= 2^kPfRescaleLog2 and the result exact (O and the row sum
@@ -153,6 +153,9 @@ __global__ void __launch_bounds__(kPfThreads, 2)
   using S = PrefillShape<D>;
   using P16 = Pack16<T>;
   constexpr int kBf16 = std::is_same<T, __nv_bfloat16>::value ? 1 : 0;
+  // bfloat16 P (8 significant bits) is fed as a high and a low part; binary16
+  // P (11 bits) keeps the outputs well within the tolerance on its own
+  constexpr int kPParts = kBf16 ? 2 : 1;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + S::kBarOff);
@@ -363,7 +366,7 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         const uint32_t pa = tbase + 64 * b;
         const uint64_t vd = b ? v_desc1 : v_desc0;
 #pragma unroll
-        for (int part = 0; part < 2; ++part)  // high then low halves of P
+        for (int part = 0; part < kPParts; ++part)  // high (then low) halves of P
 #pragma unroll
           for (int ks = 0; ks < kPfTokens / 16; ++ks)
             mma_ts(tbase + 128, pa + 32 * part + 8 * ks, vd + (uint64_t)((ks * 2048) >> 4), id_o,
@@ -475,14 +478,16 @@ __global__ void __launch_bounds__(kPfThreads, 2)
         const float p0 = ex2_approx(fmaf(x[2 * i], sc, nbase)), p1 = ex2_approx(fmaf(x[2 * i + 1], sc, nbase));
         ps4[i & 3] += p0 + p1;
         hi[i] = P16::pack(p0, p1);
-        const float2 hv = P16::unpack(hi[i]);
-        lo[i] = P16::pack(p0 - hv.x, p1 - hv.y);
+        if constexpr (kPParts == 2) {
+          const float2 hv = P16::unpack(hi[i]);
+          lo[i] = P16::pack(p0 - hv.x, p1 - hv.y);
+        }
       }
       l = l * alpha + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));  // this half's share of the row sum
       // P of this half: packed pairs at columns 16 ch .. (high) and 32 + 16 ch .. (low)
       __syncwarp();
       tmem_st16(tbase + lane_base + 64 * b + 16 * ch, hi);
-      tmem_st16(tbase + lane_base + 64 * b + 32 + 16 * ch, lo);
+      if constexpr (kPParts == 2) tmem_st16(tbase + lane_base + 64 * b + 32 + 16 * ch, lo);
       tmem_wait_st();
       if (j == ntiles - 1 && kv_end < j * kPfTokens + kPfTokens) {
         // V rows past the context may hold anything (a NaN would survive a

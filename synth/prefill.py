@@ -68,6 +68,10 @@ PRESETS = {
     "prefill": PrefillConfig("prefill", users=16, system_len=1024, user_len=("uniform", 256, 768),
                              num_heads=40, num_kv_heads=40, head_dim=128, block_size=16, dtype="bf16",
                              num_blocks=40000, value_scale=1.0, scale=1.0 / math.sqrt(128), seed=2082),
+    # the same step over binary16 caches and queries
+    "prefill_f16": PrefillConfig("prefill_f16", users=16, system_len=1024, user_len=("uniform", 256, 768),
+                                 num_heads=40, num_kv_heads=40, head_dim=128, block_size=16, dtype="f16",
+                                 num_blocks=40000, value_scale=1.0, scale=1.0 / math.sqrt(128), seed=2082),
 }
 
 
