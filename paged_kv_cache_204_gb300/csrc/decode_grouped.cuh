@@ -433,12 +433,18 @@ __device__ __forceinline__ void mma_prefix_tile(uint32_t stage, const uint32_t (
       acc[mb][3] *= alpha[1];
     }
   }
-  // P^T fragments: (token g | g+8) x (rows 2t, 2t+1) pairs, transposed
+  // P^T fragments: (token g | g+8) x (rows 2t, 2t+1) pairs, transposed.
+  // bfloat16 P (8 significant bits) goes as a high part and a remainder;
+  // binary16 P (11 bits) alone keeps the outputs within the tolerance.
+  constexpr bool kSplit = !std::is_same<T, __half>::value;
   const uint32_t h0 = M::pack(pe[0], pe[1]), h1 = M::pack(pe[2], pe[3]);
-  const float2 u0 = M::unpack(h0), u1 = M::unpack(h1);
-  const uint32_t l0 = M::pack(pe[0] - u0.x, pe[1] - u0.y), l1 = M::pack(pe[2] - u1.x, pe[3] - u1.y);
   const uint32_t bh0 = movmatrix_trans(h0), bh1 = movmatrix_trans(h1);
-  const uint32_t bl0 = movmatrix_trans(l0), bl1 = movmatrix_trans(l1);
+  uint32_t bl0 = 0u, bl1 = 0u;
+  if constexpr (kSplit) {
+    const float2 u0 = M::unpack(h0), u1 = M::unpack(h1);
+    bl0 = movmatrix_trans(M::pack(pe[0] - u0.x, pe[1] - u0.y));
+    bl1 = movmatrix_trans(M::pack(pe[2] - u1.x, pe[3] - u1.y));
+  }
   // V: lane i addresses token (i & 7) + 8 (i >> 4), chunk 2 mb + ((i >> 3) & 1)
   const int vtok = (lane & 7) + ((lane >> 4) << 3);
   const int vhi = (lane >> 3) & 1;
@@ -448,7 +454,7 @@ __device__ __forceinline__ void mma_prefix_tile(uint32_t stage, const uint32_t (
     uint32_t a[4];
     ldsm_x4_trans(vstage + sw_tile_off(vtok, 2 * mb + vhi), a);
     M::run(acc[mb], a, bh0, bh1);
-    M::run(acc[mb], a, bl0, bl1);
+    if constexpr (kSplit) M::run(acc[mb], a, bl0, bl1);
   }
 }
 
