@@ -80,6 +80,18 @@ def _bind(L: ctypes.CDLL) -> ctypes.CDLL:
     L.orc_paged_attention_fp8.restype = I
     L.orc_paged_prefill.argtypes = [P, P, P, P, P, I, P, P, I, I, I, I, I, I, I, D, I, I]
     L.orc_paged_prefill.restype = I
+    L.orc_encode_f16.argtypes = [D]
+    L.orc_encode_f16.restype = ctypes.c_uint16
+    L.orc_q4_0_quantize_block.argtypes = [P, P, P]
+    L.orc_q4_0_quantize_block.restype = None
+    L.orc_q4_0_value.argtypes = [P, I, I]
+    L.orc_q4_0_value.restype = D
+    L.orc_q4_0_quantize_row.argtypes = [P, I, I, P]
+    L.orc_q4_0_quantize_row.restype = I
+    L.orc_reshape_and_cache_q4_0.argtypes = [P, P, P, P, P, I, I, I, I, I, I]
+    L.orc_reshape_and_cache_q4_0.restype = I
+    L.orc_paged_attention_q4_0.argtypes = [P, P, P, P, P, I, P, I, I, I, I, I, I, I, D, I, I]
+    L.orc_paged_attention_q4_0.restype = I
     return L
 
 
@@ -315,6 +327,97 @@ def paged_attention_fp8(q, k_cache, v_cache, block_tables, context_lens, *, scal
         rcs = list(ex.map(lambda i: run(cuts[i], cuts[i + 1]), range(n)))
     if any(rc != 0 for rc in rcs):
         raise ValueError(f"orc_paged_attention_fp8 failed with codes {rcs}")
+    return out
+
+
+# ---- 4-bit (q4_0) KV cache -----------------------------------------------------
+
+def q4_0_row_bytes(head_dim: int) -> int:
+    """Bytes of one cache row of head_dim values: head_dim / 32 binary16
+    scales, then head_dim / 2 code bytes."""
+    return head_dim // 16 * 9
+
+
+def encode_f16(values: np.ndarray, L=None) -> np.ndarray:
+    """float64 values -> nearest binary16 bit patterns (ties to even)."""
+    L = L or lib()
+    flat = np.ascontiguousarray(values, dtype=np.float64).reshape(-1)
+    return np.array([L.orc_encode_f16(float(x)) for x in flat], dtype=np.uint16).reshape(np.shape(values))
+
+
+def q4_0_quantize_block(x: np.ndarray, L=None):
+    """32 binary32 values -> (scale bits as uint16, 16 code bytes)."""
+    L = L or lib()
+    xb = np.ascontiguousarray(x, dtype=np.float32)
+    if xb.shape != (32,):
+        raise ValueError("a q4_0 block holds 32 values")
+    d = np.zeros(1, dtype=np.uint16)
+    qs = np.zeros(16, dtype=np.uint8)
+    L.orc_q4_0_quantize_block(_ptr(xb), _ptr(d), _ptr(qs))
+    return int(d[0]), qs
+
+
+def q4_0_quantize_row(src: np.ndarray, src_dtype: str, L=None) -> np.ndarray:
+    """One row of head_dim binary16 / bfloat16 values (uint16 bits) -> its
+    9 head_dim / 16 cache bytes."""
+    L = L or lib()
+    _check_store(src, src_dtype, "src")
+    sb = np.ascontiguousarray(src).reshape(-1)
+    row = np.zeros(q4_0_row_bytes(sb.shape[0]), dtype=np.uint8)
+    rc = L.orc_q4_0_quantize_row(_ptr(sb), DTYPE_CODE[src_dtype], sb.shape[0], _ptr(row))
+    if rc != 0:
+        raise ValueError(f"orc_q4_0_quantize_row failed with code {rc}")
+    return row
+
+
+def q4_0_values(row: np.ndarray, head_dim: int, L=None) -> np.ndarray:
+    """The head_dim values a q4_0 cache row reads back as (float64)."""
+    L = L or lib()
+    rb = np.ascontiguousarray(row, dtype=np.uint8).reshape(-1)
+    return np.array([L.orc_q4_0_value(_ptr(rb), head_dim, d) for d in range(head_dim)], dtype=np.float64)
+
+
+def reshape_and_cache_q4_0(k, v, k_cache, v_cache, slot_mapping, *, num_kv_heads, head_dim, block_size,
+                           src_dtype, L=None) -> int:
+    """In place on the uint8 pools [num_blocks][kv_heads][block_size][9 D / 16]:
+    token t's rows, quantised to q4_0 blocks, go to slot slot_mapping[t].
+    Returns the number of out-of-range slots."""
+    L = L or lib()
+    for a, n in ((k, "k"), (v, "v")):
+        _check_store(a, src_dtype, n)
+    for a, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        if a.dtype != np.uint8:
+            raise TypeError(f"{n}: q4_0 pools must be uint8, got {a.dtype}")
+    sl = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    rc = L.orc_reshape_and_cache_q4_0(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(sl), sl.shape[0],
+                                      num_kv_heads, head_dim, block_size, k_cache.shape[0], DTYPE_CODE[src_dtype])
+    if rc < 0:
+        raise ValueError(f"orc_reshape_and_cache_q4_0 failed with code {rc}")
+    return rc
+
+
+def paged_attention_q4_0(q, k_cache, v_cache, block_tables, context_lens, *, scale, num_heads, num_kv_heads,
+                         head_dim, block_size, q_dtype, threads: int = 1, L=None) -> np.ndarray:
+    """Decode attention over q4_0 pools, fp64: paged_attention with every
+    K and V element read back as d * (q - 8)."""
+    L = L or lib()
+    _check_store(q, q_dtype, "q")
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B = cl.shape[0]
+    out = np.zeros((B, num_heads, head_dim), dtype=np.float64)
+
+    def run(lo, hi):
+        return L.orc_paged_attention_q4_0(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(bt),
+                                          bt.shape[1], _ptr(cl), B, num_heads, num_kv_heads, head_dim,
+                                          block_size, k_cache.shape[0], DTYPE_CODE[q_dtype], float(scale), lo, hi)
+
+    n = max(1, min(threads, B))
+    cuts = [B * i // n for i in range(n + 1)]
+    with ThreadPoolExecutor(max_workers=n) as ex:
+        rcs = list(ex.map(lambda i: run(cuts[i], cuts[i + 1]), range(n)))
+    if any(rc != 0 for rc in rcs):
+        raise ValueError(f"orc_paged_attention_q4_0 failed with codes {rcs}")
     return out
 
 

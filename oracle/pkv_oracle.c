@@ -616,3 +616,201 @@ int orc_paged_prefill(double* out, const void* q, const void* k_cache, const voi
   free(row);
   return rc;
 }
+
+/* ---- 4-bit (q4_0) KV cache ---------------------------------------------- */
+/*
+ * [QKV] "Efficient Memory Management for Large Language Model Serving with
+ * PagedAttention" (hackerpapers page), "In the conversation": a reader notes
+ * that 4-bit KV-cache quantisation, the cache type called q4_0, cuts the
+ * cache to about a quarter of its size. The pages name the format without
+ * defining it. Reading taken: the q4_0 block of the ggml tensor library,
+ * where 32 consecutive values share one binary16 scale d and each keeps a
+ * 4-bit code q in 0..15 that reads back as d * (q - 8). Quantising a block
+ * x[0..31], every step in binary32:
+ *   m   = the element of largest magnitude, sign kept (the first on ties;
+ *         +0 when every |x| is 0 or NaN)
+ *   d   = m / -8                    (m itself gets code 0)
+ *   inv = 1 / d, or 0 when d is 0
+ *   y   = x_j * inv + 8.5           (a product and a sum, each rounded)
+ *   q_j = 15 if y >= 15, else trunc(y) if y >= 0, else 0 (NaN included)
+ * Stored: d rounded to binary16 (nearest, ties to even, overflow to
+ * infinity); code byte j (0..15) of the block holds q_j in its low and
+ * q_(j+16) in its high four bits. A cache row of D values holds D/32
+ * blocks: the D/32 scales first (little-endian binary16), then the blocks'
+ * 16 code bytes in block order, 9 D / 16 bytes in all (this library's
+ * arrangement of the blocks in a row).
+ */
+
+/* double -> nearest binary16 bits (ties to even), from the format's
+ * definition: subnormals are multiples of 2^-24; in [2^E, 2^(E+1)) the
+ * spacing is 2^(E-10); values at or above 65520 overflow to infinity. */
+uint16_t orc_encode_f16(double x) {
+  if (isnan(x)) return 0x7e00;
+  const uint16_t sign = signbit(x) ? 0x8000 : 0x0000;
+  const double a = fabs(x);
+  int code;
+  if (a < ldexp(1.0, -14)) {
+    code = (int)rint(ldexp(a, 24)); /* 1024 is the smallest normal: the carry is right */
+  } else if (a >= 65520.0) {
+    code = 0x7c00;
+  } else {
+    int k;
+    frexp(a, &k); /* a = f * 2^k, f in [0.5, 1) */
+    const int E = k - 1;
+    const int n = (int)rint(ldexp(a, 10 - E)); /* in [1024, 2048] */
+    code = (E + 15) * 1024 + (n - 1024);
+  }
+  if (code > 0x7c00) code = 0x7c00;
+  return (uint16_t)(sign | code);
+}
+
+/* One block of 32 binary32 values -> scale bits and 16 code bytes. */
+void orc_q4_0_quantize_block(const float* x, uint16_t* d_bits, uint8_t* qs) {
+  float amax = 0.0f, m = 0.0f;
+  for (int j = 0; j < 32; ++j) {
+    const float a = fabsf(x[j]);
+    if (a > amax) {
+      amax = a;
+      m = x[j];
+    }
+  }
+  const float d = m / -8.0f;
+  const float inv = d != 0.0f ? 1.0f / d : 0.0f;
+  int q[32];
+  for (int j = 0; j < 32; ++j) {
+    const float prod = x[j] * inv;
+    const float y = prod + 8.5f;
+    q[j] = y >= 15.0f ? 15 : (y >= 0.0f ? (int)y : 0);
+  }
+  *d_bits = orc_encode_f16((double)d);
+  for (int j = 0; j < 16; ++j) qs[j] = (uint8_t)(q[j] | (q[j + 16] << 4));
+}
+
+/* Value of element d (0 .. head_dim-1) of a q4_0 row. */
+double orc_q4_0_value(const uint8_t* row, int head_dim, int d) {
+  const int b = d / 32, j = d % 32;
+  const uint16_t sb = (uint16_t)(row[2 * b] | (row[2 * b + 1] << 8));
+  const uint8_t byte = row[head_dim / 16 + 16 * b + (j % 16)];
+  const int q = j < 16 ? (byte & 0xf) : (byte >> 4);
+  return (double)(q - 8) * orc_decode_f16(sb);
+}
+
+/* One row of head_dim values of src_dtype (binary16 or bfloat16, converted
+ * exactly to binary32) -> 9 head_dim / 16 bytes. */
+int orc_q4_0_quantize_row(const void* src, int src_dtype, int head_dim, uint8_t* row) {
+  if ((src_dtype != ORC_F16 && src_dtype != ORC_BF16) || head_dim <= 0 || head_dim % 32) return -1;
+  for (int b = 0; b < head_dim / 32; ++b) {
+    float x[32];
+    for (int j = 0; j < 32; ++j) x[j] = (float)elem(src, (size_t)(32 * b + j), src_dtype);
+    uint16_t sb;
+    orc_q4_0_quantize_block(x, &sb, row + head_dim / 16 + 16 * b);
+    row[2 * b] = (uint8_t)(sb & 0xff);
+    row[2 * b + 1] = (uint8_t)(sb >> 8);
+  }
+  return 0;
+}
+
+/*
+ * Cache write into q4_0 pools ([QKV], [VM]): for token t with slot s >= 0,
+ * each kv head's K (V) row is quantised as above into cache row
+ * [s / bs][h][s % bs] of the [num_blocks][num_kv_heads][block_size]
+ * [9 head_dim / 16] byte pools. Returns the number of out-of-range slots
+ * (not written), or a negative code.
+ */
+int orc_reshape_and_cache_q4_0(const void* k, const void* v, uint8_t* k_cache, uint8_t* v_cache,
+                               const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                               int block_size, int num_blocks, int src_dtype) {
+  if ((src_dtype != ORC_F16 && src_dtype != ORC_BF16) || num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+      head_dim % 32 || block_size <= 0 || num_blocks <= 0)
+    return -1;
+  if (num_tokens && (!k || !v || !k_cache || !v_cache || !slot_mapping)) return -1;
+  const size_t rb = (size_t)head_dim / 16 * 9;
+  int bad = 0;
+  for (int t = 0; t < num_tokens; ++t) {
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= (int64_t)num_blocks * block_size) {
+      ++bad;
+      continue;
+    }
+    const int64_t blk = slot / block_size, off = slot % block_size;
+    for (int h = 0; h < num_kv_heads; ++h) {
+      const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + (size_t)off) * rb;
+      const size_t src = ((size_t)t * num_kv_heads + h) * head_dim * 2;
+      orc_q4_0_quantize_row((const unsigned char*)k + src, src_dtype, head_dim, k_cache + dst);
+      orc_q4_0_quantize_row((const unsigned char*)v + src, src_dtype, head_dim, v_cache + dst);
+    }
+  }
+  return bad;
+}
+
+/*
+ * Paged decode attention over q4_0 pools ([QKV], [VM]): the definition of
+ * orc_paged_attention with every K and V element read back as d * (q - 8)
+ * from its row; q in q_dtype. out[s][h][:] for s in [seq_begin, seq_end).
+ * Returns 0 or a negative code.
+ */
+int orc_paged_attention_q4_0(double* out, const void* q, const uint8_t* k_cache, const uint8_t* v_cache,
+                             const int32_t* block_tables, int max_blocks_per_seq, const int32_t* context_lens,
+                             int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                             int num_blocks, int q_dtype, double scale, int seq_begin, int seq_end) {
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens) return -1;
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return -2;
+  if (head_dim <= 0 || head_dim % 32 || block_size <= 0 || num_blocks <= 0 || !elem_bytes(q_dtype)) return -3;
+  if (seq_begin < 0 || seq_end > num_seqs || seq_begin > seq_end) return -4;
+  const int group = num_heads / num_kv_heads;
+  const size_t rb = (size_t)head_dim / 16 * 9;
+  int max_len = 0;
+  for (int s = seq_begin; s < seq_end; ++s) {
+    if (context_lens[s] < 0 || context_lens[s] > max_blocks_per_seq * block_size) return -5;
+    if (context_lens[s] > max_len) max_len = context_lens[s];
+  }
+  double* x = (double*)malloc(sizeof(double) * (size_t)(max_len > 0 ? max_len : 1));
+  size_t* row = (size_t*)malloc(sizeof(size_t) * (size_t)(max_len > 0 ? max_len : 1));
+  if (!x || !row) {
+    free(x);
+    free(row);
+    return -6;
+  }
+  int rc = 0;
+  for (int s = seq_begin; s < seq_end && rc == 0; ++s) {
+    const int L = context_lens[s];
+    for (int h = 0; h < num_heads; ++h) {
+      const int g = h / group;
+      double* o = out + ((size_t)s * num_heads + h) * head_dim;
+      if (L == 0) {
+        for (int d = 0; d < head_dim; ++d) o[d] = 0.0;
+        continue;
+      }
+      const size_t q_off = ((size_t)s * num_heads + h) * head_dim;
+      for (int t = 0; t < L; ++t) {
+        const int32_t p = block_tables[(size_t)s * max_blocks_per_seq + t / block_size];
+        if (p < 0 || p >= num_blocks) {
+          rc = -7;
+          break;
+        }
+        row[t] = (((size_t)p * num_kv_heads + g) * block_size + (size_t)(t % block_size)) * rb;
+        double acc = 0.0;
+        for (int d = 0; d < head_dim; ++d)
+          acc += elem(q, q_off + (size_t)d, q_dtype) * orc_q4_0_value(k_cache + row[t], head_dim, d);
+        x[t] = scale * acc;
+      }
+      if (rc) break;
+      double m = -INFINITY, z = 0.0;
+      for (int t = 0; t < L; ++t)
+        if (x[t] > m) m = x[t];
+      for (int t = 0; t < L; ++t) {
+        x[t] = exp(x[t] - m);
+        z += x[t];
+      }
+      for (int d = 0; d < head_dim; ++d) {
+        double acc = 0.0;
+        for (int t = 0; t < L; ++t) acc += x[t] * orc_q4_0_value(v_cache + row[t], head_dim, d);
+        o[d] = acc / z;
+      }
+    }
+  }
+  free(x);
+  free(row);
+  return rc;
+}

@@ -22,7 +22,13 @@ AssertionError when the oracle disagrees with:
   - the fp8 (E4M3) cache: the code table and round-to-nearest-even of
     PyTorch's float8_e4m3fn conversion (a library routine), saturation at
     448, ties to the even code, and attention over E4M3 pools equal bit for
-    bit to the binary32 oracle over the exactly decoded values.
+    bit to the binary32 oracle over the exactly decoded values;
+  - the 4-bit (q4_0) cache: the binary16 rounding of the scale against
+    numpy's conversion, exact blocks d (k - 8) whose codes are known, the
+    hand-derived rules (first maximum, rounding half up, the clamp at 15,
+    the zero block), the error bound of the format, byte placement of the
+    cache write, and attention over q4_0 pools equal bit for bit to the
+    binary32 oracle over the values numpy reads back from the rows.
 
 tests/test_oracle_pins.py runs them on the oracle; tests/test_oracle_mutations.py
 runs them on copies with planted mistakes and expects each copy to fail one.
@@ -464,6 +470,164 @@ def pin_fp8_cache_write(L=None):
         assert np.array_equal(kc, ek) and np.array_equal(vc, ev), f"fp8 cache write ({dtype})"
 
 
+# ---------------------------------------------------------------- 4-bit (q4_0) cache
+def _f16_of_bits(bits) -> np.ndarray:
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def _q4_row_values(row: np.ndarray, D: int) -> np.ndarray:
+    """Reference read-back of one q4_0 cache row with numpy, from the row
+    layout: D/32 binary16 scales, then 16 code bytes per block whose byte j
+    holds element j (low four bits) and element j + 16 (high four bits)."""
+    nb = D // 32
+    d = _f16_of_bits(row[:2 * nb].view(np.uint16))
+    codes = row[2 * nb:].reshape(nb, 16)
+    q = np.concatenate([codes & 0xF, codes >> 4], axis=1).astype(np.float64)  # [nb][32]
+    return ((q - 8.0) * d[:, None]).reshape(-1)
+
+
+@np.errstate(over="ignore")
+def pin_f16_encoder(L=None):
+    """The binary16 rounding of the scale against numpy's float32 -> float16
+    conversion: nearest, ties to even, subnormals, overflow to infinity."""
+    rng = np.random.default_rng(61)
+    x = [rng.standard_normal(3000) * 10.0 ** rng.integers(-9, 6, 3000), rng.uniform(-2.0 ** -14, 2.0 ** -14, 1000),
+         np.array([65504.0, 65519.0, 65520.0, 7e4, -1e6, 0.0, -0.0, 2.0 ** -25, 1.5 * 2.0 ** -24, 2.0 ** -26])]
+    pos = np.arange(0x7c00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    mids = (pos[:-1] + pos[1:]) / 2  # exact in binary32 (12 significant bits)
+    x += [mids[::7], -mids[::11]]
+    x32 = np.concatenate(x).astype(np.float32)
+    want = x32.astype(np.float16).view(np.uint16)
+    assert np.array_equal(oracle.encode_f16(x32.astype(np.float64), L), want), "binary16 rounding"
+
+
+def pin_q4_0_exact_blocks(L=None):
+    """Blocks x_j = d (k_j - 8) with integers k_j in [0, 15], k_0 = 0 and d a
+    power of two: -8 d is the first element of largest magnitude, so the
+    scale is d, every x_j / d + 8.5 = k_j + 0.5 is exact, the codes are the
+    k_j themselves, and the block reads back exactly."""
+    rng = np.random.default_rng(63)
+    for e in (-12, -3, 0, 5, 11):
+        for sgn in (1.0, -1.0):
+            d = sgn * 2.0 ** e
+            k = rng.integers(0, 16, 64)
+            k[0] = k[32] = 0
+            x = d * (k - 8.0)
+            d_bits, qs = oracle.q4_0_quantize_block(x[:32].astype(np.float32), L)
+            assert _f16_of_bits(d_bits) == d, f"q4_0 scale (d = {d})"
+            want = (k[:16] | (k[16:32] << 4)).astype(np.uint8)
+            assert np.array_equal(qs, want), f"q4_0 codes and nibble order (d = {d})"
+            # the same values as a binary16 row of two blocks
+            src = x.astype(np.float16).view(np.uint16)
+            row = oracle.q4_0_quantize_row(src, "f16", L)
+            assert row.shape == (36,) and np.array_equal(row[:4].view(np.uint16), np.array([d_bits, d_bits]))
+            assert np.array_equal(_q4_row_values(row, 64), x), f"q4_0 exact read-back (d = {d})"
+            assert np.array_equal(oracle.q4_0_values(row, 64, L), x), f"q4_0 oracle read-back (d = {d})"
+
+
+def pin_q4_0_rules(L=None):
+    """Hand-derived blocks for the rules of the format's reading.
+    (a) Ties in magnitude go to the first element: x_0 = -1, x_5 = +1, the
+        rest 0.25: m = -1, d = 0.125, x / d + 8.5 gives 0.5, 16.5 and 10.5,
+        so codes 0, 15 (clamped) and 10; scale bits 0x3000.
+    (b) Codes round half up: with d = 1 (x_0 = -8), 0.5 -> 9.0 -> code 9,
+        -0.5 -> 8.0 -> 8, 1.5 -> 10.0 -> 10, -1.5 -> 7.0 -> 7.
+    (c) A zero block: m = +0, d = -0 (scale bits 0x8000), every code 8."""
+    x = np.full(32, 0.25, dtype=np.float32)
+    x[0], x[5] = -1.0, 1.0
+    d_bits, qs = oracle.q4_0_quantize_block(x, L)
+    want = np.full(16, 0xAA, dtype=np.uint8)
+    want[0], want[5] = 0xA0, 0xAF
+    assert d_bits == 0x3000 and np.array_equal(qs, want), "q4_0 first maximum, clamp"
+    x = np.zeros(32, dtype=np.float32)
+    x[0], x[1], x[2], x[3], x[4] = -8.0, 0.5, -0.5, 1.5, -1.5
+    d_bits, qs = oracle.q4_0_quantize_block(x, L)
+    codes = np.concatenate([qs & 0xF, qs >> 4])
+    assert d_bits == 0x3C00 and list(codes[:5]) == [0, 9, 8, 10, 7] and np.all(codes[5:] == 8), \
+        "q4_0 rounding half up"
+    d_bits, qs = oracle.q4_0_quantize_block(np.zeros(32, dtype=np.float32), L)
+    assert d_bits == 0x8000 and np.all(qs == 0x88), "q4_0 zero block"
+
+
+def pin_q4_0_error_bound(L=None):
+    """Random rows (normal, heavy-tailed, tiny, bfloat16): every value reads
+    back within |d| (1 + 2^-7) of itself (half a step, or one step where the
+    code saturates at 15, plus the binary16 rounding of d), and the element of
+    largest magnitude of each block within |m| 2^-11 (its code is 0)."""
+    rng = np.random.default_rng(65)
+    for dtype, scale in (("f16", 1.0), ("f16", 3e-4), ("bf16", 50.0)):
+        for _ in range(40):
+            D = 128
+            raw = rng.standard_normal(D) * scale
+            raw[rng.integers(0, D, 3)] *= 30.0
+            src = H.round_to_storage(raw, dtype)
+            x = _dec(src, dtype)
+            row = oracle.q4_0_quantize_row(src, dtype, L)
+            got = _q4_row_values(row, D)
+            d = np.abs(_f16_of_bits(row[:8].view(np.uint16)))
+            for b in range(4):
+                xb, gb = x[32 * b:32 * b + 32], got[32 * b:32 * b + 32]
+                assert np.all(np.abs(xb - gb) <= d[b] * (1 + 2.0 ** -7)), "q4_0 error bound"
+                j = int(np.argmax(np.abs(xb)))
+                assert abs(gb[j] - xb[j]) <= abs(xb[j]) * 2.0 ** -11, "q4_0 largest element"
+
+
+def pin_q4_0_cache_write(L=None):
+    """Each (token, kv head) row lands at its slot as that row's q4_0 bytes;
+    a negative slot is skipped, an out-of-range one counted; every other
+    byte of the pools is untouched."""
+    rng = np.random.default_rng(67)
+    T, Hkv, D, bs, NB = 9, 2, 64, 4, 8
+    rb = oracle.q4_0_row_bytes(D)
+    for dtype in ("f16", "bf16"):
+        k = _rand_store(rng, (T, Hkv, D), dtype)
+        v = _rand_store(rng, (T, Hkv, D), dtype, scale=0.1)
+        slots = rng.permutation(NB * bs)[:T].astype(np.int64)
+        slots[2], slots[4] = -1, NB * bs + 3
+        kc = rng.integers(0, 256, (NB, Hkv, bs, rb), dtype=np.uint8)
+        vc = rng.integers(0, 256, (NB, Hkv, bs, rb), dtype=np.uint8)
+        ek, ev = kc.copy(), vc.copy()
+        bad = oracle.reshape_and_cache_q4_0(k, v, kc, vc, slots, num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                                            src_dtype=dtype, L=L)
+        assert bad == 1, "q4_0 out-of-range slot count"
+        for t in range(T):
+            if slots[t] < 0 or slots[t] >= NB * bs:
+                continue
+            b, r = slots[t] // bs, slots[t] % bs
+            for h in range(Hkv):
+                ek[b, h, r] = oracle.q4_0_quantize_row(np.ascontiguousarray(k[t, h]), dtype, L)
+                ev[b, h, r] = oracle.q4_0_quantize_row(np.ascontiguousarray(v[t, h]), dtype, L)
+        assert np.array_equal(kc, ek) and np.array_equal(vc, ev), f"q4_0 cache write ({dtype})"
+
+
+def pin_q4_0_attention(L=None):
+    """Every q4_0 value d (q - 8) is exact in binary32, so attention over q4_0
+    pools must equal, bit for bit, the binary32 oracle over pools holding the
+    values numpy reads back from the rows."""
+    rng = np.random.default_rng(69)
+    B, H_, Hkv, D, bs, NB = 3, 4, 2, 64, 4, 20
+    lens = np.array([1, 7, 13], dtype=np.int32)
+    _, kc16, _, bt, lens = _random_paged(rng, B, H_, Hkv, D, bs, NB, lens, "f16")
+    rb = oracle.q4_0_row_bytes(D)
+
+    def pool(sc):
+        p = rng.integers(0, 256, (NB, Hkv, bs, rb), dtype=np.uint8)
+        sbits = (rng.standard_normal((NB, Hkv, bs, D // 32)) * sc).astype(np.float16).view(np.uint16)
+        p[..., :D // 16] = sbits.view(np.uint8).reshape(NB, Hkv, bs, D // 16)
+        vals = np.stack([_q4_row_values(r, D) for r in p.reshape(-1, rb)]).reshape(NB, Hkv, bs, D)
+        return p, vals.astype(np.float32)
+
+    kq, k32 = pool(0.05)
+    vq, v32 = pool(0.3)
+    q = _rand_store(rng, (B, H_, D), "f16")
+    q32 = q.view(np.float16).astype(np.float32)
+    ref = oracle.paged_attention(q32, k32, v32, bt, lens, scale=0.3, num_heads=H_, num_kv_heads=Hkv, head_dim=D,
+                                 block_size=bs, dtype="f32", L=L)
+    got = oracle.paged_attention_q4_0(q, kq, vq, bt, lens, scale=0.3, num_heads=H_, num_kv_heads=Hkv, head_dim=D,
+                                      block_size=bs, q_dtype="f16", L=L)
+    assert np.array_equal(got, ref), "q4_0 attention"
+
+
 # ---------------------------------------------------------------- paged prefill
 def _prefill_case(rng, dtype="f16"):
     B, H_, Hkv, D, bs, NB = 3, 4, 2, 16, 4, 40
@@ -512,4 +676,6 @@ ALL_PINS = [pin_decoders, pin_context_one, pin_uniform_weights, pin_dominant_log
             pin_two_tokens, pin_gqa_mapping, pin_brute_force, pin_dense_equivalence,
             pin_placement_invariance, pin_copy_on_write, pin_split_merge,
             pin_reshape_and_cache, pin_copy_blocks, pin_e4m3_codec, pin_fp8_attention,
-            pin_fp8_cache_write, pin_prefill_single_query_is_decode, pin_prefill_prefix_dense]
+            pin_fp8_cache_write, pin_prefill_single_query_is_decode, pin_prefill_prefix_dense,
+            pin_f16_encoder, pin_q4_0_exact_blocks, pin_q4_0_rules, pin_q4_0_error_bound, pin_q4_0_cache_write,
+            pin_q4_0_attention]

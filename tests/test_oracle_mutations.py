@@ -54,6 +54,23 @@ MUTATIONS = [
     ("fp8 attention drops v_scale", "x[t] * (v_scale * orc_decode_e4m3(", "x[t] * (orc_decode_e4m3(", 0),
     ("prefill causal off by one", "const int pos = L - n + i;", "const int pos = L - n + i - 1;", 0),
     ("prefill positions from the start", "const int pos = L - n + i;", "const int pos = i;", 0),
+    ("f16 encoder ties away from zero", "(int)rint(ldexp(a, 10 - E))", "(int)floor(ldexp(a, 10 - E) + 0.5)", 0),
+    ("f16 encoder subnormal step", "code = (int)rint(ldexp(a, 24));", "code = (int)rint(ldexp(a, 23));", 0),
+    ("q4_0 offset 7", "return (double)(q - 8) * orc_decode_f16(sb);", "return (double)(q - 7) * orc_decode_f16(sb);", 0),
+    ("q4_0 nibbles swapped", "qs[j] = (uint8_t)(q[j] | (q[j + 16] << 4));",
+     "qs[j] = (uint8_t)(q[j + 16] | (q[j] << 4));", 0),
+    ("q4_0 scale sign", "const float d = m / -8.0f;", "const float d = m / 8.0f;", 0),
+    ("q4_0 rounds down", "const float y = prod + 8.5f;", "const float y = prod + 8.0f;", 0),
+    ("q4_0 last maximum on ties", "if (a > amax) {", "if (a >= amax) {", 0),
+    ("q4_0 no clamp", "q[j] = y >= 15.0f ? 15 : (y >= 0.0f ? (int)y : 0);",
+     "q[j] = y >= 16.0f ? 16 : (y >= 0.0f ? (int)y : 0) & 15;", 0),
+    ("q4_0 scales after the codes", "const uint8_t byte = row[head_dim / 16 + 16 * b + (j % 16)];",
+     "const uint8_t byte = row[16 * b + (j % 16)];", 0),
+    ("q4_0 cache write swaps K and V",
+     "orc_q4_0_quantize_row((const unsigned char*)k + src, src_dtype, head_dim, k_cache + dst);",
+     "orc_q4_0_quantize_row((const unsigned char*)v + src, src_dtype, head_dim, k_cache + dst);", 0),
+    ("q4_0 attention reads K for V", "acc += x[t] * orc_q4_0_value(v_cache + row[t], head_dim, d);",
+     "acc += x[t] * orc_q4_0_value(k_cache + row[t], head_dim, d);", 0),
 ]
 
 
