@@ -39,6 +39,7 @@ CSRC = os.path.join(ROOT, "paged_kv_cache_204_gb300", "csrc")
 PROFILES = {
     "plain": (os.path.join(ROOT, "profiles", "pa_decode_llama13b.md"), ("decode.cuh",)),
     "fp8": (os.path.join(ROOT, "profiles", "pa_decode_fp8_llama13b.md"), ("decode.cuh",)),
+    "q4": (os.path.join(ROOT, "profiles", "pa_decode_q4_0_llama13b.md"), ("decode.cuh",)),
     "grouped": (os.path.join(ROOT, "profiles", "pa_decode_grouped_cow.md"), ("decode.cuh", "decode_grouped.cuh")),
 }
 FLUSH_BYTES = 256 << 20
@@ -46,22 +47,25 @@ FALLBACK_HBM_GBS = 6800.0
 
 
 def workload_bytes(st, kv_elem_bytes: int | None = None, new_rows: int | None = None,
-                   copy_pairs: int | None = None) -> dict:
+                   copy_pairs: int | None = None, kv_row_bytes: int | None = None) -> dict:
     """Algorithmic bytes of one step: attention reads each distinct cached
     (block, row) once for K and once for V plus q, and writes out; the cache
     write reads the new rows and writes them into the pools; each
     copy-on-write pair reads and writes one whole block of both pools.
     new_rows / copy_pairs: the step's counts when they differ from the
-    structure's (a copy-on-write decode step writes one row per sample)."""
+    structure's (a copy-on-write decode step writes one row per sample).
+    kv_row_bytes: bytes of one cached row of head_dim values when they are
+    not head_dim elements (q4_0 rows)."""
     cfg = st.cfg
     es = cfg.elem_bytes
     kes = es if kv_elem_bytes is None else kv_elem_bytes  # cached element (1 for fp8 pools)
-    row = cfg.num_kv_heads * cfg.head_dim * kes          # one token, one of K/V, all kv heads, as cached
+    head_row = cfg.head_dim * kes if kv_row_bytes is None else kv_row_bytes
+    row = cfg.num_kv_heads * head_row                    # one token, one of K/V, all kv heads, as cached
     qo = st.num_seqs * cfg.num_heads * cfg.head_dim * es
     attn = 2 * st.unique_kv_tokens() * row + 2 * qo
     n_new = st.num_new_tokens if new_rows is None else new_rows
     n_pairs = st.copy_pairs.shape[0] if copy_pairs is None else copy_pairs
-    cache_write = 2 * n_new * (row // kes * es + row)  # read the new rows, write them cached
+    cache_write = 2 * n_new * (cfg.num_kv_heads * cfg.head_dim * es + row)  # read the new rows, write them cached
     copies = 2 * 2 * n_pairs * cfg.block_size * row
     return {"attention": attn, "cache_write": cache_write, "copy": copies,
             "step": attn + cache_write + copies}
@@ -477,6 +481,26 @@ def fp8_pool(pool, scale: float, chunk: int = 2048):
     return out
 
 
+def q4_pool(pool, scale_sigma: float, seed: int, chunk: int = 2048):
+    """q4_0 rows (uint8 [blocks, kv heads, block_size, 9 D / 16]) in place of
+    a 16-bit pool: uniform random code bytes and binary16 scales drawn from
+    N(0, scale_sigma^2), values of the same spread as the 16-bit data. Input
+    generation only: the timed step writes its rows with the library's q4_0
+    cache write."""
+    import torch
+    nb, hkv, bs, d = pool.shape
+    rb = d // 16 * 9
+    out = torch.empty((nb, hkv, bs, rb), dtype=torch.uint8, device=pool.device)
+    gen = torch.Generator(device=pool.device)
+    gen.manual_seed(seed)
+    for a in range(0, nb, chunk):
+        o = out[a:a + chunk]
+        o.copy_(torch.randint(0, 256, o.shape, generator=gen, device=pool.device, dtype=torch.int32).to(torch.uint8))
+        sc = (torch.randn(o.shape[:3] + (d // 32,), generator=gen, device=pool.device) * scale_sigma).half()
+        o[..., :d // 16] = sc.view(torch.uint8)
+    return out
+
+
 def kv_memory(cfg) -> dict:
     """KV memory of the workload as the library's host block manager lays it
     out ("PagedAttention: the KV cache was the bottleneck all along", sections
@@ -550,16 +574,24 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         dw.new_k, dw.new_v = dw.new_k[last].contiguous(), dw.new_v[last].contiguous()
         dw.slot_mapping = dw.slot_mapping[last].contiguous()
         dw.copy_pairs = dw.copy_pairs[:0]
-    fp8 = args.kv == "fp8"
+    fp8, q4 = args.kv == "fp8", args.kv == "q4_0"
+    if (fp8 or q4) and (args.attention != "plain" or cfg.dtype == "f32"):
+        raise SystemExit(f"--kv {args.kv} takes the plain attention of a 16-bit workload")
     if fp8:
-        if args.attention != "plain" or cfg.dtype == "f32":
-            raise SystemExit("--kv fp8 takes the plain attention of a 16-bit workload")
         dw.k_cache = fp8_pool(dw.k_cache, FP8_SCALE)
         dw.v_cache = fp8_pool(dw.v_cache, FP8_SCALE)
         torch.cuda.empty_cache()
-    kv_desc = (f"fp8 e4m3 K/V pools (per-pool scale {FP8_SCALE:.6g}; new rows rounded on write)" if fp8 else None)
+    if q4:
+        # a 32-value block of N(0, s^2) values spans about 3 s: scales near 3 s / 8
+        dw.k_cache = q4_pool(dw.k_cache, 0.4 * cfg.value_scale, cfg.seed + 1)
+        dw.v_cache = q4_pool(dw.v_cache, 0.4 * cfg.value_scale, cfg.seed + 2)
+        torch.cuda.empty_cache()
+    kv_desc = (f"fp8 e4m3 K/V pools (per-pool scale {FP8_SCALE:.6g}; new rows rounded on write)" if fp8 else
+               f"q4_0 K/V pools (blocks of 32 values, binary16 scale, 4-bit codes; {cfg.head_dim // 16 * 9}-byte "
+               f"rows; new rows quantised on write)" if q4 else None)
     nbytes = workload_bytes(st, 1 if fp8 else None, new_rows=int(dw.slot_mapping.numel()),
-                            copy_pairs=int(dw.copy_pairs.shape[0]))
+                            copy_pairs=int(dw.copy_pairs.shape[0]),
+                            kv_row_bytes=cfg.head_dim // 16 * 9 if q4 else None)
     B, H, D = st.num_seqs, cfg.num_heads, cfg.head_dim
     mcl = st.max_context_len
     grouped = args.attention == "grouped"
@@ -584,6 +616,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
             if fp8:
                 pkv.reshape_and_cache_fp8(dw.new_k, dw.new_v, dw.k_cache, dw.v_cache, dw.slot_mapping, FP8_SCALE,
                                           FP8_SCALE, dev_err=err)
+            elif q4:
+                pkv.reshape_and_cache_q4_0(dw.new_k, dw.new_v, dw.k_cache, dw.v_cache, dw.slot_mapping, dev_err=err)
             else:
                 pkv.reshape_and_cache(dw.new_k, dw.new_v, dw.k_cache, dw.v_cache, dw.slot_mapping, dev_err=err)
 
@@ -591,6 +625,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         if fp8:
             pkv.paged_attention_decode_fp8(out, dw.q, dw.k_cache, dw.v_cache, dw.block_tables, dw.context_lens,
                                            cfg.scale, FP8_SCALE, FP8_SCALE, mcl, workspace=ws, dev_err=err)
+        elif q4:
+            pkv.paged_attention_decode_q4_0(out, dw.q, dw.k_cache, dw.v_cache, dw.block_tables, dw.context_lens,
+                                            cfg.scale, mcl, workspace=ws, dev_err=err)
         elif grouped:
             pkv.paged_attention_decode_grouped(out, dw.q, dw.k_cache, dw.v_cache, dw.block_tables,
                                                dw.context_lens, cfg.scale, mcl, gs, sb, ws, dev_err=err)
@@ -685,6 +722,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
             cpu = sampled_attention_baseline(cfg, dw.k_cache, dw.v_cache, st.block_tables, st.context_lens, dw.q,
                                              args.cpu_seconds, args.cpu_seqs, "sequences (fp8 pools)",
                                              fp8_scales=(FP8_SCALE, FP8_SCALE))
+        elif q4:
+            cpu = sampled_attention_baseline(cfg, dw.k_cache, dw.v_cache, st.block_tables, st.context_lens, dw.q,
+                                             args.cpu_seconds, args.cpu_seqs, "sequences (q4_0 pools)", q4=True)
         elif cow:
             cpu = sampled_attention_baseline(cfg, dw.k_cache, dw.v_cache, st.block_tables, st.context_lens, dw.q,
                                              args.cpu_seconds, args.cpu_seqs, "samples (plain paged attention)")
@@ -698,17 +738,20 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
         "n_gpus": world, "steps": K, "warmup": max(args.warmup, 3),
         "ms_per_step": agg["step_ms"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": f"{cfg.dtype} queries, fp8_e4m3 K/V" if fp8 else cfg.dtype, "data": "synthetic",
+        "dtype": (f"{cfg.dtype} queries, fp8_e4m3 K/V" if fp8 else f"{cfg.dtype} queries, q4_0 K/V" if q4
+                  else cfg.dtype), "data": "synthetic",
         "config": config_json(cfg, st, world, args.attention, kv_desc, args.flush),
         "seqs_per_s": world * B / (agg["step_ms"] * 1e-3),
         "attention_ms": agg["decode_ms"], "cache_ops_ms": agg["cache_ms"],
         "bytes_per_step": nbytes["step"], "roofline_frac_step": nbytes["step"] / (agg["step_ms"] * 1e-3) / 1e9 / peak,
         "roofline": {"bound": "hbm",
                      "kernel": ("pa_group_prologue + pa_decode_shared_kernel" if grouped else
-                                "pa_decode_kernel<fp8 e4m3 cache>" if fp8 else "pa_decode_kernel"),
+                                "pa_decode_kernel<fp8 e4m3 cache>" if fp8 else
+                                "pa_decode_kernel<q4_0 cache>" if q4 else "pa_decode_kernel"),
                      "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": (profiled_traffic("fp8") if fp8 else profiled_traffic("plain"))
+                     "traffic": (profiled_traffic("fp8") if fp8 else profiled_traffic("q4") if q4 else
+                                 profiled_traffic("plain"))
                      if (cfg.name == WORKLOAD and not grouped) else
                      profiled_traffic("grouped") if (cfg.name == "cow" and grouped) else None,
                      "algorithmic_bytes_per_launch": nbytes["attention"], "peak_source": peak_src},
@@ -728,10 +771,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> int:
 
 
 def sampled_attention_baseline(cfg, kc, vc, block_tables, context_lens, q, min_seconds: float, n_seqs: int,
-                               what: str, fp8_scales=None) -> dict:
+                               what: str, fp8_scales=None, q4: bool = False) -> dict:
     """The fp64 oracle, as it stands, on the host cores: paged attention of
     the first n_seqs sequences over host copies of their blocks (fp8 pools
-    when fp8_scales = (k_scale, v_scale)), repeated for about min_seconds."""
+    when fp8_scales = (k_scale, v_scale), q4_0 pools when q4), repeated for
+    about min_seconds."""
     import numpy as np
     import oracle
     from synth.device import to_storage
@@ -745,20 +789,23 @@ def sampled_attention_baseline(cfg, kc, vc, block_tables, context_lens, q, min_s
     import torch
     idx = torch.from_numpy(ids.astype(np.int64)).to(kc.device)
     q_h = to_storage(q[:n])
-    if fp8_scales is None:
+    if fp8_scales is None and not q4:
         k_h, v_h = to_storage(kc[idx]), to_storage(vc[idx])
     else:
         k_h, v_h = kc[idx].cpu().numpy(), vc[idx].cpu().numpy()
     rows = {(int(b), r) for i in range(n) for j, b in enumerate(bt[i][bt[i] >= 0])
             for r in range(min(cfg.block_size, int(cl[i]) - j * cfg.block_size))}
-    kv_row = cfg.kv_bytes_per_token() // (1 if fp8_scales is None else cfg.elem_bytes)
+    kv_row = (2 * cfg.num_kv_heads * (cfg.head_dim // 16 * 9) if q4 else
+              cfg.kv_bytes_per_token() // (1 if fp8_scales is None else cfg.elem_bytes))
     nbytes = len(rows) * kv_row + 2 * n * cfg.num_heads * cfg.head_dim * cfg.elem_bytes
     kw = dict(num_heads=cfg.num_heads, num_kv_heads=cfg.num_kv_heads, head_dim=cfg.head_dim,
               block_size=cfg.block_size, threads=threads)
     times, t_start = [], time.perf_counter()
     while True:
         t0 = time.perf_counter()
-        if fp8_scales is None:
+        if q4:
+            oracle.paged_attention_q4_0(q_h, k_h, v_h, bt_c, cl, scale=cfg.scale, q_dtype=cfg.dtype, **kw)
+        elif fp8_scales is None:
             oracle.paged_attention(q_h, k_h, v_h, bt_c, cl, scale=cfg.scale, dtype=cfg.dtype, **kw)
         else:
             oracle.paged_attention_fp8(q_h, k_h, v_h, bt_c, cl, scale=cfg.scale, k_scale=fp8_scales[0],
@@ -1164,8 +1211,9 @@ def main() -> int:
     ap.add_argument("--workload", default=WORKLOAD,
                     help="synthetic workload preset (default: the LLaMA-13B-shaped step); "
                          "'beam': beam-search decode steps")
-    ap.add_argument("--kv", choices=("native", "fp8"), default="native",
-                    help="fp8: K/V pools of e4m3 codes with one scale per pool (plain attention)")
+    ap.add_argument("--kv", choices=("native", "fp8", "q4_0"), default="native",
+                    help="fp8: K/V pools of e4m3 codes with one scale per pool; q4_0: 4-bit blocks of 32 values "
+                         "with a binary16 scale (plain attention)")
     ap.add_argument("--attention", choices=("plain", "grouped"), default="plain",
                     help="grouped: siblings read shared prefix blocks once (copy-on-write workloads)")
     ap.add_argument("--flush", choices=("write+read", "write"), default="write+read",

@@ -69,8 +69,10 @@ typedef enum pkv_dtype {
   PKV_F32 = 0,      /* IEEE binary32 */
   PKV_F16 = 1,      /* IEEE binary16 */
   PKV_BF16 = 2,     /* bfloat16      */
-  PKV_FP8_E4M3 = 3  /* 8-bit float, 1 sign, 4 exponent (bias 7), 3 mantissa bits, no infinities,
+  PKV_FP8_E4M3 = 3, /* 8-bit float, 1 sign, 4 exponent (bias 7), 3 mantissa bits, no infinities,
                        largest finite 448 (OCP "E4M3"); cache element type only, see the fp8 entry points */
+  PKV_Q4_0 = 4      /* 4-bit codes in blocks of 32 values with one binary16 scale (q4_0); cache type
+                       only, rows of 9 * head_dim / 16 bytes, see the q4_0 entry points */
 } pkv_dtype;
 
 typedef enum pkv_status {
@@ -347,6 +349,56 @@ pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, const void* 
                                           int num_blocks, int max_context_len, pkv_dtype dtype,
                                           void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                           pkv_stream_t stream);
+
+/* ----------------------------------------------------------------------
+ * 4-bit (q4_0) KV cache
+ *
+ * [QKV], "In the conversation": a reader notes that 4-bit KV-cache
+ * quantisation (the cache type q4_0) cuts the cache to about a quarter. The
+ * pages name the format without defining it; this library reads it as the
+ * q4_0 block of the ggml tensor library. Every 32 consecutive values of a
+ * K or V row form a block with one binary16 scale d and a 4-bit code q per
+ * value, read back as d * (q - 8). Quantising a block x[0..31], every step
+ * in binary32:
+ *     m    = the first value of largest magnitude, sign kept (+0 when no
+ *            |x| is above 0; NaN values never qualify)
+ *     d    = m / -8, inv = 1 / d (0 when d is 0)
+ *     q_j  = 15 if y >= 15, trunc(y) if 0 <= y < 15, else 0 (NaN too),
+ *            where y = x_j * inv + 8.5 (a product and a sum, each rounded)
+ *     d is stored rounded to binary16 (nearest, ties to even; a block whose
+ *     largest magnitude exceeds 8 * 65504 gets an infinite scale).
+ * Pools hold bytes, [num_blocks][num_kv_heads][block_size][9 * head_dim / 16]:
+ * each row is its head_dim / 32 scales (little-endian binary16), then 16
+ * code bytes per block, byte j holding q_j in its low and q_(j+16) in its
+ * high four bits. A 16-bit row of 2 * head_dim bytes takes 9 * head_dim / 16
+ * (0.28 of the bytes). Queries and outputs stay binary16 or bfloat16.
+ * pkv_copy_blocks copies q4_0 blocks when given dtype PKV_Q4_0.
+ * ---------------------------------------------------------------------- */
+
+/* Write new K/V rows into q4_0 caches ([QKV], [VM]): k, v [num_tokens]
+ * [num_kv_heads][head_dim] of src_dtype (PKV_F16 or PKV_BF16, 16-byte
+ * aligned), quantised as above into the slot's row; slots, skipped
+ * padding tokens and errors as in pkv_reshape_and_cache. The result is
+ * bit-exact: the same bytes as the rule above computed on any IEEE host. */
+pkv_status pkv_reshape_and_cache_q4_0(const void* k, const void* v, void* k_cache, void* v_cache,
+                                      const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                      int head_dim, int block_size, int num_blocks, pkv_dtype src_dtype,
+                                      int32_t* dev_err, pkv_stream_t stream);
+
+/* pkv_paged_attention_decode over q4_0 caches ([QKV], [VM]): the same
+ * arguments, layouts, workspace and error behaviour, with k_cache and
+ * v_cache holding q4_0 rows and `dtype` (PKV_F16 or PKV_BF16) the type of q
+ * and out. Every K and V value is d * (q - 8) of its block: logits are
+ * scale * (q . K) and the output is the softmax-weighted sum of V, with
+ * fp32 accumulation (the codes enter tensor-core MMAs exactly, the scales
+ * multiply fp32 partial sums). */
+pkv_status pkv_paged_attention_decode_q4_0(void* out, const void* q, const void* k_cache,
+                                           const void* v_cache, const int32_t* block_tables,
+                                           const int32_t* context_lens, float scale, int num_heads,
+                                           int num_kv_heads, int head_dim, int block_size, int num_seqs,
+                                           int max_blocks_per_seq, int num_blocks, int max_context_len,
+                                           pkv_dtype dtype, void* workspace, size_t workspace_bytes,
+                                           int32_t* dev_err, pkv_stream_t stream);
 
 /* ----------------------------------------------------------------------
  * Paged prefill

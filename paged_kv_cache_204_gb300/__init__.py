@@ -13,6 +13,8 @@ Functions mirror the C entry points:
   decode_workspace_bytes  -> pkv_decode_workspace_bytes
   paged_attention_decode_grouped  -> pkv_paged_attention_decode_grouped
   reshape_and_cache_fp8, paged_attention_decode_fp8  -> the fp8 (e4m3) cache entry points
+  reshape_and_cache_q4_0, paged_attention_decode_q4_0, copy_blocks_q4_0
+                          -> the 4-bit (q4_0) cache entry points
   paged_attention_prefill -> pkv_paged_attention_prefill
   decode_grouped_workspace_bytes  -> pkv_decode_grouped_workspace_bytes
   set_wait_timeout_ns / get_wait_timeout_ns, status_string, version
@@ -41,6 +43,7 @@ DEV_ERR_BLOCK_ID, DEV_ERR_SLOT, DEV_ERR_CONTEXT_LEN, DEV_ERR_TIMEOUT, DEV_ERR_PA
 DEV_ERR_GROUP = 32
 DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2, torch.uint8: 3}  # uint8: e4m3 codes
 PKV_FP8_E4M3 = 3
+PKV_Q4_0 = 4
 
 _P, _I, _I64, _U64, _F, _SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64,
                                ctypes.c_float, ctypes.c_size_t)
@@ -71,6 +74,11 @@ lib.pkv_reshape_and_cache_fp8.restype = _I
 lib.pkv_paged_attention_decode_fp8.argtypes = [_P, _P, _P, _P, _P, _P, _F, _F, _F, _I, _I, _I, _I, _I, _I, _I,
                                                _I, _I, _P, _SZ, _P, _P]
 lib.pkv_paged_attention_decode_fp8.restype = _I
+lib.pkv_reshape_and_cache_q4_0.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P]
+lib.pkv_reshape_and_cache_q4_0.restype = _I
+lib.pkv_paged_attention_decode_q4_0.argtypes = [_P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I, _I, _I,
+                                                _P, _SZ, _P, _P]
+lib.pkv_paged_attention_decode_q4_0.restype = _I
 lib.pkv_paged_attention_prefill.argtypes = [_P, _P, _P, _P, _P, _P, _P, _F, _I, _I, _I, _I, _I, _I, _I, _I, _I,
                                               _P, _P]
 lib.pkv_paged_attention_prefill.restype = _I
@@ -209,6 +217,46 @@ def paged_attention_decode_fp8(out: torch.Tensor, q: torch.Tensor, k_cache: torc
         float(scale), float(k_scale), float(v_scale), H, Hkv, D, bs, B, block_tables.shape[1], nb,
         int(max_context_len), DTYPE_CODE[q.dtype], _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)),
         "pkv_paged_attention_decode_fp8")
+
+
+def q4_0_row_bytes(head_dim: int) -> int:
+    """Bytes of one q4_0 cache row: head_dim / 32 binary16 scales, then
+    head_dim / 2 code bytes."""
+    return head_dim // 16 * 9
+
+
+def reshape_and_cache_q4_0(k: torch.Tensor, v: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           slot_mapping: torch.Tensor, dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """k, v [T, Hkv, D] fp16/bf16; k_cache, v_cache uint8 [num_blocks, Hkv,
+    block_size, 9 D / 16] of q4_0 rows."""
+    T, Hkv, D = k.shape
+    nb, _, bs, _ = k_cache.shape
+    _check(lib.pkv_reshape_and_cache_q4_0(_ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), T,
+                                          Hkv, D, bs, nb, DTYPE_CODE[k.dtype], _ptr(dev_err), _stream(stream)),
+           "pkv_reshape_and_cache_q4_0")
+
+
+def paged_attention_decode_q4_0(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                                max_context_len: int, workspace: torch.Tensor | None = None,
+                                dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """paged_attention_decode over uint8 pools of q4_0 rows; q, out fp16/bf16."""
+    B, H, D = q.shape
+    nb, Hkv, bs, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pkv_paged_attention_decode_q4_0(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        float(scale), H, Hkv, D, bs, B, block_tables.shape[1], nb, int(max_context_len), DTYPE_CODE[q.dtype],
+        _ptr(workspace), ws_bytes, _ptr(dev_err), _stream(stream)), "pkv_paged_attention_decode_q4_0")
+
+
+def copy_blocks_q4_0(k_cache: torch.Tensor, v_cache: torch.Tensor, block_pairs: torch.Tensor, head_dim: int,
+                     dev_err: torch.Tensor | None = None, stream=None) -> None:
+    """copy_blocks over uint8 pools of q4_0 rows of head_dim values."""
+    nb, Hkv, bs, _ = k_cache.shape
+    n = block_pairs.numel() // 2
+    _check(lib.pkv_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(block_pairs), n, Hkv, int(head_dim), bs, nb,
+                               PKV_Q4_0, _ptr(dev_err), _stream(stream)), "pkv_copy_blocks")
 
 
 def paged_attention_prefill(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,

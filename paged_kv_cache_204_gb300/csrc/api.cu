@@ -18,8 +18,12 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 bool supported_head_dim(int d) { return d == 64 || d == 128; }
 bool supported_block_size(int b) { return b == 8 || b == 16 || b == 32; }
 bool valid_dtype(int t) { return t == PKV_F32 || t == PKV_F16 || t == PKV_BF16; }
-bool valid_cache_dtype(int t) { return valid_dtype(t) || t == PKV_FP8_E4M3; }
+bool valid_cache_dtype(int t) { return valid_dtype(t) || t == PKV_FP8_E4M3 || t == PKV_Q4_0; }
 int elem_bytes(int t) { return t == PKV_F32 ? 4 : (t == PKV_FP8_E4M3 ? 1 : 2); }
+// bytes of one cache row of head_dim values
+int64_t cache_row_bytes(int t, int head_dim) {
+  return t == PKV_Q4_0 ? (int64_t)head_dim / 16 * 9 : (int64_t)head_dim * elem_bytes(t);
+}
 bool valid_scale(float s) { return std::isfinite(s) && s > 0.f; }
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -196,7 +200,7 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* block_pa
   if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_pairs, 8) ||
       (dev_err && !aligned(dev_err, 4)))
     return PKV_ERR_INVALID_ARG;
-  const int64_t block_bytes = (int64_t)num_kv_heads * block_size * head_dim * elem_bytes(dtype);
+  const int64_t block_bytes = (int64_t)num_kv_heads * block_size * cache_row_bytes(dtype, head_dim);
   return launch_status(pkv::launch_copy_blocks(k_cache, v_cache, block_pairs, num_pairs, block_bytes,
                                                num_blocks, dev_err, reinterpret_cast<cudaStream_t>(stream)));
 }
@@ -277,6 +281,55 @@ pkv_status pkv_paged_attention_decode_fp8(void* out, const void* q, const void* 
                                       num_heads, num_kv_heads, block_size, num_seqs, max_blocks_per_seq,
                                       num_blocks, max_context_len, gpw, dev_err);
   p.v_scale = v_scale;
+  char* wsb = static_cast<char*>(workspace);
+  p.ws_counter = reinterpret_cast<int32_t*>(wsb + ws.counter_off);
+  p.ws_ml = reinterpret_cast<float2*>(wsb + ws.ml_off);
+  p.ws_o = reinterpret_cast<float*>(wsb + ws.o_off);
+  return launch_status(launch(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_reshape_and_cache_q4_0(const void* k, const void* v, void* k_cache, void* v_cache,
+                                      const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                      int head_dim, int block_size, int num_blocks, pkv_dtype src_dtype,
+                                      int32_t* dev_err, pkv_stream_t stream) {
+  if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks <= 0)
+    return PKV_ERR_INVALID_ARG;
+  if ((src_dtype != PKV_F16 && src_dtype != PKV_BF16) || !supported_head_dim(head_dim) ||
+      !supported_block_size(block_size))
+    return PKV_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PKV_OK;
+  if (num_kv_heads > 4 * 65535) return PKV_ERR_UNSUPPORTED;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PKV_ERR_INVALID_ARG;
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+      !aligned(slot_mapping, 8) || (dev_err && !aligned(dev_err, 4)))
+    return PKV_ERR_INVALID_ARG;
+  return launch_status(pkv::launch_reshape_and_cache_q4(k, v, k_cache, v_cache, slot_mapping, num_tokens,
+                                                        num_kv_heads, head_dim, block_size, num_blocks,
+                                                        src_dtype == PKV_BF16 ? 1 : 0, dev_err,
+                                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pkv_status pkv_paged_attention_decode_q4_0(void* out, const void* q, const void* k_cache,
+                                           const void* v_cache, const int32_t* block_tables,
+                                           const int32_t* context_lens, float scale, int num_heads,
+                                           int num_kv_heads, int head_dim, int block_size, int num_seqs,
+                                           int max_blocks_per_seq, int num_blocks, int max_context_len,
+                                           pkv_dtype dtype, void* workspace, size_t workspace_bytes,
+                                           int32_t* dev_err, pkv_stream_t stream) {
+  if (dtype != PKV_F16 && dtype != PKV_BF16 && valid_dtype(dtype)) return PKV_ERR_UNSUPPORTED;
+  const pkv_status st = check_decode_args(out, q, k_cache, v_cache, block_tables, context_lens, scale,
+                                          num_heads, num_kv_heads, head_dim, block_size, num_seqs,
+                                          max_blocks_per_seq, num_blocks, max_context_len, dtype, dev_err);
+  if (st != PKV_OK || num_seqs == 0) return st;
+  const WorkspaceLayout ws = workspace_layout(num_seqs, num_heads, head_dim);
+  if (!workspace || workspace_bytes < ws.total) return PKV_ERR_WORKSPACE;
+  if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
+  pkv::DecodeLauncher launch = pkv::decode_launcher_q4(dtype == PKV_BF16 ? 1 : 0, head_dim);
+  if (!launch) return PKV_ERR_UNSUPPORTED;
+  // one query head per warp, whatever the grouping of query heads
+  pkv::DecodeParams p = decode_params(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_heads,
+                                      num_kv_heads, block_size, num_seqs, max_blocks_per_seq, num_blocks,
+                                      max_context_len, 1, dev_err);
   char* wsb = static_cast<char*>(workspace);
   p.ws_counter = reinterpret_cast<int32_t*>(wsb + ws.counter_off);
   p.ws_ml = reinterpret_cast<float2*>(wsb + ws.ml_off);

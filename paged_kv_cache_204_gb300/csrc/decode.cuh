@@ -71,11 +71,27 @@ struct DecodeParams {
 
 constexpr int kTileTokens = 16;  // tokens of a tile of a 16- or 32-bit cache
 
-// Tokens per tile of the plain kernel: fp8 caches take 32-token tiles, so a
-// tile carries as many bytes (and a warp's per-tile work as much data) as a
-// 16-token tile of a 16-bit cache.
+// Element tag of a q4_0 cache: each row of D values is D/32 blocks of 32,
+// stored as the D/32 binary16 scales d_b, then 16 code bytes per block (byte
+// j of block b holds value 32 b + j in its low and 32 b + j + 16 in its high
+// four bits); a code q reads back as d_b (q - 8). 9 D / 16 bytes per row.
+struct Q4Row {};
+
 template <typename KT>
-constexpr int tile_tokens_for() { return sizeof(KT) == 1 ? 2 * kTileTokens : kTileTokens; }
+struct CacheKind {
+  static constexpr bool kFp8 = std::is_same<KT, __nv_fp8_e4m3>::value;
+  static constexpr bool kQ4 = std::is_same<KT, Q4Row>::value;
+  template <int D>
+  static constexpr int row_bytes() { return kQ4 ? D / 16 * 9 : D * (int)sizeof(KT); }
+};
+
+// Tokens per tile of the plain kernel: fp8 and q4_0 caches take 32-token
+// tiles, so a tile carries about as many bytes (and a warp's per-tile work
+// as much data) as a 16-token tile of a 16-bit cache.
+template <typename KT>
+constexpr int tile_tokens_for() {
+  return (CacheKind<KT>::kFp8 || CacheKind<KT>::kQ4) ? 2 * kTileTokens : kTileTokens;
+}
 constexpr int kDecodeWarps = 8;  // one resident block of 8 warps per SM (measured best)
 // fp8 caches (1 or 2 query heads per warp): a warp's per-tile work is a
 // longer latency chain for half the bytes, so more warps share an SM (as many
@@ -152,6 +168,32 @@ struct LaneDims<T, __nv_fp8_e4m3, D> {
   }
 };
 
+// q4_0 caches (tensor-core tile, one query head per warp, Q4Mma below): lane
+// sub of the CUDA-core layout ends with the head dims of the low (e < DPL/2)
+// and high (e >= DPL/2) four bits of its DPL/2 code bytes of one block: two
+// runs of DPL/2 contiguous dims.
+template <typename T, int D>
+struct LaneDims<T, Q4Row, D> {
+  static_assert(sizeof(T) == 2, "q4_0 caches take 16-bit queries");
+  static constexpr int kParts = 1;
+  static constexpr int kPartElems = D / 8;  // 8 or 16 dims
+  static constexpr int kHalf = D / 16;      // dims per run
+  static constexpr int kLanesPerBlock = 8 / (D / 32);
+  __device__ __forceinline__ static int dim(int sub, int, int e) {
+    return 32 * (sub / kLanesPerBlock) + (e < kHalf ? 0 : 16) + kHalf * (sub % kLanesPerBlock) + (e % kHalf);
+  }
+  __device__ __forceinline__ static void q(const unsigned char* row, int sub, int, float (&f)[kPartElems]) {
+    const T* r = reinterpret_cast<const T*>(row);
+#pragma unroll
+    for (int e = 0; e < kPartElems; ++e) f[e] = to_float(r[dim(sub, 0, e)]);
+  }
+  __device__ __forceinline__ static void out(unsigned char* row, int sub, int, const float (&f)[kPartElems]) {
+    T* r = reinterpret_cast<T*>(row);
+#pragma unroll
+    for (int e = 0; e < kPartElems; ++e) store_elem(r + dim(sub, 0, e), f[e]);
+  }
+};
+
 // Tensor-core tile of an fp8 cache with one query head per warp (m16n8k16,
 // binary16 operands, fp32 accumulation). Every e4m3 value is exactly a
 // binary16 value, so K and V enter the MMAs exactly; the query row enters as
@@ -217,16 +259,50 @@ struct FpMma {
   __device__ __forceinline__ static float pow2(int k) { return __int_as_float((k + 127) << 23); }
 };
 
+// Tensor-core tile of a q4_0 cache, one query head per warp (m16n8k16,
+// binary16 operands, fp32 accumulation). A code q enters the MMAs as the
+// exact binary16 integer q - 8 (the bits 0x6400 | q are 1024 + q, and
+// 1024 + 8 is subtracted); the scales stay out of the A operands:
+//
+// Scores, S^T = K q^T: tokens are M, head dims K. Lane (g, t) supplies the
+// A elements of block t (head_dim 128; head_dim 64: half t % 2 of block
+// t / 2): k-step kk takes code word kk / 2 of its part, low (kk even) or
+// high four bits, bytes 0 and 2 as MMA columns 2t, 2t + 1 and bytes 1 and 3
+// as 2t + 8, 2t + 9. Column n of the query operand holds the query only at
+// the dims of block n (zero elsewhere), so column n of S^T is the block-n
+// partial sum and the score is sum_n d_n S^T[., n] (the scales multiply
+// fp32 partial sums).
+//
+// Output, O^T += V^T P^T: head dims are M, tokens K; column 2 b + u of P^T
+// holds the high (u = 0) or low (u = 1) binary16 part of p d_b (token's
+// scale of block b), so O^T[dim, 2 b] + O^T[dim, 2 b + 1] is the output of a
+// dim of block b. Lane (g, t) reads code bytes [g D/16, (g + 1) D/16) of its
+// four token rows; byte m gives MMA rows g (low bits) and g + 8 (high bits)
+// of m-tile m; lane (g, blk(g)) ends with those dims (LaneDims<T, Q4Row, D>).
+struct Q4Mma {
+  // binary16 pair (n0 - 8, n2 - 8) of the nibbles at bits 0-3 and 16-19 of w
+  __device__ __forceinline__ static uint32_t pair(uint32_t w) {
+    const uint32_t h = (w & 0x000F000Fu) | 0x64006400u;
+    __half2 v;
+    memcpy(&v, &h, 4);
+    v = __hsub2(v, __half2half2(__ushort_as_half((unsigned short)0x6408u)));
+    uint32_t r;
+    memcpy(&r, &v, 4);
+    return r;
+  }
+};
+
 // NWO / BudgetO: explicit warps per block and ring budget (0: the defaults).
 template <typename T, int D, int GPW, typename KT = T, int NWO = 0, int BudgetO = 0>
 struct DecodeShape {
-  static constexpr bool kFp8Wide = sizeof(KT) == 1 && GPW <= 2;
-  static constexpr bool kFp8Mma = sizeof(KT) == 1 && GPW == 1;
+  static constexpr bool kQ4 = CacheKind<KT>::kQ4;  // q4_0 cache: tensor-core tile, one head per warp
+  static constexpr bool kFp8Wide = CacheKind<KT>::kFp8 && GPW <= 2;
+  static constexpr bool kFp8Mma = CacheKind<KT>::kFp8 && GPW == 1;
   static constexpr int kWarps =
-      NWO ? NWO : (kFp8Mma ? kFp8MmaWarps : kFp8Wide ? kFp8Warps2 : kDecodeWarps);
+      NWO ? NWO : ((kFp8Mma || kQ4) ? kFp8MmaWarps : kFp8Wide ? kFp8Warps2 : kDecodeWarps);
   static constexpr int kElemBytes = sizeof(T);
   static constexpr int kRowBytes = D * kElemBytes;                       // query / output row
-  static constexpr int kKvRowBytes = D * (int)sizeof(KT);                // cache row
+  static constexpr int kKvRowBytes = CacheKind<KT>::template row_bytes<D>();  // cache row
   static constexpr int kTileTokensT = tile_tokens_for<KT>();
   static constexpr int kTileBytes = kTileTokensT * kKvRowBytes;          // K (or V) rows of one tile
   // the tensor-core fp8 tile at head_dim 128 takes its K and V rows by 2-D
@@ -235,7 +311,7 @@ struct DecodeShape {
   static constexpr bool kTma = kFp8Mma && D == 128;
   static constexpr int kStageRaw = 2 * kTileBytes + GPW * kRowBytes;     // K, V, query rows
   static constexpr int kStageBytes = kTma ? (kStageRaw + 1023) / 1024 * 1024 : kStageRaw;
-  static constexpr int kRingBudget = BudgetO ? BudgetO : (kFp8Wide ? kFp8RingBudget : 128 * 1024);
+  static constexpr int kRingBudget = BudgetO ? BudgetO : ((kFp8Wide || kQ4) ? kFp8RingBudget : 128 * 1024);
   static constexpr int kStagesRaw = kRingBudget / (kWarps * 2 * kTileBytes);
   static constexpr int kStages = kStagesRaw < 1 ? 1 : (kStagesRaw > 4 ? 4 : kStagesRaw);
   static constexpr int kChunksPerRow = kRowBytes / 16;
@@ -248,6 +324,7 @@ struct DecodeShape {
   static constexpr int kScanOff = kBtOff + kWarps * kBtChunk * 4;
   static constexpr int kStartOff = kScanOff + kWarps * 8;
   static constexpr int kSmemBytes = kStartOff + kWarps * 16 + (kTma ? 1024 : 0);  // + alignment of the base
+  static_assert(!kQ4 || GPW == 1, "q4_0 caches: one query head per warp");
   static_assert(kChunksPerRow % 8 == 0, "row must split into 8 lanes of 16-byte chunks");
   static_assert(kDimsPerLane * 8 == D, "lane mapping");
   static_assert(kStageBytes % 16 == 0 && kRowBytes % 16 == 0 && kTileBytes % 16 == 0, "bulk copy alignment");
@@ -318,8 +395,9 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
                      const DecodeParams p) {
   using S = DecodeShape<T, D, GPW, KT>;
   using LD = LaneDims<T, KT, D>;
-  constexpr bool kQuant = !std::is_same<T, KT>::value;
-  constexpr bool kMma = S::kFp8Mma;    // fp8 cache, one query head per warp: tensor-core tiles
+  constexpr bool kQuant = CacheKind<KT>::kFp8;  // values are codes times p.v_scale
+  constexpr bool kQ4 = S::kQ4;
+  constexpr bool kMma = S::kFp8Mma || kQ4;     // one query head per warp: tensor-core tiles
   constexpr int NKS = D / 16;          // MMA k-steps of the scores, m-tiles of the output
   constexpr int TT = S::kTileTokensT;  // tokens per tile
   constexpr int RPG = TT / 4;          // rows of a tile per 8-lane group
@@ -504,7 +582,44 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
         l[0] = 0.f;
 #pragma unroll
         for (int mm = 0; mm < NKS; ++mm) oa[mm][0] = oa[mm][1] = oa[mm][2] = oa[mm][3] = 0.f;
-        if (nvalid > 0) {
+        if (kQ4 && nvalid > 0) {
+          // lane (g, t): the query dims of its code part (bytes [PB t, PB (t+1))
+          // of the row's codes, low then high four bits); nonzero B columns
+          // only where the column is the part's block
+          constexpr int PB = D / 8;  // code bytes of a lane's part
+          const int t = lane & 3, g = lane >> 2;
+          const int blk = t / (128 / D);
+          const int e0 = 32 * blk + (D == 128 ? 0 : 8 * (t & 1));
+          const unsigned char* qrow = ks + 2 * S::kTileBytes;
+          float qv[2][PB];
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+            for (int c = 0; c < PB / 8; ++c) {
+              float f8[8];
+              Chunk<T>::widen(*reinterpret_cast<const uint4*>(qrow + 2 * (e0 + 16 * hb + 8 * c)), f8);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) qv[hb][8 * c + e] = f8[e];
+            }
+          float amax = 0.f;
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+            for (int e = 0; e < PB; ++e) amax = fmaxf(amax, fabsf(qv[hb][e]));
+          amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
+          amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+          int k = 0;
+          if (amax > 0.f) k = min(141 - ((__float_as_int(amax) >> 23) & 0xff), 127);
+          const float sig = FpMma::pow2(max(k, -126));
+          sc_q = ldexpf(p.scale_log2, -max(k, -126));
+          const bool mine = g == blk;
+#pragma unroll
+          for (int kk = 0; kk < NKS; ++kk) {  // code word kk / 2, four bits kk % 2
+            const int hb = kk & 1, j = 4 * (kk >> 1);
+            qb[kk][0] = mine ? FpMma::pack(qv[hb][j] * sig, qv[hb][j + 2] * sig) : 0u;
+            qb[kk][1] = mine ? FpMma::pack(qv[hb][j + 1] * sig, qv[hb][j + 3] * sig) : 0u;
+          }
+        } else if (nvalid > 0) {
           // lane (g, t) takes query dims [t D/4, (t+1) D/4) as its B
           // fragments (the query fills every column of N)
           constexpr int QPL = D / 4;
@@ -536,7 +651,7 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
         }
       }
     }
-    if (first && !kMma) {
+    if constexpr (!kMma) if (first) {
       visit_from_start = cc.t == 0;
 #pragma unroll
       for (int g = 0; g < GPW; ++g) {
@@ -560,7 +675,124 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
       }
     }
 
-    if constexpr (kMma) {
+    if constexpr (kQ4) {
+      if (nvalid > 0) {
+        // ---- tensor-core tile of q4_0 rows (layouts: Q4Mma) --------------------
+        const int g = lane >> 2, t = lane & 3;
+        constexpr int MT = TT / 16;
+        constexpr int NBK = D / 32;  // blocks (scales) per row
+        constexpr int SCB = D / 16;  // scale bytes per row
+        constexpr int PB = D / 8;    // code bytes of a lane's part (scores)
+        constexpr int VB = D / 16;   // code bytes a lane reads per row (output)
+        float sacc[MT][4];
+        float x[MT][2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          sacc[mt][0] = sacc[mt][1] = sacc[mt][2] = sacc[mt][3] = 0.f;
+          uint32_t cw[2][PB / 4];  // code words of the lane's part
+          uint32_t wst[2];          // the rows' scale words of blocks 2t, 2t + 1
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            const unsigned char* row = ks + (16 * mt + g + 8 * v) * KROW;
+            uint32_t sw[NBK / 2];
+            if constexpr (D == 128) {
+              const uint2 s2 = *reinterpret_cast<const uint2*>(row);
+              const uint2 a0 = *reinterpret_cast<const uint2*>(row + SCB + PB * t);
+              const uint2 a1 = *reinterpret_cast<const uint2*>(row + SCB + PB * t + 8);
+              cw[v][0] = a0.x, cw[v][1] = a0.y, cw[v][2] = a1.x, cw[v][3] = a1.y;
+              sw[0] = s2.x, sw[1] = s2.y;
+            } else {
+              sw[0] = *reinterpret_cast<const uint32_t*>(row);
+              cw[v][0] = *reinterpret_cast<const uint32_t*>(row + SCB + PB * t);
+              cw[v][1] = *reinterpret_cast<const uint32_t*>(row + SCB + PB * t + 4);
+            }
+            wst[v] = sw[0];
+#pragma unroll
+            for (int i = 1; i < NBK / 2; ++i) wst[v] = t == i ? sw[i] : wst[v];
+          }
+#pragma unroll
+          for (int kk = 0; kk < NKS; ++kk) {
+            const uint32_t w0 = cw[0][kk >> 1] >> (4 * (kk & 1));
+            const uint32_t w1 = cw[1][kk >> 1] >> (4 * (kk & 1));
+            FpMma::mma(sacc[mt], Q4Mma::pair(w0), Q4Mma::pair(w1), Q4Mma::pair(w0 >> 8), Q4Mma::pair(w1 >> 8),
+                       qb[kk][0], qb[kk][1]);
+          }
+          // columns 2t, 2t + 1 are the partial sums of blocks 2t, 2t + 1
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            const auto half_at = [](uint32_t w, int hi) {
+              return __half2float(__ushort_as_half((unsigned short)(hi ? w >> 16 : w & 0xffffu)));
+            };
+            float part = 0.f;
+            if (2 * t < NBK) part = half_at(wst[v], 0) * sacc[mt][2 * v] + half_at(wst[v], 1) * sacc[mt][2 * v + 1];
+            part += __shfl_xor_sync(kFullMask, part, 1);
+            part += __shfl_xor_sync(kFullMask, part, 2);
+            const int tok = 16 * mt + g + 8 * v;
+            x[mt][v] = tok < nvalid ? part * sc_q : -INFINITY;
+            mx = fmaxf(mx, x[mt][v]);
+          }
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(kFullMask, mx, off));
+        const float mn = fmaxf(m[0], mx);
+        const float alpha = exp2f(m[0] - mn);  // 0 on the first tile (m = -inf)
+        m[0] = mn;
+        float pv[MT][2], ps = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            pv[mt][v] = exp2f(x[mt][v] - mn);
+            ps += pv[mt][v];
+          }
+        l[0] = l[0] * alpha + ps;
+        if (alpha != 1.f) {  // warp-uniform
+#pragma unroll
+          for (int mm = 0; mm < NKS; ++mm)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) oa[mm][e] *= alpha;
+        }
+#pragma unroll
+        for (int ks2 = 0; ks2 < MT; ++ks2) {
+          // column pair 2t, 2t + 1: p d_t of tokens 16 ks2 + g (+ 8), d_t the
+          // V row's scale of block t, as a binary16 high part and remainder
+          // (rows past the context: 0, whatever their scale bytes hold)
+          uint32_t mv[2];
+#pragma unroll
+          for (int v = 0; v < 2; ++v) {
+            const int tok = 16 * ks2 + g + 8 * v;
+            const float dvt = t < NBK ? __half2float(*reinterpret_cast<const __half*>(vs + tok * KROW + 2 * t)) : 0.f;
+            const float pd = tok < nvalid ? pv[ks2][v] * dvt : 0.f;
+            const float ph = __half2float(__float2half_rn(pd));
+            mv[v] = t < NBK ? FpMma::pack(ph, pd - ph) : 0u;
+          }
+          const uint32_t b0 = FpMma::trans(mv[0]), b1 = FpMma::trans(mv[1]);
+          // code bytes [g VB, (g+1) VB) of token rows 2t, 2t + 1, 2t + 8, 2t + 9
+          uint32_t vr[4][VB / 4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tok = 16 * ks2 + 2 * t + (i & 1) + 8 * (i >> 1);
+            const unsigned char* vrow = vs + tok * KROW + SCB + VB * g;
+            if constexpr (VB == 8) {
+              const uint2 a = *reinterpret_cast<const uint2*>(vrow);
+              vr[i][0] = a.x, vr[i][1] = a.y;
+            } else {
+              vr[i][0] = *reinterpret_cast<const uint32_t*>(vrow);
+            }
+          }
+#pragma unroll
+          for (int mm = 0; mm < NKS; ++mm) {
+            // byte mm of the two token rows of a pair into bytes 0 and 2
+            const uint32_t sel = 0x4400u + 0x1111u * (uint32_t)(mm & 3);
+            const uint32_t y01 = __byte_perm(vr[0][mm >> 2], vr[1][mm >> 2], sel);
+            const uint32_t y23 = __byte_perm(vr[2][mm >> 2], vr[3][mm >> 2], sel);
+            FpMma::mma(oa[mm], Q4Mma::pair(y01), Q4Mma::pair(y01 >> 4), Q4Mma::pair(y23), Q4Mma::pair(y23 >> 4),
+                       b0, b1);
+          }
+        }
+      }
+    } else if constexpr (kMma) {
       if (nvalid > 0) {
         // ---- tensor-core tile (layouts: FpMma) --------------------------------
         const int g = lane >> 2, t = lane & 3;
@@ -669,7 +901,7 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
       }
     }
 
-    if (!kMma && nvalid > 0) {
+    if constexpr (!kMma) if (nvalid > 0) {
       // logits of rows grp, grp+4, grp+8, grp+12
       float x[GPW][RPG];
 #pragma unroll
@@ -752,11 +984,25 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) lt += __shfl_xor_sync(kFullMask, lt, off);
         l[0] = lane < 8 ? lt : 0.f;
+        if constexpr (kQ4) {
+          // lane g < 8 takes its dims from lane (g, block of g): low bits of
+          // byte e (e < DPL/2) are row g, high bits row g + 8 of m-tile e % (DPL/2)
+          constexpr int HALF = DPL / 2;
+          const int src = 4 * (lane & 7) + (lane & 7) / (256 / D);
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) {
-          const float v = oa[e >> 1][2 * (e & 1)] + oa[e >> 1][2 * (e & 1) + 1];
-          const float w = __shfl_sync(kFullMask, v, 4 * (lane & 7));
-          o[0][e] = lane < 8 ? w : 0.f;
+          for (int e = 0; e < DPL; ++e) {
+            const int mm = e % HALF;
+            const float v = e < HALF ? oa[mm][0] + oa[mm][1] : oa[mm][2] + oa[mm][3];
+            const float w = __shfl_sync(kFullMask, v, src);
+            o[0][e] = lane < 8 ? w : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < DPL; ++e) {
+            const float v = oa[e >> 1][2 * (e & 1)] + oa[e >> 1][2 * (e & 1) + 1];
+            const float w = __shfl_sync(kFullMask, v, 4 * (lane & 7));
+            o[0][e] = lane < 8 ? w : 0.f;
+          }
         }
       }
 #pragma unroll
@@ -911,5 +1157,7 @@ DecodeLauncher decode_launcher_f16(int head_dim, int gpw_index);
 DecodeLauncher decode_launcher_bf16(int head_dim, int gpw_index);
 // fp8 e4m3 caches with 16-bit queries (decode_fp8.cu): q_is_bf16 0 -> fp16 queries.
 DecodeLauncher decode_launcher_fp8(int q_is_bf16, int head_dim, int gpw_index);
+// q4_0 caches with 16-bit queries, one query head per warp (decode_q4.cu).
+DecodeLauncher decode_launcher_q4(int q_is_bf16, int head_dim);
 
 }  // namespace pkv

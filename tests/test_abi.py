@@ -146,7 +146,43 @@ def test_fp8_host_checks(pkv):
     assert dc() == pkv.PKV_ERR_WORKSPACE
     # block copies take the 1-byte element
     assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 0, 4, 128, 16, 10, 3, None, None) == OK
-    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 2, 4, 128, 16, 10, 4, None, None) == UNS
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 2, 4, 128, 16, 10, 5, None, None) == UNS
+
+
+def test_q4_0_host_checks(pkv):
+    L = pkv.lib
+    INV, UNS, OK = pkv.PKV_ERR_INVALID_ARG, pkv.PKV_ERR_UNSUPPORTED, pkv.PKV_OK
+    # (k, v, k_cache, v_cache, slots, T, Hkv, D, bs, NB, src_dtype, err, stream)
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, 3, 4, 128, 16, 10, 1, None, None]
+
+    def rc(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.pkv_reshape_and_cache_q4_0(*a)
+    assert rc(a5=0) == OK
+    assert rc(a10=0) == UNS and rc(a10=3) == UNS and rc(a10=4) == UNS  # only 16-bit sources
+    assert rc(a7=96) == UNS and rc(a8=4) == UNS
+    assert rc(a0=None) == INV and rc(a2=FAKE + 8) == INV and rc(a4=FAKE + 4) == INV and rc(a6=0) == INV
+    # decode: (out, q, k, v, bt, cl, scale, H, Hkv, D, bs, B, MB, NB, mcl, dtype, ws, ws_bytes, err, s)
+    d = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.1, 8, 2, 128, 16, 4, 8, 100, 128, 2, None, 0, None, None]
+
+    def dc(**kw):
+        a = list(d)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return L.pkv_paged_attention_decode_q4_0(*a)
+    assert dc(a11=0) == OK
+    assert dc(a15=0) == UNS            # binary32 queries: not taken
+    assert dc(a9=80) == UNS            # head_dim outside {64, 128}
+    assert dc(a7=5) == INV             # query heads not a multiple of kv heads
+    assert dc(a6=float("inf")) == INV
+    assert dc() == pkv.PKV_ERR_WORKSPACE
+    assert dc(a16=FAKE + 8, a17=1 << 30) == INV  # misaligned workspace
+    # block copies: q4_0 rows of 9 D / 16 bytes
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 0, 4, 128, 16, 10, 4, None, None) == OK
+    assert L.pkv_copy_blocks(FAKE, FAKE, FAKE, 0, 4, 48, 16, 10, 4, None, None) == UNS
+    assert pkv.q4_0_row_bytes(128) == 72 and pkv.q4_0_row_bytes(64) == 36
 
 
 def test_prefill_host_checks(pkv):
