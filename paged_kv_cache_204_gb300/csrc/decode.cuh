@@ -90,7 +90,7 @@ struct CacheKind {
 // as much data) as a 16-token tile of a 16-bit cache.
 template <typename KT>
 constexpr int tile_tokens_for() {
-  return (CacheKind<KT>::kFp8 || CacheKind<KT>::kQ4) ? 2 * kTileTokens : kTileTokens;
+  return CacheKind<KT>::kQ4 ? 4 * kTileTokens : CacheKind<KT>::kFp8 ? 2 * kTileTokens : kTileTokens;
 }
 constexpr int kDecodeWarps = 8;  // one resident block of 8 warps per SM (measured best)
 // fp8 caches (1 or 2 query heads per warp): a warp's per-tile work is a
@@ -260,9 +260,13 @@ struct FpMma {
 };
 
 // Tensor-core tile of a q4_0 cache, one query head per warp (m16n8k16,
-// binary16 operands, fp32 accumulation). A code q enters the MMAs as the
-// exact binary16 integer q - 8 (the bits 0x6400 | q are 1024 + q, and
-// 1024 + 8 is subtracted); the scales stay out of the A operands:
+// binary16 operands, fp32 accumulation). A code q enters the MMAs as its own
+// four bits, masked in place: the binary16 subnormal q 2^-24 (low nibble)
+// or 16 q 2^-24 (high nibble), exact; the query operand of high-nibble
+// k-steps is scaled by 1/16 to match. The offset 8 and the scales stay out
+// of the A operands: sum_j (q_j - 8) x_j = 2^24 sum_j (q_j 2^-24) x_j -
+// 8 sum_j x_j, with the sums of the query (scores) and of P (output) kept
+// beside the MMAs.
 //
 // Scores, S^T = K q^T: tokens are M, head dims K. Lane (g, t) supplies the
 // A elements of block t (head_dim 128; head_dim 64: half t % 2 of block
@@ -280,16 +284,11 @@ struct FpMma {
 // four token rows; byte m gives MMA rows g (low bits) and g + 8 (high bits)
 // of m-tile m; lane (g, blk(g)) ends with those dims (LaneDims<T, Q4Row, D>).
 struct Q4Mma {
-  // binary16 pair (n0 - 8, n2 - 8) of the nibbles at bits 0-3 and 16-19 of w
-  __device__ __forceinline__ static uint32_t pair(uint32_t w) {
-    const uint32_t h = (w & 0x000F000Fu) | 0x64006400u;
-    __half2 v;
-    memcpy(&v, &h, 4);
-    v = __hsub2(v, __half2half2(__ushort_as_half((unsigned short)0x6408u)));
-    uint32_t r;
-    memcpy(&r, &v, 4);
-    return r;
-  }
+  // binary16 pair of the nibbles n0, n1 at bits 0-3 and 16-19 of w, as the
+  // subnormals n 2^-24 (the bit pattern n itself: exact)
+  __device__ __forceinline__ static uint32_t lo(uint32_t w) { return w & 0x000F000Fu; }
+  // the nibbles at bits 4-7 and 20-23, left in place: 16 n 2^-24
+  __device__ __forceinline__ static uint32_t hi(uint32_t w) { return w & 0x00F000F0u; }
 };
 
 // NWO / BudgetO: explicit warps per block and ring budget (0: the defaults).
@@ -557,6 +556,9 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
   uint32_t qb[NKS][2];
   float oa[NKS][4];
   float sc_q = 0.f;
+  // q4_0: 8 x the query sums of blocks 2t, 2t + 1 (this lane's score
+  // columns) and the running sum of this lane's P column pair (block t)
+  float q4_corr0 = 0.f, q4_corr1 = 0.f, q4_psum = 0.f;
   bool visit_from_start = true;
   const size_t H = p.num_heads;
 
@@ -582,6 +584,7 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
         l[0] = 0.f;
 #pragma unroll
         for (int mm = 0; mm < NKS; ++mm) oa[mm][0] = oa[mm][1] = oa[mm][2] = oa[mm][3] = 0.f;
+        q4_psum = 0.f;
         if (kQ4 && nvalid > 0) {
           // lane (g, t): the query dims of its code part (bytes [PB t, PB (t+1))
           // of the row's codes, low then high four bits); nonzero B columns
@@ -614,11 +617,25 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
           sc_q = ldexpf(p.scale_log2, -max(k, -126));
           const bool mine = g == blk;
 #pragma unroll
-          for (int kk = 0; kk < NKS; ++kk) {  // code word kk / 2, four bits kk % 2
+          for (int kk = 0; kk < NKS; ++kk) {  // code word kk / 2, four bits kk % 2 (high: times 1/16)
             const int hb = kk & 1, j = 4 * (kk >> 1);
-            qb[kk][0] = mine ? FpMma::pack(qv[hb][j] * sig, qv[hb][j + 2] * sig) : 0u;
-            qb[kk][1] = mine ? FpMma::pack(qv[hb][j + 1] * sig, qv[hb][j + 3] * sig) : 0u;
+            const float sk = hb ? sig * 0.0625f : sig;
+            qb[kk][0] = mine ? FpMma::pack(qv[hb][j] * sk, qv[hb][j + 2] * sk) : 0u;
+            qb[kk][1] = mine ? FpMma::pack(qv[hb][j + 1] * sk, qv[hb][j + 3] * sk) : 0u;
           }
+          // 8 x the sum of each block's scaled query (as the MMAs see it),
+          // to the lanes whose score columns hold blocks 2t and 2t + 1
+          float qs = 0.f;
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb)
+#pragma unroll
+            for (int e = 0; e < PB; ++e) qs += FpMma::unpack(FpMma::pack(qv[hb][e] * sig, 0.f)).x;
+          if (D == 64) qs += __shfl_xor_sync(kFullMask, qs, 1);  // two lanes per block
+          const int per = 128 / D;                                // lanes per block
+          const float s0 = __shfl_sync(kFullMask, qs, (lane & ~3) | ((2 * t * per) & 3));
+          const float s1 = __shfl_sync(kFullMask, qs, (lane & ~3) | (((2 * t + 1) * per) & 3));
+          q4_corr0 = 2 * t < D / 32 ? 8.f * s0 : 0.f;
+          q4_corr1 = 2 * t + 1 < D / 32 ? 8.f * s1 : 0.f;
         } else if (nvalid > 0) {
           // lane (g, t) takes query dims [t D/4, (t+1) D/4) as its B
           // fragments (the query fills every column of N)
@@ -712,11 +729,12 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
             for (int i = 1; i < NBK / 2; ++i) wst[v] = t == i ? sw[i] : wst[v];
           }
 #pragma unroll
-          for (int kk = 0; kk < NKS; ++kk) {
-            const uint32_t w0 = cw[0][kk >> 1] >> (4 * (kk & 1));
-            const uint32_t w1 = cw[1][kk >> 1] >> (4 * (kk & 1));
-            FpMma::mma(sacc[mt], Q4Mma::pair(w0), Q4Mma::pair(w1), Q4Mma::pair(w0 >> 8), Q4Mma::pair(w1 >> 8),
-                       qb[kk][0], qb[kk][1]);
+          for (int w = 0; w < PB / 4; ++w) {  // k-steps 2w (low four bits) and 2w + 1 (high)
+            const uint32_t x0 = cw[0][w], x1 = cw[1][w], y0 = x0 >> 8, y1 = x1 >> 8;
+            FpMma::mma(sacc[mt], Q4Mma::lo(x0), Q4Mma::lo(x1), Q4Mma::lo(y0), Q4Mma::lo(y1), qb[2 * w][0],
+                       qb[2 * w][1]);
+            FpMma::mma(sacc[mt], Q4Mma::hi(x0), Q4Mma::hi(x1), Q4Mma::hi(y0), Q4Mma::hi(y1), qb[2 * w + 1][0],
+                       qb[2 * w + 1][1]);
           }
           // columns 2t, 2t + 1 are the partial sums of blocks 2t, 2t + 1
 #pragma unroll
@@ -725,7 +743,9 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
               return __half2float(__ushort_as_half((unsigned short)(hi ? w >> 16 : w & 0xffffu)));
             };
             float part = 0.f;
-            if (2 * t < NBK) part = half_at(wst[v], 0) * sacc[mt][2 * v] + half_at(wst[v], 1) * sacc[mt][2 * v + 1];
+            if (2 * t < NBK)
+              part = half_at(wst[v], 0) * fmaf(sacc[mt][2 * v], 16777216.f, -q4_corr0) +
+                     half_at(wst[v], 1) * fmaf(sacc[mt][2 * v + 1], 16777216.f, -q4_corr1);
             part += __shfl_xor_sync(kFullMask, part, 1);
             part += __shfl_xor_sync(kFullMask, part, 2);
             const int tok = 16 * mt + g + 8 * v;
@@ -748,6 +768,7 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
           }
         l[0] = l[0] * alpha + ps;
         if (alpha != 1.f) {  // warp-uniform
+          q4_psum *= alpha;
 #pragma unroll
           for (int mm = 0; mm < NKS; ++mm)
 #pragma unroll
@@ -766,6 +787,8 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
             const float pd = tok < nvalid ? pv[ks2][v] * dvt : 0.f;
             const float ph = __half2float(__float2half_rn(pd));
             mv[v] = t < NBK ? FpMma::pack(ph, pd - ph) : 0u;
+            const float2 fed = FpMma::unpack(mv[v]);
+            q4_psum += fed.x + fed.y;  // the column pair's sum as the MMAs see it
           }
           const uint32_t b0 = FpMma::trans(mv[0]), b1 = FpMma::trans(mv[1]);
           // code bytes [g VB, (g+1) VB) of token rows 2t, 2t + 1, 2t + 8, 2t + 9
@@ -787,8 +810,7 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
             const uint32_t sel = 0x4400u + 0x1111u * (uint32_t)(mm & 3);
             const uint32_t y01 = __byte_perm(vr[0][mm >> 2], vr[1][mm >> 2], sel);
             const uint32_t y23 = __byte_perm(vr[2][mm >> 2], vr[3][mm >> 2], sel);
-            FpMma::mma(oa[mm], Q4Mma::pair(y01), Q4Mma::pair(y01 >> 4), Q4Mma::pair(y23), Q4Mma::pair(y23 >> 4),
-                       b0, b1);
+            FpMma::mma(oa[mm], Q4Mma::lo(y01), Q4Mma::hi(y01), Q4Mma::lo(y23), Q4Mma::hi(y23), b0, b1);
           }
         }
       }
@@ -987,12 +1009,19 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
         if constexpr (kQ4) {
           // lane g < 8 takes its dims from lane (g, block of g): low bits of
           // byte e (e < DPL/2) are row g, high bits row g + 8 of m-tile e % (DPL/2)
+          // (codes entered as q 2^-24 and 16 q 2^-24: scale back, less 8 x
+          // the P column pair's sum)
           constexpr int HALF = DPL / 2;
           const int src = 4 * (lane & 7) + (lane & 7) / (256 / D);
+          float ps8 = q4_psum;
+#pragma unroll
+          for (int off = 4; off < 32; off <<= 1) ps8 += __shfl_xor_sync(kFullMask, ps8, off);
+          ps8 *= 8.f;
 #pragma unroll
           for (int e = 0; e < DPL; ++e) {
             const int mm = e % HALF;
-            const float v = e < HALF ? oa[mm][0] + oa[mm][1] : oa[mm][2] + oa[mm][3];
+            const float v = e < HALF ? fmaf(oa[mm][0] + oa[mm][1], 16777216.f, -ps8)
+                                     : fmaf(oa[mm][2] + oa[mm][3], 1048576.f, -ps8);
             const float w = __shfl_sync(kFullMask, v, src);
             o[0][e] = lane < 8 ? w : 0.f;
           }
