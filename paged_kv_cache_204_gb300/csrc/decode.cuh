@@ -514,32 +514,30 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
         bt_j0 = j_first;
       }
     }
-    if (lane == 0) {
-      unsigned char* kdst = my_ring + (n % ST) * S::kStageBytes;
-      unsigned char* vdst = kdst + S::kTileBytes;
-      uint64_t* bar = my_bars + (n % ST);
-      uint32_t bytes = with_q ? GPW * ROW : 0;
-      for (int c2 = 0; c2 < nseg; ++c2)
-        if (t0 + c2 * seg < c.L) bytes += 2u * seg * KROW;
-      mbar_arrive_expect_tx(bar, bytes);
+    // the segments of rows that hold context tokens (one K and one V copy
+    // each) go from lanes 0 .. nsv - 1 at once, the query rows from lane nsv;
+    // lane 0 posts the bytes first
+    unsigned char* kdst = my_ring + (n % ST) * S::kStageBytes;
+    unsigned char* vdst = kdst + S::kTileBytes;
+    uint64_t* bar = my_bars + (n % ST);
+    const int nsv = min(nseg, (nvalid + seg - 1) / seg);
+    if (lane == 0) mbar_arrive_expect_tx(bar, (with_q ? GPW * ROW : 0u) + 2u * nsv * seg * KROW);
+    __syncwarp();
+    if (lane < nsv) {
+      const int t = t0 + lane * seg;
       const int kvh = (c.hg * GPW) / p.group;
-      for (int c2 = 0; c2 < nseg; ++c2) {
-        const int t = t0 + c2 * seg;
-        if (t >= c.L) break;
-        if constexpr (S::kTma) {  // boxes of {128 bytes, seg rows}, swizzled
-          const int y = (my_bt[t / bs - bt_j0] * p.num_kv_heads + kvh) * bs + (t % bs);
-          tma_load_2d(kdst + c2 * seg * KROW, &kmap, 0, y, bar);
-          tma_load_2d(vdst + c2 * seg * KROW, &vmap, 0, y, bar);
-        } else {
-          const size_t off =
-              (((size_t)my_bt[t / bs - bt_j0] * p.num_kv_heads + kvh) * bs + (t % bs)) * KROW;
-          bulk_copy_g2s(kdst + c2 * seg * KROW, kbase + off, seg * KROW, bar);
-          bulk_copy_g2s(vdst + c2 * seg * KROW, vbase + off, seg * KROW, bar);
-        }
+      if constexpr (S::kTma) {  // boxes of {128 bytes, seg rows}, swizzled
+        const int y = (my_bt[t / bs - bt_j0] * p.num_kv_heads + kvh) * bs + (t % bs);
+        tma_load_2d(kdst + lane * seg * KROW, &kmap, 0, y, bar);
+        tma_load_2d(vdst + lane * seg * KROW, &vmap, 0, y, bar);
+      } else {
+        const size_t off = (((size_t)my_bt[t / bs - bt_j0] * p.num_kv_heads + kvh) * bs + (t % bs)) * KROW;
+        bulk_copy_g2s(kdst + lane * seg * KROW, kbase + off, seg * KROW, bar);
+        bulk_copy_g2s(vdst + lane * seg * KROW, vbase + off, seg * KROW, bar);
       }
-      if (with_q)
-        bulk_copy_g2s(kdst + 2 * S::kTileBytes,
-                      qbase + ((size_t)c.s * p.num_heads + (size_t)c.hg * GPW) * ROW, GPW * ROW, bar);
+    } else if (lane == nsv && with_q) {
+      bulk_copy_g2s(kdst + 2 * S::kTileBytes, qbase + ((size_t)c.s * p.num_heads + (size_t)c.hg * GPW) * ROW,
+                    GPW * ROW, bar);
     }
   };
 
