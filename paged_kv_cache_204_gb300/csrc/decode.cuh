@@ -514,28 +514,28 @@ __global__ void __launch_bounds__(DecodeShape<T, D, GPW, KT>::kWarps * 32)
         bt_j0 = j_first;
       }
     }
-    // the segments of rows that hold context tokens (one K and one V copy
-    // each) go from lanes 0 .. nsv - 1 at once, the query rows from lane nsv;
-    // lane 0 posts the bytes first
+    // the segments of rows that hold context tokens go from lanes 0 ..
+    // 2 nsv - 1 at once (lane 2 c2 the K rows of segment c2, lane 2 c2 + 1 its
+    // V rows: copies issued from one lane queue behind one another), the
+    // query rows from lane 2 nsv; lane 0 posts the bytes first
     unsigned char* kdst = my_ring + (n % ST) * S::kStageBytes;
-    unsigned char* vdst = kdst + S::kTileBytes;
     uint64_t* bar = my_bars + (n % ST);
     const int nsv = min(nseg, (nvalid + seg - 1) / seg);
     if (lane == 0) mbar_arrive_expect_tx(bar, (with_q ? GPW * ROW : 0u) + 2u * nsv * seg * KROW);
     __syncwarp();
-    if (lane < nsv) {
-      const int t = t0 + lane * seg;
+    if (lane < 2 * nsv) {
+      const int c2 = lane >> 1, isv = lane & 1;
+      const int t = t0 + c2 * seg;
       const int kvh = (c.hg * GPW) / p.group;
+      unsigned char* dst = kdst + isv * S::kTileBytes + c2 * seg * KROW;
       if constexpr (S::kTma) {  // boxes of {128 bytes, seg rows}, swizzled
         const int y = (my_bt[t / bs - bt_j0] * p.num_kv_heads + kvh) * bs + (t % bs);
-        tma_load_2d(kdst + lane * seg * KROW, &kmap, 0, y, bar);
-        tma_load_2d(vdst + lane * seg * KROW, &vmap, 0, y, bar);
+        tma_load_2d(dst, isv ? &vmap : &kmap, 0, y, bar);
       } else {
         const size_t off = (((size_t)my_bt[t / bs - bt_j0] * p.num_kv_heads + kvh) * bs + (t % bs)) * KROW;
-        bulk_copy_g2s(kdst + lane * seg * KROW, kbase + off, seg * KROW, bar);
-        bulk_copy_g2s(vdst + lane * seg * KROW, vbase + off, seg * KROW, bar);
+        bulk_copy_g2s(dst, (isv ? vbase : kbase) + off, seg * KROW, bar);
       }
-    } else if (lane == nsv && with_q) {
+    } else if (lane == 2 * nsv && with_q) {
       bulk_copy_g2s(kdst + 2 * S::kTileBytes, qbase + ((size_t)c.s * p.num_heads + (size_t)c.hg * GPW) * ROW,
                     GPW * ROW, bar);
     }
