@@ -1446,27 +1446,26 @@ __global__ void __launch_bounds__(kSharedWarps * 32)
         tma_load_2d(st + tsr * St::kTensorBytes + cb * St::kColBytes + b * rb * 128, tsr ? &vmap : &kmap, cb * 64, y,
                     bar);
       }
-      if (with_q && lane == 0) {
-        for (int r = 0; r < c.nrows; ++r)
-          bulk_copy_g2s(st + St::kQOff + r * ROW,
-                        qbase + ((size_t)(c.lo + R * c.c + r) * H + c.h) * ROW, ROW, bar);
-      }
-    } else if (lane == 0) {
-      // a tail tile: plain K and V rows by 1-D bulk copies, the query rows
-      uint32_t bytes = with_q ? c.nrows * ROW : 0;
-      for (int c2 = 0; c2 < nseg; ++c2)
-        if (t0 + c2 * seg < c.tok_end) bytes += 2u * seg * ROW;
-      mbar_arrive_expect_tx(bar, bytes);
-      for (int c2 = 0; c2 < nseg; ++c2) {
+      // the siblings' query rows, one lane each after the boxes' lanes
+      const int qr = lane - 2 * per;
+      if (with_q && qr >= 0 && qr < c.nrows)
+        bulk_copy_g2s(st + St::kQOff + qr * ROW, qbase + ((size_t)(c.lo + R * c.c + qr) * H + c.h) * ROW, ROW, bar);
+    } else {
+      // a tail tile: plain K and V rows by 1-D bulk copies (lane 2 c2 the K
+      // rows of segment c2, lane 2 c2 + 1 its V rows: copies issued from one
+      // lane queue behind one another), the query rows from lane 2 nsv
+      const int nsv = min(nseg, (nvalid + seg - 1) / seg);
+      if (lane == 0) mbar_arrive_expect_tx(bar, (with_q ? c.nrows * ROW : 0u) + 2u * nsv * seg * ROW);
+      __syncwarp();
+      if (lane < 2 * nsv) {
+        const int c2 = lane >> 1, isv = lane & 1;
         const int t = t0 + c2 * seg;
-        if (t >= c.tok_end) break;
         const size_t off = (((size_t)my_bt[t / bs - bt_j0] * p.num_kv_heads + c.kvh) * bs + (t % bs)) * ROW;
-        bulk_copy_g2s(st + c2 * seg * ROW, kbase + off, seg * ROW, bar);
-        bulk_copy_g2s(st + St::kTensorBytes + c2 * seg * ROW, vbase + off, seg * ROW, bar);
-      }
-      if (with_q)
+        bulk_copy_g2s(st + isv * St::kTensorBytes + c2 * seg * ROW, (isv ? vbase : kbase) + off, seg * ROW, bar);
+      } else if (lane == 2 * nsv && with_q) {
         bulk_copy_g2s(st + St::kQOff, qbase + ((size_t)(c.lo + c.j) * H + (size_t)c.hg * c.nrows) * ROW,
                       c.nrows * ROW, bar);
+      }
     }
   };
 
