@@ -12,9 +12,10 @@
 //   one global sequence of T tiles. The grid is sized to the GPU (blocks that
 //   stay resident); its W warps each take one contiguous range of about T/W
 //   tiles, so every warp streams the same number of bytes.
-//   A warp walks its range tile by tile across segment boundaries. Lane 0
-//   issues 1-D bulk copies (cp.async.bulk, completion counted in bytes on an
-//   mbarrier) of the next tiles' K rows and V rows (plus the segment's query
+//   A warp walks its range tile by tile across segment boundaries. Its lanes
+//   issue 1-D bulk copies (cp.async.bulk, completion counted in bytes on an
+//   mbarrier; one lane per copy, since copies from one lane queue behind one
+//   another) of the next tiles' K rows and V rows (plus the segment's query
 //   rows at the first tile of a segment) into the warp's own ring of
 //   shared-memory slots, while all lanes compute on the current tile. There
 //   is no block-wide barrier after the start-up scan.
