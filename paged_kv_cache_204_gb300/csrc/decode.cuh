@@ -274,16 +274,18 @@ struct FpMma {
 // t / 2): k-step kk takes code word kk / 2 of its part, low (kk even) or
 // high four bits, bytes 0 and 2 as MMA columns 2t, 2t + 1 and bytes 1 and 3
 // as 2t + 8, 2t + 9. Column n of the query operand holds the query only at
-// the dims of block n (zero elsewhere), so column n of S^T is the block-n
-// partial sum and the score is sum_n d_n S^T[., n] (the scales multiply
-// fp32 partial sums).
+// the dims of block n (zero elsewhere), so column n of S^T is 2^-24 times
+// the block-n partial sum of q x and the score is sum_n d_n (2^24 S^T[., n]
+// - 8 sum_{j in n} x_j) (the scales multiply fp32 partial sums).
 //
 // Output, O^T += V^T P^T: head dims are M, tokens K; column 2 b + u of P^T
-// holds the high (u = 0) or low (u = 1) binary16 part of p d_b (token's
-// scale of block b), so O^T[dim, 2 b] + O^T[dim, 2 b + 1] is the output of a
-// dim of block b. Lane (g, t) reads code bytes [g D/16, (g + 1) D/16) of its
-// four token rows; byte m gives MMA rows g (low bits) and g + 8 (high bits)
-// of m-tile m; lane (g, blk(g)) ends with those dims (LaneDims<T, Q4Row, D>).
+// holds the high (u = 0) or low (u = 1) binary16 part of p d_b (the V row's
+// scale of block b), so for a dim of block b the output is 2^24 (2^20 for a
+// high nibble) times O^T[dim, 2 b] + O^T[dim, 2 b + 1], less 8 times the sum
+// of that column pair over the tokens. Lane (g, t) reads code bytes
+// [g D/16, (g + 1) D/16) of its four token rows; byte m gives MMA rows g
+// (low bits) and g + 8 (high bits) of m-tile m; lane (g, blk(g)) ends with
+// those dims (LaneDims<T, Q4Row, D>).
 struct Q4Mma {
   // binary16 pair of the nibbles n0, n1 at bits 0-3 and 16-19 of w, as the
   // subnormals n 2^-24 (the bit pattern n itself: exact)
